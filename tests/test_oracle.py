@@ -1,0 +1,373 @@
+"""Pins for the fp64 CPU oracle: each test ties the oracle to something other
+than its own formula -- a library routine, a closed form of a special case,
+finite differences of its own forward, or an invariant of the mathematics.
+
+The method follows "Noncausal Global Extreme-GQA Ragged Attention Full VJP"
+(sections "Hard Constraints" and "What You Have") and, for empty rows and
+recompute, "ragged flash attention gradient recompute" ("Root causes
+addressed", "Verification").
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from ragged_gqa_attention_varlen_gb300 import workloads as W
+
+D = 160
+
+
+def sigma(sm=0.75):
+    return sm / math.sqrt(D)
+
+
+def f32(x):
+    """x rounded to fp32, the slopes' storage type."""
+    return float(torch.tensor(x, dtype=torch.float32))
+
+
+def f64_problem(lq, lk, Hq, seed=0, qk_std=1.0, slope_max=0.25, **mask):
+    """Problem whose inputs are fp64 (used for exact special cases and FD)."""
+    return W.custom(lq, lk, Hq, dtype=torch.float64, seed=seed, qk_std=qk_std,
+                    slope_max=slope_max, **mask)
+
+
+# ---------------------------------------------------------------- decoding
+
+def test_decode_every_16bit_pattern(oracle_mod):
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16)
+    for dt in (torch.float16, torch.bfloat16):
+        ref = bits.view(dt).double()
+        got = torch.tensor([oracle_mod.decode(dt, int(b) & 0xFFFF) for b in range(65536)],
+                           dtype=torch.float64)
+        nan = torch.isnan(ref)
+        assert torch.equal(torch.isnan(got), nan)
+        assert torch.equal(got[~nan], ref[~nan])
+
+
+# ------------------------------------------- library special case: plain SDPA
+
+def _sdpa_reference(p, scale):
+    """Per sequence: torch SDPA in fp64 with K/V expanded over the query heads,
+    and autograd for the VJP (dk/dv sum over heads through the expand)."""
+    outs, dqs, dks, dvs, lses = [], [], [], [], []
+    for b in range(p.B):
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+        q = p.q[q0:q1].double().permute(1, 0, 2).clone().requires_grad_(True)  # [H, Lq, d]
+        k = p.k[k0:k1, 0].double().clone().requires_grad_(True)
+        v = p.v[k0:k1, 0].double().clone().requires_grad_(True)
+        do = p.dout[q0:q1].double().permute(1, 0, 2)
+        kk = k[None].expand(p.Hq, -1, -1)
+        vv = v[None].expand(p.Hq, -1, -1)
+        o = torch.nn.functional.scaled_dot_product_attention(q[None], kk[None], vv[None],
+                                                             scale=scale)[0]
+        gq, gk, gv = torch.autograd.grad(o, (q, k, v), do)
+        lse = torch.logsumexp(scale * q @ kk.transpose(-1, -2), dim=-1)
+        outs.append(o.detach().permute(1, 0, 2))
+        dqs.append(gq.permute(1, 0, 2))
+        dks.append(gk[:, None])
+        dvs.append(gv[:, None])
+        lses.append(lse.detach().permute(1, 0))
+    return (torch.cat(outs), torch.cat(lses), torch.cat(dqs), torch.cat(dks), torch.cat(dvs))
+
+
+@pytest.mark.parametrize("softcap", [0.0, 1e7])
+def test_reduces_to_sdpa_without_cap_and_alibi(oracle_mod, softcap):
+    p = f64_problem([3, 7, 1, 12], [5, 2, 9, 12], Hq=4, seed=3)
+    p.alibi_slopes.zero_()
+    p.softcap = softcap
+    r = oracle_mod.fvjp(p)
+    out, lse, dq, dk, dv = _sdpa_reference(p, sigma())
+    tol = dict(rtol=1e-9, atol=1e-11)
+    torch.testing.assert_close(r["out"], out, **tol)
+    torch.testing.assert_close(r["lse"], lse, **tol)
+    torch.testing.assert_close(r["dq"], dq, **tol)
+    torch.testing.assert_close(r["dk"], dk, **tol)
+    torch.testing.assert_close(r["dv"], dv, **tol)
+
+
+def test_fp16_inputs_decode_like_torch_in_sdpa_case(oracle_mod):
+    p = W.custom([6, 4], [3, 8], Hq=2, dtype=torch.float16, seed=5)
+    p.alibi_slopes.zero_()
+    p.softcap = 0.0
+    r = oracle_mod.fvjp(p)
+    out, lse, dq, dk, dv = _sdpa_reference(p, sigma())
+    torch.testing.assert_close(r["out"], out, rtol=1e-10, atol=1e-12)
+    torch.testing.assert_close(r["dk"], dk, rtol=1e-10, atol=1e-12)
+
+
+# --------------------------------------------------------- closed forms
+
+def test_two_keys_softcap_then_alibi_closed_form(oracle_mod):
+    """One query, two keys, q = a e0, k0 = e0, k1 = 0: s0 = sigma a, s1 = 0.
+    The ALiBi distances are |0 + 2 - 1 - j| = (1, 0), so with the cap applied
+    first, z0 = 3 tanh(sigma a / 3) - slope and z1 = 0, and the softmax over two
+    keys is the logistic function of z0."""
+    p = f64_problem([1], [2], Hq=1)
+    a, slope = 60.0, 0.3
+    p.q.zero_()
+    p.q[0, 0, 0] = a
+    p.k.zero_()
+    p.k[0, 0, 0] = 1.0
+    p.alibi_slopes.fill_(slope)
+    r = oracle_mod.fvjp(p)
+    z0 = 3.0 * math.tanh(sigma() * a / 3.0) - f32(slope)
+    w0 = 1.0 / (1.0 + math.exp(-z0))
+    expect = w0 * p.v[0, 0] + (1.0 - w0) * p.v[1, 0]
+    torch.testing.assert_close(r["out"][0, 0], expect, rtol=1e-13, atol=1e-14)
+    assert abs(float(r["lse"][0, 0]) - math.log(math.exp(z0) + 1.0)) < 1e-13
+    # the cap is active: without it the weight would differ markedly
+    z0_nocap = sigma() * a - f32(slope)
+    assert abs(1.0 / (1.0 + math.exp(-z0_nocap)) - w0) > 0.05
+
+
+# Distances |i + Lk - Lq - j| written out by hand for small shapes.
+ALIBI_TABLES = {
+    (2, 4): [[2, 1, 0, 1], [3, 2, 1, 0]],
+    (4, 2): [[2, 3], [1, 2], [0, 1], [1, 0]],
+    (3, 3): [[0, 1, 2], [1, 0, 1], [2, 1, 0]],
+}
+
+
+@pytest.mark.parametrize("shape", sorted(ALIBI_TABLES))
+def test_alibi_distance_tables(oracle_mod, shape):
+    """With q = 0 every logit is 0 (softcap of 0 is 0), so the weights are a
+    softmax of -slope * distance alone."""
+    Lq, Lk = shape
+    p = f64_problem([Lq], [Lk], Hq=2, seed=1)
+    p.q.zero_()
+    p.alibi_slopes.copy_(torch.tensor([[0.7, 0.2]]))
+    r = oracle_mod.fvjp(p)
+    dist = np.array(ALIBI_TABLES[shape], dtype=np.float64)
+    for h, slope in enumerate((0.7, 0.2)):
+        w = np.exp(-f32(slope) * dist)
+        lse = np.log(w.sum(1))
+        w = w / w.sum(1, keepdims=True)
+        expect = torch.from_numpy(w) @ p.v[:, 0]
+        torch.testing.assert_close(r["out"][:, h], expect, rtol=1e-13, atol=1e-14)
+        torch.testing.assert_close(r["lse"][:, h], torch.from_numpy(lse), rtol=1e-13, atol=1e-14)
+
+
+def test_alibi_equal_lengths_is_abs_i_minus_j(oracle_mod):
+    """North-star identity: Lq = Lk makes the distance |i - j|."""
+    L = 7
+    p = f64_problem([L], [L], Hq=1, seed=2)
+    p.q.zero_()
+    p.alibi_slopes.fill_(0.4)
+    r = oracle_mod.fvjp(p)
+    dist = np.abs(np.subtract.outer(np.arange(L), np.arange(L))).astype(np.float64)
+    w = np.exp(-f32(0.4) * dist)
+    w /= w.sum(1, keepdims=True)
+    torch.testing.assert_close(r["out"][:, 0], torch.from_numpy(w) @ p.v[:, 0], rtol=1e-13,
+                               atol=1e-14)
+
+
+# Admissible key sets written out by hand (k0 = i + Lk - Lq).
+MASK_CASES = [
+    # (Lq, Lk, causal, wl, wr, sets per row)
+    (3, 5, True, -1, -1, [{0, 1, 2}, {0, 1, 2, 3}, {0, 1, 2, 3, 4}]),
+    (3, 5, False, 1, 1, [{1, 2, 3}, {2, 3, 4}, {3, 4}]),
+    (3, 5, True, 1, -1, [{1, 2}, {2, 3}, {3, 4}]),
+    (3, 5, True, 1, 4, [{1, 2}, {2, 3}, {3, 4}]),  # causal overrides the right window
+    (5, 2, True, -1, -1, [set(), set(), set(), {0}, {0, 1}]),
+    (4, 6, False, 0, -1, [{2, 3, 4, 5}, {3, 4, 5}, {4, 5}, {5}]),
+]
+
+
+@pytest.mark.parametrize("case", MASK_CASES)
+def test_mask_admissible_sets(oracle_mod, case):
+    """q = 0 and zero slopes give uniform weights over the admissible keys."""
+    Lq, Lk, causal, wl, wr, sets = case
+    p = f64_problem([Lq], [Lk], Hq=2, seed=4, causal=causal, window_left=wl, window_right=wr)
+    p.q.zero_()
+    p.alibi_slopes.zero_()
+    r = oracle_mod.fvjp(p)
+    for i, s in enumerate(sets):
+        for h in range(2):
+            if not s:
+                assert float(r["lse"][i, h]) == -math.inf
+                assert torch.equal(r["out"][i, h], torch.zeros(D, dtype=torch.float64))
+                assert torch.equal(r["dq"][i, h], torch.zeros(D, dtype=torch.float64))
+            else:
+                expect = p.v[sorted(s), 0].mean(0)
+                torch.testing.assert_close(r["out"][i, h], expect, rtol=1e-13, atol=1e-14)
+                assert abs(float(r["lse"][i, h]) - math.log(len(s))) < 1e-13
+
+
+def test_single_key(oracle_mod):
+    """Lk = 1: out = v0, dq = dk = 0, dv0 = sum over heads and rows of dO."""
+    p = f64_problem([4, 3], [1, 1], Hq=3, seed=6, qk_std=2.0)
+    r = oracle_mod.fvjp(p)
+    for b in range(2):
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        assert torch.equal(r["out"][q0:q1], p.v[b, 0].expand(q1 - q0, 3, D))
+        torch.testing.assert_close(r["dv"][b, 0], p.dout[q0:q1].sum((0, 1)), rtol=1e-13,
+                                   atol=1e-13)
+    assert torch.all(r["dq"] == 0) and torch.all(r["dk"] == 0)
+
+
+# -------------------------------------------------- finite differences (VJP)
+
+def _loss(oracle_mod, p):
+    r = oracle_mod.fvjp(p, nthreads=1)
+    return float((r["out"] * p.dout.double()).sum())
+
+
+@pytest.mark.parametrize("mask", [dict(), dict(causal=True), dict(window_left=1, window_right=2)])
+def test_vjp_matches_central_differences(oracle_mod, mask):
+    """d<dout, out>/dx by central differences of the oracle's own forward, with
+    softcap and ALiBi active, against the analytic dq/dk/dv."""
+    p = f64_problem([3, 5], [4, 2], Hq=3, seed=7, qk_std=3.0, slope_max=0.5, **mask)
+    r = oracle_mod.fvjp(p)
+    gen = torch.Generator().manual_seed(11)
+    h = 1e-6
+    for name, grad in (("q", r["dq"]), ("k", r["dk"]), ("v", r["dv"])):
+        x = getattr(p, name)
+        for _ in range(12):
+            idx = tuple(int(torch.randint(0, n, (1,), generator=gen)) for n in x.shape)
+            old = float(x[idx])
+            x[idx] = old + h
+            lp = _loss(oracle_mod, p)
+            x[idx] = old - h
+            lm = _loss(oracle_mod, p)
+            x[idx] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - float(grad[idx])) < 1e-7 * max(1.0, abs(fd)), (name, idx, fd,
+                                                                          float(grad[idx]))
+
+
+# ------------------------------------------------------------ invariants
+
+def test_row_invariants_on_tiny(oracle_mod):
+    p = W.tiny()
+    r = oracle_mod.fvjp(p, diagnostics=True)
+    torch.testing.assert_close(r["p_rowsum"], torch.ones_like(r["p_rowsum"]), rtol=0,
+                               atol=1e-13)
+    # the gradient at the softmax input sums to zero over each row
+    assert float(r["dz_rowsum"].abs().max()) < 1e-12
+    # D is the row dot product of dO with out
+    torch.testing.assert_close(r["D"], (p.dout.double() * r["out"]).sum(-1), rtol=1e-12,
+                               atol=1e-12)
+    # dv summed over a sequence's keys equals dO summed over its rows and heads
+    for b in range(p.B):
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+        torch.testing.assert_close(r["dv"][k0:k1].sum((0, 1)),
+                                   p.dout[q0:q1].double().sum((0, 1)), rtol=1e-11, atol=1e-10)
+
+
+def test_identical_heads_scale_dk(oracle_mod):
+    """All query heads equal (and equal slopes): out per head equals the
+    single-head out, and dk/dv are Hq times the single-head values."""
+    one = f64_problem([6, 3], [5, 7], Hq=1, seed=9, qk_std=2.0)
+    Hq = 5
+    many = W.custom([6, 3], [5, 7], Hq=Hq, dtype=torch.float64, seed=9)
+    many.q.copy_(one.q.expand(-1, Hq, -1))
+    many.dout.copy_(one.dout.expand(-1, Hq, -1))
+    many.k.copy_(one.k)
+    many.v.copy_(one.v)
+    many.alibi_slopes.copy_(one.alibi_slopes.expand(-1, Hq))
+    r1, rm = oracle_mod.fvjp(one), oracle_mod.fvjp(many)
+    for h in range(Hq):
+        torch.testing.assert_close(rm["out"][:, h], r1["out"][:, 0], rtol=1e-14, atol=1e-15)
+        torch.testing.assert_close(rm["dq"][:, h], r1["dq"][:, 0], rtol=1e-14, atol=1e-15)
+    torch.testing.assert_close(rm["dk"], Hq * r1["dk"], rtol=1e-12, atol=1e-13)
+    torch.testing.assert_close(rm["dv"], Hq * r1["dv"], rtol=1e-12, atol=1e-13)
+
+
+def test_empty_rows_contribute_nothing(oracle_mod):
+    """Causal with Lq > Lk leaves rows 0..2 empty: their lse is -inf, their
+    out and dq are exactly 0, and removing their dO changes no gradient."""
+    p = f64_problem([5], [2], Hq=2, seed=12, causal=True)
+    r = oracle_mod.fvjp(p)
+    assert torch.all(r["lse"][:3] == -math.inf)
+    assert torch.all(r["out"][:3] == 0) and torch.all(r["dq"][:3] == 0)
+    p2 = f64_problem([5], [2], Hq=2, seed=12, causal=True)
+    p2.dout[:3] = 1e3
+    r2 = oracle_mod.fvjp(p2)
+    for name in ("dk", "dv"):
+        assert torch.equal(r[name], r2[name])
+    assert torch.equal(r["dq"][3:], r2["dq"][3:])
+
+
+# ------------------------------------------------------------- structure
+
+def test_sequences_are_independent_and_permutable(oracle_mod):
+    p = W.custom([4, 9, 2], [7, 3, 11], Hq=4, seed=13)
+    r = oracle_mod.fvjp(p)
+    # perturb sequence 1 only: other sequences stay bitwise identical
+    p2 = W.custom([4, 9, 2], [7, 3, 11], Hq=4, seed=13)
+    p2.q[4:13] = -p2.q[4:13]
+    p2.k[7:10] = 2 * p2.k[7:10]
+    r2 = oracle_mod.fvjp(p2)
+    for name, sl in (("out", [slice(0, 4), slice(13, 15)]), ("dq", [slice(0, 4), slice(13, 15)]),
+                     ("dk", [slice(0, 7), slice(10, 21)]), ("dv", [slice(0, 7), slice(10, 21)])):
+        for s in sl:
+            assert torch.equal(r[name][s], r2[name][s]), name
+    # reversing the sequence order (slopes rows too) reverses the outputs
+    order = [2, 1, 0]
+    lq, lk = p.lengths()
+    pr = W.custom([lq[b] for b in order], [lk[b] for b in order], Hq=4, seed=13)
+    qs = [p.q[int(p.cu_q[b]):int(p.cu_q[b + 1])] for b in order]
+    ks = [p.k[int(p.cu_k[b]):int(p.cu_k[b + 1])] for b in order]
+    vs = [p.v[int(p.cu_k[b]):int(p.cu_k[b + 1])] for b in order]
+    ds = [p.dout[int(p.cu_q[b]):int(p.cu_q[b + 1])] for b in order]
+    pr.q.copy_(torch.cat(qs))
+    pr.k.copy_(torch.cat(ks))
+    pr.v.copy_(torch.cat(vs))
+    pr.dout.copy_(torch.cat(ds))
+    pr.alibi_slopes.copy_(p.alibi_slopes[order])
+    rr = oracle_mod.fvjp(pr)
+    for name, cu, cur in (("out", p.cu_q, pr.cu_q), ("dq", p.cu_q, pr.cu_q),
+                          ("lse", p.cu_q, pr.cu_q), ("dk", p.cu_k, pr.cu_k),
+                          ("dv", p.cu_k, pr.cu_k)):
+        for nb, b in enumerate(order):
+            a = r[name][int(cu[b]):int(cu[b + 1])]
+            c = rr[name][int(cur[nb]):int(cur[nb + 1])]
+            assert torch.equal(a, c), name
+
+
+def test_thread_count_does_not_change_bits(oracle_mod):
+    p = W.tiny()
+    r1 = oracle_mod.fvjp(p, nthreads=1)
+    r5 = oracle_mod.fvjp(p, nthreads=5)
+    for name in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.equal(r1[name], r5[name])
+
+
+def test_row_sampler_matches_full_pass(oracle_mod):
+    p = W.custom([5, 17, 33], [40, 9, 64], Hq=8, dtype=torch.bfloat16, step=2, pad=192, seed=14)
+    r = oracle_mod.fvjp(p)
+    tok = torch.tensor([0, 4, 5, 21, 54, 30])
+    head = torch.tensor([0, 7, 3, 1, 6, 2], dtype=torch.int32)
+    s = oracle_mod.rows(p, tok, head)
+    for n in range(len(tok)):
+        t, h = int(tok[n]), int(head[n])
+        assert torch.equal(s["out"][n], r["out"][t, h])
+        assert torch.equal(s["dq"][n], r["dq"][t, h])
+        assert float(s["lse"][n]) == float(r["lse"][t, h])
+
+
+def test_strided_poisoned_views_match_dense(oracle_mod):
+    """Padding and skipped token rows hold NaN; the oracle never reads them."""
+    p = W.custom([5, 3], [6, 4], Hq=3, dtype=torch.float16, step=3, pad=176, seed=15)
+    r = oracle_mod.fvjp(p)
+    dense = W.custom([5, 3], [6, 4], Hq=3, dtype=torch.float16, step=1, pad=160, seed=15)
+    for name in ("q", "k", "v", "dout"):
+        getattr(dense, name).copy_(getattr(p, name))
+    rd = oracle_mod.fvjp(dense)
+    for name in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.equal(r[name], rd[name])
+    assert all(torch.isfinite(r[n]).all() for n in ("out", "dq", "dk", "dv"))
+
+
+@pytest.mark.parametrize("softcap,std", [(3.0, 1e3), (0.0, 60.0)])
+def test_extreme_logits_stay_finite(oracle_mod, softcap, std):
+    p = f64_problem([6, 4], [5, 9], Hq=2, seed=16, qk_std=std)
+    p.softcap = softcap
+    r = oracle_mod.fvjp(p, diagnostics=True)
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.isfinite(r[n]).all(), n
+    torch.testing.assert_close(r["p_rowsum"], torch.ones_like(r["p_rowsum"]), rtol=0, atol=1e-12)
