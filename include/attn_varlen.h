@@ -1,0 +1,129 @@
+/*
+ * attn_varlen.h -- C ABI of the GB300 (sm_103a) ragged GQA attention library.
+ *
+ * One fused call computes, for packed ragged (cu_seqlens) grouped-query
+ * attention with Hq query heads sharing ONE key/value head of dimension 160,
+ * the forward output and log-sum-exp and the complete vector-Jacobian product
+ * (dq, dk, dv) for a given output cotangent dout.
+ *
+ * Operation ("Noncausal Global Extreme-GQA Ragged Attention Full VJP",
+ * sections "Hard Constraints" and "What You Have"):
+ *   for sequence b with Lq = cu_q[b+1]-cu_q[b] queries and Lk = cu_k[b+1]-cu_k[b]
+ *   keys, head h, local query i and key j:
+ *     s   = (scale_multiplier / sqrt(160)) * q[i,h,:] . k[j,:]
+ *     t   = softcap * tanh(s / softcap)        (t = s when softcap <= 0)
+ *     z   = t - alibi_slopes[b,h] * |i + Lk - Lq - j|
+ *     z   = -inf where the causal/window mask forbids (i, j)
+ *     lse = ln sum_j exp(z),  out[i,h,:] = sum_j exp(z - lse) v[j,:]
+ *   and dq, dk, dv are the gradients of <dout, out> with respect to q, k, v;
+ *   dk and dv are summed over every query head that shares the K/V head
+ *   (same page, "Hard Constraints").
+ * The softcap acts on the scaled dot product before ALiBi and masking.  A row
+ * with no admissible key ("ragged flash attention gradient recompute",
+ * section "Root causes addressed", empty rows) gets out = 0, lse = -inf and
+ * contributes nothing to any gradient.
+ *
+ * Mask (the pages accept causal/window arguments without defining them; the
+ * library reads them bottom-right aligned like the ALiBi offset): with
+ * k0 = i + Lk - Lq, key j is admissible iff
+ *   (window_left < 0 or j >= k0 - window_left) and
+ *   (wr < 0 or j <= k0 + wr), where wr = 0 if causal else window_right.
+ *
+ * Layouts.  All strides are in ELEMENTS; the feature axis (160 values) is
+ * contiguous.  q, dout, out, dq are [total_q, Hq, 160] at
+ *   base + token * tok_stride + head * head_stride + feature;
+ * k, v, dk, dv are [total_k, 1, 160] at base + token * tok_stride + feature.
+ * Token and head strides may be non-dense (padded features, token steps).
+ * lse is a dense fp32 [total_q, Hq] array.  cu_q, cu_k are int32 [B+1] with
+ * cu[0] = 0, non-decreasing, cu[B] = total.  alibi_slopes is fp32 [B, Hq]
+ * with the given batch stride and head stride 1, or NULL for no ALiBi.
+ *
+ * Ownership and execution.  Every pointer argument except the scalar
+ * arguments is a DEVICE pointer owned by the caller; the library allocates
+ * nothing and keeps no pointer after the call returns.  The call validates
+ * its arguments on the host, enqueues its kernels on `stream` and returns
+ * without synchronising.  Inputs are read-only; out, dq, dk, dv and lse are
+ * fully overwritten (dk/dv rows of keys that no query attends get 0).  For a
+ * fixed build, device and input, results are bitwise identical from call to
+ * call: no reduction uses atomics.
+ *
+ * Errors.  Host-detectable problems return a negative attn_status before
+ * anything is enqueued.  Problems only visible on the device (inconsistent
+ * cu arrays, a bounded wait that ran out) are recorded in the device status
+ * word: an int32 at `device_status` if non-NULL, else the first 4 bytes of
+ * the workspace.  It is 0 after a clean call; otherwise it holds
+ * ATTN_DEV_* bits and the kernels skip their remaining work.  Read it after
+ * synchronising the stream.
+ */
+#ifndef ATTN_VARLEN_H
+#define ATTN_VARLEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = -1,     /* a null pointer, negative size, bad cu/total pair */
+  ATTN_ERR_UNSUPPORTED = -2, /* head_dim != 160, Hkv != 1, B too large */
+  ATTN_ERR_ALIGNMENT = -3,   /* base not 16-byte aligned, stride not a multiple of 8 */
+  ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+  ATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
+  ATTN_ERR_DEVICE_STATUS = -6,
+  ATTN_ERR_TIMEOUT = -7
+} attn_status;
+
+/* Bits of the device status word. */
+#define ATTN_DEV_BAD_CU 0x1          /* cu arrays not monotone / not ending at total */
+#define ATTN_DEV_TIMEOUT_FWD 0x2     /* a bounded wait in the forward kernel ran out */
+#define ATTN_DEV_TIMEOUT_DKDV 0x4    /* ... in the dk/dv kernel */
+#define ATTN_DEV_TIMEOUT_DQ 0x8      /* ... in the dq kernel */
+
+/* Largest batch (number of sequences) accepted. */
+#define ATTN_MAX_BATCH 16384
+/* The only head dimension implemented. */
+#define ATTN_HEAD_DIM 160
+
+/* Bytes of device workspace a call with these sizes needs (256-byte aligned
+ * base).  Holds the status word, the tile schedule and the fp32 row term
+ * D = rowsum(dout * out) of the backward pass. */
+size_t attn_varlen_fvjp_workspace_size(int B, int Hq, int64_t total_q, int64_t total_k);
+
+/* Forward + full VJP, fused into one call on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream).  `dtype` is the element type of q, k, v,
+ * dout, out, dq, dk, dv.  Hkv must be 1 and head_dim 160.  Every base
+ * pointer of a 16-bit tensor must be 16-byte aligned and every token/head
+ * stride a multiple of 8 elements (the tensors are staged by TMA). */
+attn_status attn_varlen_fvjp_fwd_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+/* A static description of an attn_status value. */
+const char *attn_status_string(attn_status s);
+
+/* Number of kernel launches one attn_varlen_fvjp_fwd_bwd call enqueues for
+ * these sizes (for launch accounting by callers and benchmarks). */
+int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_VARLEN_H */

@@ -1,0 +1,169 @@
+"""ctypes binding of libattn_varlen.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; PyTorch only
+provides device memory and the current stream.  There is no fallback: if the
+library is missing or no CUDA device is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_varlen.so")
+HEAD_DIM = 160
+_lib = None
+
+ATTN_F16, ATTN_BF16 = 0, 1
+DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0x8
+
+EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
+           "attn_varlen_fvjp_launch_count")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"attn_varlen error {code}: {msg}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing "
+                           "(run __graft_entry__.build() or ragged_gqa_attention_varlen_gb300/_build.py)")
+    lib = ctypes.CDLL(path)
+    P, I, L, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.attn_varlen_fvjp_workspace_size.argtypes = [I, I, L, L]
+    lib.attn_varlen_fvjp_workspace_size.restype = ctypes.c_size_t
+    lib.attn_varlen_fvjp_launch_count.argtypes = [I, I, L, L]
+    lib.attn_varlen_fvjp_launch_count.restype = I
+    lib.attn_status_string.argtypes = [I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_varlen_fvjp_fwd_bwd.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fvjp_fwd_bwd.restype = I
+    _lib = lib
+    return lib
+
+
+def workspace_size(B: int, Hq: int, total_q: int, total_k: int) -> int:
+    return int(load().attn_varlen_fvjp_workspace_size(B, Hq, total_q, total_k))
+
+
+def launch_count(B: int, Hq: int, total_q: int, total_k: int) -> int:
+    return int(load().attn_varlen_fvjp_launch_count(B, Hq, total_q, total_k))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_qlike(name, t, dtype, Hq=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.dim() != 3 or t.shape[-1] != HEAD_DIM or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be [tokens, heads, 160] with a contiguous feature axis")
+    if Hq is not None and t.shape[1] != Hq:
+        raise ValueError(f"{name} must have {Hq} heads")
+
+
+def _like(x: torch.Tensor) -> torch.Tensor:
+    """A dense tensor of x's shape and dtype on x's device."""
+    return torch.empty(x.shape, dtype=x.dtype, device=x.device)
+
+
+def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
+                          window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
+                          out=None, dq=None, dk=None, dv=None, lse=None, workspace=None,
+                          stream=None):
+    """Forward + full VJP in one library call.
+
+    q, dout: [T_q, Hq, 160]; k, v: [T_k, 1, 160] CUDA views (fp16 or bf16, any
+    token/head strides that are multiples of 8 elements).  cu_q, cu_k: int32
+    [B+1] on the device.  alibi_slopes: fp32 [B, Hq] or None.  Outputs may be
+    passed in (any strides of the same rules); otherwise dense ones are
+    allocated.  Returns dict(out, dq, dk, dv, lse, workspace).  The call is
+    asynchronous on ``stream`` (default: the current stream)."""
+    lib = load()
+    dtype = q.dtype
+    if dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("q must be fp16 or bf16")
+    Hq = q.shape[1]
+    _check_qlike("q", q, dtype)
+    _check_qlike("dout", dout, dtype, Hq)
+    _check_qlike("k", k, dtype, 1)
+    _check_qlike("v", v, dtype, 1)
+    if dout.shape[0] != q.shape[0] or v.shape[0] != k.shape[0]:
+        raise ValueError("dout must match q and v must match k in length")
+    for name, c in (("cu_q", cu_q), ("cu_k", cu_k)):
+        if not c.is_cuda or c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+    B = cu_q.numel() - 1
+    if cu_k.numel() != B + 1:
+        raise ValueError("cu_q and cu_k must have the same length")
+    if alibi_slopes is not None:
+        if (not alibi_slopes.is_cuda or alibi_slopes.dtype != torch.float32 or
+                alibi_slopes.shape != (B, Hq) or alibi_slopes.stride(1) != 1):
+            raise ValueError("alibi_slopes must be fp32 [B, Hq] on the device, head stride 1")
+    Tq, Tk = q.shape[0], k.shape[0]
+    out = _like(q) if out is None else out
+    dq = _like(q) if dq is None else dq
+    dk = _like(k) if dk is None else dk
+    dv = _like(v) if dv is None else dv
+    for name, t, H in (("out", out, Hq), ("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+        _check_qlike(name, t, dtype, H)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    ws_bytes = workspace_size(B, Hq, Tq, Tk)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    code = lib.attn_varlen_fvjp_fwd_bwd(
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
+        _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+        alibi_slopes.stride(0) if alibi_slopes is not None else 0,
+        int(bool(causal)), int(window_left), int(window_right), float(softcap),
+        float(scale_multiplier),
+        _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
+        _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
+        _ptr(lse), _ptr(workspace), workspace.numel(), None, stream.cuda_stream)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+    return dict(out=out, dq=dq, dk=dk, dv=dv, lse=lse, workspace=workspace)
+
+
+def device_status(workspace: torch.Tensor) -> int:
+    """Synchronise and read the call's device status word (0 = clean)."""
+    return int(workspace[:4].view(torch.int32).item())
+
+
+def attention_varlen_feature_full_vjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
+                                      window_left=-1, window_right=-1, softcap=3.0,
+                                      scale_multiplier=0.75):
+    """The pages' entry point: returns (out, dq, dk, dv) with the inputs' shapes
+    and dtypes ("Noncausal Global Extreme-GQA Ragged Attention Full VJP",
+    "Hard Constraints").  cu arrays of another integer type are converted to
+    int32; inputs are never modified."""
+    if cu_q.dtype != torch.int32:
+        cu_q = cu_q.to(torch.int32)
+    if cu_k.dtype != torch.int32:
+        cu_k = cu_k.to(torch.int32)
+    if k.dim() == 2:
+        k = k.unsqueeze(1)
+    if v.dim() == 2:
+        v = v.unsqueeze(1)
+    r = attention_varlen_fvjp(q, k, v, cu_q.contiguous(), cu_k.contiguous(), alibi_slopes, dout,
+                              causal, window_left, window_right, softcap, scale_multiplier)
+    return r["out"], r["dq"], r["dk"], r["dv"]

@@ -1,0 +1,70 @@
+// attn_internal.h -- parameters and launch entry points shared by the CUDA
+// translation units of the library (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+constexpr int kHeadDim = 160;
+constexpr int kChunk = 64;        // elements per 128-byte swizzled row
+constexpr int kChunks = 3;        // 64-wide chunks covering 160 features
+constexpr int kRowsQ = 128;       // query rows per forward / dq tile
+constexpr int kRowsKV = 64;       // query rows per dk/dv inner step
+constexpr int kKeys = 128;        // keys per tile
+constexpr int kThreads = 128;     // one thread per TMEM lane / tile row
+
+// Query rows of a tile are (token, head) pairs: kG consecutive heads of one
+// head group times 128/kG (or 64/kG) consecutive tokens, row r = token*G + head.
+struct Params {
+  int dtype;  // 0 fp16, 1 bf16
+  int B, Hq, G;
+  int64_t total_q, total_k;
+  // outputs (element strides)
+  void* out;
+  int64_t out_ts, out_hs;
+  void* dq;
+  int64_t dq_ts, dq_hs;
+  void* dk;
+  int64_t dk_ts;
+  void* dv;
+  int64_t dv_ts;
+  // inputs read outside TMA
+  const void* outp;  // = out, read back by the preprocess kernel
+  const void* dout;
+  int64_t do_ts, do_hs;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const float* slopes;  // may be null
+  int64_t slopes_bs;
+  int causal, wl, wr;
+  float softcap;  // <= 0: no cap
+  float sigma;    // scale_multiplier / sqrt(160)
+  float* lse;     // [total_q, Hq]
+  float* Dbuf;    // [total_q, Hq]
+  int32_t* status;
+  int32_t* counters;  // [4]: fwd, dkdv, dq tile counters
+  int32_t* sched;     // schedule arrays, see sched.cu
+};
+
+// Layout of the schedule arrays inside Params::sched (all int32):
+//   [0, B)          fwd/dq sequence order (longest key range first)
+//   [B, 2B+1)       fwd/dq item prefix over that order
+//   [2B+1, 3B+1)    dk/dv sequence order (longest query range first)
+//   [3B+1, 4B+2)    dk/dv item prefix over that order
+inline int sched_words(int B) { return 4 * B + 2; }
+
+cudaError_t launch_sched(const Params& p, cudaStream_t s);
+cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int grid, cudaStream_t s);
+cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
+cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq64, const CUtensorMap& tdo64,
+                        const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t s);
+cudaError_t launch_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                      const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t s);
+cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
+                             cudaStream_t s);
+cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,257 @@
+// host.cu -- the C ABI: argument validation, TMA tensor-map encoding and the
+// launch sequence of one fused forward + VJP call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "../../include/attn_varlen.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (f) return f;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  f = reinterpret_cast<EncodeTiledFn>(ptr);
+  fn.store(f);
+  return f;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace layout: [status + counters | schedule | D].
+struct WsLayout {
+  size_t status, counters, sched, dbuf, total;
+};
+
+WsLayout ws_layout(int B, int Hq, int64_t total_q) {
+  WsLayout w;
+  w.status = 0;
+  w.counters = 16;
+  w.sched = kAlign;
+  w.dbuf = w.sched + align_up(sizeof(int32_t) * static_cast<size_t>(sched_words(B)));
+  w.total = w.dbuf + align_up(sizeof(float) * static_cast<size_t>(total_q) * Hq);
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
+
+// [T, H, 160] view -> 3-D map (feature, head, token) with a box of
+// 64 features x G heads x (rows/G) tokens, 128-byte swizzle.
+bool encode_q(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
+              int64_t hs, int G, int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(G),
+                       static_cast<cuuint32_t>(rows / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [T, 1, 160] view -> 2-D map (feature, token), box 64 x 128 keys.
+bool encode_kv(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t ts) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ts) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kKeys)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int head_group(int Hq) {
+  int g = 16;
+  while (Hq % g) g >>= 1;
+  return g;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" size_t attn_varlen_fvjp_workspace_size(int B, int Hq, int64_t total_q,
+                                                  int64_t total_k) {
+  (void)total_k;
+  if (B < 0 || Hq <= 0 || total_q < 0) return 0;
+  return ws_layout(B, Hq, total_q).total;
+}
+
+extern "C" int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k) {
+  (void)B;
+  (void)Hq;
+  if (total_q == 0 && total_k == 0) return 0;
+  if (total_q == 0) return 2;  // dk, dv zero fills
+  if (total_k == 0) return 3;  // out, dq zero fills, lse fill
+  return 5;                    // schedule, forward, preprocess, dk/dv, dq
+}
+
+extern "C" const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_ALIGNMENT: return "pointer or stride not aligned for TMA (16 B / 8 elements)";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_DEVICE_STATUS: return "device reported an error in the status word";
+    case ATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
+  }
+  return "unknown status";
+}
+
+extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, void* out, int64_t out_ts, int64_t out_hs, void* dq, int64_t dq_ts,
+    int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts,
+    int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
+    void* stream_ptr) {
+  (void)k_hs;
+  (void)v_hs;
+  (void)dk_hs;
+  (void)dv_hs;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  // ---- host-side validation (nothing is enqueued on failure)
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
+  if (head_dim != kHeadDim || Hkv != 1) return ATTN_ERR_UNSUPPORTED;
+  if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
+  if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 && (total_q != 0 || total_k != 0)) return ATTN_ERR_INVALID;
+  if (!(softcap == softcap) || !(scale_multiplier == scale_multiplier)) return ATTN_ERR_INVALID;
+  if (B > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID;
+  if (alibi_slopes && slopes_batch_stride < Hq && B > 1) return ATTN_ERR_INVALID;
+  const bool has_q = total_q > 0, has_k = total_k > 0;
+  if (has_q && (!q || !dout || !out || !dq || !lse)) return ATTN_ERR_INVALID;
+  if (has_k && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID;
+  if (has_q) {
+    for (const void* ptr : {q, dout, static_cast<const void*>(out), static_cast<const void*>(dq)})
+      if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+    for (int64_t s : {q_ts, q_hs, do_ts, do_hs, out_ts, out_hs, dq_ts, dq_hs})
+      if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+  }
+  if (has_k) {
+    for (const void* ptr : {k, v, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+      if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+    for (int64_t s : {k_ts, v_ts, dk_ts, dv_ts})
+      if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+  }
+  const WsLayout ws = ws_layout(B, Hq, total_q);
+  if (!workspace || workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  p.dtype = dtype;
+  p.B = B;
+  p.Hq = Hq;
+  p.G = head_group(Hq);
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.out = out;
+  p.out_ts = out_ts;
+  p.out_hs = out_hs;
+  p.dq = dq;
+  p.dq_ts = dq_ts;
+  p.dq_hs = dq_hs;
+  p.dk = dk;
+  p.dk_ts = dk_ts;
+  p.dv = dv;
+  p.dv_ts = dv_ts;
+  p.outp = out;
+  p.dout = dout;
+  p.do_ts = do_ts;
+  p.do_hs = do_hs;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.slopes = alibi_slopes;
+  p.slopes_bs = slopes_batch_stride;
+  p.causal = causal ? 1 : 0;
+  p.wl = window_left;
+  p.wr = window_right;
+  p.softcap = softcap;
+  p.sigma = static_cast<float>(static_cast<double>(scale_multiplier) / 12.649110640673518);
+  p.lse = lse;
+  p.Dbuf = reinterpret_cast<float*>(wsb + ws.dbuf);
+  p.status = device_status ? device_status : reinterpret_cast<int32_t*>(wsb + ws.status);
+  p.counters = reinterpret_cast<int32_t*>(wsb + ws.counters);
+  p.sched = reinterpret_cast<int32_t*>(wsb + ws.sched);
+
+  // ---- degenerate sizes: no query or no key at all
+  if (!has_q || !has_k) {
+    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (has_k) {  // no queries: dk = dv = 0
+      e = launch_zero_fill(dk, total_k, 1, dk_ts, 8, stream);
+      if (e == cudaSuccess) e = launch_zero_fill(dv, total_k, 1, dv_ts, 8, stream);
+    }
+    if (has_q) {  // no keys: every row is empty
+      e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, stream);
+      if (e == cudaSuccess) e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, stream);
+      if (e == cudaSuccess) e = launch_fill_f32(lse, total_q * Hq, -INFINITY, stream);
+    }
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+
+  // ---- TMA tensor maps
+  if (!encode_fn()) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tdo, tq64, tdo64, tk, tv;
+  if (!encode_q(&tq, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
+      !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+      !encode_q(&tq64, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsKV) ||
+      !encode_q(&tdo64, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsKV) ||
+      !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts))
+    return ATTN_ERR_ALIGNMENT;
+
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  // Upper bounds of the tile counts (the device schedule has the exact ones).
+  const int64_t rows_tok = kRowsQ / p.G;
+  const int64_t qtiles_max = (total_q / rows_tok + B) * (Hq / p.G);
+  const int64_t ktiles_max = total_k / kKeys + B;
+  const int grid_q = static_cast<int>(qtiles_max < sms ? qtiles_max : sms);
+  const int grid_k = static_cast<int>(ktiles_max < sms ? ktiles_max : sms);
+
+  if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_fwd(p, tq, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_dkdv(p, tq64, tdo64, tk, tv, grid_k, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_dq(p, tq, tdo, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}

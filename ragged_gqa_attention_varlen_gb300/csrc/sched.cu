@@ -1,0 +1,188 @@
+// sched.cu -- the ragged tile scheduler, the D = rowsum(dO * O) preprocess
+// of the backward pass, and fill kernels for degenerate sizes.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/attn_varlen.h"
+#include "attn_internal.h"
+#include "sched.cuh"
+
+namespace attn {
+
+// One block.  Validates cu_q/cu_k, resets the status word and the tile
+// counters, and builds both tile orders (see attn_internal.h for the array
+// layout).  Sorting is by counting rank (descending work, ties by index), so
+// the order is a deterministic function of the lengths.
+__global__ void __launch_bounds__(1024) sched_kernel(Params p) {
+  const int B = p.B;
+  const int tid = threadIdx.x;
+  __shared__ int bad;
+  if (tid == 0) {
+    bad = (p.cu_q[0] != 0 || p.cu_k[0] != 0 || p.cu_q[B] != p.total_q ||
+           p.cu_k[B] != p.total_k);
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += blockDim.x) {
+    if (p.cu_q[b + 1] < p.cu_q[b] || p.cu_k[b + 1] < p.cu_k[b]) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  int32_t* ord_f = p.sched;
+  int32_t* pre_f = p.sched + B;
+  int32_t* ord_b = p.sched + 2 * B + 1;
+  int32_t* pre_b = p.sched + 3 * B + 1;
+  if (bad) {
+    // No tiles: every later kernel finds nothing to do.
+    for (int b = tid; b <= B; b += blockDim.x) {
+      pre_f[b] = 0;
+      pre_b[b] = 0;
+      if (b < B) {
+        ord_f[b] = 0;
+        ord_b[b] = 0;
+      }
+    }
+    if (tid == 0) *p.status = ATTN_DEV_BAD_CU;
+    return;
+  }
+  if (tid == 0) {
+    *p.status = 0;
+    for (int i = 0; i < 4; ++i) p.counters[i] = 0;
+  }
+  for (int b = tid; b < B; b += blockDim.x) {
+    int lk = p.cu_k[b + 1] - p.cu_k[b];
+    int lq = p.cu_q[b + 1] - p.cu_q[b];
+    int rf = 0, rb = 0;
+    for (int c = 0; c < B; ++c) {
+      int lkc = p.cu_k[c + 1] - p.cu_k[c];
+      int lqc = p.cu_q[c + 1] - p.cu_q[c];
+      rf += (lkc > lk) || (lkc == lk && c < b);
+      rb += (lqc > lq) || (lqc == lq && c < b);
+    }
+    ord_f[rf] = b;
+    ord_b[rb] = b;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int rows_tok = kRowsQ / p.G;
+    const int ngroups = p.Hq / p.G;
+    int acc_f = 0, acc_b = 0;
+    for (int r = 0; r < B; ++r) {
+      pre_f[r] = acc_f;
+      pre_b[r] = acc_b;
+      int bf = ord_f[r], bb = ord_b[r];
+      int lq = p.cu_q[bf + 1] - p.cu_q[bf];
+      int lk = p.cu_k[bb + 1] - p.cu_k[bb];
+      acc_f += ((lq + rows_tok - 1) / rows_tok) * ngroups;
+      acc_b += (lk + kKeys - 1) / kKeys;
+    }
+    pre_f[B] = acc_f;
+    pre_b[B] = acc_b;
+  }
+}
+
+cudaError_t launch_sched(const Params& p, cudaStream_t s) {
+  sched_kernel<<<1, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// D[t, h] = sum_f dO[t,h,f] * O[t,h,f] in fp32 over the stored (rounded)
+// output.  One warp per (token, head) row; lanes 0..19 each take 8 features.
+template <typename T>
+__device__ __forceinline__ float dot8(uint4 a, uint4 b);
+
+template <>
+__device__ __forceinline__ float dot8<__half>(uint4 a, uint4 b) {
+  const __half2* x = reinterpret_cast<const __half2*>(&a);
+  const __half2* y = reinterpret_cast<const __half2*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 fx = __half22float2(x[i]), fy = __half22float2(y[i]);
+    acc = fmaf(fx.x, fy.x, acc);
+    acc = fmaf(fx.y, fy.y, acc);
+  }
+  return acc;
+}
+
+template <>
+__device__ __forceinline__ float dot8<__nv_bfloat16>(uint4 a, uint4 b) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 fx = __bfloat1622float2(x[i]), fy = __bfloat1622float2(y[i]);
+    acc = fmaf(fx.x, fy.x, acc);
+    acc = fmaf(fx.y, fy.y, acc);
+  }
+  return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) preprocess_kernel(Params p) {
+  if (*p.status != 0) return;
+  const int64_t rows = p.total_q * p.Hq;
+  const int lane = threadIdx.x & 31;
+  int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride_rows = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const T* o = static_cast<const T*>(p.outp);
+  const T* d = static_cast<const T*>(p.dout);
+  for (; row < rows; row += stride_rows) {
+    const int64_t t = row / p.Hq;
+    const int h = static_cast<int>(row - t * p.Hq);
+    float acc = 0.f;
+    if (lane < kHeadDim / 8) {
+      uint4 a = *reinterpret_cast<const uint4*>(o + t * p.out_ts + h * p.out_hs + lane * 8);
+      uint4 b = *reinterpret_cast<const uint4*>(d + t * p.do_ts + h * p.do_hs + lane * 8);
+      acc = dot8<T>(a, b);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) p.Dbuf[row] = acc;
+  }
+}
+
+cudaError_t launch_preprocess(const Params& p, cudaStream_t s) {
+  const int64_t rows = p.total_q * p.Hq;
+  if (rows == 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  if (p.dtype == 1)
+    preprocess_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+  else
+    preprocess_kernel<__half><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Zero a strided [T, H, 160] 16-bit tensor, 16 bytes per thread.
+__global__ void zero_fill_kernel(uint16_t* base, int64_t T, int H, int64_t ts, int64_t hs) {
+  const int64_t units = T * H * (kHeadDim / 8);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t row = u / (kHeadDim / 8);
+    int c = static_cast<int>(u - row * (kHeadDim / 8));
+    int64_t t = row / H;
+    int h = static_cast<int>(row - t * H);
+    *reinterpret_cast<uint4*>(base + t * ts + h * hs + c * 8) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
+                             cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  zero_fill_kernel<<<152 * 8, 256, 0, s>>>(static_cast<uint16_t*>(base), T, H, ts, hs);
+  return cudaGetLastError();
+}
+
+__global__ void fill_f32_kernel(float* base, int64_t n, float value) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    base[i] = value;
+}
+
+cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  fill_f32_kernel<<<152 * 4, 256, 0, s>>>(base, n, value);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,76 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+declared in include/attn_varlen.h, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ragged_gqa_attention_varlen_gb300 import _build, binding
+
+    _build.build()
+    return binding.load()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "attn_varlen_fvjp_fwd_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(-3).decode().startswith("pointer or stride")
+
+
+def test_workspace_size_grows_with_rows(lib):
+    a = lib.attn_varlen_fvjp_workspace_size(4, 16, 100, 50)
+    b = lib.attn_varlen_fvjp_workspace_size(4, 16, 1000, 50)
+    assert b - a >= 900 * 16 * 4
+    assert a % 256 == 0 and b % 256 == 0
+
+
+def _call(lib, **over):
+    """A call whose arguments pass or fail host validation; the fake device
+    pointers are never dereferenced because every case fails validation."""
+    fake = 0x10000  # 16-byte aligned, never touched
+    a = dict(dtype=0, B=2, Hq=16, Hkv=1, hd=160, tq=10, tk=12,
+             q=fake, qts=16 * 160, qhs=160, k=fake, kts=160, khs=160, v=fake, vts=160, vhs=160,
+             do=fake, dts=16 * 160, dhs=160, cuq=fake, cuk=fake, sl=fake, slb=16,
+             causal=0, wl=-1, wr=-1, cap=3.0, sm=0.75,
+             out=fake, ots=16 * 160, ohs=160, dq=fake, dqts=16 * 160, dqhs=160,
+             dk=fake, dkts=160, dkhs=160, dv=fake, dvts=160, dvhs=160,
+             lse=fake, ws=fake, wsb=0, st=None, stream=None)
+    a.update(over)
+    return lib.attn_varlen_fvjp_fwd_bwd(*a.values())
+
+
+def test_host_validation_codes(lib):
+    assert _call(lib, dtype=7) == -1
+    assert _call(lib, hd=128) == -2
+    assert _call(lib, Hkv=2) == -2
+    assert _call(lib, B=20000) == -2
+    assert _call(lib, q=0x10008) == -3          # base not 16-byte aligned
+    assert _call(lib, qhs=164) == -3            # stride not a multiple of 8 elements
+    assert _call(lib, ws=0) == -4               # no workspace
+    assert _call(lib, wsb=16) == -4             # workspace too small
+    assert _call(lib, B=0) == -1                # B = 0 with tokens
+    assert _call(lib, q=None) == -1

@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances: relative Frobenius <= 1e-2 (fp16) / 2e-2 (bf16) and max-abs <=
+5e-2 max|ref| on out/dq/dk/dv; lse within 1e-3 absolute, -inf rows exact.
+Repeated calls must be bitwise identical; inputs must not change.
+"""
+import math
+
+import pytest
+import torch
+
+from helpers import check_all, check_lse, check_tensor, nan_like_strided, row_mask, view_bytes_hash
+from ragged_gqa_attention_varlen_gb300 import binding as BND
+from ragged_gqa_attention_varlen_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from ragged_gqa_attention_varlen_gb300 import _build
+
+    _build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return BND.load()
+
+
+def run(p, **kw):
+    r = BND.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                  p.causal, p.window_left, p.window_right, p.softcap,
+                                  p.scale_multiplier, **kw)
+    torch.cuda.synchronize()
+    st = BND.device_status(r["workspace"])
+    assert st == 0, f"device status {st:#x}"
+    return r
+
+
+def bits_equal(a, b):
+    it = torch.int16 if a.element_size() == 2 else torch.int32
+    return bool((a.contiguous().view(it) == b.contiguous().view(it)).all())
+
+
+def parity(p_cpu, oracle_mod, seq_sel=None):
+    p = p_cpu.to("cuda")
+    res = run(p)
+    ref = oracle_mod.fvjp(p_cpu, seq_sel=seq_sel)
+    if seq_sel is None:
+        return check_all(res, ref, p_cpu.dtype), res
+    mq, mk = row_mask(p_cpu, seq_sel)
+    return check_all(res, ref, p_cpu.dtype, rows=mq, keys=mk), res
+
+
+# ---------------------------------------------------------------- tiny config
+
+TINY_MASKS = [dict(), dict(causal=True), dict(window_left=16, window_right=16),
+              dict(causal=True, window_left=16, window_right=16)]
+
+
+@pytest.mark.parametrize("mask", TINY_MASKS, ids=["global", "causal", "win16", "causal_win16"])
+def test_tiny_parity(oracle_mod, mask):
+    parity(W.tiny(**mask), oracle_mod)
+
+
+def test_tiny_bitwise_repeat_and_inputs_unchanged():
+    p = W.tiny().to("cuda")
+    hashes = [view_bytes_hash(getattr(p, n)) for n in ("q", "k", "v", "dout")]
+    r1 = run(p)
+    snap = {n: r1[n].clone() for n in ("out", "dq", "dk", "dv", "lse")}
+    r2 = run(p)
+    for n, x in snap.items():
+        assert bits_equal(x, r2[n]), n
+    assert hashes == [view_bytes_hash(getattr(p, n)) for n in ("q", "k", "v", "dout")]
+
+
+def test_strided_outputs_written_exactly_and_match_dense():
+    """Outputs given as NaN-filled padded views: every valid element is written,
+    padding stays NaN, values equal the dense-output call bit for bit."""
+    p = W.q_short(length_scale=0.125).to("cuda")
+    dense = run(p)
+    outs = dict(out=nan_like_strided(p.q), dq=nan_like_strided(p.dout), dk=nan_like_strided(p.k),
+                dv=nan_like_strided(p.v))
+    strided = run(p, **outs)
+    for n in ("out", "dq", "dk", "dv"):
+        assert torch.equal(strided[n].contiguous(), dense[n]), n
+        base = strided[n].untyped_storage()
+        raw = torch.empty(0, dtype=strided[n].dtype, device="cuda").set_(base)
+        n_nan = int(torch.isnan(raw).sum())
+        assert n_nan == raw.numel() - strided[n].numel(), n
+
+
+# ------------------------------------------------- scaled replicas (full oracle)
+
+REPLICAS = [
+    ("q_short_k_long", dict(length_scale=0.25), None),
+    ("k_short_q_long", dict(length_scale=0.125), None),
+    ("mixed_h64", dict(length_scale=1 / 16), None),
+    ("mixed_h80", dict(length_scale=1 / 16), None),
+    ("long_balanced", dict(length_scale=1 / 32), [0, 7, 13, 23]),
+]
+
+
+@pytest.mark.parametrize("name,kw,sel", REPLICAS, ids=[r[0] for r in REPLICAS])
+def test_replica_parity(oracle_mod, name, kw, sel):
+    p = W.WORKLOADS[name](**kw)
+    parity(p, oracle_mod, seq_sel=sel)
+
+
+# ----------------------------------------------------------------- edge cases
+
+EDGE = [
+    dict(lq=[0, 5, 3, 0, 9], lk=[4, 0, 6, 0, 130], Hq=16),          # empty sequences
+    dict(lq=[1], lk=[1], Hq=48),                                     # single token each
+    dict(lq=[1000], lk=[1000], Hq=16, dtype=torch.bfloat16),         # many tiles, ragged tail
+    dict(lq=[16, 8], lk=[128, 256], Hq=16),                          # exact tile multiples
+    dict(lq=[7, 33, 2], lk=[300, 5, 129], Hq=1),                     # one head (G = 1)
+    dict(lq=[7, 33, 2], lk=[300, 5, 129], Hq=3),                     # odd head count
+    dict(lq=[17, 9], lk=[150, 70], Hq=80, dtype=torch.bfloat16, step=2, pad=192),
+    dict(lq=[40, 3], lk=[20, 200], Hq=16, causal=True),              # empty rows (Lq > Lk)
+    dict(lq=[40, 300], lk=[200, 140], Hq=16, window_left=5, window_right=60),
+    dict(lq=[40, 300], lk=[200, 140], Hq=16, causal=True, window_left=70),
+    dict(lq=[30, 12], lk=[200, 40], Hq=16, qk_std=100.0),           # saturated softcap
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[f"edge{i}" for i in range(len(EDGE))])
+def test_edge_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    p = W.custom(lq, lk, Hq, **case)
+    parity(p, oracle_mod)
+
+
+def test_no_cap_large_logits(oracle_mod):
+    p = W.custom([50, 20], [300, 90], 16, qk_std=6.0)
+    p.softcap = 0.0
+    parity(p, oracle_mod)
+
+
+def test_no_keys_at_all():
+    p = W.custom([5, 3], [0, 0], 16).to("cuda")
+    r = run(p)
+    assert torch.all(r["out"] == 0) and torch.all(r["dq"] == 0)
+    assert torch.all(r["lse"] == -math.inf)
+
+
+def test_no_queries_at_all():
+    p = W.custom([0, 0], [7, 3], 16).to("cuda")
+    r = run(p)
+    assert torch.all(r["dk"] == 0) and torch.all(r["dv"] == 0)
+
+
+def test_bad_cu_sets_device_status():
+    """A non-monotone cu_q is caught on the device: the status word gets the
+    bad-cu bit and no kernel computes anything."""
+    p = W.custom([5, 6], [7, 8], 16).to("cuda")
+    p.cu_q = torch.tensor([0, 9, 11], dtype=torch.int32, device="cuda")  # total 11, ok
+    p.cu_q[1] = 12  # now cu_q[1] > cu_q[2]
+    r = BND.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout)
+    torch.cuda.synchronize()
+    assert BND.device_status(r["workspace"]) == BND.DEV_BAD_CU
+
+
+def test_host_rejects_misaligned_stride():
+    p = W.custom([5], [7], 16).to("cuda")
+    base = torch.zeros((5, 16, 164), dtype=p.q.dtype, device="cuda")
+    q = base[:, :, :160]
+    q.copy_(p.q)
+    with pytest.raises(BND.AttnError) as e:
+        BND.attention_varlen_fvjp(q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout)
+    assert e.value.code == -3
+
+
+# ------------------------------------------- full-size configs, sampled checks
+
+FULL = ["q_short_k_long", "k_short_q_long", "mixed_h64", "mixed_h80", "long_balanced"]
+
+
+def _sample_rows(p, gen, n=48):
+    """Packed (token, head) rows: first and last token of random sequences and
+    random interior tokens, random heads."""
+    toks, heads = [], []
+    lq, _ = p.lengths()
+    nonempty = [b for b in range(p.B) if lq[b] > 0]
+    for s in range(n):
+        b = nonempty[int(torch.randint(0, len(nonempty), (1,), generator=gen))]
+        q0 = int(p.cu_q[b])
+        off = [0, lq[b] - 1, int(torch.randint(0, lq[b], (1,), generator=gen))][s % 3]
+        toks.append(q0 + off)
+        heads.append(int(torch.randint(0, p.Hq, (1,), generator=gen)))
+    return torch.tensor(toks), torch.tensor(heads, dtype=torch.int32)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(oracle_mod, name):
+    p = W.WORKLOADS[name](device="cuda")
+    r1 = run(p)
+    snap = {n: r1[n].clone() for n in ("out", "dq", "dk", "dv", "lse")}
+    r2 = run(p)
+    for n, x in snap.items():  # bitwise repeat at full size
+        assert bits_equal(x, r2[n]), n
+    gen = torch.Generator().manual_seed(99)
+    tok, head = _sample_rows(p, gen)
+    # per-sequence CPU copies keep the oracle's input small
+    lq, lk = p.lengths()
+    got_out, got_dq, got_lse, ref_out, ref_dq, ref_lse = [], [], [], [], [], []
+    for b in sorted(set(int(torch.searchsorted(p.cu_q.cpu(), t, right=True)) - 1 for t in tok)):
+        sel = [n for n in range(len(tok)) if int(p.cu_q[b]) <= int(tok[n]) < int(p.cu_q[b + 1])]
+        if not sel:
+            continue
+        sp = p.sequence(b)
+        q0 = int(p.cu_q[b])
+        rr = oracle_mod.rows(sp, tok[sel] - q0, head[sel])
+        for m, n in enumerate(sel):
+            t, h = int(tok[n]), int(head[n])
+            got_out.append(r1["out"][t, h].float().cpu())
+            got_dq.append(r1["dq"][t, h].float().cpu())
+            got_lse.append(r1["lse"][t, h].cpu())
+            ref_out.append(rr["out"][m])
+            ref_dq.append(rr["dq"][m])
+            ref_lse.append(rr["lse"][m])
+    check_tensor("out(sampled)", torch.stack(got_out), torch.stack(ref_out), p.dtype)
+    check_tensor("dq(sampled)", torch.stack(got_dq), torch.stack(ref_dq), p.dtype)
+    check_lse(torch.stack(got_lse), torch.stack(ref_lse))
+    # dk/dv in full on the cheapest sequences (by Lq*Lk), except for the
+    # balanced long case where every sequence is too large for the oracle
+    if name != "long_balanced":
+        work = sorted(range(p.B), key=lambda b: lq[b] * lk[b])
+        for b in [w for w in work if lq[w] > 0 and lk[w] > 0][:2]:
+            sp = p.sequence(b)
+            ref = oracle_mod.fvjp(sp)
+            k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+            check_tensor(f"dk(seq {b})", r1["dk"][k0:k1].cpu(), ref["dk"], p.dtype)
+            check_tensor(f"dv(seq {b})", r1["dv"][k0:k1].cpu(), ref["dv"], p.dtype)
+    # a property at any size: per sequence, sum_j dv_j = sum_{h,i} dO_i
+    for b in range(p.B):
+        if lq[b] == 0 or lk[b] == 0:
+            continue
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+        lhs = r1["dv"][k0:k1].double().sum((0, 1)).cpu()
+        rhs = p.dout[q0:q1].double().sum((0, 1)).cpu()
+        err = float((lhs - rhs).norm() / max(float(rhs.norm()), 1e-30))
+        assert err < 2e-2, (b, err)
