@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark: fused forward + full VJP of ragged GQA attention on GB300.
+
+One step = one library call (schedule, forward, preprocess, dk/dv, dq) over
+the long balanced workload: 24 sequences with Lq = Lk ~ U[6144, 12288],
+Hq = 96 query heads sharing one K/V head, head_dim 160, bf16, token-strided
+(step 2) views, ALiBi slopes 2^(-8h/96).  Throughput counts 4 Lq Lk d
+forward and 10 Lq Lk d backward flops per head (TFLOP/s); latency is
+ms_per_step.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ragged_gqa_attention_varlen_gb300 import workloads  # noqa: E402
+
+METRIC = "fwd+full-VJP TFLOP/s & latency (d=160, Hq 48-96, Hkv=1), % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+HEAD_DIM = 160
+
+
+def counted_flops(p) -> float:
+    """4 Lq Lk d (forward) + 10 Lq Lk d (backward) per query head."""
+    return 14.0 * HEAD_DIM * p.Hq * p.sum_lq_lk()
+
+
+def kernel_flops(p) -> dict:
+    """Algorithmic flops each kernel contributes to the counted total: the
+    forward's two matmuls (4d), dk/dv's four (S^T, dP^T, dV, dK: 8d) and dq's
+    dQ = dS K (2d); dq's recompute of S and dP is not counted."""
+    u = HEAD_DIM * p.Hq * p.sum_lq_lk()
+    return {"forward": 4 * u, "dkdv": 8 * u, "dq": 2 * u, "schedule": 0.0, "preprocess": 0.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+        except Exception:
+            bus = None
+        self.target = bus
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.target:
+                cmd += ["-i", self.target]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (timing only; no data path)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_rank: float, seconds_per_rank: float, steps: int, world: int):
+    """Whole-job throughput: all ranks' counted flops over the slowest rank's
+    time.  Returns (TFLOP/s, ms per step)."""
+    t = max_over_ranks(seconds_per_rank, world)
+    return flops_per_rank * steps * world / t / 1e12, t / steps * 1e3
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(seconds: float, seed: int = 5):
+    """Time the fp64 oracle on whole sequences of the long balanced workload
+    scaled to 1/8 of its lengths (same structure, heads, slopes), one sequence
+    after another until ``seconds`` pass.  Returns (TFLOP/s, threads, text)."""
+    import oracle
+
+    oracle.build()
+    p = workloads.long_balanced(seed=seed, length_scale=0.125)
+    lq, lk = p.lengths()
+    flops, t0, done, nthreads = 0.0, time.perf_counter(), 0, 0
+    for b in range(p.B):
+        r = oracle.fvjp(p, seq_sel=[b])
+        nthreads = r["threads"]
+        flops += 14.0 * HEAD_DIM * p.Hq * lq[b] * lk[b]
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    text = (f"oracle fvjp (fp64, all outputs) on {done} whole sequence(s) of the long balanced "
+            f"workload at 1/8 length (Lq=Lk={lq[0]}..), Hq={p.Hq}; {dt:.1f} s")
+    return flops / dt / 1e12, nthreads, text, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    p = workloads.long_balanced(seed=5, length_scale=0.1)
+    lq, lk = p.lengths()
+    b = min(range(p.B), key=lambda i: lq[i] * lk[i])  # shortest sequence: bounded step
+    flops = 14.0 * HEAD_DIM * p.Hq * lq[b] * lk[b]
+    for _ in range(args.warmup):
+        oracle.fvjp(p, seq_sel=[b])
+    times = []
+    nthreads = 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = oracle.fvjp(p, seq_sel=[b])
+        times.append(time.perf_counter() - t0)
+        nthreads = r["threads"]
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    sample = (f"one step = oracle fvjp (fp64) of sequence {b} of the long balanced workload at "
+              f"1/10 length (Lq=Lk={lq[b]}, Hq={p.Hq})")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "long_balanced", "sample": "1/10 length, one sequence"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def pinned_copy(x: torch.Tensor) -> torch.Tensor:
+    """Pinned host copy of a device tensor's whole storage (its padded base)."""
+    st = x.untyped_storage()
+    n = st.nbytes()
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h.copy_(torch.empty(0, dtype=torch.uint8, device=x.device).set_(st))
+    return h
+
+
+def storage_bytes_view(x: torch.Tensor) -> torch.Tensor:
+    return torch.empty(0, dtype=torch.uint8, device=x.device).set_(x.untyped_storage())
+
+
+def run_gpu(args, world, rank, local):
+    from ragged_gqa_attention_varlen_gb300 import _build, binding
+
+    _build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False)
+    flops = counted_flops(p)
+    kflops = kernel_flops(p)
+    out = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
+    dq = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
+    dk = torch.empty(p.k.shape, dtype=p.k.dtype, device=dev)
+    dv = torch.empty(p.v.shape, dtype=p.v.dtype, device=dev)
+    lse = torch.empty((p.total_q, p.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.workspace_size(p.B, p.Hq, p.total_q, p.total_k), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(out=out, dq=dq, dk=dk, dv=dv, lse=lse, workspace=ws, stream=stream)
+
+    def call():
+        binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                      False, -1, -1, p.softcap, p.scale_multiplier, **kw)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    status = binding.device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x}")
+
+    # ---- device-resident timing, per-kernel events on the launching stream
+    nk = len(binding.KERNELS)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in ev:  # torch creates the CUDA event at its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(args.steps):
+        binding.record_events_next_call(ev[s])
+        call()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_s = start.elapsed_time(end) / 1e3
+    status = binding.device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x}")
+    per_kernel = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) /
+                  args.steps for i, name in enumerate(binding.KERNELS)}
+    value, ms = aggregate(flops, total_s, args.steps, world)
+    launches = binding.launch_count(p.B, p.Hq, p.total_q, p.total_k) * args.steps
+
+    # ---- roofline of the dominant kernel
+    pk, kind = peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_kind": f"{kind} bf16 sustained"}
+    whole_frac = value / world / pk["bf16_tflops"]
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, p, kw, flops, stream, world)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, generated on device)",
+            "config": {"workload": "long_balanced", "B": p.B, "Hq": p.Hq, "Hkv": 1,
+                       "head_dim": HEAD_DIM, "token_step": 2, "total_q": p.total_q,
+                       "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
+                       "counted_tflop_per_step": flops / 1e12,
+                       "l2": "inputs larger than L2 (q view alone is "
+                             f"{p.q.numel() * 2 / 1e9:.1f} GB)"},
+            "latency_ms": ms, "frac_of_bf16_peak": whole_frac,
+            "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
+            "clocks": clk, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, cores, sample, _ = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, p, kw, flops, stream, world):
+    """Same call with the inputs in pinned host memory: every step copies the
+    inputs' storage host->device, runs the call, and copies every result
+    device->host, all inside the timed region."""
+    from ragged_gqa_attention_varlen_gb300 import binding
+
+    ins = [p.q, p.k, p.v, p.dout, p.cu_q, p.cu_k, p.alibi_slopes]
+    host_in = [pinned_copy(x) for x in ins]
+    dev_in = [storage_bytes_view(x) for x in ins]
+    outs = [kw["out"], kw["dq"], kw["dk"], kw["dv"], kw["lse"]]
+    host_out = [torch.empty(x.numel() * x.element_size(), dtype=torch.uint8, pin_memory=True)
+                for x in outs]
+    dev_out = [storage_bytes_view(x) for x in outs]
+    h2d = sum(h.numel() for h in host_in)
+    d2h = sum(h.numel() for h in host_out)
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                      False, -1, -1, p.softcap, p.scale_multiplier, **kw)
+        for d, h in zip(dev_out, host_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    value, ms = aggregate(flops, start.elapsed_time(end) / 1e3, args.steps, world)
+    return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "gpu_launches": binding.launch_count(
+                p.B, p.Hq, p.total_q, p.total_k) * args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    run_gpu(args, world, rank, local)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -122,6 +122,15 @@ const char *attn_status_string(attn_status s);
  * these sizes (for launch accounting by callers and benchmarks). */
 int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k);
 
+/* Timing hook: the next attn_varlen_fvjp_fwd_bwd call made by THIS host
+ * thread records events[0] before its first kernel and events[i] after its
+ * i-th kernel (i = 1..n-1; the five kernels are schedule, forward,
+ * preprocess, dk/dv, dq), then forgets the events.  `events` holds
+ * cudaEvent_t handles owned by the caller; n must be 6 (or 0 to cancel).
+ * Returns ATTN_ERR_INVALID for any other n.  Used by benchmarks to time each
+ * kernel on the launching stream. */
+attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,8 @@ ATTN_F16, ATTN_BF16 = 0, 1
 DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0x8
 
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
-           "attn_varlen_fvjp_launch_count")
+           "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events")
+KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
 
 class AttnError(RuntimeError):
@@ -49,6 +50,8 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
         [P, P, ctypes.c_size_t, P, P])
     lib.attn_varlen_fvjp_fwd_bwd.restype = I
+    lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
+    lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
     return lib
 
@@ -59,6 +62,18 @@ def workspace_size(B: int, Hq: int, total_q: int, total_k: int) -> int:
 
 def launch_count(B: int, Hq: int, total_q: int, total_k: int) -> int:
     return int(load().attn_varlen_fvjp_launch_count(B, Hq, total_q, total_k))
+
+
+def record_events_next_call(events):
+    """Arm the library's one-shot timing hook for the next call on this host
+    thread: ``events`` is a list of 6 torch.cuda.Event (created with timing)."""
+    lib = load()
+    if len(events) != 6 or any(e.cuda_event == 0 for e in events):
+        raise ValueError("need 6 created events (torch creates an event at its first record())")
+    arr = (ctypes.c_void_p * 6)(*[e.cuda_event for e in events])
+    code = lib.attn_varlen_fvjp_record_events(arr, 6)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
 
 
 def _ptr(t):

@@ -90,6 +90,10 @@ int sm_count() {
   return n;
 }
 
+// Events of the timing hook (one-shot, per host thread).
+thread_local cudaEvent_t g_events[6];
+thread_local int g_nevents = 0;
+
 int head_group(int Hq) {
   int g = 16;
   while (Hq % g) g >>= 1;
@@ -115,6 +119,17 @@ extern "C" int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int
   if (total_q == 0) return 2;  // dk, dv zero fills
   if (total_k == 0) return 3;  // out, dq zero fills, lse fill
   return 5;                    // schedule, forward, preprocess, dk/dv, dq
+}
+
+extern "C" attn_status attn_varlen_fvjp_record_events(void* const* events, int n) {
+  if (n == 0) {
+    g_nevents = 0;
+    return ATTN_OK;
+  }
+  if (n != 6 || !events) return ATTN_ERR_INVALID;
+  for (int i = 0; i < 6; ++i) g_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_nevents = 6;
+  return ATTN_OK;
 }
 
 extern "C" const char* attn_status_string(attn_status s) {
@@ -248,10 +263,21 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   const int grid_q = static_cast<int>(qtiles_max < sms ? qtiles_max : sms);
   const int grid_k = static_cast<int>(ktiles_max < sms ? ktiles_max : sms);
 
+  const int nev = g_nevents;
+  g_nevents = 0;
+  auto mark = [&](int i) {
+    if (nev) cudaEventRecord(g_events[i], stream);
+  };
+  mark(0);
   if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  mark(1);
   if (launch_fwd(p, tq, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  mark(3);
   if (launch_dkdv(p, tq64, tdo64, tk, tv, grid_k, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  mark(4);
   if (launch_dq(p, tq, tdo, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  mark(5);
   return ATTN_OK;
 }

@@ -160,8 +160,9 @@ def build(name, lq, lk, Hq, dtype, step, pad, slopes, qk_std=1.0, v_std=1.0, do_
     _fill_normal(k, qk_std, gen)
     _fill_normal(v, v_std, gen)
     _fill_normal(dout, do_std, gen)
-    return Problem(name=name, dtype=dtype, B=len(lq), Hq=Hq, cu_q=cu_q, cu_k=cu_k, q=q, k=k,
-                   v=v, dout=dout, alibi_slopes=slopes.contiguous(),
+    return Problem(name=name, dtype=dtype, B=len(lq), Hq=Hq, cu_q=cu_q.to(device),
+                   cu_k=cu_k.to(device), q=q, k=k, v=v, dout=dout,
+                   alibi_slopes=slopes.contiguous().to(device),
                    meta=dict(step=step, pad=pad, seed=seed), **mask)
 
 
