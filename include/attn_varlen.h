@@ -75,7 +75,8 @@ typedef enum {
   ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
   ATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
   ATTN_ERR_DEVICE_STATUS = -6,
-  ATTN_ERR_TIMEOUT = -7
+  ATTN_ERR_TIMEOUT = -7,
+  ATTN_ERR_SCRATCH_LIMIT = -8 /* needs more than the no-allocation entry point's scratch */
 } attn_status;
 
 /* Bits of the device status word. */
@@ -130,6 +131,52 @@ int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_
  * Returns ATTN_ERR_INVALID for any other n.  Used by benchmarks to time each
  * kernel on the launching stream. */
 attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
+
+/* Size of the fixed device scratch array used by
+ * attn_varlen_fvjp_fwd_bwd_noalloc (64 MiB). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* The same fused forward + VJP call for callers that cannot allocate device
+ * memory -- for example a plugin inside a host framework that owns every
+ * device allocation, or a latency-critical service that forbids allocator
+ * calls (which can synchronise the device) while it serves.  The pages have
+ * no counterpart; this is a deployment convenience.
+ *
+ * Arguments are those of attn_varlen_fvjp_fwd_bwd without the workspace: the
+ * caller still passes every input and output.  Instead of a workspace the
+ * call uses one device array of ATTN_NOALLOC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library holds it until the process exits.
+ * The call allocates nothing (no cudaMalloc, no allocating library routine).
+ *
+ * Limits and sharing:
+ *  - Problems whose attn_varlen_fvjp_workspace_size exceeds the array (about
+ *    16.7 million query rows total_q * Hq, with the schedule of up to
+ *    ATTN_MAX_BATCH sequences) are rejected with ATTN_ERR_SCRATCH_LIMIT
+ *    before anything is enqueued.
+ *  - Every call on a device uses the same array, which keeps the last call's
+ *    contents.  The call resets what must start at zero itself.  Calls whose
+ *    work overlaps on the GPU (other streams, other host threads) race on the
+ *    array and give wrong results; serialise them.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - With device_status NULL the status word is the first int32 of the
+ *    array, which the caller cannot read; pass a device_status pointer to
+ *    see device-side errors. */
+attn_status attn_varlen_fvjp_fwd_bwd_noalloc(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    float *lse, int32_t *device_status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,9 @@ ATTN_F16, ATTN_BF16 = 0, 1
 DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0x8
 
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
-           "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events")
+           "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
+           "attn_varlen_fvjp_fwd_bwd_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
 
@@ -50,6 +52,10 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
         [P, P, ctypes.c_size_t, P, P])
     lib.attn_varlen_fvjp_fwd_bwd.restype = I
+    lib.attn_varlen_fvjp_fwd_bwd_noalloc.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
+        [P, P, P])
+    lib.attn_varlen_fvjp_fwd_bwd_noalloc.restype = I
     lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
     lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
@@ -157,6 +163,37 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     if code != 0:
         raise AttnError(code, lib.attn_status_string(code).decode())
     return dict(out=out, dq=dq, dk=dk, dv=dv, lse=lse, workspace=workspace)
+
+
+def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv, lse,
+                                  device_status, causal=False, window_left=-1, window_right=-1,
+                                  softcap=3.0, scale_multiplier=0.75, stream=None):
+    """The library's no-allocation entry point: the caller passes every input
+    and output (plus an int32 device status word); the library uses its own
+    fixed scratch array instead of a workspace, for callers that may not
+    allocate device memory.  Asynchronous on ``stream``."""
+    lib = load()
+    dtype = q.dtype
+    Hq = q.shape[1]
+    for name, t, H in (("q", q, Hq), ("dout", dout, Hq), ("k", k, 1), ("v", v, 1),
+                       ("out", out, Hq), ("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+        _check_qlike(name, t, dtype, H)
+    B = cu_q.numel() - 1
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    code = lib.attn_varlen_fvjp_fwd_bwd_noalloc(
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, q.shape[0],
+        k.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
+        _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+        alibi_slopes.stride(0) if alibi_slopes is not None else 0,
+        int(bool(causal)), int(window_left), int(window_right), float(softcap),
+        float(scale_multiplier),
+        _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
+        _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
+        _ptr(lse), _ptr(device_status), stream.cuda_stream)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
 
 
 def device_status(workspace: torch.Tensor) -> int:

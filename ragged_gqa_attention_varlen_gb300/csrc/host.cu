@@ -142,6 +142,8 @@ extern "C" const char* attn_status_string(attn_status s) {
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_DEVICE_STATUS: return "device reported an error in the status word";
     case ATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case ATTN_ERR_SCRATCH_LIMIT:
+      return "problem needs more than the no-allocation entry point's fixed scratch";
   }
   return "unknown status";
 }

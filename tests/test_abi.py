@@ -74,3 +74,17 @@ def test_host_validation_codes(lib):
     assert _call(lib, wsb=16) == -4             # workspace too small
     assert _call(lib, B=0) == -1                # B = 0 with tokens
     assert _call(lib, q=None) == -1
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
+    """The no-allocation entry point refuses, before touching the device, a
+    problem whose workspace would exceed its fixed scratch array."""
+    fake = 0x10000
+    big_q = (64 << 20) // (4 * 96) + 1  # D alone needs more than the scratch
+    args = [0, 2, 96, 1, 160, big_q, 12,
+            fake, 96 * 160, 160, fake, 160, 160, fake, 160, 160, fake, 96 * 160, 160,
+            fake, fake, fake, 96, 0, -1, -1, 3.0, 0.75,
+            fake, 96 * 160, 160, fake, 96 * 160, 160, fake, 160, 160, fake, 160, 160,
+            fake, None, None]
+    assert lib.attn_varlen_fvjp_fwd_bwd_noalloc(*args) == -8
+    assert b"scratch" in lib.attn_status_string(-8)
