@@ -242,7 +242,8 @@ def run_gpu(args, world, rank, local):
     binding.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False)
+    p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False,
+                                length_scale=args.length_scale)
     flops = counted_flops(p)
     kflops = kernel_flops(p)
     out = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
@@ -314,7 +315,9 @@ def run_gpu(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, generated on device)",
-            "config": {"workload": "long_balanced", "B": p.B, "Hq": p.Hq, "Hkv": 1,
+            "config": {"workload": "long_balanced" + (
+                           "" if args.length_scale == 1.0 else f" x{args.length_scale} length"),
+                       "B": p.B, "Hq": p.Hq, "Hkv": 1,
                        "head_dim": HEAD_DIM, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
                        "counted_tflop_per_step": flops / 1e12,
@@ -382,6 +385,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--length-scale", type=float, default=1.0,
+                    help="scale every sequence length (small cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
