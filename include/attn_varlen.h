@@ -84,6 +84,7 @@ typedef enum {
 #define ATTN_DEV_TIMEOUT_FWD 0x2     /* a bounded wait in the forward kernel ran out */
 #define ATTN_DEV_TIMEOUT_DKDV 0x4    /* ... in the dk/dv kernel */
 #define ATTN_DEV_TIMEOUT_DQ 0x8      /* ... in the dq kernel */
+#define ATTN_DEV_SMEM_ALIGN 0x10     /* dynamic shared memory base not 1024-byte aligned */
 
 /* Largest batch (number of sequences) accepted. */
 #define ATTN_MAX_BATCH 16384

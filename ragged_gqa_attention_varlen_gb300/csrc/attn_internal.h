@@ -60,9 +60,11 @@ cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap
                        const CUtensorMap& tv, int grid, cudaStream_t s);
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq64, const CUtensorMap& tdo64,
-                        const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t s);
+                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tkt,
+                        const CUtensorMap& tvt, int grid, cudaStream_t s);
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                      const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t s);
+                      const CUtensorMap& tqt, const CUtensorMap& tdot, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& tvt, int grid, cudaStream_t s);
 cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
                              cudaStream_t s);
 cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s);

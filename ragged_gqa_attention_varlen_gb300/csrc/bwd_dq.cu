@@ -7,10 +7,20 @@
 // tiles so that every dq row is written once, by one CTA, with no atomics:
 // repeated calls are bitwise identical.
 //
-// Tile: the forward's 128 query rows.  Per key tile:
-//   S  = Q K^T, dP = dO V^T     two M=128 N=128 K=160 MMAs into TMEM
-//   dS                          registers, one thread per row, 16-bit to smem
-//   dQ += dS K                  M=128 N=160 K=128 into TMEM
+// Tile: the forward's 128 query rows.  Per key tile j:
+//   S_j  = Q K_j^T, dP_j = dO V_j^T   M=128 N=128 K=160, fp32 in TMEM
+//   dS_j                              elementwise warps; written back over
+//                                     dP_j as 16-bit pairs
+//   dQ  += dS_j K_j                   M=128 N=160 K=128, A operand from TMEM
+//
+// Warp roles (320 threads): warp 0 loads (Q, dO once per tile; K through two
+// slots, V through one), warp 1 issues the MMAs, warps 2-9 do the elementwise
+// work (two warps per TMEM lane quadrant, each taking 64 of the 128 keys).
+// The elementwise warps release S_j as soon as they have read it, so S_{j+1}
+// runs on the tensor core while dS_j is still being formed.  Q, dO and V are
+// only K-major operands here and keep their last 32 features in a 64-byte-
+// swizzled chunk; K is also the MN-major operand of dQ and stays in three
+// 128-byte-swizzled chunks.
 #include "../../include/attn_varlen.h"
 #include "common.cuh"
 #include "sched.cuh"
@@ -18,18 +28,27 @@
 namespace attn {
 
 namespace dqk {
-constexpr uint32_t kTile = 16384;
+constexpr int kThreadsDQ = 320;
+constexpr uint32_t kTile = 16384;            // 64-feature chunk of 128 rows
+constexpr uint32_t kTail = 8192;             // features 128..159 of 128 rows
+constexpr uint32_t kTailed = 2 * kTile + kTail;
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffDO = 3 * kTile;
-constexpr uint32_t kOffK = 6 * kTile;
-constexpr uint32_t kOffV = 9 * kTile;
-constexpr uint32_t kOffDS = 12 * kTile;  // 2 chunks
-constexpr uint32_t kOffBar = 14 * kTile;
-constexpr uint32_t kSmem = kOffBar + 64 + 1024;
+constexpr uint32_t kOffDO = kTailed;
+constexpr uint32_t kOffK = 2 * kTailed;      // two K slots, 3 full chunks each
+constexpr uint32_t kOffV = kOffK + 2 * 3 * kTile;
+constexpr uint32_t kOffBar = kOffV + kTailed;
+constexpr uint32_t kSmem = kOffBar + 256;    // base checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColP = 128;
 constexpr uint32_t kColQ = 256;
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[2], k_empty[2], v_full, v_empty;
+  uint64_t s_full, s_free, dp_full, p_full, dq_done;
+  uint64_t o_full, o_empty, drain;
+};
 }  // namespace dqk
 
 __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
@@ -40,44 +59,58 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq,
-              const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv) {
+              const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tqt,
+              const __grid_constant__ CUtensorMap tdot, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tvt) {
   using namespace dqk;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   uint8_t* sQ = sm + kOffQ;
   uint8_t* sDO = sm + kOffDO;
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
-  uint8_t* sDS = sm + kOffDS;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffBar);  // q+do, k, v, mma
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 4);
-  int* s_item = reinterpret_cast<int*>(s_tmem + 1);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 2);
+  Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_status = reinterpret_cast<int*>(s_tmem + 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int ntiles = qtile_count(p);
-  if (tid == 0)
-    *s_item = (*reinterpret_cast<volatile int32_t*>(p.status) != 0) ? ntiles
-                                                                     : atomicAdd(p.counters + 2, 1);
+  if (tid == 0) {
+    *s_status = *reinterpret_cast<volatile int32_t*>(p.status);
+    if (smem_addr(sm) & 1023u) {
+      atomicOr(p.status, ATTN_DEV_SMEM_ALIGN);
+      *s_status = 1;
+    }
+  }
   __syncthreads();
-  int item = *s_item;
-  if (item >= ntiles) return;
+  if (*s_status != 0 || static_cast<int>(blockIdx.x) >= ntiles) return;
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 8);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 8);
+    mbar_init(&bars->drain, 1);
     fence_barrier_init();
     *s_abort = 0;
-    prefetch_tensormap(&tq);
-    prefetch_tensormap(&tdo);
-    prefetch_tensormap(&tk);
-    prefetch_tensormap(&tv);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -85,199 +118,276 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem + kColS, tP = tmem + kColP, tQ = tmem + kColQ;
-
-  uint32_t ph_q = 0, ph_k = 0, ph_v = 0, ph_m = 0;
-  bool pend_q = false, pend_k = false, pend_v = false, pend_m = false;
-  const LogitMap lm = make_logit_map(p);
-  const bool masked = masking(p);
-  constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-  constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
   const int G = p.G;
 
-  while (true) {
-    QTile t;
-    qtile_decode(p, item, t);
-    const int r = tid;
-    const int i_loc = t.tok + r / G;
-    const int h = t.hg * G + r % G;
-    const bool row_valid = i_loc < t.Lq;
-    const float slope2 = p.slopes ? __ldg(p.slopes + t.b * p.slopes_bs + h) * kLog2e : 0.f;
-    const int nkt = (t.Lk + kKeys - 1) / kKeys;
-    const int pos_off = i_loc + t.Lk - t.Lq;
-    float lse2 = INFINITY, Drow = 0.f;  // rows outside the sequence get P = 0
-    if (row_valid) {
-      const int64_t ri = static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h;
-      const float lse = p.lse[ri];
-      lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-      Drow = p.Dbuf[ri];
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tq);
+      prefetch_tensormap(&tdo);
+      prefetch_tensormap(&tqt);
+      prefetch_tensormap(&tdot);
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+      prefetch_tensormap(&tvt);
+      uint32_t g = 0;  // key tiles loaded
+      int tcount = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        QTile t;
+        qtile_decode(p, item, t);
+        const int n = (t.Lk + kKeys - 1) / kKeys;
+        if (tcount > 0 && !(ok = mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kTailed);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(sQ + c * kTile, &tq, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
+          tma_load_3d(sDO + c * kTile, &tdo, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
+        }
+        tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
+        tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
+        for (int j = 0; j < n && ok; ++j, ++g) {
+          const int key = t.k0 + j * kKeys;
+          const int ks = g & 1;
+          if (g >= 2 && !(ok = mbar_wait(&bars->k_empty[ks], ((g - 2) >> 1) & 1, s_abort))) break;
+          mbar_arrive_expect_tx(&bars->k_full[ks], 3 * kTile);
+          for (int c = 0; c < 3; ++c)
+            tma_load_2d(sK + (ks * 3 + c) * kTile, &tk, &bars->k_full[ks], c * kChunk, key);
+          if (g >= 1 && !(ok = mbar_wait(&bars->v_empty, (g - 1) & 1, s_abort))) {
+            ++g;  // the K fill above is armed
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full, kTailed);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sV + c * kTile, &tv, &bars->v_full, c * kChunk, key);
+          tma_load_2d(sV + 2 * kTile, &tvt, &bars->v_full, 2 * kChunk, key);
+        }
+      }
+      if (*s_abort) {
+        if (tcount > 0) drain_wait_dq(&bars->q_full, (tcount - 1) & 1);
+        for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f) drain_wait_dq(&bars->k_full[f & 1], (f >> 1) & 1);
+        if (g > 0) drain_wait_dq(&bars->v_full, (g - 1) & 1);
+      }
     }
-
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bar[0], 6 * kTile);
-      for (int c = 0; c < 3; ++c) {
-        tma_load_3d(sQ + c * kTile, &tq, &bar[0], c * kChunk, t.hg * G, t.q0 + t.tok);
-        tma_load_3d(sDO + c * kTile, &tdo, &bar[0], c * kChunk, t.hg * G, t.q0 + t.tok);
-      }
-      pend_q = true;
-    }
-
-    for (int kt = 0; kt < nkt; ++kt) {
-      const int key0 = kt * kKeys;
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[1], 3 * kTile);
-        for (int c = 0; c < 3; ++c)
-          tma_load_2d(sK + c * kTile, &tk, &bar[1], c * kChunk, t.k0 + key0);
-        mbar_arrive_expect_tx(&bar[2], 3 * kTile);
-        for (int c = 0; c < 3; ++c)
-          tma_load_2d(sV + c * kTile, &tv, &bar[2], c * kChunk, t.k0 + key0);
-        pend_k = pend_v = true;
-        bool ok = true;
-        if (pend_q) {
-          ok = mbar_wait(&bar[0], ph_q, s_abort);
-          if (ok) {
-            ph_q ^= 1;
-            pend_q = false;
-          }
-        }
-        ok = ok && mbar_wait(&bar[1], ph_k, s_abort);
-        if (ok) {
-          ph_k ^= 1;
-          pend_k = false;
-        }
-        ok = ok && mbar_wait(&bar[2], ph_v, s_abort);
-        if (ok) {
-          ph_v ^= 1;
-          pend_v = false;
-          tc_fence_after();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
+      const uint32_t qb = smem_addr(sQ), db = smem_addr(sDO), vb = smem_addr(sV);
+      // K-major operand stored as two 128-byte-swizzled chunks + a 64-byte tail
+      auto tailed = [&](uint32_t base, int k) -> uint64_t {
+        return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
+                     : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
+      };
+      uint32_t g = 0;
+      int tcount = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t gs) -> bool {  // S = Q K^T
+        if (gs >= 1 && !mbar_wait(&bars->s_free, (gs - 1) & 1, s_abort)) return false;
+        if (!mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_addr(sK + (gs & 1) * 3 * kTile);
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-            umma_ss(tS, sdesc_sw128(smem_addr(sQ) + off, 16, 1024),
-                    sdesc_sw128(smem_addr(sK) + off, 16, 1024), kIdS, k > 0);
-          }
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-            umma_ss(tP, sdesc_sw128(smem_addr(sDO) + off, 16, 1024),
-                    sdesc_sw128(smem_addr(sV) + off, 16, 1024), kIdS, k > 0);
-          }
-          umma_commit(&bar[3]);
-          pend_m = true;
-        }
-      }
-      __syncwarp();
-      if (mbar_wait(&bar[3], ph_m, s_abort)) {
-        ph_m ^= 1;
-        pend_m = false;
-      }
-      __syncthreads();
-      if (*s_abort) break;
-      tc_fence_after();
-
-      // ---- dS for row r, 32 keys at a time
-#pragma unroll 1
-      for (int c = 0; c < kKeys / 32; ++c) {
-        float sv[32], pv[32];
-        tmem_ld32(tS + lane + c * 32, sv);
-        tmem_ld32(tP + lane + c * 32, pv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int jg = key0 + c * 32 + j;
-          float th;
-          float z = logit2(lm, sv[j], slope2, fabsf(static_cast<float>(pos_off - jg)), &th);
-          bool adm = jg < t.Lk;
-          if (masked) adm = adm && admissible(p, t.Lq, t.Lk, i_loc, jg);
-          const float P = adm ? ex2_approx(z - lse2) : 0.f;
-          const float g = lm.capped ? fmaf(-th, th, 1.f) : 1.f;
-          sv[j] = P * (pv[j] - Drow) * g;
-        }
-        store_row32_sw128<BF16>(sDS, kTile, r, c * 32, sv);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-
-      if (tid == 0) {
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          umma_ss(tmem + kColS, tailed(qb, k),
+                  sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
+        umma_commit(&bars->s_full);
+        return true;
+      };
+      auto issue_dp = [&](uint32_t gs) -> bool {  // dP = dO V^T
+        if (gs >= 1 && !mbar_wait(&bars->dq_done, (gs - 1) & 1, s_abort)) return false;
+        if (!mbar_wait(&bars->v_full, gs & 1, s_abort)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kKeys / 16; ++k) {
-          umma_ss(tQ, sdesc_sw128(smem_addr(sDS) + (k >> 2) * kTile + (k & 3) * 32, 16, 1024),
-                  sdesc_sw128(smem_addr(sK) + k * 2048, kTile, 1024), kIdQ, (kt > 0 || k > 0));
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
+        umma_commit(&bars->dp_full);
+        umma_commit(&bars->v_empty);
+        return true;
+      };
+      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        QTile t;
+        qtile_decode(p, item, t);
+        const int n = (t.Lk + kKeys - 1) / kKeys;
+        if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;
+        if (n == 0) {
+          mbar_arrive(&bars->q_empty);
+          if (tcount > 0 && !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort))) break;
+          mbar_arrive(&bars->o_full);
+          continue;
         }
-        umma_commit(&bar[3]);
-        pend_m = true;
-      }
-      __syncwarp();
-      if (mbar_wait(&bar[3], ph_m, s_abort)) {
-        ph_m ^= 1;
-        pend_m = false;
-      }
-      __syncthreads();
-      if (*s_abort) break;
-    }
-    if (*s_abort) break;
-    if (tid == 0 && pend_q) {
-      if (mbar_wait(&bar[0], ph_q, s_abort)) {
-        ph_q ^= 1;
-        pend_q = false;
-      }
-    }
-
-    // ---- epilogue: dq = sigma * dQ
-    tc_fence_after();
-    uint16_t* qrow = static_cast<uint16_t*>(p.dq) + static_cast<int64_t>(t.q0 + i_loc) * p.dq_ts +
-                     static_cast<int64_t>(h) * p.dq_hs;
+        if (!(ok = issue_s(g)) || !(ok = issue_dp(g))) break;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t gg = g + j;
+          if (j + 1 < n && !(ok = issue_s(gg + 1))) break;
+          if (j + 1 == n) umma_commit(&bars->q_empty);  // last S and dP of this tile issued
+          if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
+          if (j == 0 && tcount > 0 &&
+              !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort)))
+            break;
+          tc_fence_after();
+          const uint32_t kb = smem_addr(sK + (gg & 1) * 3 * kTile);
+          // keys 16k..16k+15: half k/4, pair column 8*(k%4) of that half's region
 #pragma unroll
-    for (int c = 0; c < kHeadDim / 32; ++c) {
-      float o[32];
-      tmem_ld32(tQ + lane + c * 32, o);
-      tmem_wait_ld();
+          for (int k = 0; k < kKeys / 16; ++k)
+            umma_ts(tmem + kColQ, tmem + kColP + (k >> 2) * 64 + (k & 3) * 8,
+                    sdesc_sw128(kb + k * 2048, kTile, 1024), kIdQ, (j > 0 || k > 0));
+          umma_commit(&bars->dq_done);
+          umma_commit(&bars->k_empty[gg & 1]);
+          if (j + 1 == n) umma_commit(&bars->o_full);
+          else if (!(ok = issue_dp(gg + 1))) break;
+        }
+        g += n;
+      }
+      umma_commit(&bars->drain);
+      drain_wait_dq(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;  // keys [64*half, 64*half + 64) of each tile
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const LogitMap lm = make_logit_map(p);
+    const bool masked = masking(p);
+    uint32_t g = 0;
+    int tcount = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      QTile t;
+      qtile_decode(p, item, t);
+      const int n = (t.Lk + kKeys - 1) / kKeys;
+      const int i_loc = t.tok + r / G;
+      const int h = t.hg * G + r % G;
+      const bool row_valid = i_loc < t.Lq;
+      const float slope2 = p.slopes ? __ldg(p.slopes + t.b * p.slopes_bs + h) * kLog2e : 0.f;
+      const int pos_off = i_loc + t.Lk - t.Lq;
+      float lse2 = INFINITY, Drow = 0.f;  // rows outside the sequence get P = 0
+      if (row_valid) {
+        const int64_t ri = static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h;
+        const float lse = p.lse[ri];
+        lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+        Drow = p.Dbuf[ri];
+      }
+      for (int j = 0; j < n; ++j) {
+        const uint32_t gg = g + j;
+        const int key0 = j * kKeys + half * 64;
+        const float pos0 = static_cast<float>(pos_off - key0);
+        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        float x[64];
+        tmem_ld32(tmem + kColS + half * 64 + lane_addr, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(tmem + kColS + half * 64 + 32 + lane_addr,
+                  *reinterpret_cast<float(*)[32]>(x + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten now
+        // Two batches of 32 columns; within a batch all tanh, then the exponent
+        // arguments, then all exp2, so dependent MUFU results are far apart.
+        const bool edge = masked || key0 + 64 > t.Lk;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float* xb = x + b * 32;
+          float th[32];
+          if (lm.capped) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float bias =
+                fmaf(-slope2, fabsf(pos0 - static_cast<float>(b * 32 + c)), -lse2);
+            xb[c] = lm.capped ? fmaf(th[c], lm.out_scale, bias) : fmaf(xb[c], lm.in_scale, bias);
+          }
+          if (edge) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int jg = key0 + b * 32 + c;
+              bool adm = jg < t.Lk;
+              if (masked) adm = adm && admissible(p, t.Lq, t.Lk, i_loc, jg);
+              xb[c] = adm ? xb[c] : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) xb[c] = ex2_approx(xb[c]);  // P
+          if (lm.capped) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);  // P (1 - tanh^2)
+          }
+        }
+        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        const uint32_t pbuf = tmem + kColP + half * 64 + lane_addr;
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float d[32];
+          tmem_ld32(pbuf + cc * 32, d);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            pk[cc * 16 + (c >> 1)] = Pack<BF16>::two(x[cc * 32 + c] * (d[c] - Drow),
+                                                     x[cc * 32 + c + 1] * (d[c + 1] - Drow));
+        }
+        // dS pairs over this half's first 32 (already read) dP columns
+        tmem_st16(pbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(pbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+      }
+      if (!ok) break;
+      g += n;
+      // ---- epilogue: dq = sigma * dQ, this half's 80 features
+      if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
+      tc_fence_after();
+      uint16_t* qrow = static_cast<uint16_t*>(p.dq) + static_cast<int64_t>(t.q0 + i_loc) * p.dq_ts +
+                       static_cast<int64_t>(h) * p.dq_hs + half * 80;
+      const uint32_t acc = tmem + kColQ + half * 80 + lane_addr;
+      float o[80];
+      tmem_ld32(acc, *reinterpret_cast<float(*)[32]>(o));
+      tmem_ld32(acc + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+      {
+        float tail16[32];
+        tmem_ld32(acc + 64 - 16, tail16);  // columns 48..79 (overlap keeps the load x32)
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[64 + i] = tail16[16 + i];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_empty);
       if (row_valid) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 10; ++u) {
           float w[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = nkt > 0 ? o[8 * u + i] * p.sigma : 0.f;
-          *reinterpret_cast<uint4*>(qrow + c * 32 + u * 8) = pack8<BF16>(w);
+          for (int i = 0; i < 8; ++i) w[i] = n > 0 ? o[8 * u + i] * p.sigma : 0.f;
+          *reinterpret_cast<uint4*>(qrow + u * 8) = pack8<BF16>(w);
         }
       }
     }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) *s_item = atomicAdd(p.counters + 2, 1);
-    __syncthreads();
-    item = *s_item;
-    if (item >= ntiles) break;
   }
 
-  if (*s_abort) {
-    if (tid == 0) {
-      atomicOr(p.status, ATTN_DEV_TIMEOUT_DQ);
-      if (pend_q) drain_wait_dq(&bar[0], ph_q);
-      if (pend_k) drain_wait_dq(&bar[1], ph_k);
-      if (pend_v) drain_wait_dq(&bar[2], ph_v);
-      if (pend_m) drain_wait_dq(&bar[3], ph_m);
-    }
-  }
-  tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *s_abort) atomicOr(p.status, ATTN_DEV_TIMEOUT_DQ);
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                      const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t s) {
+                      const CUtensorMap& tqt, const CUtensorMap& tdot, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& tvt, int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = dq_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, kThreads, dqk::kSmem, s>>>(p, tq, tdo, tk, tv);
+    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq, tdo, tqt, tdot, tk, tv, tvt);
   } else {
     auto k = dq_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, kThreads, dqk::kSmem, s>>>(p, tq, tdo, tk, tv);
+    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq, tdo, tqt, tdot, tk, tv, tvt);
   }
   return cudaGetLastError();
 }

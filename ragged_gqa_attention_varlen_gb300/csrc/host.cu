@@ -54,31 +54,38 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
 
 // [T, H, 160] view -> 3-D map (feature, head, token) with a box of
-// 64 features x G heads x (rows/G) tokens, 128-byte swizzle.
+// 64 features x G heads x (rows/G) tokens and the 128-byte swizzle, or (tail)
+// 32 features (128..159) with the 64-byte swizzle.
 bool encode_q(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
-              int64_t hs, int G, int rows) {
+              int64_t hs, int G, int rows, bool tail = false) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(G),
-                       static_cast<cuuint32_t>(rows / G)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(tail ? kHeadDim - 2 * kChunk : kChunk),
+                       static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(rows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     tail ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [T, 1, 160] view -> 2-D map (feature, token), box 64 x 128 keys.
-bool encode_kv(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t ts) {
+// [T, 1, 160] view -> 2-D map (feature, token), box 64 x 128 keys with the
+// 128-byte swizzle, or (tail) 32 x 128 with the 64-byte swizzle for features
+// 128..159.
+bool encode_kv(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t ts,
+               bool tail = false) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ts) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kKeys)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(tail ? kHeadDim - 2 * kChunk : kChunk),
+                       static_cast<cuuint32_t>(kKeys)};
   cuuint32_t estr[2] = {1, 1};
   return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     tail ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -248,12 +255,16 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
 
   // ---- TMA tensor maps
   if (!encode_fn()) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tdo, tq64, tdo64, tk, tv;
+  CUtensorMap tq, tdo, tqt, tdot, tq64, tdo64, tk, tv, tkt, tvt;
   if (!encode_q(&tq, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
       !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+      !encode_q(&tqt, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ, true) ||
+      !encode_q(&tdot, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ, true) ||
       !encode_q(&tq64, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsKV) ||
       !encode_q(&tdo64, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsKV) ||
-      !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts))
+      !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts) ||
+      !encode_kv(&tkt, dtype, k, total_k, k_ts, true) ||
+      !encode_kv(&tvt, dtype, v, total_k, v_ts, true))
     return ATTN_ERR_ALIGNMENT;
 
   const int sms = sm_count();
@@ -277,9 +288,11 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
-  if (launch_dkdv(p, tq64, tdo64, tk, tv, grid_k, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_dkdv(p, tq64, tdo64, tk, tv, tkt, tvt, grid_k, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   mark(4);
-  if (launch_dq(p, tq, tdo, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_dq(p, tq, tdo, tqt, tdot, tk, tv, tvt, grid_q, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   mark(5);
   return ATTN_OK;
 }

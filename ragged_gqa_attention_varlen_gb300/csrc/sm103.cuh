@@ -138,6 +138,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory descriptor for a K-major operand stored with the 64-byte
+// swizzle: rows of 32 16-bit elements (64 bytes), 8-row groups 512 bytes apart
+// (SBO), layout code 4.  Stepping K by 16 elements adds 32 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;  // LBO unused for swizzled K-major
+  d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
+// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
 //   1 = bf16), 15/16 A/B major (0 = K-major, 1 = MN-major), 17-22 N >> 3,
