@@ -56,8 +56,9 @@ struct Params {
 inline int sched_words(int B) { return 4 * B + 2; }
 
 cudaError_t launch_sched(const Params& p, cudaStream_t s);
-cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int grid, cudaStream_t s);
+cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqt,
+                       const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
+                       int grid, cudaStream_t s);
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq64, const CUtensorMap& tdo64,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tkt,

@@ -35,7 +35,6 @@ namespace attn {
 
 namespace kv {
 constexpr int kThreadsKV = 320;
-constexpr int kEW = 256;  // elementwise threads (warps 2..9)
 constexpr int kStages = 3;
 constexpr uint32_t kTile = 16384;   // 64-feature chunk of a 128-key tile
 constexpr uint32_t kTail = 8192;    // features 128..159 of a 128-key tile (64 B rows)
@@ -68,6 +67,7 @@ struct Bars {
   uint64_t s_full[2], s_free[2];
   uint64_t dp_full, dp_free, p_full;
   uint64_t acc_full, acc_empty, drain;
+  uint64_t cols_x[2];  // per-step scalars published (one arrival per elementwise warp)
 };
 }  // namespace kv
 
@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->cols_x[0], 8);
+    mbar_init(&bars->cols_x[1], 8);
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         float a = 0.f, b = 0.f, c = 0.f;
         fetch(t, 0, a, b, c);
         publish(cols + (g & 1), a, b, c);
-        named_barrier(1, kEW);
+        if (!(ok = warp_exchange(&bars->cols_x[g & 1], (g >> 1) & 1, s_abort))) break;
       }
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
@@ -405,7 +407,8 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         if (lane == 0) mbar_arrive(&bars->p_full);
         if (more) {
           publish(cols + ((gg + 1) & 1), na, nb, nc);
-          named_barrier(1, kEW);
+          if (!(ok = warp_exchange(&bars->cols_x[(gg + 1) & 1], ((gg + 1) >> 1) & 1, s_abort)))
+            break;
         }
       }
       if (!ok) break;

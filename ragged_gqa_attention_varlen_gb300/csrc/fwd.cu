@@ -14,10 +14,18 @@
 //                         is written back over S_j as 16-bit pairs
 //   O  += P_j V_j         tcgen05.mma with P_j read from TMEM
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (Q once per tile, K and
-// V through a 3-slot ring), warp 1 issues the MMAs, warps 2-5 run the
-// softmax and the epilogue.  S is double-buffered in TMEM so the tensor core
-// computes S_{j+1} while the softmax works on S_j.
+// Warp roles (320 threads): warp 0 issues TMA loads (lane 0: Q once per tile
+// and K through two slots; lane 1: V through two slots, so a K load never
+// waits for a V slot), warp 1 issues the MMAs, warps 2-9 run the
+// softmax and the epilogue -- two warps per TMEM lane quadrant, each taking
+// 64 of the 128 keys of a tile (the row max is exchanged through shared
+// memory), so every SM sub-partition has two warps to hide MUFU latency.  S
+// is double-buffered in TMEM so the tensor core computes S_{j+1} while the
+// softmax works on S_j.
+//
+// Q and K are only K-major operands here and keep features 128..159 in a
+// 64-byte-swizzled chunk; V is the MN-major operand of P V and stays in three
+// 128-byte-swizzled chunks.
 //
 // Key tiles are visited starting with the one that holds the ALiBi peak of
 // the tile's rows (the key aligned with the query, where the distance is 0),
@@ -33,23 +41,28 @@
 namespace attn {
 
 namespace fwd {
-constexpr int kThreadsF = 192;
-constexpr int kSlots = 3;
+constexpr int kThreadsF = 320;
 constexpr uint32_t kTile = 16384;        // one 64-feature chunk of a 128-row tile
-constexpr uint32_t kTile3 = 3 * kTile;   // a whole 128 x 160 tile
+constexpr uint32_t kTail = 8192;         // features 128..159 of 128 rows (64-byte rows)
+constexpr uint32_t kTailed = 2 * kTile + kTail;
+constexpr uint32_t kTile3 = 3 * kTile;   // a whole 128 x 160 tile in 128-byte rows
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffSlot = kTile3;    // kSlots tiles of K or V
-constexpr uint32_t kOffBar = kOffSlot + kSlots * kTile3;
-constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr uint32_t kOffK = kTailed;      // two K slots
+constexpr uint32_t kOffV = kOffK + 2 * kTailed;  // two V slots
+constexpr uint32_t kOffMax = kOffV + 2 * kTile3;  // [2 steps][2 halves][128] fp32
+constexpr uint32_t kOffSum = kOffMax + 2 * 2 * 128 * 4;     // [2 tiles][2 halves][128] fp32
+constexpr uint32_t kOffBar = kOffSum + 2 * 2 * 128 * 4;
+constexpr uint32_t kSmem = kOffBar + 256;  // the dynamic base is checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;          // S0: [0,128), S1: [128,256), O: [256,416)
 constexpr float kRescale = 8.f;          // lazy-rescale threshold (base 2)
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t slot_full[kSlots], slot_empty[kSlots];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2];
   uint64_t o_full, o_empty, drain;
+  uint64_t mx_x[2], l_x[2];  // row-max and row-sum exchanges between the halves
 };
 }  // namespace fwd
 
@@ -71,13 +84,16 @@ __device__ __forceinline__ void key_order(const QTile& t, int& n, int& t0) {
 template <bool BF16>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq,
-               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv) {
   using namespace fwd;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   uint8_t* sQ = sm + kOffQ;
-  uint8_t* sSlot = sm + kOffSlot;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+  float* sMax = reinterpret_cast<float*>(sm + kOffMax);
+  float* sSum = reinterpret_cast<float*>(sm + kOffSum);
   Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -87,25 +103,35 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int ntiles = qtile_count(p);
-  if (tid == 0) *s_status = *reinterpret_cast<volatile int32_t*>(p.status);
+  if (tid == 0) {
+    *s_status = *reinterpret_cast<volatile int32_t*>(p.status);
+    if (smem_addr(sm) & 1023u) {
+      atomicOr(p.status, ATTN_DEV_SMEM_ALIGN);
+      *s_status = 1;
+    }
+  }
   __syncthreads();
   if (*s_status != 0 || static_cast<int>(blockIdx.x) >= ntiles) return;  // uniform
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&bars->slot_full[s], 1);
-      mbar_init(&bars->slot_empty[s], 1);
-    }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->k_full[b], 1);
+      mbar_init(&bars->k_empty[b], 1);
+      mbar_init(&bars->v_full[b], 1);
+      mbar_init(&bars->v_empty[b], 1);
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], 1);
-      mbar_init(&bars->p_full[b], 4);
+      mbar_init(&bars->p_full[b], 8);
     }
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_empty, 4);
+    mbar_init(&bars->o_empty, 8);
     mbar_init(&bars->drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->mx_x[b], 8);
+      mbar_init(&bars->l_x[b], 8);
+    }
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -121,11 +147,17 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tq);
-      prefetch_tensormap(&tk);
-      prefetch_tensormap(&tv);
-      uint32_t fill = 0;
+    if (lane < 2) {
+      const bool kq = lane == 0;  // lane 0: Q and K; lane 1: V
+      if (kq) {
+        prefetch_tensormap(&tq);
+        prefetch_tensormap(&tqt);
+        prefetch_tensormap(&tk);
+        prefetch_tensormap(&tkt);
+      } else {
+        prefetch_tensormap(&tv);
+      }
+      uint32_t g = 0;  // key steps loaded
       int tcount = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
@@ -133,30 +165,38 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         qtile_decode(p, item, t);
         int n, t0;
         key_order(t, n, t0);
-        if (tcount > 0 && !(ok = mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
-        mbar_arrive_expect_tx(&bars->q_full, kTile3);
-        for (int c = 0; c < 3; ++c)
-          tma_load_3d(sQ + c * kTile, &tq, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
-        for (int jj = 0; jj < n && ok; ++jj) {
-          const int kt = (t0 + jj) % n;
-          for (int kv = 0; kv < 2; ++kv, ++fill) {
-            const int s = fill % kSlots;
-            if (fill >= kSlots &&
-                !(ok = mbar_wait(&bars->slot_empty[s], (fill / kSlots - 1) & 1, s_abort)))
-              break;
-            mbar_arrive_expect_tx(&bars->slot_full[s], kTile3);
-            uint8_t* dst = sSlot + s * kTile3;
+        if (kq) {
+          if (tcount > 0 && !(ok = mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
+          mbar_arrive_expect_tx(&bars->q_full, kTailed);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(sQ + c * kTile, &tq, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
+          tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
+        }
+        for (int jj = 0; jj < n; ++jj, ++g) {
+          const int key = t.k0 + ((t0 + jj) % n) * kKeys;
+          const int s = g & 1;
+          if (g >= 2 && !(ok = mbar_wait(kq ? &bars->k_empty[s] : &bars->v_empty[s],
+                                         ((g - 2) >> 1) & 1, s_abort)))
+            break;
+          if (kq) {
+            mbar_arrive_expect_tx(&bars->k_full[s], kTailed);
+            uint8_t* dst = sK + s * kTailed;
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d(dst + c * kTile, &tk, &bars->k_full[s], c * kChunk, key);
+            tma_load_2d(dst + 2 * kTile, &tkt, &bars->k_full[s], 2 * kChunk, key);
+          } else {
+            mbar_arrive_expect_tx(&bars->v_full[s], kTile3);
+            uint8_t* dst = sV + s * kTile3;
             for (int c = 0; c < 3; ++c)
-              tma_load_2d(dst + c * kTile, kv ? &tv : &tk, &bars->slot_full[s], c * kChunk,
-                          t.k0 + kt * kKeys);
+              tma_load_2d(dst + c * kTile, &tv, &bars->v_full[s], c * kChunk, key);
           }
         }
       }
       if (*s_abort) {
         // let every load this thread started land before the CTA exits
-        if (tcount > 0) drain_wait(&bars->q_full, (tcount - 1) & 1);
-        for (uint32_t f = fill > kSlots ? fill - kSlots : 0; f < fill; ++f)
-          drain_wait(&bars->slot_full[f % kSlots], (f / kSlots) & 1);
+        if (kq && tcount > 0) drain_wait(&bars->q_full, (tcount - 1) & 1);
+        for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f)
+          drain_wait(kq ? &bars->k_full[f & 1] : &bars->v_full[f & 1], (f >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -167,22 +207,23 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint32_t g = 0;  // global key-step counter of this CTA
       int tcount = 0;
       bool ok = true;
+      // K-major operand stored as two 128-byte-swizzled chunks + a 64-byte tail
+      auto tailed = [&](uint32_t base, int k) -> uint64_t {
+        return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
+                     : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
+      };
       auto issue_s = [&](uint32_t gs) -> bool {
-        const uint32_t f = 2 * gs;  // K fill index of step gs
-        if (!mbar_wait(&bars->slot_full[f % kSlots], (f / kSlots) & 1, s_abort)) return false;
+        if (!mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort)) return false;
         if (gs >= 2 && !mbar_wait(&bars->s_free[gs & 1], ((gs - 2) >> 1) & 1, s_abort))
           return false;
         tc_fence_after();
-        const uint32_t kb = smem_addr(sSlot + (f % kSlots) * kTile3);
+        const uint32_t kb = smem_addr(sK + (gs & 1) * kTailed);
         const uint32_t qb = smem_addr(sQ);
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k) {
-          const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-          umma_ss(tmem + (gs & 1) * 128, sdesc_sw128(qb + off, 16, 1024),
-                  sdesc_sw128(kb + off, 16, 1024), kIdS, k > 0);
-        }
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          umma_ss(tmem + (gs & 1) * 128, tailed(qb, k), tailed(kb, k), kIdS, k > 0);
         umma_commit(&bars->s_full[gs & 1]);
-        umma_commit(&bars->slot_empty[f % kSlots]);
+        umma_commit(&bars->k_empty[gs & 1]);
         return true;
       };
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
@@ -209,17 +250,17 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           if (jj == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort)))
             break;
-          const uint32_t f = 2 * gg + 1;  // V fill index
-          if (!(ok = mbar_wait(&bars->slot_full[f % kSlots], (f / kSlots) & 1, s_abort))) break;
+          if (!(ok = mbar_wait(&bars->v_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
           tc_fence_after();
-          const uint32_t vb = smem_addr(sSlot + (f % kSlots) * kTile3);
+          const uint32_t vb = smem_addr(sV + (gg & 1) * kTile3);
           const uint32_t pa = tmem + (gg & 1) * 128;
+          // keys 16k..16k+15: half k/4, pair column 8*(k%4) of that half's region
 #pragma unroll
           for (int k = 0; k < kKeys / 16; ++k)
-            umma_ts(tmem + kColO, pa + k * 8, sdesc_sw128(vb + k * 2048, kTile, 1024), kIdO,
-                    (jj > 0 || k > 0));
+            umma_ts(tmem + kColO, pa + (k >> 2) * 64 + (k & 3) * 8,
+                    sdesc_sw128(vb + k * 2048, kTile, 1024), kIdO, (jj > 0 || k > 0));
           umma_commit(&bars->s_free[gg & 1]);
-          umma_commit(&bars->slot_empty[f % kSlots]);
+          umma_commit(&bars->v_empty[gg & 1]);
           if (jj == n - 1) umma_commit(&bars->o_full);
         }
         g += n;
@@ -231,6 +272,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;  // keys [64*half, 64*half + 64) of each tile
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
@@ -248,78 +290,93 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       const bool row_valid = i_loc < t.Lq;
       const float slope2 = p.slopes ? __ldg(p.slopes + t.b * p.slopes_bs + h) * kLog2e : 0.f;
       const int pos_off = i_loc + t.Lk - t.Lq;  // dist(j) = |pos_off - j|
-      float m_run = -INFINITY, l = 0.f;
+      float m_run = -INFINITY, l = 0.f;          // l: this half's share of the row sum
       for (int jj = 0; jj < n; ++jj) {
         const uint32_t gg = g + jj;
-        const int key0 = ((t0 + jj) % n) * kKeys;
-        const uint32_t sb = tmem + (gg & 1) * 128 + lane_addr;
+        const int key0 = ((t0 + jj) % n) * kKeys + half * 64;
+        const uint32_t sb = tmem + (gg & 1) * 128 + half * 64 + lane_addr;
         if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
         tc_fence_after();
-        float x[kKeys];
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c)
-          tmem_ld32(sb + c * 32, *reinterpret_cast<float(*)[32]>(x + c * 32));
+        float x[64];
+        tmem_ld32(sb, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(sb + 32, *reinterpret_cast<float(*)[32]>(x + 32));
         tmem_wait_ld();
         const float pos0 = static_cast<float>(pos_off - key0);
-        const bool edge = masked || key0 + kKeys > t.Lk;
-        float mx = -INFINITY;
-        if (lm.capped) {
+        const bool edge = masked || key0 + 64 > t.Lk;
+        // batched: all tanh of a 32-column group, then the logits
 #pragma unroll
-          for (int j = 0; j < kKeys; ++j) {
-            const float th = tanh_approx(x[j] * lm.in_scale);
-            x[j] = fmaf(th, lm.out_scale, -slope2 * fabsf(pos0 - static_cast<float>(j)));
+        for (int b = 0; b < 2; ++b) {
+          float* xb = x + b * 32;
+          if (lm.capped) {
+            float th[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              xb[c] = fmaf(th[c], lm.out_scale,
+                           -slope2 * fabsf(pos0 - static_cast<float>(b * 32 + c)));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              xb[c] = fmaf(xb[c], lm.in_scale,
+                           -slope2 * fabsf(pos0 - static_cast<float>(b * 32 + c)));
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < kKeys; ++j)
-            x[j] = fmaf(x[j], lm.in_scale, -slope2 * fabsf(pos0 - static_cast<float>(j)));
         }
         if (edge) {
 #pragma unroll
-          for (int j = 0; j < kKeys; ++j) {
-            const int jg = key0 + j;
+          for (int c = 0; c < 64; ++c) {
+            const int jg = key0 + c;
             bool adm = jg < t.Lk;
             if (masked) adm = adm && admissible(p, t.Lq, t.Lk, i_loc, jg);
-            x[j] = adm ? x[j] : -INFINITY;
+            x[c] = adm ? x[c] : -INFINITY;
           }
         }
+        float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < kKeys; ++j) mx = fmaxf(mx, x[j]);
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, x[c]);
+        // the row max over both halves of the tile
+        float* mxs = sMax + (gg & 1) * 256;
+        mxs[half * 128 + r] = mx;
+        if (!(ok = warp_exchange(&bars->mx_x[gg & 1], (gg >> 1) & 1, s_abort))) break;
+        mx = fmaxf(mx, mxs[(half ^ 1) * 128 + r]);
         const float m_new = fmaxf(m_run, mx);
         const bool need = m_new > m_run + kRescale;
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.f;
         if (jj > 0 && __any_sync(0xffffffffu, need)) {
           // O must absorb the new max: wait for the previous P V, then scale
+          // this half's 80 columns
           const uint32_t gp = gg - 1;
           if (!(ok = mbar_wait_warp(&bars->s_free[gp & 1], (gp >> 1) & 1, s_abort))) break;
           tc_fence_after();
+          const uint32_t ob = tmem + kColO + half * 80 + lane_addr;
 #pragma unroll 1
-          for (int c = 0; c < kHeadDim / 32; ++c) {
-            float o[32];
-            tmem_ld32(tmem + kColO + lane_addr + c * 32, o);
+          for (int c = 0; c < 3; ++c) {  // columns 0..31, 32..63, 48..79 (overlap is harmless:
+            float o[32];                 // the overlapping 16 are scaled only once below)
+            tmem_ld32(ob + (c < 2 ? c * 32 : 48), o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem + kColO + lane_addr + c * 32, o);
+            for (int i = 0; i < 32; ++i)
+              if (c < 2 || i >= 16) o[i] *= alpha;
+            tmem_st32(ob + (c < 2 ? c * 32 : 48), o);
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
         if (need) {
           l *= alpha;
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        uint32_t pk[kKeys / 2];
+        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < kKeys; j += 2) {
-          const float p0 = ex2_approx(x[j] - m_use);
-          const float p1 = ex2_approx(x[j + 1] - m_use);
-          l += p0 + p1;
-          pk[j >> 1] = Pack<BF16>::two(p0, p1);
+        for (int c = 0; c < 64; ++c) x[c] = ex2_approx(x[c] - m_use);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          l += x[c] + x[c + 1];
+          pk[c >> 1] = Pack<BF16>::two(x[c], x[c + 1]);
         }
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c)
-          tmem_st16(sb + c * 16, *reinterpret_cast<uint32_t(*)[16]>(pk + c * 16));
+        // P pairs over the first 32 columns of this half's own (already read) S region
+        tmem_st16(sb, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(sb + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -327,34 +384,43 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       }
       if (!ok) break;
       g += n;
-      // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2
+      // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2; each half 80 features
+      float* ls = sSum + (tcount & 1) * 256;
+      ls[half * 128 + r] = l;
+      if (!(ok = warp_exchange(&bars->l_x[tcount & 1], (tcount >> 1) & 1, s_abort))) break;
+      const float lt = l + ls[(half ^ 1) * 128 + r];
       if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      if (row_valid)
+      const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
+      if (row_valid && half == 0)
         p.lse[static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h] =
-            (l > 0.f) ? (m_run + log2f(l)) * kLn2 : -INFINITY;
-      uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                       static_cast<int64_t>(t.q0 + i_loc) * p.out_ts +
-                       static_cast<int64_t>(h) * p.out_hs;
-#pragma unroll 1
-      for (int c = 0; c < kHeadDim / 32; ++c) {
-        float o[32];
-        tmem_ld32(tmem + kColO + lane_addr + c * 32, o);
+            (lt > 0.f) ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+      const uint32_t ob = tmem + kColO + half * 80 + lane_addr;
+      float o[80];
+      tmem_ld32(ob, *reinterpret_cast<float(*)[32]>(o));
+      tmem_ld32(ob + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+      {
+        float tail[32];
+        tmem_ld32(ob + 48, tail);  // columns 48..79 (x32 load; 48..63 already held)
         tmem_wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float w[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = n > 0 ? o[8 * u + i] * inv : 0.f;
-            *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = pack8<BF16>(w);
-          }
-        }
+        for (int i = 0; i < 16; ++i) o[64 + i] = tail[16 + i];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_empty);
+      if (row_valid) {
+        uint16_t* orow = static_cast<uint16_t*>(p.out) +
+                         static_cast<int64_t>(t.q0 + i_loc) * p.out_ts +
+                         static_cast<int64_t>(h) * p.out_hs + half * 80;
+#pragma unroll
+        for (int u = 0; u < 10; ++u) {
+          float w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = n > 0 ? o[8 * u + i] * inv : 0.f;
+          *reinterpret_cast<uint4*>(orow + u * 8) = pack8<BF16>(w);
+        }
+      }
     }
   }
 
@@ -364,16 +430,17 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int grid, cudaStream_t s) {
+cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqt,
+                       const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
+                       int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = fwd_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tk, tv);
+    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tqt, tk, tkt, tv);
   } else {
     auto k = fwd_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tk, tv);
+    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tqt, tk, tkt, tv);
   }
   return cudaGetLastError();
 }

@@ -284,7 +284,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(0);
   if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(1);
-  if (launch_fwd(p, tq, tk, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_fwd(p, tq, tqt, tk, tkt, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);

@@ -84,6 +84,19 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
+// Exchange point among warps: every lane's prior shared-memory writes become
+// visible to the other warps that arrive on `bar` (an mbarrier counting one
+// arrival per warp), then the warp waits for the phase with the time limit
+// of mbar_wait.  Unlike bar.sync, a warp that gives up never leaves the
+// others blocked for good.
+__device__ __forceinline__ bool warp_exchange(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort) {
+  __threadfence_block();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  return mbar_wait_warp(bar, parity, abort);
+}
+
 // ---------------------------------------------------------------- TMA loads
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -151,10 +164,6 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
   return d;
 }
 
-// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 // Instruction descriptor of tcgen05.mma.kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
