@@ -11,12 +11,16 @@ constexpr int kHeadDim = 160;
 constexpr int kChunk = 64;        // elements per 128-byte swizzled row
 constexpr int kChunks = 3;        // 64-wide chunks covering 160 features
 constexpr int kRowsQ = 128;       // query rows per forward / dq tile
-constexpr int kRowsKV = 64;       // query rows per dk/dv inner step
 constexpr int kKeys = 128;        // keys per tile
-constexpr int kThreads = 128;     // one thread per TMEM lane / tile row
+constexpr int kThreads = 384;     // warpgroup 0: loads + MMA issue; warpgroups 1-2: elementwise
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
+// warpgroup 0 gives registers up to the two elementwise warpgroups.
+constexpr int kRegsLow = 96;
+constexpr int kRegsHigh = 200;
+static_assert(4 * kRegsLow + 8 * kRegsHigh <= 12 * 168, "register split exceeds the launch");
 
-// Query rows of a tile are (token, head) pairs: kG consecutive heads of one
-// head group times 128/kG (or 64/kG) consecutive tokens, row r = token*G + head.
+// Query rows of a tile are (token, head) pairs: G consecutive heads of one
+// head group times 128/G consecutive tokens, row r = token*G + head.
 struct Params {
   int dtype;  // 0 fp16, 1 bf16
   int B, Hq, G;

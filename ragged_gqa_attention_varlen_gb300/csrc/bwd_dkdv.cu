@@ -8,25 +8,30 @@
 // addressed").
 //
 // One CTA owns 128 keys of one sequence and keeps their dK and dV
-// accumulators in TMEM (2 x 160 fp32 columns) while it walks every 64-row
-// query step (64/G tokens x G heads) of the sequence in a fixed order, so the
-// reduction order over heads and queries never changes: no atomics, bitwise
-// repeatable.  Per query step, keys in the MMA M dimension:
-//   S^T  = K Q^T, dP^T = V dO^T      M=128 N=64 K=160, shared-memory operands
-//   P^T, dS^T                        elementwise warps (thread = key), written
-//                                    back into TMEM as 16-bit pairs
-//   dV  += P^T dO, dK += dS^T Q      M=128 N=160 K=64, A operand from TMEM
+// accumulators in TMEM (2 x 160 fp32 columns) while it walks every 128-row
+// query step (128/G tokens x G heads, the forward's query tile) of the
+// sequence in a fixed order, so the reduction order over heads and queries
+// never changes: no atomics, bitwise repeatable.  Per query step, keys in the
+// MMA M dimension (every MMA has N >= 128, which keeps the shared-memory
+// operand traffic within what the tensor core can consume at full rate):
+//   S^T  = K Q^T        M=128 N=128 K=160 -> TMEM columns [320, 448)
+//   P^T                 elementwise warps; 16-bit pairs over read S^T columns
+//   dP^T = V dO^T       M=128 N=128 K=160 -> TMEM columns [384, 512), issued as
+//                       soon as S^T has been read (it overlaps S^T's upper half)
+//   dS^T                elementwise warps; 16-bit pairs over read dP^T columns
+//   dV  += P^T dO, dK += dS^T Q      M=128 N=160 K=128, A operand from TMEM
 //
-// Warp roles (320 threads): warp 0 loads (K, V once per key tile; Q and dO
-// through a 3-stage ring), warp 1 issues the MMAs, warps 2-9 compute P^T and
-// dS^T and write dk/dv -- two warps per TMEM lane quadrant, each taking half
-// of the step's 64 query columns, so every SM sub-partition has two warps to
-// hide MUFU and load latency.  They also fetch the next step's per-column
-// scalars (lse, D, slope, aligned key position) while the current step runs.  S^T is
-// double-buffered so S^T of the next step runs while this step's elementwise
-// work is in flight.  K and V keep their last 32 features in a 64-byte-
-// swizzled chunk (they are only K-major A operands here), which leaves room
-// for the third Q/dO stage.
+// Warp roles (384 threads, 12 warps): warp 0 loads (K, V once per key tile; Q through
+// two slots, dO through one), warp 1 issues the MMAs, warps 4-11 compute P^T
+// and dS^T and write dk/dv -- two warps per TMEM lane quadrant, each taking
+// 64 of the step's 128 query columns.  They also fetch the next step's
+// per-column scalars (lse, D, slope, aligned key position) while the current
+// step runs.  K and V are only K-major operands here and keep their last 32
+// features in a 64-byte-swizzled chunk; Q and dO are also MN-major operands
+// (of dK and dV) and stay in three 128-byte-swizzled chunks.
+// Warps 2-3 only complete warpgroup 0, which hands most of its registers to
+// the elementwise warpgroups (setmaxnreg), so those can keep every column's
+// MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
 #include "common.cuh"
 #include "sched.cuh"
@@ -34,40 +39,36 @@
 namespace attn {
 
 namespace kv {
-constexpr int kThreadsKV = 320;
-constexpr int kStages = 3;
-constexpr uint32_t kTile = 16384;   // 64-feature chunk of a 128-key tile
-constexpr uint32_t kTail = 8192;    // features 128..159 of a 128-key tile (64 B rows)
+constexpr int kThreadsKV = kThreads;  // 12 warps
+constexpr uint32_t kTile = 16384;   // 64-feature chunk of 128 rows
+constexpr uint32_t kTail = 8192;    // features 128..159 of 128 rows (64-byte rows)
 constexpr uint32_t kKV = 2 * kTile + kTail;
-constexpr uint32_t kTileQ = 8192;   // 64-feature chunk of a 64-row query step
+constexpr uint32_t kTile3 = 3 * kTile;
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kKV;
-constexpr uint32_t kOffStage = 2 * kKV;             // stages of (Q, dO)
-constexpr uint32_t kStage = 6 * kTileQ;             // Q 3 chunks + dO 3 chunks
-constexpr uint32_t kOffCol = kOffStage + kStages * kStage;  // 2 buffers of scalars
-constexpr uint32_t kColBytes = 4 * 64 * 4;
-constexpr uint32_t kOffBar = kOffCol + 2 * kColBytes;
+constexpr uint32_t kOffQ = 2 * kKV;              // two Q slots
+constexpr uint32_t kOffDO = kOffQ + 2 * kTile3;  // one dO slot
+constexpr uint32_t kOffCol = kOffDO + kTile3;    // the step's column scalars
+constexpr uint32_t kOffBar = kOffCol + 4 * 128 * 4;
 constexpr uint32_t kSmem = kOffBar + 256;  // the dynamic base is checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDV = 0;
 constexpr uint32_t kColDK = 160;
-constexpr uint32_t kColS = 320;    // two 64-column S^T buffers: [320,384), [384,448)
-constexpr uint32_t kColP = 448;    // dP^T: [448, 512)
+constexpr uint32_t kColS = 320;  // S^T: [320, 448); P^T pairs: [320, 384)
+constexpr uint32_t kColP = 384;  // dP^T: [384, 512); dS^T pairs: [384,416) and [448,480)
 
-struct Cols {  // per-column scalars of one query step
-  float lse2[64];   // lse * log2(e); +inf where no P exists (row outside / empty)
-  float D[64];
-  float slope2[64];  // slope * log2(e)
-  float pos[64];     // i + Lk - Lq (the key aligned with query row i)
+struct Cols {  // per-column scalars of one query step (column = token * G + head)
+  float lse2[128];    // lse * log2(e); +inf where no P exists (row outside / empty)
+  float D[128];
+  float slope2[128];  // slope * log2(e)
+  float pos[128];     // i + Lk - Lq (the key aligned with query row i)
 };
 
 struct Bars {
   uint64_t kv_full, kv_empty;
-  uint64_t st_full[kStages], st_empty[kStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t dp_full, dp_free, p_full;
-  uint64_t acc_full, acc_empty, drain;
-  uint64_t cols_x[2];  // per-step scalars published (one arrival per elementwise warp)
+  uint64_t q_full[2], q_empty[2], do_full, do_empty;
+  uint64_t s_full, s_read, dp_full, p_full, ds_full, dk_done;
+  uint64_t acc_full, acc_empty, cols_x, drain;
 };
 }  // namespace kv
 
@@ -89,7 +90,8 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
   uint8_t* sm = smem_raw;
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
-  uint8_t* sStage = sm + kOffStage;
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sDO = sm + kOffDO;
   Cols* cols = reinterpret_cast<Cols*>(sm + kOffCol);
   Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 1);
@@ -114,22 +116,22 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->st_full[s], 1);
-      mbar_init(&bars->st_empty[s], 1);
-    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 1);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
     }
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_read, 8);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 1);
     mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
+    mbar_init(&bars->cols_x, 8);
     mbar_init(&bars->drain, 1);
-    mbar_init(&bars->cols_x[0], 8);
-    mbar_init(&bars->cols_x[1], 8);
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -142,9 +144,13 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int G = p.G;
-  const int step_tok = kRowsKV / G;
+  const int step_tok = kRowsQ / G;
   const int ngroups = p.Hq / G;
 
+  // Each role runs inside the branch that set its register budget, so the
+  // compiler allocates each branch against its own budget.
+  if (warp < 4) {
+  warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -154,7 +160,8 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
       prefetch_tensormap(&tv);
       prefetch_tensormap(&tkt);
       prefetch_tensormap(&tvt);
-      uint32_t armed = 0;  // stage fills armed
+      uint32_t g = 0;                  // query steps armed
+      uint32_t dfill = 0;              // dO fills armed
       int tcount = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
@@ -169,67 +176,49 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         }
         tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, t.k0 + t.key);
         tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, t.k0 + t.key);
-        for (int st = 0; st < nsteps; ++st, ++armed) {
-          const int s = armed % kStages;
-          const int tok0 = (st / ngroups) * step_tok;
+        for (int st = 0; st < nsteps; ++st) {
+          const int tok = t.q0 + (st / ngroups) * step_tok;
           const int hg = st % ngroups;
-          if (armed >= kStages &&
-              !(ok = mbar_wait(&bars->st_empty[s], (armed / kStages - 1) & 1, s_abort)))
-            break;
-          mbar_arrive_expect_tx(&bars->st_full[s], 6 * kTileQ);
-          uint8_t* dst = sStage + s * kStage;
-          for (int c = 0; c < 3; ++c) {
-            tma_load_3d(dst + c * kTileQ, &tq, &bars->st_full[s], c * kChunk, hg * G, t.q0 + tok0);
-            tma_load_3d(dst + (3 + c) * kTileQ, &tdo, &bars->st_full[s], c * kChunk, hg * G,
-                        t.q0 + tok0);
-          }
+          const int s = g & 1;
+          // Q of step g (its slot was last read by dK of step g - 2)
+          if (g >= 2 && !(ok = mbar_wait(&bars->q_empty[s], ((g - 2) >> 1) & 1, s_abort))) break;
+          mbar_arrive_expect_tx(&bars->q_full[s], kTile3);
+          for (int c = 0; c < 3; ++c)
+            tma_load_3d(sQ + s * kTile3 + c * kTile, &tq, &bars->q_full[s], c * kChunk, hg * G, tok);
+          ++g;
+          // dO of the step (its slot was last read by dV of the previous step)
+          if (dfill >= 1 && !(ok = mbar_wait(&bars->do_empty, (dfill - 1) & 1, s_abort))) break;
+          mbar_arrive_expect_tx(&bars->do_full, kTile3);
+          for (int c = 0; c < 3; ++c)
+            tma_load_3d(sDO + c * kTile, &tdo, &bars->do_full, c * kChunk, hg * G, tok);
+          ++dfill;
         }
       }
       if (*s_abort) {
         if (tcount > 0) drain_wait_kv(&bars->kv_full, (tcount - 1) & 1);
-        for (uint32_t f = armed > kStages ? armed - kStages : 0; f < armed; ++f)
-          drain_wait_kv(&bars->st_full[f % kStages], (f / kStages) & 1);
+        for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f)
+          drain_wait_kv(&bars->q_full[f & 1], (f >> 1) & 1);
+        if (dfill > 0) drain_wait_kv(&bars->do_full, (dfill - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(128, 64, BF16, false, false);
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t kIdG = idesc_f16(128, kHeadDim, BF16, false, true);
-      const uint32_t kb = smem_addr(sK), vb = smem_addr(sV);
-      uint32_t g = 0;
-      int tcount = 0;
-      bool ok = true;
-      // A = K or V (features 0..127 in 128-byte-swizzled chunks, 128..159 in
-      // a 64-byte-swizzled chunk); B = the step's Q or dO chunks.
+      const uint32_t kb = smem_addr(sK), vb = smem_addr(sV), db = smem_addr(sDO);
+      // A = K or V: features 0..127 in 128-byte-swizzled chunks, 128..159 in a
+      // 64-byte-swizzled chunk.  B = the step's Q or dO (three 128-byte chunks).
       auto a_desc = [&](uint32_t base, int k) -> uint64_t {
         return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
                      : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
       };
-      auto issue_st = [&](uint32_t gs) -> bool {  // S^T = K Q^T for step gs
-        if (!mbar_wait(&bars->st_full[gs % kStages], (gs / kStages) & 1, s_abort)) return false;
-        if (gs >= 2 && !mbar_wait(&bars->s_free[gs & 1], ((gs - 2) >> 1) & 1, s_abort))
-          return false;
-        tc_fence_after();
-        const uint32_t qb = smem_addr(sStage + (gs % kStages) * kStage);
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + kColS + (gs & 1) * 64, a_desc(kb, k),
-                  sdesc_sw128(qb + (k >> 2) * kTileQ + (k & 3) * 32, 16, 1024), kIdS, k > 0);
-        umma_commit(&bars->s_full[gs & 1]);
-        return true;
+      auto b_desc = [&](uint32_t base, int k) -> uint64_t {
+        return sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
       };
-      auto issue_dpt = [&](uint32_t gs) -> bool {  // dP^T = V dO^T for step gs
-        if (gs >= 1 && !mbar_wait(&bars->dp_free, (gs - 1) & 1, s_abort)) return false;
-        tc_fence_after();
-        const uint32_t db = smem_addr(sStage + (gs % kStages) * kStage + 3 * kTileQ);
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + kColP, a_desc(vb, k),
-                  sdesc_sw128(db + (k >> 2) * kTileQ + (k & 3) * 32, 16, 1024), kIdS, k > 0);
-        umma_commit(&bars->dp_full);
-        return true;
-      };
+      uint32_t g = 0;
+      int tcount = 0;
+      bool ok = true;
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
         KTile t;
         ktile_decode(p, item, t);
@@ -241,35 +230,51 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
           mbar_arrive(&bars->acc_full);
           continue;
         }
-        if (!(ok = issue_st(g)) || !(ok = issue_dpt(g))) break;
         for (int st = 0; st < nsteps; ++st) {
           const uint32_t gg = g + st;
-          if (st + 1 < nsteps && !(ok = issue_st(gg + 1))) break;
+          const uint32_t qb = smem_addr(sQ + (gg & 1) * kTile3);
+          // S^T = K Q^T, once the previous step's dK (last reader of the
+          // region) is done
+          if (!(ok = mbar_wait(&bars->q_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
+          if (gg >= 1 && !(ok = mbar_wait(&bars->dk_done, (gg - 1) & 1, s_abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            umma_ss(tmem + kColS, a_desc(kb, k), b_desc(qb, k), kIdS, k > 0);
+          umma_commit(&bars->s_full);
+          // dP^T = V dO^T over S^T's upper half once S^T has been read
+          if (!(ok = mbar_wait(&bars->s_read, gg & 1, s_abort))) break;
+          if (!(ok = mbar_wait(&bars->do_full, gg & 1, s_abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            umma_ss(tmem + kColP, a_desc(vb, k), b_desc(db, k), kIdS, k > 0);
+          umma_commit(&bars->dp_full);
+          // dV += P^T dO; query rows 16k..16k+15 are pair columns
+          // 320 + 32*(k/4) + 8*(k%4)
           if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
           if (st == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
             break;
           tc_fence_after();
-          const uint32_t sb = smem_addr(sStage + (gg % kStages) * kStage);
-          const uint32_t pa = tmem + kColS + (gg & 1) * 64;
-          // query rows 16k..16k+15 of the step: half k/2, pair column 8*(k%2)
 #pragma unroll
-          for (int k = 0; k < kRowsKV / 16; ++k)  // dV += P^T dO
-            umma_ts(tmem + kColDV, pa + (k >> 1) * 32 + (k & 1) * 8,
-                    sdesc_sw128(sb + 3 * kTileQ + k * 2048, kTileQ, 1024), kIdG,
-                    (st > 0 || k > 0));
+          for (int k = 0; k < kRowsQ / 16; ++k)
+            umma_ts(tmem + kColDV, tmem + kColS + (k >> 2) * 32 + (k & 3) * 8,
+                    sdesc_sw128(db + k * 2048, kTile, 1024), kIdG, (st > 0 || k > 0));
+          umma_commit(&bars->do_empty);
+          // dK += dS^T Q; query rows 16k..16k+15 are pair columns
+          // 384 + 64*(k/4) + 8*(k%4)
+          if (!(ok = mbar_wait(&bars->ds_full, gg & 1, s_abort))) break;
+          tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kRowsKV / 16; ++k)  // dK += dS^T Q
-            umma_ts(tmem + kColDK, tmem + kColP + (k >> 1) * 32 + (k & 1) * 8,
-                    sdesc_sw128(sb + k * 2048, kTileQ, 1024), kIdG, (st > 0 || k > 0));
-          umma_commit(&bars->s_free[gg & 1]);
-          umma_commit(&bars->dp_free);
-          umma_commit(&bars->st_empty[gg % kStages]);
+          for (int k = 0; k < kRowsQ / 16; ++k)
+            umma_ts(tmem + kColDK, tmem + kColP + (k >> 2) * 64 + (k & 3) * 8,
+                    sdesc_sw128(qb + k * 2048, kTile, 1024), kIdG, (st > 0 || k > 0));
+          umma_commit(&bars->dk_done);
+          umma_commit(&bars->q_empty[gg & 1]);
           if (st == nsteps - 1) {
             umma_commit(&bars->acc_full);
             umma_commit(&bars->kv_empty);
-          } else if (!(ok = issue_dpt(gg + 1))) {
-            break;
           }
         }
         g += nsteps;
@@ -277,24 +282,25 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
       umma_commit(&bars->drain);
       drain_wait_kv(&bars->drain, 0);
     }
+  }
   } else {
+  warpgroup_reg_alloc<kRegsHigh>();
+  {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;  // which 32 of the step's 64 query columns
+    const int half = (warp - 4) >> 2;  // query columns [64*half, 64*half + 64)
     const int r = quad * 32 + lane;    // key within the tile (TMEM lane)
-    const int e = (warp - 2) * 32 + lane;
+    const int e = (warp - 4) * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
     const bool masked = masking(p);
     const int wr = p.causal ? 0 : p.wr;
-    // Threads 0..127 of this role also fetch one scalar column of a query
-    // step: 0..63 the lse, slope and aligned position of column e, 64..127
-    // the D of column e - 64.
-    const int lc = e & 63;
-    const bool fetcher = e < 128;
-    const bool loads_d = e >= 64;
+    // Each thread also fetches one scalar column of a query step: threads
+    // 0..127 the lse, slope and aligned position of column e, 128..255 the D
+    // of column e - 128.
+    const int lc = e & 127;
+    const bool loads_d = e >= 128;
     auto fetch = [&](const KTile& t, int st, float& a, float& b, float& c) {
-      if (!fetcher) return;
       const int i = (st / ngroups) * step_tok + lc / G;
       const int h = (st % ngroups) * G + lc % G;
       const int64_t ri = static_cast<int64_t>(t.q0 + i) * p.Hq + h;
@@ -307,14 +313,13 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         c = static_cast<float>(i + t.Lk - t.Lq);
       }
     };
-    auto publish = [&](Cols* cs, float a, float b, float c) {
-      if (!fetcher) return;
+    auto publish = [&](float a, float b, float c) {
       if (loads_d) {
-        cs->D[lc] = a;
+        cols->D[lc] = a;
       } else {
-        cs->lse2[lc] = a;
-        cs->slope2[lc] = b;
-        cs->pos[lc] = c;
+        cols->lse2[lc] = a;
+        cols->slope2[lc] = b;
+        cols->pos[lc] = c;
       }
     };
     uint32_t g = 0;
@@ -326,90 +331,107 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
       const int nsteps = ((t.Lq + step_tok - 1) / step_tok) * ngroups;
       const int j = t.key + r;
       const float jf = static_cast<float>(j);
-      if (nsteps > 0) {
-        float a = 0.f, b = 0.f, c = 0.f;
-        fetch(t, 0, a, b, c);
-        publish(cols + (g & 1), a, b, c);
-        if (!(ok = warp_exchange(&bars->cols_x[g & 1], (g >> 1) & 1, s_abort))) break;
-      }
+      float na = 0.f, nb = 0.f, nc = 0.f;
+      if (nsteps > 0) fetch(t, 0, na, nb, nc);
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
-        const Cols* cs = cols + (gg & 1);
-        const bool more = st + 1 < nsteps;
-        float na = 0.f, nb = 0.f, nc = 0.f;
-        if (more) fetch(t, st + 1, na, nb, nc);  // lands while this step runs
-        const uint32_t sbuf = tmem + kColS + (gg & 1) * 64 + half * 32 + lane_addr;
-        const uint32_t pbuf = tmem + kColP + half * 32 + lane_addr;
-        // this half's 32 columns of the per-column scalars
-        const float4* s_l2 = reinterpret_cast<const float4*>(cs->lse2 + half * 32);
-        const float4* s_sl = reinterpret_cast<const float4*>(cs->slope2 + half * 32);
-        const float4* s_ps = reinterpret_cast<const float4*>(cs->pos + half * 32);
-        const float4* s_d = reinterpret_cast<const float4*>(cs->D + half * 32);
-        if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
+        // publish this step's scalars into the single scalar buffer once every
+        // warp is done with the previous step's (its dS^T, the last use, is
+        // signalled by ds_full of that step)
+        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->ds_full, (gg - 1) & 1, s_abort))) break;
+        publish(na, nb, nc);
+        if (!(ok = warp_exchange(&bars->cols_x, gg & 1, s_abort))) break;
+        if (st + 1 < nsteps) fetch(t, st + 1, na, nb, nc);  // lands while this step runs
+        const float4* s_l2 = reinterpret_cast<const float4*>(cols->lse2 + half * 64);
+        const float4* s_sl = reinterpret_cast<const float4*>(cols->slope2 + half * 64);
+        const float4* s_ps = reinterpret_cast<const float4*>(cols->pos + half * 64);
+        const float4* s_d = reinterpret_cast<const float4*>(cols->D + half * 64);
+        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
         tc_fence_after();
-        float x[32];
-        tmem_ld32(sbuf, x);
+        float x[64];
+        const uint32_t sbuf = tmem + kColS + half * 64 + lane_addr;
+        tmem_ld32(sbuf, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(sbuf + 32, *reinterpret_cast<float(*)[32]>(x + 32));
         tmem_wait_ld();
-        // Batched so that dependent MUFU results are 32 instructions apart:
-        // all tanh, then all biases and exponent arguments, then all exp2.
-        float th[32], z[32];
-        if (lm.capped) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_read);
+        // P and P (1 - tanh^2), two batches of 32 columns: all tanh, then the
+        // exponent arguments, then all exp2
+        uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) th[c] = tanh_approx(x[c] * lm.in_scale);
-        }
+        for (int b = 0; b < 2; ++b) {
+          float* xb = x + b * 32;
+          float th[32];
+          if (lm.capped) {
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l2 = s_l2[q4], sl = s_sl[q4], ps = s_ps[q4];
-          const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
-          const float slv[4] = {sl.x, sl.y, sl.z, sl.w};
-          const float psv[4] = {ps.x, ps.y, ps.z, ps.w};
+            for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
+          }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = q4 * 4 + u;
-            // base-2 logit minus lse: t*c*log2e - slope2*|pos - j| - lse2
-            const float bias = fmaf(-slv[u], fabsf(psv[u] - jf), -l2v[u]);
-            z[c] = lm.capped ? fmaf(th[c], lm.out_scale, bias) : fmaf(x[c], lm.in_scale, bias);
-            if (masked) {
-              const bool adm = (p.wl < 0 || jf >= psv[u] - static_cast<float>(p.wl)) &&
-                               (wr < 0 || jf <= psv[u] + static_cast<float>(wr));
-              z[c] = adm ? z[c] : -INFINITY;
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l2 = s_l2[b * 8 + q4], sl = s_sl[b * 8 + q4], ps = s_ps[b * 8 + q4];
+            const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+            const float slv[4] = {sl.x, sl.y, sl.z, sl.w};
+            const float psv[4] = {ps.x, ps.y, ps.z, ps.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = q4 * 4 + u;
+              // base-2 logit minus lse: t*c*log2e - slope2*|pos - j| - lse2
+              const float bias = fmaf(-slv[u], fabsf(psv[u] - jf), -l2v[u]);
+              float z = lm.capped ? fmaf(th[c], lm.out_scale, bias)
+                                  : fmaf(xb[c], lm.in_scale, bias);
+              if (masked) {
+                const bool adm = (p.wl < 0 || jf >= psv[u] - static_cast<float>(p.wl)) &&
+                                 (wr < 0 || jf <= psv[u] + static_cast<float>(wr));
+                z = adm ? z : -INFINITY;
+              }
+              xb[c] = z;
             }
           }
-        }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) z[c] = ex2_approx(z[c]);  // P
-        uint32_t pk[16];
+          for (int c = 0; c < 32; ++c) xb[c] = ex2_approx(xb[c]);  // P
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          pk[c >> 1] = Pack<BF16>::two(z[c], z[c + 1]);
-          // P * (1 - tanh^2): dS = this * (dP - D)
-          x[c] = lm.capped ? z[c] * fmaf(-th[c], th[c], 1.f) : z[c];
-          x[c + 1] = lm.capped ? z[c + 1] * fmaf(-th[c + 1], th[c + 1], 1.f) : z[c + 1];
-        }
-        tmem_st16(sbuf, pk);  // P^T pairs over this half's own (already read) columns
-        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
-        tc_fence_after();
-        float d[32];
-        tmem_ld32(pbuf, d);
-        tmem_wait_ld();
+          for (int c = 0; c < 32; c += 2) pk[b * 16 + (c >> 1)] = Pack<BF16>::two(xb[c], xb[c + 1]);
+          if (lm.capped) {
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 dd = s_d[q4];
-          pk[q4 * 2] = Pack<BF16>::two(x[q4 * 4] * (d[q4 * 4] - dd.x),
-                                       x[q4 * 4 + 1] * (d[q4 * 4 + 1] - dd.y));
-          pk[q4 * 2 + 1] = Pack<BF16>::two(x[q4 * 4 + 2] * (d[q4 * 4 + 2] - dd.z),
-                                           x[q4 * 4 + 3] * (d[q4 * 4 + 3] - dd.w));
+            for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);
+          }
         }
-        tmem_st16(pbuf, pk);
+        // P^T pairs: this half's 64 columns -> 32 pair columns at 320 + 32*half,
+        // which may still hold S^T of the other half until every warp has read it
+        if (!(ok = mbar_wait_warp(&bars->s_read, gg & 1, s_abort))) break;
+        const uint32_t pdst = tmem + kColS + half * 32 + lane_addr;
+        tmem_st16(pdst, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(pdst + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
-        if (more) {
-          publish(cols + ((gg + 1) & 1), na, nb, nc);
-          if (!(ok = warp_exchange(&bars->cols_x[(gg + 1) & 1], ((gg + 1) >> 1) & 1, s_abort)))
-            break;
+        // dS^T = P (1 - tanh^2) (dP - D), written over this half's own dP^T columns
+        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        const uint32_t pbuf = tmem + kColP + half * 64 + lane_addr;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float d[32];
+          tmem_ld32(pbuf + cc * 32, d);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 dd = s_d[cc * 8 + q4];
+            const float* xx = x + cc * 32 + q4 * 4;
+            pk[cc * 16 + q4 * 2] = Pack<BF16>::two(xx[0] * (d[q4 * 4] - dd.x),
+                                                   xx[1] * (d[q4 * 4 + 1] - dd.y));
+            pk[cc * 16 + q4 * 2 + 1] = Pack<BF16>::two(xx[2] * (d[q4 * 4 + 2] - dd.z),
+                                                       xx[3] * (d[q4 * 4 + 3] - dd.w));
+          }
         }
+        tmem_st16(pbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(pbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ds_full);
       }
       if (!ok) break;
       g += nsteps;
@@ -442,23 +464,24 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
     }
   }
 
+  }
   __syncthreads();
   if (tid == 0 && *s_abort) atomicOr(p.status, ATTN_DEV_TIMEOUT_DKDV);
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq64, const CUtensorMap& tdo64,
+cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tkt,
                         const CUtensorMap& tvt, int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = dkdv_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kv::kThreadsKV, kv::kSmem, s>>>(p, tq64, tdo64, tk, tv, tkt, tvt);
+    k<<<grid, kv::kThreadsKV, kv::kSmem, s>>>(p, tq, tdo, tk, tv, tkt, tvt);
   } else {
     auto k = dkdv_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kv::kThreadsKV, kv::kSmem, s>>>(p, tq64, tdo64, tk, tv, tkt, tvt);
+    k<<<grid, kv::kThreadsKV, kv::kSmem, s>>>(p, tq, tdo, tk, tv, tkt, tvt);
   }
   return cudaGetLastError();
 }

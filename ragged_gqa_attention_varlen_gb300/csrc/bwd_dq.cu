@@ -13,14 +13,17 @@
 //                                     dP_j as 16-bit pairs
 //   dQ  += dS_j K_j                   M=128 N=160 K=128, A operand from TMEM
 //
-// Warp roles (320 threads): warp 0 loads (Q, dO once per tile; K through two
-// slots, V through one), warp 1 issues the MMAs, warps 2-9 do the elementwise
+// Warp roles (384 threads, 12 warps): warp 0 loads (Q, dO once per tile; K through two
+// slots, V through one), warp 1 issues the MMAs, warps 4-11 do the elementwise
 // work (two warps per TMEM lane quadrant, each taking 64 of the 128 keys).
 // The elementwise warps release S_j as soon as they have read it, so S_{j+1}
 // runs on the tensor core while dS_j is still being formed.  Q, dO and V are
 // only K-major operands here and keep their last 32 features in a 64-byte-
 // swizzled chunk; K is also the MN-major operand of dQ and stays in three
 // 128-byte-swizzled chunks.
+// Warps 2-3 only complete warpgroup 0, which hands most of its registers to
+// the elementwise warpgroups (setmaxnreg), so those can keep every column's
+// MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
 #include "common.cuh"
 #include "sched.cuh"
@@ -28,7 +31,7 @@
 namespace attn {
 
 namespace dqk {
-constexpr int kThreadsDQ = 320;
+constexpr int kThreadsDQ = kThreads;  // 12 warps
 constexpr uint32_t kTile = 16384;            // 64-feature chunk of 128 rows
 constexpr uint32_t kTail = 8192;             // features 128..159 of 128 rows
 constexpr uint32_t kTailed = 2 * kTile + kTail;
@@ -120,6 +123,10 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   const uint32_t tmem = *s_tmem;
   const int G = p.G;
 
+  // Each role runs inside the branch that set its register budget, so the
+  // compiler allocates each branch against its own budget.
+  if (warp < 4) {
+  warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -242,10 +249,13 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       umma_commit(&bars->drain);
       drain_wait_dq(&bars->drain, 0);
     }
+  }
   } else {
+  warpgroup_reg_alloc<kRegsHigh>();
+  {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;  // keys [64*half, 64*half + 64) of each tile
+    const int half = (warp - 4) >> 2;  // keys [64*half, 64*half + 64) of each tile
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
@@ -371,6 +381,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     }
   }
 
+  }
   __syncthreads();
   if (tid == 0 && *s_abort) atomicOr(p.status, ATTN_DEV_TIMEOUT_DQ);
   tc_fence_after();

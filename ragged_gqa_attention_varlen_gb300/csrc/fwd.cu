@@ -11,12 +11,12 @@
 // 128-key K and V tiles.  Per key tile j:
 //   S_j = Q K_j^T         tcgen05.mma (Q, K from shared memory), fp32 in TMEM
 //   P_j = exp2(z - m)     softmax warps, one thread per row (TMEM lane); P_j
-//                         is written back over S_j as 16-bit pairs
+//                         goes to its own TMEM region as 16-bit pairs
 //   O  += P_j V_j         tcgen05.mma with P_j read from TMEM
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (lane 0: Q once per tile
+// Warp roles (384 threads, 12 warps): warp 0 issues TMA loads (lane 0: Q once per tile
 // and K through two slots; lane 1: V through two slots, so a K load never
-// waits for a V slot), warp 1 issues the MMAs, warps 2-9 run the
+// waits for a V slot), warp 1 issues the MMAs, warps 4-11 run the
 // softmax and the epilogue -- two warps per TMEM lane quadrant, each taking
 // 64 of the 128 keys of a tile (the row max is exchanged through shared
 // memory), so every SM sub-partition has two warps to hide MUFU latency.  S
@@ -34,6 +34,9 @@
 // taken relative to the stale max and stays below 2^8.  With the softcap
 // (|t| <= c) and ALiBi (<= 0) no later tile can exceed the first tile's max
 // by more than 2*c*log2(e) = 8.66, so rescales are rare.
+// Warps 2-3 only complete warpgroup 0, which hands most of its registers to
+// the elementwise warpgroups (setmaxnreg), so those can keep every column's
+// MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
 #include "common.cuh"
 #include "sched.cuh"
@@ -41,7 +44,7 @@
 namespace attn {
 
 namespace fwd {
-constexpr int kThreadsF = 320;
+constexpr int kThreadsF = kThreads;  // 12 warps
 constexpr uint32_t kTile = 16384;        // one 64-feature chunk of a 128-row tile
 constexpr uint32_t kTail = 8192;         // features 128..159 of 128 rows (64-byte rows)
 constexpr uint32_t kTailed = 2 * kTile + kTail;
@@ -54,13 +57,14 @@ constexpr uint32_t kOffSum = kOffMax + 2 * 2 * 128 * 4;     // [2 tiles][2 halve
 constexpr uint32_t kOffBar = kOffSum + 2 * 2 * 128 * 4;
 constexpr uint32_t kSmem = kOffBar + 256;  // the dynamic base is checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;          // S0: [0,128), S1: [128,256), O: [256,416)
+constexpr uint32_t kColP = 256;          // S0: [0,128), S1: [128,256), P: [256,320)
+constexpr uint32_t kColO = 320;          // O: [320, 480)
 constexpr float kRescale = 8.f;          // lazy-rescale threshold (base 2)
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t s_full[2], s_read[2], p_full[2], pv_done;
   uint64_t o_full, o_empty, drain;
   uint64_t mx_x[2], l_x[2];  // row-max and row-sum exchanges between the halves
 };
@@ -122,9 +126,10 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       mbar_init(&bars->v_full[b], 1);
       mbar_init(&bars->v_empty[b], 1);
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 1);
+      mbar_init(&bars->s_read[b], 8);
       mbar_init(&bars->p_full[b], 8);
     }
+    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
     mbar_init(&bars->drain, 1);
@@ -145,6 +150,10 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   const uint32_t tmem = *s_tmem;
   const int G = p.G;
 
+  // Each role runs inside the branch that set its register budget, so the
+  // compiler allocates each branch against its own budget.
+  if (warp < 4) {
+  warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane < 2) {
@@ -214,7 +223,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       };
       auto issue_s = [&](uint32_t gs) -> bool {
         if (!mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort)) return false;
-        if (gs >= 2 && !mbar_wait(&bars->s_free[gs & 1], ((gs - 2) >> 1) & 1, s_abort))
+        // the buffer's previous S (step gs - 2) has been read by the softmax
+        if (gs >= 2 && !mbar_wait(&bars->s_read[gs & 1], ((gs - 2) >> 1) & 1, s_abort))
           return false;
         tc_fence_after();
         const uint32_t kb = smem_addr(sK + (gs & 1) * kTailed);
@@ -253,13 +263,12 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           if (!(ok = mbar_wait(&bars->v_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
           tc_fence_after();
           const uint32_t vb = smem_addr(sV + (gg & 1) * kTile3);
-          const uint32_t pa = tmem + (gg & 1) * 128;
-          // keys 16k..16k+15: half k/4, pair column 8*(k%4) of that half's region
+          // keys 16k..16k+15: pair columns 8k..8k+7 of the P region
 #pragma unroll
           for (int k = 0; k < kKeys / 16; ++k)
-            umma_ts(tmem + kColO, pa + (k >> 2) * 64 + (k & 3) * 8,
-                    sdesc_sw128(vb + k * 2048, kTile, 1024), kIdO, (jj > 0 || k > 0));
-          umma_commit(&bars->s_free[gg & 1]);
+            umma_ts(tmem + kColO, tmem + kColP + k * 8, sdesc_sw128(vb + k * 2048, kTile, 1024),
+                    kIdO, (jj > 0 || k > 0));
+          umma_commit(&bars->pv_done);
           umma_commit(&bars->v_empty[gg & 1]);
           if (jj == n - 1) umma_commit(&bars->o_full);
         }
@@ -269,10 +278,13 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       umma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
+  }
   } else {
+  warpgroup_reg_alloc<kRegsHigh>();
+  {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;  // keys [64*half, 64*half + 64) of each tile
+    const int half = (warp - 4) >> 2;  // keys [64*half, 64*half + 64) of each tile
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
@@ -301,6 +313,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         tmem_ld32(sb, *reinterpret_cast<float(*)[32]>(x));
         tmem_ld32(sb + 32, *reinterpret_cast<float(*)[32]>(x + 32));
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_read[gg & 1]);  // S_gg may be overwritten
         const float pos0 = static_cast<float>(pos_off - key0);
         const bool edge = masked || key0 + 64 > t.Lk;
         // batched: all tanh of a 32-column group, then the logits
@@ -342,16 +357,15 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         const float m_new = fmaxf(m_run, mx);
         const bool need = m_new > m_run + kRescale;
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.f;
+        // the previous P V has finished reading the P region (and adding to O)
+        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->pv_done, (gg - 1) & 1, s_abort))) break;
+        tc_fence_after();
         if (jj > 0 && __any_sync(0xffffffffu, need)) {
-          // O must absorb the new max: wait for the previous P V, then scale
-          // this half's 80 columns
-          const uint32_t gp = gg - 1;
-          if (!(ok = mbar_wait_warp(&bars->s_free[gp & 1], (gp >> 1) & 1, s_abort))) break;
-          tc_fence_after();
+          // O must absorb the new max: scale this half's 80 columns
           const uint32_t ob = tmem + kColO + half * 80 + lane_addr;
 #pragma unroll 1
-          for (int c = 0; c < 3; ++c) {  // columns 0..31, 32..63, 48..79 (overlap is harmless:
-            float o[32];                 // the overlapping 16 are scaled only once below)
+          for (int c = 0; c < 3; ++c) {  // columns 0..31, 32..63, 48..79 (the overlapping
+            float o[32];                 // 16 are scaled once, on the second pass)
             tmem_ld32(ob + (c < 2 ? c * 32 : 48), o);
             tmem_wait_ld();
 #pragma unroll
@@ -374,9 +388,10 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           l += x[c] + x[c + 1];
           pk[c >> 1] = Pack<BF16>::two(x[c], x[c + 1]);
         }
-        // P pairs over the first 32 columns of this half's own (already read) S region
-        tmem_st16(sb, *reinterpret_cast<uint32_t(*)[16]>(pk));
-        tmem_st16(sb + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+        // this half's 64 keys -> 32 pair columns of the P region
+        const uint32_t pb = tmem + kColP + half * 32 + lane_addr;
+        tmem_st16(pb, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(pb + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -424,6 +439,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     }
   }
 
+  }
   __syncthreads();
   if (tid == 0 && *s_abort) atomicOr(p.status, ATTN_DEV_TIMEOUT_FWD);
   tc_fence_after();

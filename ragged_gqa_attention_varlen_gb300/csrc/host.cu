@@ -255,13 +255,11 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
 
   // ---- TMA tensor maps
   if (!encode_fn()) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tdo, tqt, tdot, tq64, tdo64, tk, tv, tkt, tvt;
+  CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt;
   if (!encode_q(&tq, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
       !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
       !encode_q(&tqt, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ, true) ||
       !encode_q(&tdot, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ, true) ||
-      !encode_q(&tq64, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsKV) ||
-      !encode_q(&tdo64, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsKV) ||
       !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts) ||
       !encode_kv(&tkt, dtype, k, total_k, k_ts, true) ||
       !encode_kv(&tvt, dtype, v, total_k, v_ts, true))
@@ -288,7 +286,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
-  if (launch_dkdv(p, tq64, tdo64, tk, tv, tkt, tvt, grid_k, stream) != cudaSuccess)
+  if (launch_dkdv(p, tq, tdo, tk, tv, tkt, tvt, grid_k, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(4);
   if (launch_dq(p, tq, tdo, tqt, tdot, tk, tv, tvt, grid_q, stream) != cudaSuccess)

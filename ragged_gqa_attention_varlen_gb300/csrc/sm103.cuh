@@ -293,6 +293,19 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute it).  A kernel launched with T threads at R registers each may move
+// registers from one warpgroup to the others as long as the per-warpgroup
+// counts, times 128 threads, sum to at most T * R.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2_approx(float x) {
