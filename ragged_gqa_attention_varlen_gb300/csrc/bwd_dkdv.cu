@@ -346,6 +346,26 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         const float4* s_sl = reinterpret_cast<const float4*>(cols->slope2 + half * 64);
         const float4* s_ps = reinterpret_cast<const float4*>(cols->pos + half * 64);
         const float4* s_d = reinterpret_cast<const float4*>(cols->D + half * 64);
+        // Everything that does not depend on S^T first, while S^T is being
+        // computed: the base-2 bias -slope2*|pos - j| - lse2 of each column.
+        float bias[64];
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 l2 = s_l2[q4], sl = s_sl[q4], ps = s_ps[q4];
+          const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+          const float slv[4] = {sl.x, sl.y, sl.z, sl.w};
+          const float psv[4] = {ps.x, ps.y, ps.z, ps.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float bv = fmaf(-slv[u], fabsf(psv[u] - jf), -l2v[u]);
+            if (masked) {
+              const bool adm = (p.wl < 0 || jf >= psv[u] - static_cast<float>(p.wl)) &&
+                               (wr < 0 || jf <= psv[u] + static_cast<float>(wr));
+              bv = adm ? bv : -INFINITY;
+            }
+            bias[q4 * 4 + u] = bv;
+          }
+        }
         if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
         tc_fence_after();
         float x[64];
@@ -356,46 +376,29 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_read);
-        // P and P (1 - tanh^2), two batches of 32 columns: all tanh, then the
-        // exponent arguments, then all exp2
+        // P = exp2(t*c*log2e + bias) and P (1 - tanh^2), in two batches of 32:
+        // all tanh (in place of S), then all exp2 (in place of the bias)
         uint32_t pk[32];
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           float* xb = x + b * 32;
-          float th[32];
+          float* zb = bias + b * 32;
           if (lm.capped) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
+            for (int c = 0; c < 32; ++c) xb[c] = tanh_approx(xb[c] * lm.in_scale);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) zb[c] = fmaf(xb[c], lm.out_scale, zb[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) zb[c] = fmaf(xb[c], lm.in_scale, zb[c]);
           }
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 l2 = s_l2[b * 8 + q4], sl = s_sl[b * 8 + q4], ps = s_ps[b * 8 + q4];
-            const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
-            const float slv[4] = {sl.x, sl.y, sl.z, sl.w};
-            const float psv[4] = {ps.x, ps.y, ps.z, ps.w};
+          for (int c = 0; c < 32; ++c) zb[c] = ex2_approx(zb[c]);  // P
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = q4 * 4 + u;
-              // base-2 logit minus lse: t*c*log2e - slope2*|pos - j| - lse2
-              const float bias = fmaf(-slv[u], fabsf(psv[u] - jf), -l2v[u]);
-              float z = lm.capped ? fmaf(th[c], lm.out_scale, bias)
-                                  : fmaf(xb[c], lm.in_scale, bias);
-              if (masked) {
-                const bool adm = (p.wl < 0 || jf >= psv[u] - static_cast<float>(p.wl)) &&
-                                 (wr < 0 || jf <= psv[u] + static_cast<float>(wr));
-                z = adm ? z : -INFINITY;
-              }
-              xb[c] = z;
-            }
-          }
+          for (int c = 0; c < 32; c += 2) pk[b * 16 + (c >> 1)] = Pack<BF16>::two(zb[c], zb[c + 1]);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) xb[c] = ex2_approx(xb[c]);  // P
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) pk[b * 16 + (c >> 1)] = Pack<BF16>::two(xb[c], xb[c + 1]);
-          if (lm.capped) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);
-          }
+          for (int c = 0; c < 32; ++c)  // P (1 - tanh^2): dS = this * (dP - D)
+            xb[c] = lm.capped ? zb[c] * fmaf(-xb[c], xb[c], 1.f) : zb[c];
         }
         // P^T pairs: this half's 64 columns -> 32 pair columns at 320 + 32*half,
         // which may still hold S^T of the other half until every warp has read it
@@ -407,6 +410,15 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
+        // D of each column into the (now free) bias registers before dP^T lands
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 dd = s_d[q4];
+          bias[q4 * 4] = dd.x;
+          bias[q4 * 4 + 1] = dd.y;
+          bias[q4 * 4 + 2] = dd.z;
+          bias[q4 * 4 + 3] = dd.w;
+        }
         // dS^T = P (1 - tanh^2) (dP - D), written over this half's own dP^T columns
         if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
         tc_fence_after();
@@ -417,14 +429,10 @@ __global__ void __launch_bounds__(kv::kThreadsKV, 1)
           tmem_ld32(pbuf + cc * 32, d);
           tmem_wait_ld();
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 dd = s_d[cc * 8 + q4];
-            const float* xx = x + cc * 32 + q4 * 4;
-            pk[cc * 16 + q4 * 2] = Pack<BF16>::two(xx[0] * (d[q4 * 4] - dd.x),
-                                                   xx[1] * (d[q4 * 4 + 1] - dd.y));
-            pk[cc * 16 + q4 * 2 + 1] = Pack<BF16>::two(xx[2] * (d[q4 * 4 + 2] - dd.z),
-                                                       xx[3] * (d[q4 * 4 + 3] - dd.w));
-          }
+          for (int c = 0; c < 32; c += 2)
+            pk[cc * 16 + (c >> 1)] =
+                Pack<BF16>::two(x[cc * 32 + c] * (d[c] - bias[cc * 32 + c]),
+                                x[cc * 32 + c + 1] * (d[c + 1] - bias[cc * 32 + c + 1]));
         }
         tmem_st16(pbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
         tmem_st16(pbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
