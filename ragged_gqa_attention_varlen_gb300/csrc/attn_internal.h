@@ -15,7 +15,7 @@ constexpr int kKeys = 128;        // keys per tile
 constexpr int kThreads = 384;     // warpgroup 0: loads + MMA issue; warpgroups 1-2: elementwise
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
 // warpgroup 0 gives registers up to the two elementwise warpgroups.
-constexpr int kRegsLow = 96;
+constexpr int kRegsLow = 104;
 constexpr int kRegsHigh = 200;
 static_assert(4 * kRegsLow + 8 * kRegsHigh <= 12 * 168, "register split exceeds the launch");
 
