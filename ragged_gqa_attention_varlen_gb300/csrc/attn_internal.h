@@ -64,8 +64,8 @@ cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap
                        const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
                        int grid, cudaStream_t s);
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
-cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq64, const CUtensorMap& tdo64,
-                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tkt,
+cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                        const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
                         const CUtensorMap& tvt, int grid, cudaStream_t s);
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                       const CUtensorMap& tqt, const CUtensorMap& tdot, const CUtensorMap& tk,

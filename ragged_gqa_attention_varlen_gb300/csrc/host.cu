@@ -286,7 +286,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
-  if (launch_dkdv(p, tq, tdo, tk, tv, tkt, tvt, grid_k, stream) != cudaSuccess)
+  if (launch_dkdv(p, tq, tdo, tk, tkt, tv, tvt, grid_k, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(4);
   if (launch_dq(p, tq, tdo, tqt, tdot, tk, tv, tvt, grid_q, stream) != cudaSuccess)
