@@ -93,9 +93,10 @@ struct Pair {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq,
-                const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv,
+    dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
+                const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
+                const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk2,
+                const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv2,
                 const __grid_constant__ CUtensorMap tvt) {
   using namespace kv;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -171,66 +172,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Every slot has a fill count; fill n waits for the release of fill n-1.
-    if (lane == 0) {
-      // K and V once per key tile, Q of every step through two slots
+    // The whole warp walks the fills in the order their slots are released
+    // (Q of step g after dK of step g - 2, dO of step g after dV of step
+    // g - 1); each tile's boxes are issued from separate lanes, since the
+    // load rate grows with the number of issuing threads.
+    if (lane < 4) {
+      prefetch_tensormap(&tq2);
       prefetch_tensormap(&tq);
-      prefetch_tensormap(&tk);
-      prefetch_tensormap(&tkt);
-      prefetch_tensormap(&tv);
-      prefetch_tensormap(&tvt);
-      uint32_t nkv = 0;
-      Pair nq;
-      bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x) {
-        KTile t;
-        ktile_decode(p, item, t);
-        const int nsteps = step_count(t);
-        const int key = t.k0 + t.key;
-        if (nkv > 0 && !(ok = mbar_wait(&bars->kv_empty, (nkv - 1) & 1, s_abort))) break;
-        mbar_arrive_expect_tx(&bars->kv_full, 2 * kKV);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(sK + c * kTile, &tk, &bars->kv_full, c * kChunk, key);
-          tma_load_2d(sV + c * kTile, &tv, &bars->kv_full, c * kChunk, key);
-        }
-        tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, key);
-        tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
-        ++nkv;
-        for (int st = 0; st < nsteps; ++st) {
-          const int s = (nq.c0 + nq.c1) & 1;
-          const uint32_t n = nq.bump(s);
-          if (n > 0 && !(ok = mbar_wait(&bars->q_empty[s], (n - 1) & 1, s_abort))) break;
-          const int tok = t.q0 + (st / ngroups) * step_tok;
-          const int h0 = (st % ngroups) * G;
-          mbar_arrive_expect_tx(&bars->q_full[s], kTile3);
-          for (int c = 0; c < 3; ++c)
-            tma_load_3d(sQ + s * kTile3 + c * kTile, &tq, &bars->q_full[s], c * kChunk, h0, tok);
-        }
-      }
-      if (*s_abort) {
-        if (nkv > 0) drain_wait_kv(&bars->kv_full, (nkv - 1) & 1);
-        for (int s = 0; s < 2; ++s)
-          if (nq.get(s) > 0) drain_wait_kv(&bars->q_full[s], (nq.get(s) - 1) & 1);
-      }
-    } else if (lane == 1) {
-      // dO of every step through one slot
+      prefetch_tensormap(&tdo2);
       prefetch_tensormap(&tdo);
-      uint32_t nd = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x) {
-        KTile t;
-        ktile_decode(p, item, t);
-        const int nsteps = step_count(t);
-        for (int st = 0; st < nsteps; ++st, ++nd) {
-          if (nd > 0 && !(ok = mbar_wait(&bars->do_empty, (nd - 1) & 1, s_abort))) break;
-          const int tok = t.q0 + (st / ngroups) * step_tok;
-          const int h0 = (st % ngroups) * G;
-          mbar_arrive_expect_tx(&bars->do_full, kTile3);
-          for (int c = 0; c < 3; ++c)
-            tma_load_3d(sDO + c * kTile, &tdo, &bars->do_full, c * kChunk, h0, tok);
+    } else if (lane < 8) {
+      prefetch_tensormap(&tk2);
+      prefetch_tensormap(&tkt);
+      prefetch_tensormap(&tv2);
+      prefetch_tensormap(&tvt);
+    }
+    constexpr int kPrefetchHead = 4;  // the first steps of a key tile, prefetched with K/V
+    uint32_t nkv = 0, ndo = 0;
+    Pair nq;
+    bool ok = true;
+    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x) {
+      KTile t;
+      ktile_decode(p, item, t);
+      const int nsteps = step_count(t);
+      const int key = t.k0 + t.key;
+      if (nkv > 0 && !(ok = mbar_wait_warp(&bars->kv_empty, (nkv - 1) & 1, s_abort))) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full, 2 * kKV);
+      __syncwarp();
+      if (lane == 0) tma_load_3d(sK, &tk2, &bars->kv_full, 0, key, 0);
+      if (lane == 1) tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, key);
+      if (lane == 2) tma_load_3d(sV, &tv2, &bars->kv_full, 0, key, 0);
+      if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
+      if (lane >= 4 && lane < 8) {
+        for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
+          const int ptok = t.q0 + (sp / ngroups) * step_tok;
+          const int ph0 = (sp % ngroups) * G;
+          if (lane == 4) tma_prefetch_4d(&tq2, 0, ph0, ptok, 0);
+          if (lane == 5) tma_prefetch_3d(&tq, 2 * kChunk, ph0, ptok);
+          if (lane == 6) tma_prefetch_4d(&tdo2, 0, ph0, ptok, 0);
+          if (lane == 7) tma_prefetch_3d(&tdo, 2 * kChunk, ph0, ptok);
         }
       }
-      if (*s_abort && nd > 0) drain_wait_kv(&bars->do_full, (nd - 1) & 1);
+      ++nkv;
+      // Q and dO stream from memory (a sequence's Q alone can exceed L2): the
+      // tiles of step st + kPrefetch are requested into L2 while step st is
+      // loaded, so the loads that the ring can afford to wait for hit L2.
+      constexpr int kPrefetch = 4;
+      for (int st = 0; st < nsteps; ++st, ++ndo) {
+        const int tok = t.q0 + (st / ngroups) * step_tok;
+        const int h0 = (st % ngroups) * G;
+        if (lane >= 4 && lane < 8 && st + kPrefetch < nsteps) {
+          const int sp = st + kPrefetch;
+          const int ptok = t.q0 + (sp / ngroups) * step_tok;
+          const int ph0 = (sp % ngroups) * G;
+          if (lane == 4) tma_prefetch_4d(&tq2, 0, ph0, ptok, 0);
+          if (lane == 5) tma_prefetch_3d(&tq, 2 * kChunk, ph0, ptok);
+          if (lane == 6) tma_prefetch_4d(&tdo2, 0, ph0, ptok, 0);
+          if (lane == 7) tma_prefetch_3d(&tdo, 2 * kChunk, ph0, ptok);
+        }
+        // Q of the step into slot g & 1
+        const int s = (nq.c0 + nq.c1) & 1;
+        const uint32_t n = nq.bump(s);
+        if (n > 0 && !(ok = mbar_wait_warp(&bars->q_empty[s], (n - 1) & 1, s_abort))) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->q_full[s], kTile3);
+        __syncwarp();
+        uint8_t* dq = sQ + s * kTile3;
+        if (lane == 0) tma_load_4d(dq, &tq2, &bars->q_full[s], 0, h0, tok, 0);
+        if (lane == 1) tma_load_3d(dq + 2 * kTile, &tq, &bars->q_full[s], 2 * kChunk, h0, tok);
+        // dO of the step
+        if (ndo > 0 && !(ok = mbar_wait_warp(&bars->do_empty, (ndo - 1) & 1, s_abort))) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->do_full, kTile3);
+        __syncwarp();
+        if (lane == 2) tma_load_4d(sDO, &tdo2, &bars->do_full, 0, h0, tok, 0);
+        if (lane == 3) tma_load_3d(sDO + 2 * kTile, &tdo, &bars->do_full, 2 * kChunk, h0, tok);
+      }
+    }
+    if (*s_abort && lane == 0) {
+      if (nkv > 0) drain_wait_kv(&bars->kv_full, (nkv - 1) & 1);
+      for (int s = 0; s < 2; ++s)
+        if (nq.get(s) > 0) drain_wait_kv(&bars->q_full[s], (nq.get(s) - 1) & 1);
+      if (ndo > 0) drain_wait_kv(&bars->do_full, (ndo - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -241,15 +262,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A = K or V: features 0..127 in 128-byte-swizzled chunks, 128..159 in a
       // 64-byte-swizzled chunk.  B = Q or dO, three 128-byte-swizzled chunks,
       // K-major (S^T, dP^T) or MN-major (dK, dV: N = features, K = query rows).
-      auto a_desc = [](uint32_t base, int k) -> uint64_t {
-        return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
-                     : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
+      // Descriptors are built once; each K step adds a byte offset.
+      const SDesc kA = sdesc_split(sdesc_sw128(kb, 16, 1024));
+      const SDesc kT = sdesc_split(sdesc_sw64(kb + 2 * kTile));
+      const SDesc vA = sdesc_split(sdesc_sw128(vb, 16, 1024));
+      const SDesc vT = sdesc_split(sdesc_sw64(vb + 2 * kTile));
+      const SDesc dK = sdesc_split(sdesc_sw128(db, 16, 1024));
+      const SDesc dMN = sdesc_split(sdesc_sw128(db, kTile, 1024));
+      // Q slot s: its descriptors differ from slot 0's by s * kTile3 in the address
+      const SDesc qK0 = sdesc_split(sdesc_sw128(smem_addr(sQ), 16, 1024));
+      const SDesc qMN0 = sdesc_split(sdesc_sw128(smem_addr(sQ), kTile, 1024));
+      auto qslot = [](SDesc d, uint32_t gg) { return SDesc{d.lo + (gg & 1) * (kTile3 >> 4), d.hi}; };
+      // D = A B^T over the 160 features (K-major A and B)
+      auto mma_kmajor = [&](uint32_t d, SDesc a, SDesc at, SDesc b) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
+          umma_ss_off(d, a, off, b, off, kIdS, k > 0);
+        }
+        umma_ss_off(d, at, 0, b, 2 * kTile, kIdS, 1);
+        umma_ss_off(d, at, 32, b, 2 * kTile + 32, kIdS, 1);
       };
-      auto b_desc = [](uint32_t base, int k) -> uint64_t {
-        return sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024);
-      };
-      auto mn_desc = [](uint32_t base, int k) -> uint64_t {
-        return sdesc_sw128(base + k * 2048, kTile, 1024);
+      // D (+)= X^T B over the step's 128 query rows; rows 16k..16k+15 are the
+      // pair columns 448 + 32*(k/4) + 8*(k%4)
+      auto mma_x = [&](uint32_t d, SDesc bmn, bool acc) {
+#pragma unroll
+        for (int k = 0; k < kRowsQ / 16; ++k)
+          umma_ts_off(d, tmem + kColX + (k >> 2) * 32 + (k & 3) * 8, bmn, k * 2048, kIdG,
+                      (acc || k > 0) ? 1u : 0u);
       };
       uint32_t g = 0;  // query steps of all earlier tiles
       int tcount = 0;
@@ -270,36 +310,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](uint32_t gg) -> bool {
           if (!mbar_wait(&bars->q_full[gg & 1], (gg >> 1) & 1, s_abort)) return false;
           tc_fence_after();
-          const uint32_t qb = smem_addr(sQ + (gg & 1) * kTile3);
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ss(tmem + kColSP, a_desc(kb, k), b_desc(qb, k), kIdS, k > 0);
+          mma_kmajor(tmem + kColSP, kA, kT, qslot(qK0, gg));
           umma_commit(&bars->s_full);
           return true;
         };
         if (!(ok = issue_s(g))) break;
         for (int st = 0; st < nsteps && ok; ++st) {
           const uint32_t gg = g + st;
-          const uint32_t qb = smem_addr(sQ + (gg & 1) * kTile3);
           // dP^T = V dO^T over SP once S^T has been read
           if (!(ok = mbar_wait(&bars->s_read, gg & 1, s_abort))) break;
           if (!(ok = mbar_wait(&bars->do_full, gg & 1, s_abort))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ss(tmem + kColSP, a_desc(vb, k), b_desc(db, k), kIdS, k > 0);
+          mma_kmajor(tmem + kColSP, vA, vT, dK);
           umma_commit(&bars->dp_full);
-          // dV += P^T dO; query rows 16k..16k+15 are the pair columns
-          // 448 + 32*(k/4) + 8*(k%4)
+          // dV += P^T dO
           if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
           if (st == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
             break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kRowsQ / 16; ++k)
-            umma_ts(tmem + kColDV, tmem + kColX + (k >> 2) * 32 + (k & 3) * 8, mn_desc(db, k),
-                    kIdG, (st > 0 || k > 0));
+          mma_x(tmem + kColDV, dMN, st > 0);
           umma_commit(&bars->dv_done);
           umma_commit(&bars->do_empty);
           // S^T of the next step over SP once dP^T has been read
@@ -307,13 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(&bars->dp_read, gg & 1, s_abort))) break;
             if (!(ok = issue_s(gg + 1))) break;
           }
-          // dK += dS^T Q, same pair layout
+          // dK += dS^T Q
           if (!(ok = mbar_wait(&bars->ds_full, gg & 1, s_abort))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kRowsQ / 16; ++k)
-            umma_ts(tmem + kColDK, tmem + kColX + (k >> 2) * 32 + (k & 3) * 8, mn_desc(qb, k),
-                    kIdG, (st > 0 || k > 0));
+          mma_x(tmem + kColDK, qslot(qMN0, gg), st > 0);
           umma_commit(&bars->dk_done);
           umma_commit(&bars->q_empty[gg & 1]);
         }
@@ -458,10 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 a4 = pa[q4], m4 = pm[q4];
-            bias[q4 * 4] = fmaf(m4.x, rf, a4.x);
-            bias[q4 * 4 + 1] = fmaf(m4.y, rf, a4.y);
-            bias[q4 * 4 + 2] = fmaf(m4.z, rf, a4.z);
-            bias[q4 * 4 + 3] = fmaf(m4.w, rf, a4.w);
+            fma2(bias[q4 * 4], bias[q4 * 4 + 1], m4.x, m4.y, rf, rf, a4.x, a4.y);
+            fma2(bias[q4 * 4 + 2], bias[q4 * 4 + 3], m4.z, m4.w, rf, rf, a4.z, a4.w);
           }
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:
@@ -499,30 +524,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_read);
-        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) and P (1 - tanh^2), in two
+        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) and -P (1 - tanh^2), in two
         // batches of 32: all tanh (in place of S), then all exp2 (in place of
-        // the bias)
+        // the bias); pairs of columns share the f32x2 instructions
         uint32_t pk[32];
+        const float is = lm.in_scale, os = lm.out_scale;
 #pragma unroll
         for (int bt = 0; bt < 2; ++bt) {
           float* xb = x + bt * 32;
           float* zb = bias + bt * 32;
           if (lm.capped) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) xb[c] = tanh_approx(xb[c] * lm.in_scale);
+            for (int c = 0; c < 32; c += 2) mul2(xb[c], xb[c + 1], xb[c], xb[c + 1], is, is);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) zb[c] = fmaf(xb[c], lm.out_scale, zb[c]);
+            for (int c = 0; c < 32; ++c) xb[c] = tanh_approx(xb[c]);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2)
+              fma2(zb[c], zb[c + 1], xb[c], xb[c + 1], os, os, zb[c], zb[c + 1]);
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) zb[c] = fmaf(xb[c], lm.in_scale, zb[c]);
+            for (int c = 0; c < 32; c += 2)
+              fma2(zb[c], zb[c + 1], xb[c], xb[c + 1], is, is, zb[c], zb[c + 1]);
           }
 #pragma unroll
           for (int c = 0; c < 32; ++c) zb[c] = ex2_approx(zb[c]);  // P
 #pragma unroll
           for (int c = 0; c < 32; c += 2) pk[bt * 16 + (c >> 1)] = Pack<BF16>::two(zb[c], zb[c + 1]);
+          // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
+          if (lm.capped) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)  // P (1 - tanh^2): dS = this * (dP - D)
-            xb[c] = lm.capped ? zb[c] * fmaf(-xb[c], xb[c], 1.f) : zb[c];
+            for (int c = 0; c < 32; c += 2) {
+              float u0, u1;
+              fma2(u0, u1, xb[c], xb[c + 1], xb[c], xb[c + 1], -1.f, -1.f);
+              mul2(xb[c], xb[c + 1], zb[c], zb[c + 1], u0, u1);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) xb[c] = -zb[c];
+          }
         }
         // P^T pairs: this half's 64 columns -> 32 pair columns at 448 + 32*half,
         // once dK of the previous step has read X
@@ -550,25 +589,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->d_empty);
-        // dS^T = P (1 - tanh^2) (dP - D)
+        // dS^T = P (1 - tanh^2) (dP - D) = x (D - dP)
         if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
         tc_fence_after();
         {
+          auto ds_pairs = [&](const float* d, int c0) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float e0, e1, s0, s1;
+              fma2(e0, e1, d[c], d[c + 1], -1.f, -1.f, bias[c0 + c], bias[c0 + c + 1]);
+              mul2(s0, s1, x[c0 + c], x[c0 + c + 1], e0, e1);
+              pk[(c0 + c) >> 1] = Pack<BF16>::two(s0, s1);
+            }
+          };
           float d0[32], d1[32];
           tmem_ld32(spbuf, d0);
           tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            pk[c >> 1] = Pack<BF16>::two(x[c] * (d0[c] - bias[c]), x[c + 1] * (d0[c + 1] - bias[c + 1]));
+          ds_pairs(d0, 0);
           tmem_ld32(spbuf + 32, d1);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->dp_read);
-#pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            pk[16 + (c >> 1)] = Pack<BF16>::two(x[32 + c] * (d1[c] - bias[32 + c]),
-                                                x[32 + c + 1] * (d1[c + 1] - bias[32 + c + 1]));
+          ds_pairs(d1, 32);
         }
         // dS^T pairs over P^T once dV has read it
         if (!(ok = mbar_wait_warp(&bars->dv_done, gg & 1, s_abort))) break;
@@ -618,17 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
-                        const CUtensorMap& tvt, int grid, cudaStream_t s) {
+cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
+                        const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
+                        const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
+                        int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = dkdv_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq, tdo, tk, tkt, tv, tvt);
+    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
   } else {
     auto k = dkdv_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq, tdo, tk, tkt, tv, tvt);
+    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
   }
   return cudaGetLastError();
 }

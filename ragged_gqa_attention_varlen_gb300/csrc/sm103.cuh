@@ -117,6 +117,31 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+// Bring a box of a tensor into L2 without a shared-memory destination.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -184,6 +209,42 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// A shared-memory descriptor as two 32-bit halves.  The start address field
+// (bits 0-13, address >> 4) is in the low half and shared-memory addresses
+// stay below 256 KB, so advancing the operand by a byte offset adds
+// offset >> 4 to the low half without a carry.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_split(uint64_t d) {
+  return SDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+// umma_ss with both operands given as a base descriptor plus a byte offset.
+__device__ __forceinline__ void umma_ss_off(uint32_t d_tmem, SDesc a, uint32_t a_off, SDesc b,
+                                            uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc),
+      "r"(accumulate)
+      : "memory");
+}
+
+// umma_ts with the B operand given as a base descriptor plus a byte offset.
+__device__ __forceinline__ void umma_ts_off(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
+                                            uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -321,6 +382,19 @@ __device__ __forceinline__ void warpgroup_reg_dealloc() {
 }
 
 // ---------------------------------------------------------------- math
+
+// Elementwise operations on two fp32 values (kept as scalar operations: the
+// packed f32x2 forms constrain register pairing enough to cause spills in the
+// elementwise warps).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  d0 = fmaf(a0, b0, c0);
+  d1 = fmaf(a1, b1, c1);
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  d0 = a0 * b0;
+  d1 = a1 * b1;
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
