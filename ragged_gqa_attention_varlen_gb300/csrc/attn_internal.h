@@ -60,9 +60,9 @@ struct Params {
 inline int sched_words(int B) { return 4 * B + 2; }
 
 cudaError_t launch_sched(const Params& p, cudaStream_t s);
-cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqt,
-                       const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
-                       int grid, cudaStream_t s);
+cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
+                       const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
+                       const CUtensorMap& tv, int grid, cudaStream_t s);
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
 // Tensor maps: *2 load feature chunks 0-1 of a tile in one box; tq/tdo load
 // chunk 2 (features 128..191, the part past 159 filled with zeros); tkt/tvt

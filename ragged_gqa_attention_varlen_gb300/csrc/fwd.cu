@@ -87,9 +87,10 @@ __device__ __forceinline__ void key_order(const QTile& t, int& n, int& t0) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
-    fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq,
-               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv) {
+    fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
+               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk2,
+               const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv2,
+               const __grid_constant__ CUtensorMap tv) {
   using namespace fwd;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -156,15 +157,19 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane < 2) {
-      const bool kq = lane == 0;  // lane 0: Q and K; lane 1: V
+    // Lanes 0 and 2 load Q and K, lanes 1 and 3 load V.  Features 0..127 of a
+    // tile arrive in one box (lanes 0, 1), the rest in a second (lanes 2, 3):
+    // a TMA operation costs about the same time whatever its size, and
+    // separate issuing threads overlap theirs.
+    if (lane < 4) {
+      const bool kq = (lane & 1) == 0;
+      const bool lead = lane < 2;  // arrives on the full barriers
+      const unsigned gmask = kq ? 0x5u : 0xAu;
       if (kq) {
-        prefetch_tensormap(&tq);
-        prefetch_tensormap(&tqt);
-        prefetch_tensormap(&tk);
-        prefetch_tensormap(&tkt);
+        prefetch_tensormap(lead ? &tq2 : &tqt);
+        prefetch_tensormap(lead ? &tk2 : &tkt);
       } else {
-        prefetch_tensormap(&tv);
+        prefetch_tensormap(lead ? &tv2 : &tv);
       }
       uint32_t g = 0;  // key steps loaded
       int tcount = 0;
@@ -175,34 +180,43 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         int n, t0;
         key_order(t, n, t0);
         if (kq) {
-          if (tcount > 0 && !(ok = mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
-          mbar_arrive_expect_tx(&bars->q_full, kTailed);
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(sQ + c * kTile, &tq, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
-          tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
+          if (tcount > 0 &&
+              !(ok = __all_sync(gmask, mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))))
+            break;
+          if (lead) mbar_arrive_expect_tx(&bars->q_full, kTailed);
+          __syncwarp(gmask);
+          if (lead)
+            tma_load_4d(sQ, &tq2, &bars->q_full, 0, t.hg * G, t.q0 + t.tok, 0);
+          else
+            tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
         }
         for (int jj = 0; jj < n; ++jj, ++g) {
           const int key = t.k0 + ((t0 + jj) % n) * kKeys;
           const int s = g & 1;
-          if (g >= 2 && !(ok = mbar_wait(kq ? &bars->k_empty[s] : &bars->v_empty[s],
-                                         ((g - 2) >> 1) & 1, s_abort)))
+          if (g >= 2 && !(ok = __all_sync(gmask, mbar_wait(kq ? &bars->k_empty[s] : &bars->v_empty[s],
+                                                            ((g - 2) >> 1) & 1, s_abort))))
             break;
           if (kq) {
-            mbar_arrive_expect_tx(&bars->k_full[s], kTailed);
             uint8_t* dst = sK + s * kTailed;
-            for (int c = 0; c < 2; ++c)
-              tma_load_2d(dst + c * kTile, &tk, &bars->k_full[s], c * kChunk, key);
-            tma_load_2d(dst + 2 * kTile, &tkt, &bars->k_full[s], 2 * kChunk, key);
+            if (lead) mbar_arrive_expect_tx(&bars->k_full[s], kTailed);
+            __syncwarp(gmask);
+            if (lead)
+              tma_load_3d(dst, &tk2, &bars->k_full[s], 0, key, 0);
+            else
+              tma_load_2d(dst + 2 * kTile, &tkt, &bars->k_full[s], 2 * kChunk, key);
           } else {
-            mbar_arrive_expect_tx(&bars->v_full[s], kTile3);
             uint8_t* dst = sV + s * kTile3;
-            for (int c = 0; c < 3; ++c)
-              tma_load_2d(dst + c * kTile, &tv, &bars->v_full[s], c * kChunk, key);
+            if (lead) mbar_arrive_expect_tx(&bars->v_full[s], kTile3);
+            __syncwarp(gmask);
+            if (lead)
+              tma_load_3d(dst, &tv2, &bars->v_full[s], 0, key, 0);
+            else
+              tma_load_2d(dst + 2 * kTile, &tv, &bars->v_full[s], 2 * kChunk, key);
           }
         }
       }
-      if (*s_abort) {
-        // let every load this thread started land before the CTA exits
+      if (*s_abort && lead) {
+        // let every load this group started land before the CTA exits
         if (kq && tcount > 0) drain_wait(&bars->q_full, (tcount - 1) & 1);
         for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f)
           drain_wait(kq ? &bars->k_full[f & 1] : &bars->v_full[f & 1], (f >> 1) & 1);
@@ -446,17 +460,17 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqt,
-                       const CUtensorMap& tk, const CUtensorMap& tkt, const CUtensorMap& tv,
-                       int grid, cudaStream_t s) {
+cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
+                       const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
+                       const CUtensorMap& tv, int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = fwd_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tqt, tk, tkt, tv);
+    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   } else {
     auto k = fwd_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq, tqt, tk, tkt, tv);
+    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   }
   return cudaGetLastError();
 }

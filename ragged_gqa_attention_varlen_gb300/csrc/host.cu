@@ -319,7 +319,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(0);
   if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(1);
-  if (launch_fwd(p, tq, tqt, tk, tkt, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_fwd(p, tq2, tqt, tk2, tkt, tv2, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
