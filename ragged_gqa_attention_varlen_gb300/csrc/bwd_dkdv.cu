@@ -528,40 +528,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // batches of 32: all tanh (in place of S), then all exp2 (in place of
         // the bias); pairs of columns share the f32x2 instructions
         uint32_t pk[32];
-        const float is = lm.in_scale, os = lm.out_scale;
+        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) and -P (1 - tanh^2) on
+        // column pairs (f32x2 arithmetic), in two batches of 16 pairs: all
+        // tanh (in place of S), then all exp2 (in place of the bias)
+        uint64_t x2[32], z2[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x2[i] = f2_make(x[2 * i], x[2 * i + 1]);
+          z2[i] = f2_make(bias[2 * i], bias[2 * i + 1]);
+        }
+        const uint64_t is2 = f2_make(lm.in_scale, lm.in_scale);
+        const uint64_t os2 = f2_make(lm.out_scale, lm.out_scale);
+        const uint64_t m12 = f2_make(-1.f, -1.f);
 #pragma unroll
         for (int bt = 0; bt < 2; ++bt) {
-          float* xb = x + bt * 32;
-          float* zb = bias + bt * 32;
+          uint64_t* xb = x2 + bt * 16;
+          uint64_t* zb = z2 + bt * 16;
           if (lm.capped) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) mul2(xb[c], xb[c + 1], xb[c], xb[c + 1], is, is);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) xb[c] = tanh_approx(xb[c]);
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              fma2(zb[c], zb[c + 1], xb[c], xb[c + 1], os, os, zb[c], zb[c + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              fma2(zb[c], zb[c + 1], xb[c], xb[c + 1], is, is, zb[c], zb[c + 1]);
-          }
-#pragma unroll
-          for (int c = 0; c < 32; ++c) zb[c] = ex2_approx(zb[c]);  // P
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) pk[bt * 16 + (c >> 1)] = Pack<BF16>::two(zb[c], zb[c + 1]);
-          // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
-          if (lm.capped) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float u0, u1;
-              fma2(u0, u1, xb[c], xb[c + 1], xb[c], xb[c + 1], -1.f, -1.f);
-              mul2(xb[c], xb[c + 1], zb[c], zb[c + 1], u0, u1);
+            for (int c = 0; c < 16; ++c) {
+              const uint64_t v = f2_mul(xb[c], is2);
+              xb[c] = f2_make(tanh_approx(f2_lo(v)), tanh_approx(f2_hi(v)));
             }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) zb[c] = f2_fma(xb[c], os2, zb[c]);
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) xb[c] = -zb[c];
+            for (int c = 0; c < 16; ++c) zb[c] = f2_fma(xb[c], is2, zb[c]);
           }
+#pragma unroll
+          for (int c = 0; c < 16; ++c)  // P
+            zb[c] = f2_make(ex2_approx(f2_lo(zb[c])), ex2_approx(f2_hi(zb[c])));
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[bt * 16 + c] = Pack<BF16>::two(f2_lo(zb[c]), f2_hi(zb[c]));
+          // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            xb[c] = lm.capped ? f2_mul(zb[c], f2_fma(xb[c], xb[c], m12)) : f2_mul(zb[c], m12);
         }
         // P^T pairs: this half's 64 columns -> 32 pair columns at 448 + 32*half,
         // once dK of the previous step has read X
@@ -596,10 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto ds_pairs = [&](const float* d, int c0) {
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              float e0, e1, s0, s1;
-              fma2(e0, e1, d[c], d[c + 1], -1.f, -1.f, bias[c0 + c], bias[c0 + c + 1]);
-              mul2(s0, s1, x[c0 + c], x[c0 + c + 1], e0, e1);
-              pk[(c0 + c) >> 1] = Pack<BF16>::two(s0, s1);
+              const uint64_t e = f2_fma(f2_make(d[c], d[c + 1]), m12,
+                                        f2_make(bias[c0 + c], bias[c0 + c + 1]));
+              const uint64_t v = f2_mul(x2[(c0 + c) >> 1], e);
+              pk[(c0 + c) >> 1] = Pack<BF16>::two(f2_lo(v), f2_hi(v));
             }
           };
           float d0[32], d1[32];

@@ -418,6 +418,41 @@ __device__ __forceinline__ void warpgroup_reg_dealloc() {
 
 // ---------------------------------------------------------------- math
 
+// Two fp32 values in one 64-bit register (low half = first), for the f32x2
+// arithmetic of the sm_100 family: each lane is the correctly rounded scalar
+// result.  Keeping pairs in 64-bit variables lets the register allocator
+// place them as aligned pairs.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+  float lo;
+  asm("{\n\t.reg .b32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  float hi;
+  asm("{\n\t.reg .b32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Elementwise operations on two fp32 values (kept as scalar operations: the
 // packed f32x2 forms constrain register pairing enough to cause spills in the
 // elementwise warps).
