@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
                 const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk2,
                 const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv2,
-                const __grid_constant__ CUtensorMap tvt) {
+                const __grid_constant__ CUtensorMap tvt, const __grid_constant__ CUtensorMap tqf,
+                const __grid_constant__ CUtensorMap tdof) {
   using namespace kv;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -181,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tq);
       prefetch_tensormap(&tdo2);
       prefetch_tensormap(&tdo);
+    } else if (lane < 6) {
+      prefetch_tensormap(lane == 4 ? &tqf : &tdof);
     } else if (lane < 8) {
       prefetch_tensormap(&tk2);
       prefetch_tensormap(&tkt);
@@ -203,14 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 1) tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, key);
       if (lane == 2) tma_load_3d(sV, &tv2, &bars->kv_full, 0, key, 0);
       if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
-      if (lane >= 4 && lane < 8) {
+      if (lane >= 4 && lane < 6) {
         for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
           const int ptok = t.q0 + (sp / ngroups) * step_tok;
           const int ph0 = (sp % ngroups) * G;
-          if (lane == 4) tma_prefetch_4d(&tq2, 0, ph0, ptok, 0);
-          if (lane == 5) tma_prefetch_3d(&tq, 2 * kChunk, ph0, ptok);
-          if (lane == 6) tma_prefetch_4d(&tdo2, 0, ph0, ptok, 0);
-          if (lane == 7) tma_prefetch_3d(&tdo, 2 * kChunk, ph0, ptok);
+          if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
+          if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
         }
       }
       ++nkv;
@@ -221,14 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < nsteps; ++st, ++ndo) {
         const int tok = t.q0 + (st / ngroups) * step_tok;
         const int h0 = (st % ngroups) * G;
-        if (lane >= 4 && lane < 8 && st + kPrefetch < nsteps) {
+        if (lane >= 4 && lane < 6 && st + kPrefetch < nsteps) {
           const int sp = st + kPrefetch;
           const int ptok = t.q0 + (sp / ngroups) * step_tok;
           const int ph0 = (sp % ngroups) * G;
-          if (lane == 4) tma_prefetch_4d(&tq2, 0, ph0, ptok, 0);
-          if (lane == 5) tma_prefetch_3d(&tq, 2 * kChunk, ph0, ptok);
-          if (lane == 6) tma_prefetch_4d(&tdo2, 0, ph0, ptok, 0);
-          if (lane == 7) tma_prefetch_3d(&tdo, 2 * kChunk, ph0, ptok);
+          if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
+          if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
         }
         // Q of the step into slot g & 1
         const int s = (nq.c0 + nq.c1) & 1;
@@ -323,6 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           mma_kmajor(tmem + kColSP, vA, vT, dK);
           umma_commit(&bars->dp_full);
+          // S^T of the next step over SP once dP^T has been read (the
+          // elementwise warps read dP^T before they compute P and dS, so this
+          // product overlaps that work)
+          if (st + 1 < nsteps) {
+            if (!(ok = mbar_wait(&bars->dp_read, gg & 1, s_abort))) break;
+            if (!(ok = issue_s(gg + 1))) break;
+          }
           // dV += P^T dO
           if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
           if (st == 0 && tcount > 0 &&
@@ -332,11 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_x(tmem + kColDV, dMN, st > 0);
           umma_commit(&bars->dv_done);
           umma_commit(&bars->do_empty);
-          // S^T of the next step over SP once dP^T has been read
-          if (st + 1 < nsteps) {
-            if (!(ok = mbar_wait(&bars->dp_read, gg & 1, s_abort))) break;
-            if (!(ok = issue_s(gg + 1))) break;
-          }
           // dK += dS^T Q
           if (!(ok = mbar_wait(&bars->ds_full, gg & 1, s_abort))) break;
           tc_fence_after();
@@ -474,98 +475,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
         const int b = gg & 1;
+        // S^T: read it and release SP for dP^T
+        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        const uint32_t spbuf = tmem + kColSP + half * 64 + lane_addr;
+        uint64_t t2[32];  // column pairs: S, then tanh, then -P (1 - tanh^2)
+        {
+          float x[64];
+          tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(x));
+          tmem_ld32(spbuf + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t2[i] = f2_make(x[2 * i], x[2 * i + 1]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_read);
+        const uint64_t is2 = f2_make(lm.in_scale, lm.in_scale);
+        const uint64_t os2 = f2_make(lm.out_scale, lm.out_scale);
+        const uint64_t m12 = f2_make(-1.f, -1.f);
+        if (lm.capped) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t v = f2_mul(t2[i], is2);
+            t2[i] = f2_make(tanh_approx(f2_lo(v)), tanh_approx(f2_hi(v)));
+          }
+        }
+        // dP^T: read it and release SP for S^T of the next step
+        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        float d[64];
+        tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(d));
+        tmem_ld32(spbuf + 32, *reinterpret_cast<float(*)[32]>(d + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dp_read);
+        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) per group of 4 columns, with
+        // the base-2 bias -slope2 * |i + Lk - Lq - j| - lse2 formed from the
+        // staged column scalars (a + m * j when the tile lies on one side of
+        // every column's aligned key)
         if (!(ok = mbar_wait_warp(&bars->am_full[b], (gg >> 1) & 1, s_abort))) break;
-        // The base-2 bias of this half's columns before S^T lands:
-        // -slope2 * |i + Lk - Lq - j| - lse2, linear in the key when the
-        // tile lies on one side of every column's aligned key.
-        float bias[64];
         const float4* pa = reinterpret_cast<const float4*>(cols->a[b] + half * 64);
         const float4* pm = reinterpret_cast<const float4*>(cols->m[b] + half * 64);
+        uint32_t pk[32];
+        auto p_group = [&](int q4, float b0, float b1, float b2, float b3) {
+          const uint64_t z0 = f2_fma(t2[2 * q4], lm.capped ? os2 : is2, f2_make(b0, b1));
+          const uint64_t z1 = f2_fma(t2[2 * q4 + 1], lm.capped ? os2 : is2, f2_make(b2, b3));
+          const uint64_t p0 = f2_make(ex2_approx(f2_lo(z0)), ex2_approx(f2_hi(z0)));
+          const uint64_t p1 = f2_make(ex2_approx(f2_lo(z1)), ex2_approx(f2_hi(z1)));
+          pk[2 * q4] = Pack<BF16>::two(f2_lo(p0), f2_hi(p0));
+          pk[2 * q4 + 1] = Pack<BF16>::two(f2_lo(p1), f2_hi(p1));
+          // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
+          t2[2 * q4] = lm.capped ? f2_mul(p0, f2_fma(t2[2 * q4], t2[2 * q4], m12)) : f2_mul(p0, m12);
+          t2[2 * q4 + 1] =
+              lm.capped ? f2_mul(p1, f2_fma(t2[2 * q4 + 1], t2[2 * q4 + 1], m12)) : f2_mul(p1, m12);
+        };
         if ((cols->general[b][0] | cols->general[b][1]) == 0) {
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 a4 = pa[q4], m4 = pm[q4];
-            fma2(bias[q4 * 4], bias[q4 * 4 + 1], m4.x, m4.y, rf, rf, a4.x, a4.y);
-            fma2(bias[q4 * 4 + 2], bias[q4 * 4 + 3], m4.z, m4.w, rf, rf, a4.z, a4.w);
+            p_group(q4, fmaf(m4.x, rf, a4.x), fmaf(m4.y, rf, a4.y), fmaf(m4.z, rf, a4.z),
+                    fmaf(m4.w, rf, a4.w));
           }
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:
-          // prel = i + Lk - Lq - key0 of column c is tok0 + c / G + off
+          // prel = i + Lk - Lq - key0 of column c is tok0 + c / G + off,
+          // a + m * prel = -lse2 and |m| = slope2
           const int tok0 = (st / ngroups) * step_tok;
           const int off = t.Lk - t.Lq - t.key;
-#pragma unroll
+#pragma unroll 1
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 a4 = pa[q4], m4 = pm[q4];
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+            float bv[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const int c = half * 64 + q4 * 4 + v;
               const float prel = static_cast<float>(tok0 + (c >> lgG) + off);
-              float bv = fmaf(-fabsf(mv[v]), fabsf(prel - rf), fmaf(mv[v], prel, av[v]));
+              bv[v] = fmaf(-fabsf(mv[v]), fabsf(prel - rf), fmaf(mv[v], prel, av[v]));
               if (masked) {
                 const bool adm = (wl < 0 || rf >= prel - static_cast<float>(wl)) &&
                                  (wr < 0 || rf <= prel + static_cast<float>(wr));
-                bv = adm ? bv : -INFINITY;
+                bv[v] = adm ? bv[v] : -INFINITY;
               }
-              bias[q4 * 4 + v] = bv;
             }
+            // the pair arrays are indexed by q4 at run time here: route through
+            // the unrolled form so they stay in registers
+#pragma unroll
+            for (int qq = 0; qq < 16; ++qq)
+              if (qq == q4) p_group(qq, bv[0], bv[1], bv[2], bv[3]);
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->am_empty[b]);
-        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
-        tc_fence_after();
-        float x[64];
-        const uint32_t spbuf = tmem + kColSP + half * 64 + lane_addr;
-        tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(x));
-        tmem_ld32(spbuf + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_read);
-        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) and -P (1 - tanh^2), in two
-        // batches of 32: all tanh (in place of S), then all exp2 (in place of
-        // the bias); pairs of columns share the f32x2 instructions
-        uint32_t pk[32];
-        // P = exp2(c*log2e*tanh(sigma*x/c) + bias) and -P (1 - tanh^2) on
-        // column pairs (f32x2 arithmetic), in two batches of 16 pairs: all
-        // tanh (in place of S), then all exp2 (in place of the bias)
-        uint64_t x2[32], z2[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x2[i] = f2_make(x[2 * i], x[2 * i + 1]);
-          z2[i] = f2_make(bias[2 * i], bias[2 * i + 1]);
-        }
-        const uint64_t is2 = f2_make(lm.in_scale, lm.in_scale);
-        const uint64_t os2 = f2_make(lm.out_scale, lm.out_scale);
-        const uint64_t m12 = f2_make(-1.f, -1.f);
-#pragma unroll
-        for (int bt = 0; bt < 2; ++bt) {
-          uint64_t* xb = x2 + bt * 16;
-          uint64_t* zb = z2 + bt * 16;
-          if (lm.capped) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint64_t v = f2_mul(xb[c], is2);
-              xb[c] = f2_make(tanh_approx(f2_lo(v)), tanh_approx(f2_hi(v)));
-            }
-#pragma unroll
-            for (int c = 0; c < 16; ++c) zb[c] = f2_fma(xb[c], os2, zb[c]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) zb[c] = f2_fma(xb[c], is2, zb[c]);
-          }
-#pragma unroll
-          for (int c = 0; c < 16; ++c)  // P
-            zb[c] = f2_make(ex2_approx(f2_lo(zb[c])), ex2_approx(f2_hi(zb[c])));
-#pragma unroll
-          for (int c = 0; c < 16; ++c) pk[bt * 16 + c] = Pack<BF16>::two(f2_lo(zb[c]), f2_hi(zb[c]));
-          // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            xb[c] = lm.capped ? f2_mul(zb[c], f2_fma(xb[c], xb[c], m12)) : f2_mul(zb[c], m12);
-        }
         // P^T pairs: this half's 64 columns -> 32 pair columns at 448 + 32*half,
         // once dK of the previous step has read X
         if (gg >= 1 && !(ok = mbar_wait_warp(&bars->dk_done, (gg - 1) & 1, s_abort))) break;
@@ -577,45 +581,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
-        // D of each column into the (now free) bias registers
+        // dS^T = P (1 - tanh^2) (dP - D) = t2 (D - dP), D per group of 4 columns
         if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) break;
         {
           const float4* pd = reinterpret_cast<const float4*>(cols->D + half * 64);
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 d4 = pd[q4];
-            bias[q4 * 4] = d4.x;
-            bias[q4 * 4 + 1] = d4.y;
-            bias[q4 * 4 + 2] = d4.z;
-            bias[q4 * 4 + 3] = d4.w;
+            const uint64_t e0 = f2_fma(f2_make(d[4 * q4], d[4 * q4 + 1]), m12, f2_make(d4.x, d4.y));
+            const uint64_t e1 = f2_fma(f2_make(d[4 * q4 + 2], d[4 * q4 + 3]), m12, f2_make(d4.z, d4.w));
+            const uint64_t v0 = f2_mul(t2[2 * q4], e0);
+            const uint64_t v1 = f2_mul(t2[2 * q4 + 1], e1);
+            pk[2 * q4] = Pack<BF16>::two(f2_lo(v0), f2_hi(v0));
+            pk[2 * q4 + 1] = Pack<BF16>::two(f2_lo(v1), f2_hi(v1));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->d_empty);
-        // dS^T = P (1 - tanh^2) (dP - D) = x (D - dP)
-        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
-        tc_fence_after();
-        {
-          auto ds_pairs = [&](const float* d, int c0) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const uint64_t e = f2_fma(f2_make(d[c], d[c + 1]), m12,
-                                        f2_make(bias[c0 + c], bias[c0 + c + 1]));
-              const uint64_t v = f2_mul(x2[(c0 + c) >> 1], e);
-              pk[(c0 + c) >> 1] = Pack<BF16>::two(f2_lo(v), f2_hi(v));
-            }
-          };
-          float d0[32], d1[32];
-          tmem_ld32(spbuf, d0);
-          tmem_wait_ld();
-          ds_pairs(d0, 0);
-          tmem_ld32(spbuf + 32, d1);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->dp_read);
-          ds_pairs(d1, 32);
-        }
         // dS^T pairs over P^T once dV has read it
         if (!(ok = mbar_wait_warp(&bars->dv_done, gg & 1, s_abort))) break;
         tc_fence_after();
@@ -667,15 +649,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                         const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
-                        int grid, cudaStream_t s) {
+                        const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = dkdv_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
+    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   } else {
     auto k = dkdv_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
+    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   }
   return cudaGetLastError();
 }

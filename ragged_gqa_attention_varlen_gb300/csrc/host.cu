@@ -123,6 +123,23 @@ bool encode_kv_pair(CUtensorMap* m, int dtype, const void* base, int64_t T, int6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A whole query tile (160 features x G heads x rows/G tokens) as one
+// unswizzled box, for L2 prefetches only.
+bool encode_q_full(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
+                   int64_t hs, int G, int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(G),
+                       static_cast<cuuint32_t>(rows / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -288,8 +305,10 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
 
   // ---- TMA tensor maps
   if (!encode_fn()) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2;
-  if (!encode_q_pair(&tq2, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
+  CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2, tqf, tdof;
+  if (!encode_q_full(&tqf, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
+      !encode_q_full(&tdof, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+      !encode_q_pair(&tq2, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
       !encode_q_pair(&tdo2, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
       !encode_kv_pair(&tk2, dtype, k, total_k, k_ts) ||
       !encode_kv_pair(&tv2, dtype, v, total_k, v_ts) ||
@@ -323,7 +342,8 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
-  if (launch_dkdv(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, grid_k, stream) != cudaSuccess)
+  if (launch_dkdv(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid_k, stream) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(4);
   if (launch_dq(p, tq, tdo, tqt, tdot, tk, tv, tvt, grid_q, stream) != cudaSuccess)
