@@ -14,6 +14,7 @@ on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -222,6 +223,22 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
+def dram_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` on the long balanced workload, from
+    the committed ncu capture in profiles/, or None when the capture does not
+    apply to the kernel as built now (its source file changed since)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_long_balanced.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)["kernels"][kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+                return None
+        return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def pinned_copy(x: torch.Tensor) -> torch.Tensor:
     """Pinned host copy of a device tensor's whole storage (its padded base)."""
     st = x.untyped_storage()
@@ -302,7 +319,8 @@ def run_gpu(args, world, rank, local):
     achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": dram_traffic(dom) if args.length_scale == 1.0 else None,
                 "peak_kind": f"{kind} bf16 sustained"}
     whole_frac = value / world / pk["bf16_tflops"]
 
