@@ -16,7 +16,9 @@
 //
 // Warp roles (384 threads, 12 warps): warp 0 issues TMA loads (lane 0: Q once per tile
 // and K through two slots; lane 1: V through two slots, so a K load never
-// waits for a V slot), warp 1 issues the MMAs, warps 4-11 run the
+// waits for a V slot), warp 1 issues the S products and warp 2 the P V
+// products (two issuing threads: an MMA issue blocks while the tensor pipe is
+// busy, so one thread could not wait for P_j while S_{j+1} is queued), warps 4-11 run the
 // softmax and the epilogue -- two warps per TMEM lane quadrant, each taking
 // 64 of the 128 keys of a tile (the row max is exchanged through shared
 // memory), so every SM sub-partition has two warps to hide MUFU latency.  S
@@ -34,7 +36,7 @@
 // taken relative to the stale max and stays below 2^8.  With the softcap
 // (|t| <= c) and ALiBi (<= 0) no later tile can exceed the first tile's max
 // by more than 2*c*log2(e) = 8.66, so rescales are rare.
-// Warps 2-3 only complete warpgroup 0, which hands most of its registers to
+// Warp 3 only completes warpgroup 0, which hands most of its registers to
 // the elementwise warpgroups (setmaxnreg), so those can keep every column's
 // MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);  // one commit per issuing thread
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->mx_x[b], 8);
       mbar_init(&bars->l_x[b], 8);
@@ -223,10 +225,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t kIdO = idesc_f16(128, kHeadDim, BF16, false, true);
       uint32_t g = 0;  // global key-step counter of this CTA
       int tcount = 0;
       bool ok = true;
@@ -234,21 +235,6 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       auto tailed = [&](uint32_t base, int k) -> uint64_t {
         return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
                      : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
-      };
-      auto issue_s = [&](uint32_t gs) -> bool {
-        if (!mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort)) return false;
-        // the buffer's previous S (step gs - 2) has been read by the softmax
-        if (gs >= 2 && !mbar_wait(&bars->s_read[gs & 1], ((gs - 2) >> 1) & 1, s_abort))
-          return false;
-        tc_fence_after();
-        const uint32_t kb = smem_addr(sK + (gs & 1) * kTailed);
-        const uint32_t qb = smem_addr(sQ);
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + (gs & 1) * 128, tailed(qb, k), tailed(kb, k), kIdS, k > 0);
-        umma_commit(&bars->s_full[gs & 1]);
-        umma_commit(&bars->k_empty[gs & 1]);
-        return true;
       };
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
         QTile t;
@@ -258,18 +244,51 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;
         if (n == 0) {  // no keys: nothing to multiply; keep every phase count
           mbar_arrive(&bars->q_empty);
+          continue;
+        }
+        for (int jj = 0; jj < n; ++jj) {
+          const uint32_t gs = g + jj;
+          if (!(ok = mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort))) break;
+          // the buffer's previous S (step gs - 2) has been read by the softmax
+          if (gs >= 2 && !(ok = mbar_wait(&bars->s_read[gs & 1], ((gs - 2) >> 1) & 1, s_abort)))
+            break;
+          tc_fence_after();
+          const uint32_t kb = smem_addr(sK + (gs & 1) * kTailed);
+          const uint32_t qb = smem_addr(sQ);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            umma_ss(tmem + (gs & 1) * 128, tailed(qb, k), tailed(kb, k), kIdS, k > 0);
+          umma_commit(&bars->s_full[gs & 1]);
+          umma_commit(&bars->k_empty[gs & 1]);
+          if (jj == n - 1) umma_commit(&bars->q_empty);
+        }
+        g += n;
+      }
+      // every MMA this thread issued completes before the CTA moves on
+      umma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ O += P V issuer
+    // A second issuing thread, so that the wait for P_j and the bookkeeping
+    // between groups overlap the S products queued by warp 1.
+    if (lane == 0) {
+      constexpr uint32_t kIdO = idesc_f16(128, kHeadDim, BF16, false, true);
+      uint32_t g = 0;
+      int tcount = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        QTile t;
+        qtile_decode(p, item, t);
+        int n, t0;
+        key_order(t, n, t0);
+        if (n == 0) {
           if (tcount > 0 && !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort))) break;
           mbar_arrive(&bars->o_full);
           continue;
         }
-        if (!(ok = issue_s(g))) break;
-        if (n == 1) umma_commit(&bars->q_empty);
         for (int jj = 0; jj < n; ++jj) {
           const uint32_t gg = g + jj;
-          if (jj + 1 < n) {
-            if (!(ok = issue_s(gg + 1))) break;
-            if (jj + 1 == n - 1) umma_commit(&bars->q_empty);
-          }
           if (!(ok = mbar_wait(&bars->p_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
           if (jj == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort)))
@@ -288,7 +307,6 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         }
         g += n;
       }
-      // every MMA this thread issued completes before the CTA moves on
       umma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
