@@ -9,19 +9,21 @@
 //
 // Tile: the forward's 128 query rows.  Per key tile j:
 //   S_j  = Q K_j^T, dP_j = dO V_j^T   M=128 N=128 K=160, fp32 in TMEM
-//   dS_j                              elementwise warps; written back over
-//                                     dP_j as 16-bit pairs
+//   dS_j                              elementwise warps; written as 16-bit
+//                                     pairs to a TMEM region of its own
 //   dQ  += dS_j K_j                   M=128 N=160 K=128, A operand from TMEM
 //
 // Warp roles (384 threads, 12 warps): warp 0 loads (Q, dO once per tile; K through two
-// slots, V through one), warp 1 issues the MMAs, warps 4-11 do the elementwise
-// work (two warps per TMEM lane quadrant, each taking 64 of the 128 keys).
-// The elementwise warps release S_j as soon as they have read it, so S_{j+1}
-// runs on the tensor core while dS_j is still being formed.  Q, dO and V are
+// slots, V through one), warp 1 issues the S and dP products, warp 2 the dQ
+// products, warps 4-11 do the elementwise work (two warps per TMEM lane
+// quadrant, each taking 64 of the 128 keys).  The elementwise warps release
+// S_j and dP_j as soon as they have read them, so S_{j+1} and dP_{j+1} run on
+// the tensor core while dS_j is still being formed; dS_j has its own TMEM
+// region, so dP_{j+1} never waits for dQ += dS_j K_j.  Q, dO and V are
 // only K-major operands here and keep their last 32 features in a 64-byte-
 // swizzled chunk; K is also the MN-major operand of dQ and stays in three
 // 128-byte-swizzled chunks.
-// Warps 2-3 only complete warpgroup 0, which hands most of its registers to
+// Warp 3 only completes warpgroup 0, which hands most of its registers to
 // the elementwise warpgroups (setmaxnreg), so those can keep every column's
 // MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
@@ -43,13 +45,14 @@ constexpr uint32_t kOffBar = kOffV + kTailed;
 constexpr uint32_t kSmem = kOffBar + 256;    // base checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 128;
-constexpr uint32_t kColQ = 256;
+constexpr uint32_t kColP = 128;   // dP
+constexpr uint32_t kColDS = 256;  // dS as 16-bit pairs
+constexpr uint32_t kColQ = 320;   // dQ accumulator
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t s_full, s_free, dp_full, p_full, dq_done;
+  uint64_t s_full, s_free, dp_full, dp_free, p_full, dq_done;
   uint64_t o_full, o_empty, drain;
 };
 }  // namespace dqk
@@ -105,11 +108,12 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 8);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 8);
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);  // one commit per issuing thread
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -176,10 +180,9 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S, dP issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
       const uint32_t qb = smem_addr(sQ), db = smem_addr(sDO), vb = smem_addr(sV);
       // K-major operand stored as two 128-byte-swizzled chunks + a 64-byte tail
       auto tailed = [&](uint32_t base, int k) -> uint64_t {
@@ -189,29 +192,6 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       uint32_t g = 0;
       int tcount = 0;
       bool ok = true;
-      auto issue_s = [&](uint32_t gs) -> bool {  // S = Q K^T
-        if (gs >= 1 && !mbar_wait(&bars->s_free, (gs - 1) & 1, s_abort)) return false;
-        if (!mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_addr(sK + (gs & 1) * 3 * kTile);
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + kColS, tailed(qb, k),
-                  sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
-        umma_commit(&bars->s_full);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t gs) -> bool {  // dP = dO V^T
-        if (gs >= 1 && !mbar_wait(&bars->dq_done, (gs - 1) & 1, s_abort)) return false;
-        if (!mbar_wait(&bars->v_full, gs & 1, s_abort)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
-        umma_commit(&bars->dp_full);
-        umma_commit(&bars->v_empty);
-        return true;
-      };
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
@@ -219,30 +199,71 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;
         if (n == 0) {
           mbar_arrive(&bars->q_empty);
+          continue;
+        }
+        for (int j = 0; j < n; ++j) {
+          const uint32_t gs = g + j;
+          // S = Q K^T once the previous S has been read
+          if (gs >= 1 && !(ok = mbar_wait(&bars->s_free, (gs - 1) & 1, s_abort))) break;
+          if (!(ok = mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort))) break;
+          tc_fence_after();
+          const uint32_t kb = smem_addr(sK + (gs & 1) * 3 * kTile);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            umma_ss(tmem + kColS, tailed(qb, k),
+                    sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
+          umma_commit(&bars->s_full);
+          // dP = dO V^T once the previous dP has been read
+          if (gs >= 1 && !(ok = mbar_wait(&bars->dp_free, (gs - 1) & 1, s_abort))) break;
+          if (!(ok = mbar_wait(&bars->v_full, gs & 1, s_abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
+          umma_commit(&bars->dp_full);
+          umma_commit(&bars->v_empty);
+          if (j + 1 == n) umma_commit(&bars->q_empty);  // last S and dP of this tile issued
+        }
+        g += n;
+      }
+      umma_commit(&bars->drain);
+      drain_wait_dq(&bars->drain, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dQ issuer
+    // A second issuing thread: an MMA issue blocks while the tensor pipe is
+    // busy, so the wait for dS_j must not sit behind the S and dP products
+    // of the next key tile.
+    if (lane == 0) {
+      constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
+      uint32_t g = 0;
+      int tcount = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        QTile t;
+        qtile_decode(p, item, t);
+        const int n = (t.Lk + kKeys - 1) / kKeys;
+        if (n == 0) {
           if (tcount > 0 && !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort))) break;
           mbar_arrive(&bars->o_full);
           continue;
         }
-        if (!(ok = issue_s(g)) || !(ok = issue_dp(g))) break;
         for (int j = 0; j < n; ++j) {
           const uint32_t gg = g + j;
-          if (j + 1 < n && !(ok = issue_s(gg + 1))) break;
-          if (j + 1 == n) umma_commit(&bars->q_empty);  // last S and dP of this tile issued
           if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
           if (j == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort)))
             break;
           tc_fence_after();
           const uint32_t kb = smem_addr(sK + (gg & 1) * 3 * kTile);
-          // keys 16k..16k+15: half k/4, pair column 8*(k%4) of that half's region
+          // keys 16k..16k+15: pair columns 8k..8k+7 of the dS region
 #pragma unroll
           for (int k = 0; k < kKeys / 16; ++k)
-            umma_ts(tmem + kColQ, tmem + kColP + (k >> 2) * 64 + (k & 3) * 8,
+            umma_ts(tmem + kColQ, tmem + kColDS + k * 8,
                     sdesc_sw128(kb + k * 2048, kTile, 1024), kIdQ, (j > 0 || k > 0));
           umma_commit(&bars->dq_done);
           umma_commit(&bars->k_empty[gg & 1]);
           if (j + 1 == n) umma_commit(&bars->o_full);
-          else if (!(ok = issue_dp(gg + 1))) break;
         }
         g += n;
       }
@@ -335,14 +356,23 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           float d[32];
           tmem_ld32(pbuf + cc * 32, d);
           tmem_wait_ld();
+          if (cc == 1) {  // all of dP read: the next dP may be computed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->dp_free);
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
             pk[cc * 16 + (c >> 1)] = Pack<BF16>::two(x[cc * 32 + c] * (d[c] - Drow),
                                                      x[cc * 32 + c + 1] * (d[c + 1] - Drow));
         }
-        // dS pairs over this half's first 32 (already read) dP columns
-        tmem_st16(pbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
-        tmem_st16(pbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+        // dS pairs: this half's 64 keys -> 32 pair columns of the dS region,
+        // once dQ of the previous key tile has read it
+        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->dq_done, (gg - 1) & 1, s_abort))) break;
+        tc_fence_after();
+        const uint32_t dsbuf = tmem + kColDS + half * 32 + lane_addr;
+        tmem_st16(dsbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(dsbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
