@@ -14,7 +14,7 @@
 //   dQ  += dS_j K_j                   M=128 N=160 K=128, A operand from TMEM
 //
 // Warp roles (384 threads, 12 warps): warp 0 loads (Q, dO once per tile; K through two
-// slots, V through one), warp 1 issues the S and dP products, warp 2 the dQ
+// slots, V through one; each tile as two boxes from two lanes), warp 1 issues the S and dP products, warp 2 the dQ
 // products, warps 4-11 do the elementwise work (two warps per TMEM lane
 // quadrant, each taking 64 of the 128 keys).  The elementwise warps release
 // S_j and dP_j as soon as they have read them, so S_{j+1} and dP_{j+1} run on
@@ -66,10 +66,11 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
-    dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq,
-              const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tqt,
-              const __grid_constant__ CUtensorMap tdot, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tvt) {
+    dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
+              const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tdo2,
+              const __grid_constant__ CUtensorMap tdot, const __grid_constant__ CUtensorMap tk2,
+              const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv2,
+              const __grid_constant__ CUtensorMap tvt) {
   using namespace dqk;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -133,51 +134,62 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   warpgroup_reg_dealloc<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp walks the fills; each tile's boxes are issued from
+    // separate lanes (features 0..127 of a tile in one box, the rest in a
+    // second), since a TMA operation costs about the same time whatever its
+    // size and separate issuing threads overlap theirs.
     if (lane == 0) {
-      prefetch_tensormap(&tq);
-      prefetch_tensormap(&tdo);
+      prefetch_tensormap(&tq2);
+      prefetch_tensormap(&tk2);
+    } else if (lane == 1) {
       prefetch_tensormap(&tqt);
-      prefetch_tensormap(&tdot);
       prefetch_tensormap(&tk);
-      prefetch_tensormap(&tv);
+    } else if (lane == 2) {
+      prefetch_tensormap(&tdo2);
+      prefetch_tensormap(&tv2);
+    } else if (lane == 3) {
+      prefetch_tensormap(&tdot);
       prefetch_tensormap(&tvt);
-      uint32_t g = 0;  // key tiles loaded
-      int tcount = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
-        QTile t;
-        qtile_decode(p, item, t);
-        const int n = (t.Lk + kKeys - 1) / kKeys;
-        if (tcount > 0 && !(ok = mbar_wait(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kTailed);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sQ + c * kTile, &tq, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
-          tma_load_3d(sDO + c * kTile, &tdo, &bars->q_full, c * kChunk, t.hg * G, t.q0 + t.tok);
+    }
+    uint32_t g = 0;  // key tiles loaded
+    int tcount = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      QTile t;
+      qtile_decode(p, item, t);
+      const int n = (t.Lk + kKeys - 1) / kKeys;
+      const int h0 = t.hg * G, tok = t.q0 + t.tok;
+      if (tcount > 0 && !(ok = mbar_wait_warp(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 2 * kTailed);
+      __syncwarp();
+      if (lane == 0) tma_load_4d(sQ, &tq2, &bars->q_full, 0, h0, tok, 0);
+      if (lane == 1) tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, h0, tok);
+      if (lane == 2) tma_load_4d(sDO, &tdo2, &bars->q_full, 0, h0, tok, 0);
+      if (lane == 3) tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, h0, tok);
+      for (int j = 0; j < n && ok; ++j, ++g) {
+        const int key = t.k0 + j * kKeys;
+        const int ks = g & 1;
+        if (g >= 2 && !(ok = mbar_wait_warp(&bars->k_empty[ks], ((g - 2) >> 1) & 1, s_abort)))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[ks], 3 * kTile);
+        __syncwarp();
+        uint8_t* dk = sK + ks * 3 * kTile;
+        if (lane == 0) tma_load_3d(dk, &tk2, &bars->k_full[ks], 0, key, 0);
+        if (lane == 1) tma_load_2d(dk + 2 * kTile, &tk, &bars->k_full[ks], 2 * kChunk, key);
+        if (g >= 1 && !(ok = mbar_wait_warp(&bars->v_empty, (g - 1) & 1, s_abort))) {
+          ++g;  // the K fill above is armed
+          break;
         }
-        tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
-        tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
-        for (int j = 0; j < n && ok; ++j, ++g) {
-          const int key = t.k0 + j * kKeys;
-          const int ks = g & 1;
-          if (g >= 2 && !(ok = mbar_wait(&bars->k_empty[ks], ((g - 2) >> 1) & 1, s_abort))) break;
-          mbar_arrive_expect_tx(&bars->k_full[ks], 3 * kTile);
-          for (int c = 0; c < 3; ++c)
-            tma_load_2d(sK + (ks * 3 + c) * kTile, &tk, &bars->k_full[ks], c * kChunk, key);
-          if (g >= 1 && !(ok = mbar_wait(&bars->v_empty, (g - 1) & 1, s_abort))) {
-            ++g;  // the K fill above is armed
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->v_full, kTailed);
-          for (int c = 0; c < 2; ++c)
-            tma_load_2d(sV + c * kTile, &tv, &bars->v_full, c * kChunk, key);
-          tma_load_2d(sV + 2 * kTile, &tvt, &bars->v_full, 2 * kChunk, key);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full, kTailed);
+        __syncwarp();
+        if (lane == 2) tma_load_3d(sV, &tv2, &bars->v_full, 0, key, 0);
+        if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->v_full, 2 * kChunk, key);
       }
-      if (*s_abort) {
-        if (tcount > 0) drain_wait_dq(&bars->q_full, (tcount - 1) & 1);
-        for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f) drain_wait_dq(&bars->k_full[f & 1], (f >> 1) & 1);
-        if (g > 0) drain_wait_dq(&bars->v_full, (g - 1) & 1);
-      }
+    }
+    if (*s_abort && lane == 0) {
+      if (tcount > 0) drain_wait_dq(&bars->q_full, (tcount - 1) & 1);
+      for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f) drain_wait_dq(&bars->k_full[f & 1], (f >> 1) & 1);
+      if (g > 0) drain_wait_dq(&bars->v_full, (g - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S, dP issuer
@@ -418,17 +430,18 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                      const CUtensorMap& tqt, const CUtensorMap& tdot, const CUtensorMap& tk,
-                      const CUtensorMap& tv, const CUtensorMap& tvt, int grid, cudaStream_t s) {
+cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
+                      const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
+                      const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
+                      int grid, cudaStream_t s) {
   if (p.dtype == 1) {
     auto k = dq_kernel<true>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq, tdo, tqt, tdot, tk, tv, tvt);
+    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt);
   } else {
     auto k = dq_kernel<false>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq, tdo, tqt, tdot, tk, tv, tvt);
+    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt);
   }
   return cudaGetLastError();
 }

@@ -346,7 +346,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
       cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(4);
-  if (launch_dq(p, tq, tdo, tqt, tdot, tk, tv, tvt, grid_q, stream) != cudaSuccess)
+  if (launch_dq(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt, grid_q, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(5);
   return ATTN_OK;
