@@ -18,15 +18,14 @@
 //                 then (once dP^T has been read) S^T of the next step
 //   X  [448,512): P^T as 16-bit pairs, read by dV += P^T dO; then dS^T, read
 //                 by dK += dS^T Q; then P^T of the next step
-// so the tensor core issues dP^T(g), dV(g), S^T(g+1), dK(g) in that order and
-// computes S^T of the next step while the elementwise warps finish dS of this
-// one.
+// so the tensor core computes S^T of the next step while the elementwise
+// warps finish dS of this one.
 //
-// Warp roles (384 threads, 12 warps): warp 0 loads tiles with TMA (lane 0 the
-// K/V tiles and the two Q slots, lane 1 the dO slot), warp 1 issues the MMAs,
-// warps 2-3 stage each query step's per-column scalars (bias coefficients and
-// D), warps 4-11 compute P^T and dS^T and write dk/dv -- two warps per TMEM
-// lane quadrant, each taking 64 of the step's 128 query columns.
+// Warp roles (384 threads, 12 warps): warp 0 loads tiles with TMA, warp 1
+// issues S^T and dP^T, warp 3 issues dV and dK, warp 2 stages each query
+// step's per-column scalars (bias coefficients and D), warps 4-11 compute P^T
+// and dS^T and write dk/dv -- two warps per TMEM lane quadrant, each taking 64
+// of the step's 128 query columns.
 //
 // Shared memory: K and V are K-major operands only and keep features 128..159
 // in a 64-byte-swizzled chunk (40 KB each).  Q and dO are also MN-major
@@ -48,7 +47,7 @@ struct Cols {          // per-column scalars (column = token * G + head)
   float a[2][128];     // bias at key r = a + m * r (base 2) when the step is one-sided
   float m[2][128];
   float D[128];
-  int general[2][2];   // per buffer and staging warp: some column needs |i - j| or a mask
+  int general[2][2];   // [buffer][0]: some column needs |i - j| or a mask ([b][1] stays 0)
 };
 
 struct Bars {
@@ -133,11 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
-      mbar_init(&bars->am_full[s], 2);
+      mbar_init(&bars->am_full[s], 1);
       mbar_init(&bars->am_empty[s], 8);
     }
     mbar_init(&bars->do_full, 1);
-    mbar_init(&bars->do_empty, 1);
+    mbar_init(&bars->do_empty, 2);  // dO is read by dP^T (warp 1) and dV (warp 3)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_read, 8);
     mbar_init(&bars->dp_full, 1);
@@ -148,9 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 8);
-    mbar_init(&bars->d_full, 2);
+    mbar_init(&bars->d_full, 1);
     mbar_init(&bars->d_empty, 8);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);  // one commit per issuing thread
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -252,8 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nq.get(s) > 0) drain_wait_kv(&bars->q_full[s], (nq.get(s) - 1) & 1);
       if (ndo > 0) drain_wait_kv(&bars->do_full, (ndo - 1) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S^T and dP^T (they pass through SP in turn), warp 3 the
+    // dV and dK accumulations.  An MMA issue blocks while the tensor pipe is
+    // busy, so with one issuing thread the wait for P^T or dS^T of a step
+    // would hold back the next step's S^T and dP^T (and the reverse).
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t kIdG = idesc_f16(128, kHeadDim, BF16, false, true);
@@ -293,80 +296,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0;  // query steps of all earlier tiles
       int tcount = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
-        KTile t;
-        ktile_decode(p, item, t);
-        const int nsteps = step_count(t);
-        if (!(ok = mbar_wait(&bars->kv_full, tcount & 1, s_abort))) break;
-        if (nsteps == 0) {  // no queries: dk = dv = 0; keep every phase count
-          mbar_arrive(&bars->kv_empty);
-          if (tcount > 0 && !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort))) break;
-          mbar_arrive(&bars->acc_full);
-          continue;
-        }
-        // S^T of step gg into SP (its previous content, dP^T of step gg - 1,
-        // has been read: ds_full or dp_read of that step was waited for)
+      if (warp == 1) {
+        // S^T of step gg into SP once the previous content of SP (dP^T of
+        // step gg - 1) has been read
         auto issue_s = [&](uint32_t gg) -> bool {
+          if (gg >= 1 && !mbar_wait(&bars->dp_read, (gg - 1) & 1, s_abort)) return false;
           if (!mbar_wait(&bars->q_full[gg & 1], (gg >> 1) & 1, s_abort)) return false;
           tc_fence_after();
           mma_kmajor(tmem + kColSP, kA, kT, qslot(qK0, gg));
           umma_commit(&bars->s_full);
           return true;
         };
-        if (!(ok = issue_s(g))) break;
-        for (int st = 0; st < nsteps && ok; ++st) {
-          const uint32_t gg = g + st;
-          // dP^T = V dO^T over SP once S^T has been read
-          if (!(ok = mbar_wait(&bars->s_read, gg & 1, s_abort))) break;
-          if (!(ok = mbar_wait(&bars->do_full, gg & 1, s_abort))) break;
-          tc_fence_after();
-          mma_kmajor(tmem + kColSP, vA, vT, dK);
-          umma_commit(&bars->dp_full);
-          // S^T of the next step over SP once dP^T has been read (the
-          // elementwise warps read dP^T before they compute P and dS, so this
-          // product overlaps that work)
-          if (st + 1 < nsteps) {
-            if (!(ok = mbar_wait(&bars->dp_read, gg & 1, s_abort))) break;
-            if (!(ok = issue_s(gg + 1))) break;
+        for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+          KTile t;
+          ktile_decode(p, item, t);
+          const int nsteps = step_count(t);
+          if (!(ok = mbar_wait(&bars->kv_full, tcount & 1, s_abort))) break;
+          if (nsteps == 0) {  // no queries: keep every phase count
+            mbar_arrive(&bars->kv_empty);
+            continue;
           }
-          // dV += P^T dO
-          if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
-          if (st == 0 && tcount > 0 &&
-              !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
-            break;
-          tc_fence_after();
-          mma_x(tmem + kColDV, dMN, st > 0);
-          umma_commit(&bars->dv_done);
-          umma_commit(&bars->do_empty);
-          // dK += dS^T Q
-          if (!(ok = mbar_wait(&bars->ds_full, gg & 1, s_abort))) break;
-          tc_fence_after();
-          mma_x(tmem + kColDK, qslot(qMN0, gg), st > 0);
-          umma_commit(&bars->dk_done);
-          umma_commit(&bars->q_empty[gg & 1]);
+          if (!(ok = issue_s(g))) break;
+          for (int st = 0; st < nsteps && ok; ++st) {
+            const uint32_t gg = g + st;
+            // dP^T = V dO^T over SP once S^T has been read
+            if (!(ok = mbar_wait(&bars->s_read, gg & 1, s_abort))) break;
+            if (!(ok = mbar_wait(&bars->do_full, gg & 1, s_abort))) break;
+            tc_fence_after();
+            mma_kmajor(tmem + kColSP, vA, vT, dK);
+            umma_commit(&bars->dp_full);
+            umma_commit(&bars->do_empty);
+            // S^T of the next step over SP once dP^T has been read (this
+            // product overlaps the elementwise warps' dS work)
+            if (st + 1 < nsteps && !(ok = issue_s(gg + 1))) break;
+          }
+          if (!ok) break;
+          umma_commit(&bars->kv_empty);  // K and V are read by S^T and dP^T only
+          g += nsteps;
         }
-        if (!ok) break;
-        umma_commit(&bars->acc_full);
-        umma_commit(&bars->kv_empty);
-        g += nsteps;
+      } else {
+        for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+          KTile t;
+          ktile_decode(p, item, t);
+          const int nsteps = step_count(t);
+          if (nsteps == 0) {  // no queries: dk = dv = 0
+            if (tcount > 0 && !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
+              break;
+            mbar_arrive(&bars->acc_full);
+            continue;
+          }
+          for (int st = 0; st < nsteps && ok; ++st) {
+            const uint32_t gg = g + st;
+            // dV += P^T dO
+            if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
+            if (st == 0 && tcount > 0 &&
+                !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
+              break;
+            tc_fence_after();
+            mma_x(tmem + kColDV, dMN, st > 0);
+            umma_commit(&bars->dv_done);
+            umma_commit(&bars->do_empty);
+            // dK += dS^T Q (S^T, the other reader of the Q slot, has completed)
+            if (!(ok = mbar_wait(&bars->ds_full, gg & 1, s_abort))) break;
+            tc_fence_after();
+            mma_x(tmem + kColDK, qslot(qMN0, gg), st > 0);
+            umma_commit(&bars->dk_done);
+            umma_commit(&bars->q_empty[gg & 1]);
+          }
+          if (!ok) break;
+          umma_commit(&bars->acc_full);
+          g += nsteps;
+        }
       }
       umma_commit(&bars->drain);
       drain_wait_kv(&bars->drain, 0);
     }
-  } else {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ column scalars
-    // Thread u of warps 2-3 stages columns u and u + 64 of every query step:
-    // the bias coefficients into a two-deep ring, D into one buffer.  The
-    // global loads of a step are issued two steps before it is staged.
-    const int w = warp - 2;
-    const int u = w * 32 + lane;
+    // Lane u of warp 2 stages columns u, u + 32, u + 64 and u + 96 of every
+    // query step: the bias coefficients into a two-deep ring, D into one
+    // buffer.  The global loads of a step are issued two steps before it is
+    // staged.
+    const int u = lane;
     const bool masked = masking(p);
     struct Pos {  // a (key tile, query step) of this CTA
       int item, st, nsteps;
       KTile t;
     };
     struct Vals {
-      float lse[2], sl2[2], D[2];
+      float lse[4], sl2[4], D[4];
     };
     auto seek = [&](Pos& q) {
       while (q.item < ntiles) {
@@ -387,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto fetch = [&](const Pos& q, Vals& v) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int lc = u + 64 * hh;
+      for (int hh = 0; hh < 4; ++hh) {
+        const int lc = u + 32 * hh;
         const int i = (q.st / ngroups) * step_tok + lc / G;
         const int h = (q.st % ngroups) * G + lc % G;
         const bool live = q.item < ntiles;
@@ -418,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       bool straddle = false;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int lc = u + 64 * hh;
+      for (int hh = 0; hh < 4; ++hh) {
+        const int lc = u + 32 * hh;
         const int i = (q0.st / ngroups) * step_tok + lc / G;
         const float nl2 = v0.lse[hh] == -INFINITY ? -INFINITY : -v0.lse[hh] * kLog2e;
         const float sl2 = v0.sl2[hh] * kLog2e;
@@ -434,14 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         straddle |= !right && prel < static_cast<float>(kKeys - 1) && i < q0.t.Lq;
       }
       const bool gen = __any_sync(0xffffffffu, straddle) || masked;
-      if (lane == 0) cols->general[b][w] = gen ? 1 : 0;
+      if (lane == 0) {
+        cols->general[b][0] = gen ? 1 : 0;
+        cols->general[b][1] = 0;
+      }
       __threadfence_block();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->am_full[b]);
       // D of the step, once every elementwise warp is done with the previous one
       if (gg >= 1 && !(ok = mbar_wait_warp(&bars->d_empty, (gg - 1) & 1, s_abort))) break;
-      cols->D[u] = v0.D[0];
-      cols->D[u + 64] = v0.D[1];
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) cols->D[u + 32 * hh] = v0.D[hh];
       __threadfence_block();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->d_full);
@@ -501,16 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             t2[i] = f2_make(tanh_approx(f2_lo(v)), tanh_approx(f2_hi(v)));
           }
         }
-        // dP^T: read it and release SP for S^T of the next step
-        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
-        tc_fence_after();
-        float d[64];
-        tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(d));
-        tmem_ld32(spbuf + 32, *reinterpret_cast<float(*)[32]>(d + 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->dp_read);
         // P = exp2(c*log2e*tanh(sigma*x/c) + bias) per group of 4 columns, with
         // the base-2 bias -slope2 * |i + Lk - Lq - j| - lse2 formed from the
         // staged column scalars (a + m * j when the tile lies on one side of
@@ -581,6 +592,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
+        // dP^T: read it and release SP for S^T of the next step (P^T went out
+        // first, so dV, and with it the release of the dO slot, starts early)
+        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
+        tc_fence_after();
+        float d[64];
+        tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(d));
+        tmem_ld32(spbuf + 32, *reinterpret_cast<float(*)[32]>(d + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dp_read);
         // dS^T = P (1 - tanh^2) (dP - D) = t2 (D - dP), D per group of 4 columns
         if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) break;
         {
