@@ -64,6 +64,10 @@ struct Pack<true> {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+  // The two packed values back as an fp32 pair (f2_make order).
+  __device__ __forceinline__ static uint64_t unpack(uint32_t v) {
+    return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  }
 };
 
 template <>
@@ -71,6 +75,10 @@ struct Pack<false> {
   __device__ __forceinline__ static uint32_t two(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint64_t unpack(uint32_t v) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    return f2_make(f.x, f.y);
   }
 };
 

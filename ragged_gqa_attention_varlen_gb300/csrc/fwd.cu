@@ -29,7 +29,10 @@
 // 64-byte-swizzled chunk; V is the MN-major operand of P V and stays in three
 // 128-byte-swizzled chunks.
 //
-// Key tiles are visited starting with the one that holds the ALiBi peak of
+// With the softcap (c <= 9.5) P is taken against a per-row reference fixed
+// before the first key tile (see row_bound), so the softmax needs no running
+// max.  Otherwise (no cap, or a larger one):
+// key tiles are visited starting with the one that holds the ALiBi peak of
 // the tile's rows (the key aligned with the query, where the distance is 0),
 // so the running max is (nearly) final after the first tile.  O is rescaled
 // only when a row's max grows by more than 8 (base-2 units); until then P is
@@ -77,6 +80,32 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) break;
   }
+}
+
+// Largest softcap that takes the fixed-reference softmax: P = 2^(z - ref)
+// with ref = the row's ALiBi term at its admissible key nearest to (slope
+// >= 0) or farthest from (slope < 0) the aligned key.  Every logit of the
+// row is then at most c*log2(e) above ref and the largest at least that far
+// below it, so P stays within [2^-14, 2^14] for the row maximum and below
+// 2^14 everywhere: inside the normal range of fp16 and bf16.
+constexpr float kFixedCapMax = 9.5f;
+
+// The fixed reference of a row whose aligned key is k0 (base 2).  A row with
+// no admissible key gets 0 (every P is then exp2(-inf) = 0).
+__device__ __forceinline__ float row_bound(const Params& p, int Lk, int k0, float slope2) {
+  int64_t lo = 0, hi = static_cast<int64_t>(Lk) - 1;
+  if (masking(p)) {
+    const int wr = p.causal ? 0 : p.wr;
+    if (p.wl >= 0) lo = max(lo, static_cast<int64_t>(k0) - p.wl);
+    if (wr >= 0) hi = min(hi, static_cast<int64_t>(k0) + wr);
+  }
+  if (lo > hi) return 0.f;
+  int64_t d;
+  if (slope2 >= 0.f)
+    d = k0 < lo ? lo - k0 : (k0 > hi ? k0 - hi : 0);
+  else
+    d = max(k0 - lo, hi - k0);
+  return -slope2 * static_cast<float>(d);
 }
 
 // First key tile to visit and the tile count for a query tile.
@@ -321,6 +350,10 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
     const bool masked = masking(p);
+    // With the softcap every logit of a row lies within 2c of a bound known
+    // before any key is seen, so P is taken against that bound: no row max,
+    // no exchange between the halves, no rescale of O.
+    const bool fixed = lm.capped && p.softcap <= kFixedCapMax;
     uint32_t g = 0;
     int tcount = 0;
     bool ok = true;
@@ -335,6 +368,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       const float slope2 = p.slopes ? __ldg(p.slopes + t.b * p.slopes_bs + h) * kLog2e : 0.f;
       const int pos_off = i_loc + t.Lk - t.Lq;  // dist(j) = |pos_off - j|
       float m_run = -INFINITY, l = 0.f;          // l: this half's share of the row sum
+      uint64_t l2 = f2_make(0.f, 0.f), lu2 = l2;  // fixed reference: row sums as pairs
+      if (fixed) m_run = row_bound(p, t.Lk, pos_off, slope2);
+      const float bref = fixed ? m_run : 0.f;  // subtracted inside the logit
       for (int jj = 0; jj < n; ++jj) {
         const uint32_t gg = g + jj;
         const int key0 = ((t0 + jj) % n) * kKeys + half * 64;
@@ -361,12 +397,12 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c)
               xb[c] = fmaf(th[c], lm.out_scale,
-                           -slope2 * fabsf(pos0 - static_cast<float>(b * 32 + c)));
+                           fmaf(-slope2, fabsf(pos0 - static_cast<float>(b * 32 + c)), -bref));
           } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c)
               xb[c] = fmaf(xb[c], lm.in_scale,
-                           -slope2 * fabsf(pos0 - static_cast<float>(b * 32 + c)));
+                           fmaf(-slope2, fabsf(pos0 - static_cast<float>(b * 32 + c)), -bref));
           }
         }
         if (edge) {
@@ -377,6 +413,31 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
             if (masked) adm = adm && admissible(p, t.Lq, t.Lk, i_loc, jg);
             x[c] = adm ? x[c] : -INFINITY;
           }
+        }
+        if (fixed) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            x[c] = ex2_approx(x[c]);  // the reference is inside the logit
+            x[c + 1] = ex2_approx(x[c + 1]);
+            pk[c >> 1] = Pack<BF16>::two(x[c], x[c + 1]);
+            // two row sums: of P (for lse) and of the rounded P that
+            // multiplies V (for out, which is then exactly a weighted mean of
+            // V rows: one key gives out = v)
+            lu2 = f2_add(lu2, f2_make(x[c], x[c + 1]));
+            l2 = f2_add(l2, Pack<BF16>::unpack(pk[c >> 1]));
+          }
+          // the previous P V has finished reading the P region
+          if (gg >= 1 && !(ok = mbar_wait_warp(&bars->pv_done, (gg - 1) & 1, s_abort))) break;
+          tc_fence_after();
+          const uint32_t pb = tmem + kColP + half * 32 + lane_addr;
+          tmem_st16(pb, *reinterpret_cast<uint32_t(*)[16]>(pk));
+          tmem_st16(pb + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->p_full[gg & 1]);
+          continue;
         }
         float mx = -INFINITY;
 #pragma unroll
@@ -431,14 +492,23 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       }
       if (!ok) break;
       g += n;
+      float lr = 0.f;  // rounded-P sum (fixed reference)
+      if (fixed) {
+        l = f2_lo(lu2) + f2_hi(lu2);
+        lr = f2_lo(l2) + f2_hi(l2);
+      }
       // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2; each half 80 features
       float* ls = sSum + (tcount & 1) * 256;
+      float* lrs = sMax + (tcount & 1) * 256;  // the max exchange is idle here
       ls[half * 128 + r] = l;
+      if (fixed) lrs[half * 128 + r] = lr;
       if (!(ok = warp_exchange(&bars->l_x[tcount & 1], (tcount >> 1) & 1, s_abort))) break;
       const float lt = l + ls[(half ^ 1) * 128 + r];
+      const float lrt = fixed ? lr + lrs[(half ^ 1) * 128 + r] : 0.f;
       if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
       tc_fence_after();
-      const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
+      const float lnorm = fixed ? lrt : lt;
+      const float inv = (lnorm > 0.f) ? 1.f / lnorm : 0.f;
       if (row_valid && half == 0)
         p.lse[static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h] =
             (lt > 0.f) ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
