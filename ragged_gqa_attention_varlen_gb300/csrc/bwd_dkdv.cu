@@ -543,11 +543,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               lm.capped ? f2_mul(p1, f2_fma(t2[2 * q4 + 1], t2[2 * q4 + 1], m12)) : f2_mul(p1, m12);
         };
         if ((cols->general[b][0] | cols->general[b][1]) == 0) {
+          // one-sided tile: in three passes (all exponents, all exp2, then
+          // the packing and chain factors), so the 64 MUFU operations issue
+          // back to back
+          const uint64_t r2 = f2_make(rf, rf);
+          uint64_t z[32];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 a4 = pa[q4], m4 = pm[q4];
-            p_group(q4, fmaf(m4.x, rf, a4.x), fmaf(m4.y, rf, a4.y), fmaf(m4.z, rf, a4.z),
-                    fmaf(m4.w, rf, a4.w));
+            const uint64_t b0 = f2_fma(f2_make(m4.x, m4.y), r2, f2_make(a4.x, a4.y));
+            const uint64_t b1 = f2_fma(f2_make(m4.z, m4.w), r2, f2_make(a4.z, a4.w));
+            z[2 * q4] = f2_fma(t2[2 * q4], lm.capped ? os2 : is2, b0);
+            z[2 * q4 + 1] = f2_fma(t2[2 * q4 + 1], lm.capped ? os2 : is2, b1);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            z[i] = f2_make(ex2_approx(f2_lo(z[i])), ex2_approx(f2_hi(z[i])));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            pk[i] = Pack<BF16>::two(f2_lo(z[i]), f2_hi(z[i]));
+            // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
+            t2[i] = lm.capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
           }
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:
