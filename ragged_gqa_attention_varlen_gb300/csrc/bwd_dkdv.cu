@@ -347,8 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int st = 0; st < nsteps && ok; ++st) {
             const uint32_t gg = g + st;
-            // dV += P^T dO
+            // dV += P^T dO (P^T is written before dP^T is read, so the dO
+            // tile's arrival is not implied by p_full: wait for it here too)
             if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
+            if (!(ok = mbar_wait(&bars->do_full, gg & 1, s_abort))) break;
             if (st == 0 && tcount > 0 &&
                 !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
               break;
