@@ -218,13 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tiles of step st + kPrefetch are requested into L2 while step st is
       // loaded, so the loads that the ring can afford to wait for hit L2.
       constexpr int kPrefetch = 4;
-      for (int st = 0; st < nsteps; ++st, ++ndo) {
-        const int tok = t.q0 + (st / ngroups) * step_tok;
-        const int h0 = (st % ngroups) * G;
+      // step st = (token block stb, head group shg); (ptb, phg) is step
+      // st + kPrefetch; both advance without a division per step
+      auto advance = [&](int& tb, int& hg) {
+        if (++hg == ngroups) {
+          hg = 0;
+          ++tb;
+        }
+      };
+      int stb = 0, shg = 0, ptb = kPrefetch / ngroups, phg = kPrefetch % ngroups;
+      for (int st = 0; st < nsteps; ++st, ++ndo, advance(stb, shg), advance(ptb, phg)) {
+        const int tok = t.q0 + stb * step_tok;
+        const int h0 = shg * G;
         if (lane >= 4 && lane < 6 && st + kPrefetch < nsteps) {
-          const int sp = st + kPrefetch;
-          const int ptok = t.q0 + (sp / ngroups) * step_tok;
-          const int ph0 = (sp % ngroups) * G;
+          const int ptok = t.q0 + ptb * step_tok;
+          const int ph0 = phg * G;
           if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
           if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
         }

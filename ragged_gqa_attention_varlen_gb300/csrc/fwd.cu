@@ -221,8 +221,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           else
             tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
         }
-        for (int jj = 0; jj < n; ++jj, ++g) {
-          const int key = t.k0 + ((t0 + jj) % n) * kKeys;
+        // kt: key tile of step jj, (t0 + jj) mod n
+        for (int jj = 0, kt = t0; jj < n; ++jj, ++g, kt = (kt + 1 == n) ? 0 : kt + 1) {
+          const int key = t.k0 + kt * kKeys;
           const int s = g & 1;
           if (g >= 2 && !(ok = __all_sync(gmask, mbar_wait(kq ? &bars->k_empty[s] : &bars->v_empty[s],
                                                             ((g - 2) >> 1) & 1, s_abort))))
@@ -371,9 +372,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint64_t l2 = f2_make(0.f, 0.f), lu2 = l2;  // fixed reference: row sums as pairs
       if (fixed) m_run = row_bound(p, t.Lk, pos_off, slope2);
       const float bref = fixed ? m_run : 0.f;  // subtracted inside the logit
-      for (int jj = 0; jj < n; ++jj) {
+      for (int jj = 0, kt = t0; jj < n; ++jj, kt = (kt + 1 == n) ? 0 : kt + 1) {
         const uint32_t gg = g + jj;
-        const int key0 = ((t0 + jj) % n) * kKeys + half * 64;
+        const int key0 = kt * kKeys + half * 64;
         const uint32_t sb = tmem + (gg & 1) * 128 + half * 64 + lane_addr;
         if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
         tc_fence_after();
