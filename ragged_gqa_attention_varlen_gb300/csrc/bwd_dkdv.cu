@@ -389,8 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // staged.
     const int u = lane;
     const bool masked = masking(p);
-    struct Pos {  // a (key tile, query step) of this CTA
-      int item, st, nsteps;
+    const int lgGs = __ffs(G) - 1;  // G is a power of two
+    struct Pos {  // a (key tile, query step) of this CTA; st = tb * ngroups + hg
+      int item, st, tb, hg, nsteps;
       KTile t;
     };
     struct Vals {
@@ -407,9 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto next = [&](const Pos& q) {
       Pos n = q;
       if (q.item >= ntiles) return n;
-      if (++n.st < n.nsteps) return n;
+      if (++n.st < n.nsteps) {
+        if (++n.hg == ngroups) {
+          n.hg = 0;
+          ++n.tb;
+        }
+        return n;
+      }
       n.item += gridDim.x;
-      n.st = 0;
+      n.st = n.tb = n.hg = 0;
       seek(n);
       return n;
     };
@@ -417,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
         const int lc = u + 32 * hh;
-        const int i = (q.st / ngroups) * step_tok + lc / G;
-        const int h = (q.st % ngroups) * G + lc % G;
+        const int i = q.tb * step_tok + (lc >> lgGs);
+        const int h = q.hg * G + (lc & (G - 1));
         const bool live = q.item < ntiles;
         const bool valid = live && i < q.t.Lq;
         const int64_t ri = static_cast<int64_t>(q.t.q0 + i) * p.Hq + h;
@@ -429,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Pos q0;
     q0.item = blockIdx.x;
-    q0.st = 0;
+    q0.st = q0.tb = q0.hg = 0;
     q0.t = KTile{};
     seek(q0);
     Pos q1 = next(q0);
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
         const int lc = u + 32 * hh;
-        const int i = (q0.st / ngroups) * step_tok + lc / G;
+        const int i = q0.tb * step_tok + (lc >> lgGs);
         const float nl2 = v0.lse[hh] == -INFINITY ? -INFINITY : -v0.lse[hh] * kLog2e;
         const float sl2 = v0.sl2[hh] * kLog2e;
         const float prel = static_cast<float>(i + q0.t.Lk - q0.t.Lq - q0.t.key);
