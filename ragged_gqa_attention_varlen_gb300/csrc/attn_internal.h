@@ -38,6 +38,8 @@ struct Params {
   const void* outp;  // = out, read back by the preprocess kernel
   const void* dout;
   int64_t do_ts, do_hs;
+  const void* q;  // read row by row by the dq kernel (into TMEM)
+  int64_t q_ts, q_hs;
   const int32_t* cu_q;
   const int32_t* cu_k;
   const float* slopes;  // may be null

@@ -8,20 +8,24 @@
 // repeated calls are bitwise identical.
 //
 // Tile: the forward's 128 query rows.  Per key tile j:
-//   S_j  = Q K_j^T, dP_j = dO V_j^T   M=128 N=128 K=160, fp32 in TMEM
-//   dS_j                              elementwise warps; written as 16-bit
-//                                     pairs to a TMEM region of its own
-//   dQ  += dS_j K_j                   M=128 N=160 K=128, A operand from TMEM
+//   S_j  = Q K_j^T    M=128 N=128 K=160, Q from TMEM, K from shared memory
+//   dP_j = dO V_j^T   M=128 N=128 K=160, both from shared memory
+//   dS_j              elementwise warps; written as 16-bit pairs over the
+//                     columns of dP_j they have read
+//   dQ  += dS_j K_j   M=128 N=160 K=128, A operand from TMEM
 //
-// Warp roles (384 threads, 12 warps): warp 0 loads (Q, dO once per tile; K through two
-// slots, V through one; each tile as two boxes from two lanes), warp 1 issues the S and dP products, warp 2 the dQ
-// products, warps 4-11 do the elementwise work (two warps per TMEM lane
-// quadrant, each taking 64 of the 128 keys).  The elementwise warps release
-// S_j and dP_j as soon as they have read them, so S_{j+1} and dP_{j+1} run on
-// the tensor core while dS_j is still being formed; dS_j has its own TMEM
-// region, so dP_{j+1} never waits for dQ += dS_j K_j.  Q, dO and V are
-// only K-major operands here and keep their last 32 features in a 64-byte-
-// swizzled chunk; K is also the MN-major operand of dQ and stays in three
+// Warp roles (384 threads, 12 warps): warp 0 loads with TMA (dO once per
+// tile; K through three slots, V through one; each tile as two boxes from two
+// lanes), warp 1 issues the S and dP products, warp 2 the dQ products,
+// warps 4-11 do the elementwise work (two warps per TMEM lane quadrant, each
+// taking 64 of the 128 keys) and, at the start of each tile, copy the tile's
+// Q rows from global memory into TMEM.  Q lives in TMEM so that shared memory
+// holds three K slots: K of a key tile is read twice, by S early in the step
+// and by dQ at its end, and with two slots the load of K_{j+2} (which waits
+// for dQ of tile j) arrived after S_{j+2} was due.  S as a TMEM-A product also
+// reads half the shared-memory bytes of the SS form.  dO and V are only
+// K-major operands and keep their last 32 features in a 64-byte-swizzled
+// chunk; K is also the MN-major operand of dQ and stays in three
 // 128-byte-swizzled chunks.
 // Warp 3 only completes warpgroup 0, which hands most of its registers to
 // the elementwise warpgroups (setmaxnreg), so those can keep every column's
@@ -37,23 +41,37 @@ constexpr int kThreadsDQ = kThreads;  // 12 warps
 constexpr uint32_t kTile = 16384;            // 64-feature chunk of 128 rows
 constexpr uint32_t kTail = 8192;             // features 128..159 of 128 rows
 constexpr uint32_t kTailed = 2 * kTile + kTail;
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffDO = kTailed;
-constexpr uint32_t kOffK = 2 * kTailed;      // two K slots, 3 full chunks each
-constexpr uint32_t kOffV = kOffK + 2 * 3 * kTile;
+constexpr int kKSlots = 3;
+constexpr uint32_t kOffDO = 0;
+constexpr uint32_t kOffK = kTailed;          // three K slots, 3 full chunks each
+constexpr uint32_t kOffV = kOffK + kKSlots * 3 * kTile;
 constexpr uint32_t kOffBar = kOffV + kTailed;
 constexpr uint32_t kSmem = kOffBar + 256;    // base checked to be 1024-aligned
+static_assert(kSmem <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColP = 128;   // dP
-constexpr uint32_t kColDS = 256;  // dS as 16-bit pairs
-constexpr uint32_t kColQ = 320;   // dQ accumulator
+constexpr uint32_t kColP = 128;   // dP, then dS as 16-bit pairs over its read columns
+constexpr uint32_t kColQ = 256;   // dQ accumulator
+constexpr uint32_t kColQt = 416;  // the tile's Q rows as 16-bit pairs (80 columns)
 
 struct Bars {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t s_full, s_free, dp_full, dp_free, p_full, dq_done;
+  uint64_t q_full, q_empty, qt_full;
+  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full, v_empty;
+  uint64_t s_full, s_free, dp_full, p_full, dq_done;
   uint64_t o_full, o_empty, drain;
+};
+
+// Position in a three-slot ring: slot = n mod 3 and use = n / 3, advanced
+// without a division.
+struct Ring3 {
+  int slot = 0;
+  uint32_t use = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == kKSlots) {
+      slot = 0;
+      ++use;
+    }
+  }
 };
 }  // namespace dqk
 
@@ -74,7 +92,6 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   using namespace dqk;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
-  uint8_t* sQ = sm + kOffQ;
   uint8_t* sDO = sm + kOffDO;
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
@@ -100,7 +117,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(&bars->qt_full, 8);
+    for (int s = 0; s < kKSlots; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
     }
@@ -109,7 +127,6 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 8);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 8);
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->dq_done, 1);
     mbar_init(&bars->o_full, 1);
@@ -139,19 +156,18 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     // second), since a TMA operation costs about the same time whatever its
     // size and separate issuing threads overlap theirs.
     if (lane == 0) {
-      prefetch_tensormap(&tq2);
+      prefetch_tensormap(&tdo2);
       prefetch_tensormap(&tk2);
     } else if (lane == 1) {
-      prefetch_tensormap(&tqt);
+      prefetch_tensormap(&tdot);
       prefetch_tensormap(&tk);
     } else if (lane == 2) {
-      prefetch_tensormap(&tdo2);
       prefetch_tensormap(&tv2);
     } else if (lane == 3) {
-      prefetch_tensormap(&tdot);
       prefetch_tensormap(&tvt);
     }
     uint32_t g = 0;  // key tiles loaded
+    Ring3 kr;        // K slot of key tile g
     int tcount = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
@@ -160,24 +176,23 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       const int n = (t.Lk + kKeys - 1) / kKeys;
       const int h0 = t.hg * G, tok = t.q0 + t.tok;
       if (tcount > 0 && !(ok = mbar_wait_warp(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 2 * kTailed);
+      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, kTailed);
       __syncwarp();
-      if (lane == 0) tma_load_4d(sQ, &tq2, &bars->q_full, 0, h0, tok, 0);
-      if (lane == 1) tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, h0, tok);
-      if (lane == 2) tma_load_4d(sDO, &tdo2, &bars->q_full, 0, h0, tok, 0);
-      if (lane == 3) tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, h0, tok);
-      for (int j = 0; j < n && ok; ++j, ++g) {
+      if (lane == 0) tma_load_4d(sDO, &tdo2, &bars->q_full, 0, h0, tok, 0);
+      if (lane == 1) tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, h0, tok);
+      for (int j = 0; j < n && ok; ++j, ++g, kr.next()) {
         const int key = t.k0 + j * kKeys;
-        const int ks = g & 1;
-        if (g >= 2 && !(ok = mbar_wait_warp(&bars->k_empty[ks], ((g - 2) >> 1) & 1, s_abort)))
+        if (kr.use > 0 &&
+            !(ok = mbar_wait_warp(&bars->k_empty[kr.slot], (kr.use - 1) & 1, s_abort)))
           break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[ks], 3 * kTile);
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[kr.slot], 3 * kTile);
         __syncwarp();
-        uint8_t* dk = sK + ks * 3 * kTile;
-        if (lane == 0) tma_load_3d(dk, &tk2, &bars->k_full[ks], 0, key, 0);
-        if (lane == 1) tma_load_2d(dk + 2 * kTile, &tk, &bars->k_full[ks], 2 * kChunk, key);
+        uint8_t* dk = sK + kr.slot * 3 * kTile;
+        if (lane == 0) tma_load_3d(dk, &tk2, &bars->k_full[kr.slot], 0, key, 0);
+        if (lane == 1) tma_load_2d(dk + 2 * kTile, &tk, &bars->k_full[kr.slot], 2 * kChunk, key);
         if (g >= 1 && !(ok = mbar_wait_warp(&bars->v_empty, (g - 1) & 1, s_abort))) {
           ++g;  // the K fill above is armed
+          kr.next();
           break;
         }
         if (lane == 0) mbar_arrive_expect_tx(&bars->v_full, kTailed);
@@ -187,46 +202,52 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       }
     }
     if (*s_abort && lane == 0) {
+      // let every load this warp started land before the CTA exits
       if (tcount > 0) drain_wait_dq(&bars->q_full, (tcount - 1) & 1);
-      for (uint32_t f = g > 2 ? g - 2 : 0; f < g; ++f) drain_wait_dq(&bars->k_full[f & 1], (f >> 1) & 1);
+      for (uint32_t f = g > kKSlots ? g - kKSlots : 0; f < g; ++f)
+        drain_wait_dq(&bars->k_full[f % kKSlots], (f / kKSlots) & 1);
       if (g > 0) drain_wait_dq(&bars->v_full, (g - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S, dP issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-      const uint32_t qb = smem_addr(sQ), db = smem_addr(sDO), vb = smem_addr(sV);
+      const uint32_t db = smem_addr(sDO), vb = smem_addr(sV);
       // K-major operand stored as two 128-byte-swizzled chunks + a 64-byte tail
       auto tailed = [&](uint32_t base, int k) -> uint64_t {
         return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
                      : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
       };
       uint32_t g = 0;
+      Ring3 kr;
       int tcount = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         const int n = (t.Lk + kKeys - 1) / kKeys;
-        if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;
+        if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;   // dO tile
+        if (!(ok = mbar_wait(&bars->qt_full, tcount & 1, s_abort))) break;  // Q rows in TMEM
         if (n == 0) {
           mbar_arrive(&bars->q_empty);
           continue;
         }
-        for (int j = 0; j < n; ++j) {
+        for (int j = 0; j < n; ++j, kr.next()) {
           const uint32_t gs = g + j;
           // S = Q K^T once the previous S has been read
           if (gs >= 1 && !(ok = mbar_wait(&bars->s_free, (gs - 1) & 1, s_abort))) break;
-          if (!(ok = mbar_wait(&bars->k_full[gs & 1], (gs >> 1) & 1, s_abort))) break;
+          if (!(ok = mbar_wait(&bars->k_full[kr.slot], kr.use & 1, s_abort))) break;
           tc_fence_after();
-          const uint32_t kb = smem_addr(sK + (gs & 1) * 3 * kTile);
+          const uint32_t kb = smem_addr(sK + kr.slot * 3 * kTile);
+          // features 16k..16k+15 of Q: pair columns 8k..8k+7 of its region
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ss(tmem + kColS, tailed(qb, k),
+            umma_ts(tmem + kColS, tmem + kColQt + k * 8,
                     sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
           umma_commit(&bars->s_full);
-          // dP = dO V^T once the previous dP has been read
-          if (gs >= 1 && !(ok = mbar_wait(&bars->dp_free, (gs - 1) & 1, s_abort))) break;
+          // dP = dO V^T once dQ of the previous key tile has read dS (written
+          // over the previous dP, after it was read)
+          if (gs >= 1 && !(ok = mbar_wait(&bars->dq_done, (gs - 1) & 1, s_abort))) break;
           if (!(ok = mbar_wait(&bars->v_full, gs & 1, s_abort))) break;
           tc_fence_after();
 #pragma unroll
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
             umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
           umma_commit(&bars->dp_full);
           umma_commit(&bars->v_empty);
-          if (j + 1 == n) umma_commit(&bars->q_empty);  // last S and dP of this tile issued
+          if (j + 1 == n) umma_commit(&bars->q_empty);  // last dP of this tile issued
         }
         g += n;
       }
@@ -249,6 +270,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     if (lane == 0) {
       constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
       uint32_t g = 0;
+      Ring3 kr;
       int tcount = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
@@ -260,21 +282,21 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           mbar_arrive(&bars->o_full);
           continue;
         }
-        for (int j = 0; j < n; ++j) {
+        for (int j = 0; j < n; ++j, kr.next()) {
           const uint32_t gg = g + j;
           if (!(ok = mbar_wait(&bars->p_full, gg & 1, s_abort))) break;
           if (j == 0 && tcount > 0 &&
               !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort)))
             break;
           tc_fence_after();
-          const uint32_t kb = smem_addr(sK + (gg & 1) * 3 * kTile);
-          // keys 16k..16k+15: pair columns 8k..8k+7 of the dS region
+          const uint32_t kb = smem_addr(sK + kr.slot * 3 * kTile);
+          // keys 16k..16k+15: half k/4, pair column 8*(k%4) of that half's dP columns
 #pragma unroll
           for (int k = 0; k < kKeys / 16; ++k)
-            umma_ts(tmem + kColQ, tmem + kColDS + k * 8,
+            umma_ts(tmem + kColQ, tmem + kColP + (k >> 2) * 64 + (k & 3) * 8,
                     sdesc_sw128(kb + k * 2048, kTile, 1024), kIdQ, (j > 0 || k > 0));
           umma_commit(&bars->dq_done);
-          umma_commit(&bars->k_empty[gg & 1]);
+          umma_commit(&bars->k_empty[kr.slot]);
           if (j + 1 == n) umma_commit(&bars->o_full);
         }
         g += n;
@@ -293,6 +315,44 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
     const bool masked = masking(p);
+    const int lgG = __ffs(G) - 1;  // G is a power of two
+    // This lane's Q row of a tile into TMEM: features 80*half..80*half+79 as
+    // 40 pair columns (raw 16-bit pairs, the A-operand layout).  Rows outside
+    // the sequence get zeros.  Written once the previous tile's last S has
+    // completed (the caller has waited for it), then signalled to the S issuer.
+    auto load_q = [&](int qitem) -> bool {
+      QTile tq;
+      qtile_decode(p, qitem, tq);
+      const int il = tq.tok + (r >> lgG);
+      const int hq = tq.hg * G + (r & (G - 1));
+      uint32_t w[40];
+      if (il < tq.Lq) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(p.q) + static_cast<int64_t>(tq.q0 + il) * p.q_ts +
+            static_cast<int64_t>(hq) * p.q_hs + half * 80);
+#pragma unroll
+        for (int u = 0; u < 10; ++u) {
+          const uint4 v = __ldg(src + u);
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 40; ++u) w[u] = 0u;
+      }
+      const uint32_t qa = tmem + kColQt + half * 40 + lane_addr;
+      tmem_st16(qa, *reinterpret_cast<uint32_t(*)[16]>(w));
+      tmem_st16(qa + 16, *reinterpret_cast<uint32_t(*)[16]>(w + 16));
+      tmem_st8(qa + 32, *reinterpret_cast<uint32_t(*)[8]>(w + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->qt_full);
+      return true;
+    };
+    if (static_cast<int>(blockIdx.x) < ntiles) load_q(blockIdx.x);
     uint32_t g = 0;
     int tcount = 0;
     bool ok = true;
@@ -368,23 +428,14 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           float d[32];
           tmem_ld32(pbuf + cc * 32, d);
           tmem_wait_ld();
-          if (cc == 1) {  // all of dP read: the next dP may be computed
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->dp_free);
-          }
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
             pk[cc * 16 + (c >> 1)] = Pack<BF16>::two(x[cc * 32 + c] * (d[c] - Drow),
                                                      x[cc * 32 + c + 1] * (d[c + 1] - Drow));
         }
-        // dS pairs: this half's 64 keys -> 32 pair columns of the dS region,
-        // once dQ of the previous key tile has read it
-        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->dq_done, (gg - 1) & 1, s_abort))) break;
-        tc_fence_after();
-        const uint32_t dsbuf = tmem + kColDS + half * 32 + lane_addr;
-        tmem_st16(dsbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
-        tmem_st16(dsbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+        // dS pairs over this half's first 32 (already read) dP columns
+        tmem_st16(pbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        tmem_st16(pbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -392,6 +443,9 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       }
       if (!ok) break;
       g += n;
+      // Q of this warp's next tile (every S of this tile has completed: its
+      // last s_full was waited for above)
+      if (item + static_cast<int>(gridDim.x) < ntiles) load_q(item + gridDim.x);
       // ---- epilogue: dq = sigma * dQ, this half's 80 features
       if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
       tc_fence_after();

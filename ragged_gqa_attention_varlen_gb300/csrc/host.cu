@@ -270,6 +270,9 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   p.dv_ts = dv_ts;
   p.outp = out;
   p.dout = dout;
+  p.q = q;
+  p.q_ts = q_ts;
+  p.q_hs = q_hs;
   p.do_ts = do_ts;
   p.do_hs = do_hs;
   p.cu_q = cu_q;
