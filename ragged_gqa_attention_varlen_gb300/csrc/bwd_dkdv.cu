@@ -54,6 +54,7 @@ struct Bars {
   uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty;
   uint64_t s_full, s_read, dp_full, dp_read, p_full, dv_done, ds_full, dk_done;
   uint64_t acc_full, acc_empty, am_full[2], am_empty[2], d_full, d_empty, drain;
+  TileRing ring;  // key tiles drawn by warp 0 for the whole CTA
 };
 
 constexpr uint32_t kOffK = 0;
@@ -150,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->d_full, 1);
     mbar_init(&bars->d_empty, 8);
     mbar_init(&bars->drain, 2);  // one commit per issuing thread
+    // readers: the two MMA threads, the staging warp, the 8 elementwise warps
+    tile_ring_init(&bars->ring, 11);
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -193,7 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nkv = 0, ndo = 0;
     Pair nq;
     bool ok = true;
-    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x) {
+    uint32_t kpub = 0;
+    int item = -1, item_next = -1;
+    ok = tile_publish(&bars->ring, kpub, p.counters + 1, ntiles, &item, s_abort);
+    if (ok && item >= 0) ok = tile_publish(&bars->ring, kpub, p.counters + 1, ntiles, &item_next, s_abort);
+    for (; item >= 0 && ok; item = item_next,
+         ok = ok && (item < 0 || tile_publish(&bars->ring, kpub, p.counters + 1, ntiles,
+                                              &item_next, s_abort))) {
       KTile t;
       ktile_decode(p, item, t);
       const int nsteps = step_count(t);
@@ -315,7 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bars->s_full);
           return true;
         };
-        for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        uint32_t ktake = 0;
+        int item = -1;
+        for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
           KTile t;
           ktile_decode(p, item, t);
           const int nsteps = step_count(t);
@@ -343,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           g += nsteps;
         }
       } else {
-        for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+        uint32_t ktake = 0;
+        int item = -1;
+        for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
           KTile t;
           ktile_decode(p, item, t);
           const int nsteps = step_count(t);
@@ -397,12 +410,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     struct Vals {
       float lse[4], sl2[4], D[4];
     };
+    // the warp reads the tile stream as far ahead as its lookahead needs;
+    // a position past the end has item = ntiles
+    uint32_t ktake = 0;
+    bool sok = true;
+    auto take = [&]() -> int {
+      int it = -1;
+      if (sok) sok = tile_take_warp(&bars->ring, ktake, &it, s_abort);
+      return (sok && it >= 0) ? it : ntiles;
+    };
     auto seek = [&](Pos& q) {
       while (q.item < ntiles) {
         ktile_decode(p, q.item, q.t);
         q.nsteps = step_count(q.t);
         if (q.nsteps > 0) return;
-        q.item += gridDim.x;
+        q.item = take();
       }
     };
     auto next = [&](const Pos& q) {
@@ -415,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return n;
       }
-      n.item += gridDim.x;
+      n.item = take();
       n.st = n.tb = n.hg = 0;
       seek(n);
       return n;
@@ -435,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     Pos q0;
-    q0.item = blockIdx.x;
+    q0.item = take();
     q0.st = q0.tb = q0.hg = 0;
     q0.t = KTile{};
     seek(q0);
@@ -506,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     int tcount = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+    uint32_t ktake = 0;
+    int item = -1;
+    for (; (ok = tile_take_warp(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
       KTile t;
       ktile_decode(p, item, t);
       const int nsteps = step_count(t);

@@ -8,6 +8,7 @@
 // computes, so results stay bitwise reproducible.
 #pragma once
 #include "attn_internal.h"
+#include "sm103.cuh"
 
 namespace attn {
 
@@ -70,6 +71,68 @@ __device__ __forceinline__ void ktile_decode(const Params& p, int n, KTile& t) {
   t.k0 = __ldg(p.cu_k + b);
   t.Lq = __ldg(p.cu_q + b + 1) - t.q0;
   t.Lk = __ldg(p.cu_k + b + 1) - t.k0;
+}
+
+// Dynamic tile stream of a persistent CTA.  Warp 0 draws tile numbers from
+// a global counter (so tiles start in the schedule's longest-first order)
+// and publishes them through a four-deep ring in shared memory; every other
+// role of the CTA reads the same sequence, which ends with -1.  What a tile
+// computes never depends on which CTA computes it, so drawing tiles at run
+// time keeps the results bitwise repeatable, while SMs that run faster take
+// more tiles (the SMs of one GPU were measured to differ by up to ~10 %).
+struct TileRing {
+  int32_t item[4];
+  uint64_t full[4], empty[4];
+};
+
+__device__ __forceinline__ void tile_ring_init(TileRing* r, uint32_t consumers) {
+  for (int s = 0; s < 4; ++s) {
+    mbar_init(&r->full[s], 1);
+    mbar_init(&r->empty[s], consumers);
+  }
+}
+
+// Whole warp: draw the next tile, publish it as entry k (or -1 when none is
+// left) and return it in *out.  False if a wait gave up.
+__device__ __forceinline__ bool tile_publish(TileRing* r, uint32_t& k, int32_t* counter,
+                                             int ntiles, int* out, volatile int* abort) {
+  const int slot = k & 3;
+  if (k >= 4 && !mbar_wait_warp(&r->empty[slot], ((k >> 2) - 1) & 1, abort)) return false;
+  int it = 0;
+  if ((threadIdx.x & 31) == 0) {
+    it = atomicAdd(counter, 1);
+    if (it >= ntiles) it = -1;
+    r->item[slot] = it;
+  }
+  it = __shfl_sync(0xffffffffu, it, 0);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r->full[slot]);
+  ++k;
+  *out = it;
+  return true;
+}
+
+// One thread: read entry k of the stream.
+__device__ __forceinline__ bool tile_take(TileRing* r, uint32_t& k, int* out,
+                                          volatile int* abort) {
+  const int slot = k & 3;
+  if (!mbar_wait(&r->full[slot], (k >> 2) & 1, abort)) return false;
+  *out = *reinterpret_cast<volatile int32_t*>(&r->item[slot]);
+  mbar_arrive(&r->empty[slot]);
+  ++k;
+  return true;
+}
+
+// Whole warp: read entry k of the stream (one arrival for the warp).
+__device__ __forceinline__ bool tile_take_warp(TileRing* r, uint32_t& k, int* out,
+                                               volatile int* abort) {
+  const int slot = k & 3;
+  if (!mbar_wait_warp(&r->full[slot], (k >> 2) & 1, abort)) return false;
+  *out = *reinterpret_cast<volatile int32_t*>(&r->item[slot]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[slot]);
+  ++k;
+  return true;
 }
 
 // Key j of local query i is admissible under the causal/window mask.
