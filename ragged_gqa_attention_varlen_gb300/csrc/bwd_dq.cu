@@ -46,8 +46,6 @@ constexpr uint32_t kOffDO = 0;
 constexpr uint32_t kOffK = kTailed;          // three K slots, 3 full chunks each
 constexpr uint32_t kOffV = kOffK + kKSlots * 3 * kTile;
 constexpr uint32_t kOffBar = kOffV + kTailed;
-constexpr uint32_t kSmem = kOffBar + 256;    // base checked to be 1024-aligned
-static_assert(kSmem <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColP = 128;   // dP, then dS as 16-bit pairs over its read columns
@@ -59,7 +57,11 @@ struct Bars {
   uint64_t k_full[kKSlots], k_empty[kKSlots], v_full, v_empty;
   uint64_t s_full, s_free, dp_full, p_full, dq_done;
   uint64_t o_full, o_empty, drain;
+  TileRing ring;  // query tiles drawn by warp 0 for the whole CTA
 };
+// barriers, then the TMEM base address, the abort flag and the status copy
+constexpr uint32_t kSmem = kOffBar + sizeof(Bars) + 16;  // base checked to be 1024-aligned
+static_assert(kSmem <= 232448, "shared memory");
 
 // Position in a three-slot ring: slot = n mod 3 and use = n / 3, advanced
 // without a division.
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
     mbar_init(&bars->drain, 2);  // one commit per issuing thread
+    tile_ring_init(&bars->ring, 10);  // the two MMA threads, the 8 elementwise warps
     fence_barrier_init();
     *s_abort = 0;
   }
@@ -170,7 +173,13 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     Ring3 kr;        // K slot of key tile g
     int tcount = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+    uint32_t kpub = 0;
+    int item = -1, item_next = -1;
+    ok = tile_publish(&bars->ring, kpub, p.counters + 2, ntiles, &item, s_abort);
+    if (ok && item >= 0) ok = tile_publish(&bars->ring, kpub, p.counters + 2, ntiles, &item_next, s_abort);
+    for (; item >= 0 && ok; item = item_next, ++tcount,
+         ok = ok && (item < 0 || tile_publish(&bars->ring, kpub, p.counters + 2, ntiles,
+                                              &item_next, s_abort))) {
       QTile t;
       qtile_decode(p, item, t);
       const int n = (t.Lk + kKeys - 1) / kKeys;
@@ -222,7 +231,9 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       Ring3 kr;
       int tcount = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      uint32_t ktake = 0;
+      int item = -1;
+      for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         const int n = (t.Lk + kKeys - 1) / kKeys;
@@ -273,7 +284,9 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       Ring3 kr;
       int tcount = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      uint32_t ktake = 0;
+      int item = -1;
+      for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         const int n = (t.Lk + kKeys - 1) / kKeys;
@@ -352,11 +365,13 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       if (lane == 0) mbar_arrive(&bars->qt_full);
       return true;
     };
-    if (static_cast<int>(blockIdx.x) < ntiles) load_q(blockIdx.x);
     uint32_t g = 0;
     int tcount = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+    uint32_t ktake = 0;
+    int item = -1;
+    bool ok = tile_take_warp(&bars->ring, ktake, &item, s_abort);
+    if (ok && item >= 0) load_q(item);
+    for (int item_next = -1; ok && item >= 0; item = item_next, ++tcount) {
       QTile t;
       qtile_decode(p, item, t);
       const int n = (t.Lk + kKeys - 1) / kKeys;
@@ -443,9 +458,10 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       }
       if (!ok) break;
       g += n;
-      // Q of this warp's next tile (every S of this tile has completed: its
-      // last s_full was waited for above)
-      if (item + static_cast<int>(gridDim.x) < ntiles) load_q(item + gridDim.x);
+      // Q of the next tile (every S of this tile has completed: its last
+      // s_full was waited for above)
+      if (!(ok = tile_take_warp(&bars->ring, ktake, &item_next, s_abort))) break;
+      if (item_next >= 0) load_q(item_next);
       // ---- epilogue: dq = sigma * dQ, this half's 80 features
       if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
       tc_fence_after();

@@ -39,7 +39,8 @@
 // taken relative to the stale max and stays below 2^8.  With the softcap
 // (|t| <= c) and ALiBi (<= 0) no later tile can exceed the first tile's max
 // by more than 2*c*log2(e) = 8.66, so rescales are rare.
-// Warp 3 only completes warpgroup 0, which hands most of its registers to
+// Warp 3 draws the query tiles from a global counter for the whole CTA
+// (see TileRing).  Warpgroup 0 hands most of its registers to
 // the elementwise warpgroups (setmaxnreg), so those can keep every column's
 // MUFU/FMA chain of a batch in flight.
 #include "../../include/attn_varlen.h"
@@ -60,7 +61,6 @@ constexpr uint32_t kOffV = kOffK + 2 * kTailed;  // two V slots
 constexpr uint32_t kOffMax = kOffV + 2 * kTile3;  // [2 steps][2 halves][128] fp32
 constexpr uint32_t kOffSum = kOffMax + 2 * 2 * 128 * 4;     // [2 tiles][2 halves][128] fp32
 constexpr uint32_t kOffBar = kOffSum + 2 * 2 * 128 * 4;
-constexpr uint32_t kSmem = kOffBar + 256;  // the dynamic base is checked to be 1024-aligned
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 256;          // S0: [0,128), S1: [128,256), P: [256,320)
 constexpr uint32_t kColO = 320;          // O: [320, 480)
@@ -72,7 +72,11 @@ struct Bars {
   uint64_t s_full[2], s_read[2], p_full[2], pv_done;
   uint64_t o_full, o_empty, drain;
   uint64_t mx_x[2], l_x[2];  // row-max and row-sum exchanges between the halves
+  TileRing ring;             // query tiles drawn by warp 3 for the whole CTA
 };
+// barriers, then the TMEM base address, the abort flag and the status copy
+constexpr uint32_t kSmem = kOffBar + sizeof(Bars) + 16;  // base checked to be 1024-aligned
+static_assert(kSmem <= 232448, "shared memory");
 }  // namespace fwd
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -165,6 +169,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 8);
     mbar_init(&bars->drain, 2);  // one commit per issuing thread
+    // readers: the K and the V load groups, the two MMA threads, 8 softmax warps
+    tile_ring_init(&bars->ring, 12);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->mx_x[b], 8);
       mbar_init(&bars->l_x[b], 8);
@@ -205,7 +211,18 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint32_t g = 0;  // key steps loaded
       int tcount = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      // each load group reads the tile stream through its lead lane
+      uint32_t ktake = 0;
+      auto take = [&](int& it) -> bool {
+        int v = -1, good = 1;
+        if (lead) good = tile_take(&bars->ring, ktake, &v, s_abort) ? 1 : 0;
+        v = __shfl_sync(gmask, v, kq ? 0 : 1);
+        good = __shfl_sync(gmask, good, kq ? 0 : 1);
+        it = v;
+        return good != 0;
+      };
+      int item = -1;
+      for (; (ok = take(item)) && item >= 0; ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         int n, t0;
@@ -266,7 +283,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         return k < 8 ? sdesc_sw128(base + (k >> 2) * kTile + (k & 3) * 32, 16, 1024)
                      : sdesc_sw64(base + 2 * kTile + (k - 8) * 32);
       };
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      uint32_t ktake = 0;
+      int item = -1;
+      for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         int n, t0;
@@ -307,7 +326,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint32_t g = 0;
       int tcount = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+      uint32_t ktake = 0;
+      int item = -1;
+      for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
         qtile_decode(p, item, t);
         int n, t0;
@@ -340,6 +361,12 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       umma_commit(&bars->drain);
       drain_wait(&bars->drain, 0);
     }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ tile stream
+    uint32_t kpub = 0;
+    int it = 0;
+    bool ok = true;
+    while (ok && it >= 0) ok = tile_publish(&bars->ring, kpub, p.counters, ntiles, &it, s_abort);
   }
   } else {
   warpgroup_reg_alloc<kRegsHigh>();
@@ -358,7 +385,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     uint32_t g = 0;
     int tcount = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < ntiles && ok; item += gridDim.x, ++tcount) {
+    uint32_t ktake = 0;
+    int item = -1;
+    for (; (ok = tile_take_warp(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
       QTile t;
       qtile_decode(p, item, t);
       int n, t0;
