@@ -298,7 +298,6 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     start.record(stream)
     for s in range(args.steps):
-        binding.record_events_next_call(ev[s])
         call()
     end.record(stream)
     torch.cuda.synchronize()
@@ -308,6 +307,13 @@ def run_gpu(args, world, rank, local):
     status = binding.device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
+    # per-kernel split from separate calls with an event between every two
+    # kernels (the events keep dq from overlapping the tail of dk/dv, so the
+    # timed calls above carry none)
+    for s in range(args.steps):
+        binding.record_events_next_call(ev[s])
+        call()
+    torch.cuda.synchronize()
     per_kernel = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) /
                   args.steps for i, name in enumerate(binding.KERNELS)}
     value, ms = aggregate(flops, total_s, args.steps, world)

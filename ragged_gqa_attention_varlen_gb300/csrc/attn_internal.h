@@ -77,7 +77,7 @@ cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorM
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
-                      int grid, cudaStream_t s);
+                      int grid, bool overlap, cudaStream_t s);
 cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
                              cudaStream_t s);
 cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s);

@@ -116,6 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int ntiles = ktile_count(p);
+  // the next kernel (dq, launched as a programmatic dependent) reads nothing
+  // this one writes, so it may be scheduled as soon as SMs free up
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     *s_status = *reinterpret_cast<volatile int32_t*>(p.status);
     // every tile here needs a 1024-byte-aligned base (swizzle atoms)

@@ -503,17 +503,23 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
-                      int grid, cudaStream_t s) {
-  if (p.dtype == 1) {
-    auto k = dq_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt);
-  } else {
-    auto k = dq_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
-    k<<<grid, dqk::kThreadsDQ, dqk::kSmem, s>>>(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt);
-  }
-  return cudaGetLastError();
+                      int grid, bool overlap, cudaStream_t s) {
+  auto k = p.dtype == 1 ? dq_kernel<true> : dq_kernel<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
+  // With `overlap` the launch is a programmatic dependent of the kernel before
+  // it (dk/dv, which signals at its start): dq reads nothing dk/dv writes, so
+  // its CTAs may start on the SMs that dk/dv's last CTAs leave idle.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(dqk::kThreadsDQ);
+  cfg.dynamicSmemBytes = dqk::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt);
 }
 
 }  // namespace attn

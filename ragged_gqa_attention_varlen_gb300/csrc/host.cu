@@ -349,7 +349,9 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
       cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(4);
-  if (launch_dq(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt, grid_q, stream) != cudaSuccess)
+  // dq may overlap the tail of dk/dv (no per-kernel events in between)
+  if (launch_dq(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt, grid_q, nev == 0, stream) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
   mark(5);
   return ATTN_OK;
