@@ -117,6 +117,50 @@ attn_status attn_varlen_fvjp_fwd_bwd(
     float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
     void *stream);
 
+/* The two halves of the fused call, for training loops that run the forward
+ * pass and, later, the backward pass: the steps either side of the fused
+ * call of the same page ("Noncausal Global Extreme-GQA Ragged Attention Full
+ * VJP", "What You Have": the function returns out and the gradients; the
+ * backward recomputes the softmax from the stored lse as in "ragged flash
+ * attention gradient recompute", "Root causes addressed").
+ *
+ * attn_varlen_fwd writes out and lse only (same arguments, layouts and rules
+ * as attn_varlen_fvjp_fwd_bwd without dout, dq, dk, dv).
+ *
+ * attn_varlen_bwd reads out and lse as written by attn_varlen_fwd (or the
+ * fused call) for the same q, k, v, cu arrays, slopes, mask, softcap and
+ * scale, and writes dq, dk, dv.  out and lse are inputs here and are not
+ * modified.  The workspace is the one attn_varlen_fvjp_workspace_size sizes;
+ * it need not be the one the forward used.  For the same inputs the three
+ * calls give bitwise the same out, lse, dq, dk and dv: they run the same
+ * kernels. */
+attn_status attn_varlen_fwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+attn_status attn_varlen_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    const void *out, int64_t out_tok_stride, int64_t out_head_stride, const float *lse,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
+
 /* A static description of an attn_status value. */
 const char *attn_status_string(attn_status s);
 

@@ -21,7 +21,7 @@ DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0
 
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
-           "attn_varlen_fvjp_fwd_bwd_noalloc")
+           "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -56,6 +56,14 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
         [P, P, P])
     lib.attn_varlen_fvjp_fwd_bwd_noalloc.restype = I
+    lib.attn_varlen_fwd.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 3 + [P, P, P, L, I, I, I, F, F] + [P, L, L] +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fwd.restype = I
+    lib.attn_varlen_bwd.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L, P] +
+        [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_bwd.restype = I
     lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
     lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
@@ -163,6 +171,116 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     if code != 0:
         raise AttnError(code, lib.attn_status_string(code).decode())
     return dict(out=out, dq=dq, dk=dk, dv=dv, lse=lse, workspace=workspace)
+
+
+def _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout=None):
+    """Validate the inputs shared by every entry point; returns (dtype, B, Hq)."""
+    dtype = q.dtype
+    if dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("q must be fp16 or bf16")
+    Hq = q.shape[1]
+    _check_qlike("q", q, dtype)
+    _check_qlike("k", k, dtype, 1)
+    _check_qlike("v", v, dtype, 1)
+    if v.shape[0] != k.shape[0]:
+        raise ValueError("v must match k in length")
+    if dout is not None:
+        _check_qlike("dout", dout, dtype, Hq)
+        if dout.shape[0] != q.shape[0]:
+            raise ValueError("dout must match q in length")
+    for name, c in (("cu_q", cu_q), ("cu_k", cu_k)):
+        if not c.is_cuda or c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+    B = cu_q.numel() - 1
+    if cu_k.numel() != B + 1:
+        raise ValueError("cu_q and cu_k must have the same length")
+    if alibi_slopes is not None:
+        if (not alibi_slopes.is_cuda or alibi_slopes.dtype != torch.float32 or
+                alibi_slopes.shape != (B, Hq) or alibi_slopes.stride(1) != 1):
+            raise ValueError("alibi_slopes must be fp32 [B, Hq] on the device, head stride 1")
+    return dtype, B, Hq
+
+
+def _workspace(workspace, B, Hq, Tq, Tk, device):
+    ws_bytes = workspace_size(B, Hq, Tq, Tk)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window_left=-1,
+                         window_right=-1, softcap=3.0, scale_multiplier=0.75, out=None, lse=None,
+                         workspace=None, stream=None):
+    """Forward only: returns (out, lse).  Same argument rules as
+    attention_varlen_fvjp; lse is fp32 [T_q, Hq] (natural log), the value the
+    backward call reads back.  Asynchronous on ``stream``."""
+    lib = load()
+    dtype, B, Hq = _check_common(q, k, v, cu_q, cu_k, alibi_slopes)
+    Tq, Tk = q.shape[0], k.shape[0]
+    out = _like(q) if out is None else out
+    _check_qlike("out", out, dtype, Hq)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
+    _check_lse(lse, Tq, Hq)
+    workspace = _workspace(workspace, B, Hq, Tq, Tk, q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    code = lib.attn_varlen_fwd(
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1),
+        _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+        alibi_slopes.stride(0) if alibi_slopes is not None else 0,
+        int(bool(causal)), int(window_left), int(window_right), float(softcap),
+        float(scale_multiplier), _ptr(out), out.stride(0), out.stride(1),
+        _ptr(lse), _ptr(workspace), workspace.numel(), None, stream.cuda_stream)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+    return out, lse
+
+
+def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, causal=False,
+                         window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
+                         dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward only: given the forward's out and lse for the same inputs and
+    options, returns (dq, dk, dv).  out and lse are read, not modified.  For
+    the same inputs the result is bitwise the one attention_varlen_fvjp gives.
+    Asynchronous on ``stream``."""
+    lib = load()
+    dtype, B, Hq = _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout)
+    Tq, Tk = q.shape[0], k.shape[0]
+    _check_qlike("out", out, dtype, Hq)
+    if out.shape[0] != Tq:
+        raise ValueError("out must match q in length")
+    _check_lse(lse, Tq, Hq)
+    dq = _like(q) if dq is None else dq
+    dk = _like(k) if dk is None else dk
+    dv = _like(v) if dv is None else dv
+    for name, t, H in (("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+        _check_qlike(name, t, dtype, H)
+    workspace = _workspace(workspace, B, Hq, Tq, Tk, q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    code = lib.attn_varlen_bwd(
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
+        _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+        alibi_slopes.stride(0) if alibi_slopes is not None else 0,
+        int(bool(causal)), int(window_left), int(window_right), float(softcap),
+        float(scale_multiplier), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
+        _ptr(dq), dq.stride(0), dq.stride(1), _ptr(dk), dk.stride(0), dk.stride(1),
+        _ptr(dv), dv.stride(0), dv.stride(1),
+        _ptr(workspace), workspace.numel(), None, stream.cuda_stream)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+    return dq, dk, dv
+
+
+def _check_lse(lse, Tq, Hq):
+    if (not lse.is_cuda or lse.dtype != torch.float32 or lse.shape != (Tq, Hq) or
+            not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous fp32 [{Tq}, {Hq}] CUDA tensor")
 
 
 def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv, lse,

@@ -205,8 +205,14 @@ extern "C" const char* attn_status_string(attn_status s) {
   return "unknown status";
 }
 
-extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
-    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+namespace {
+constexpr int kModeFwd = 1;  // out, lse
+constexpr int kModeBwd = 2;  // dq, dk, dv from out and lse
+
+// The three entry points share one body: host-side validation, the tensor
+// maps, and the launches of the requested passes.
+attn_status run_call(
+    int mode, attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
     const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
     const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
     const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
@@ -215,6 +221,7 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
     int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts,
     int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
     void* stream_ptr) {
+  const bool fwd = (mode & kModeFwd) != 0, bwd = (mode & kModeBwd) != 0;
   (void)k_hs;
   (void)v_hs;
   (void)dk_hs;
@@ -231,19 +238,33 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   if (B > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID;
   if (alibi_slopes && slopes_batch_stride < Hq && B > 1) return ATTN_ERR_INVALID;
   const bool has_q = total_q > 0, has_k = total_k > 0;
-  if (has_q && (!q || !dout || !out || !dq || !lse)) return ATTN_ERR_INVALID;
-  if (has_k && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID;
+  if (has_q && (!q || !out || !lse)) return ATTN_ERR_INVALID;
+  if (has_q && bwd && (!dout || !dq)) return ATTN_ERR_INVALID;
+  if (has_k && (!k || !v)) return ATTN_ERR_INVALID;
+  if (has_k && bwd && (!dk || !dv)) return ATTN_ERR_INVALID;
   if (has_q) {
-    for (const void* ptr : {q, dout, static_cast<const void*>(out), static_cast<const void*>(dq)})
+    for (const void* ptr : {q, static_cast<const void*>(out)})
       if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
-    for (int64_t s : {q_ts, q_hs, do_ts, do_hs, out_ts, out_hs, dq_ts, dq_hs})
+    for (int64_t s : {q_ts, q_hs, out_ts, out_hs})
       if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (bwd) {
+      for (const void* ptr : {dout, static_cast<const void*>(dq)})
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+      for (int64_t s : {do_ts, do_hs, dq_ts, dq_hs})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    }
   }
   if (has_k) {
-    for (const void* ptr : {k, v, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    for (const void* ptr : {k, v})
       if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
-    for (int64_t s : {k_ts, v_ts, dk_ts, dv_ts})
+    for (int64_t s : {k_ts, v_ts})
       if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (bwd) {
+      for (const void* ptr : {static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+      for (int64_t s : {dk_ts, dv_ts})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    }
   }
   const WsLayout ws = ws_layout(B, Hq, total_q);
   if (!workspace || workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -294,14 +315,16 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   if (!has_q || !has_k) {
     if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
     cudaError_t e = cudaSuccess;
-    if (has_k) {  // no queries: dk = dv = 0
+    if (has_k && bwd) {  // no queries: dk = dv = 0
       e = launch_zero_fill(dk, total_k, 1, dk_ts, 8, stream);
       if (e == cudaSuccess) e = launch_zero_fill(dv, total_k, 1, dv_ts, 8, stream);
     }
     if (has_q) {  // no keys: every row is empty
-      e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, stream);
-      if (e == cudaSuccess) e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, stream);
-      if (e == cudaSuccess) e = launch_fill_f32(lse, total_q * Hq, -INFINITY, stream);
+      if (fwd) {
+        if (e == cudaSuccess) e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, stream);
+        if (e == cudaSuccess) e = launch_fill_f32(lse, total_q * Hq, -INFINITY, stream);
+      }
+      if (bwd && e == cudaSuccess) e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, stream);
     }
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
@@ -310,18 +333,19 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   if (!encode_fn()) return ATTN_ERR_CUDA;
   CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2, tqf, tdof;
   if (!encode_q_full(&tqf, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_q_full(&tdof, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
       !encode_q_pair(&tq2, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_q_pair(&tdo2, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
       !encode_kv_pair(&tk2, dtype, k, total_k, k_ts) ||
       !encode_kv_pair(&tv2, dtype, v, total_k, v_ts) ||
       !encode_q(&tq, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
       !encode_q(&tqt, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ, true) ||
-      !encode_q(&tdot, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ, true) ||
       !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts) ||
       !encode_kv(&tkt, dtype, k, total_k, k_ts, true) ||
       !encode_kv(&tvt, dtype, v, total_k, v_ts, true))
+    return ATTN_ERR_ALIGNMENT;
+  if (bwd && (!encode_q_full(&tdof, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+              !encode_q_pair(&tdo2, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+              !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
+              !encode_q(&tdot, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ, true)))
     return ATTN_ERR_ALIGNMENT;
 
   const int sms = sm_count();
@@ -333,15 +357,18 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
   const int grid_q = static_cast<int>(qtiles_max < sms ? qtiles_max : sms);
   const int grid_k = static_cast<int>(ktiles_max < sms ? ktiles_max : sms);
 
-  const int nev = g_nevents;
-  g_nevents = 0;
+  // the timing hook applies to the fused call only
+  const int nev = (fwd && bwd) ? g_nevents : 0;
+  if (fwd && bwd) g_nevents = 0;
   auto mark = [&](int i) {
     if (nev) cudaEventRecord(g_events[i], stream);
   };
   mark(0);
   if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(1);
-  if (launch_fwd(p, tq2, tqt, tk2, tkt, tv2, tv, grid_q, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (fwd && launch_fwd(p, tq2, tqt, tk2, tkt, tv2, tv, grid_q, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (!bwd) return ATTN_OK;
   mark(2);
   if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(3);
@@ -355,4 +382,57 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
     return ATTN_ERR_CUDA;
   mark(5);
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_varlen_fvjp_fwd_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, void* out, int64_t out_ts, int64_t out_hs, void* dq, int64_t dq_ts,
+    int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts,
+    int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
+    void* stream) {
+  return run_call(kModeFwd | kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts,
+                  q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k,
+                  alibi_slopes, slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, dq, dq_ts, dq_hs, dk, dk_ts, dk_hs, dv,
+                  dv_ts, dv_hs, lse, workspace, workspace_bytes, device_status, stream);
+}
+
+extern "C" attn_status attn_varlen_fwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const int32_t* cu_q, const int32_t* cu_k,
+    const float* alibi_slopes, int64_t slopes_batch_stride, int causal, int window_left,
+    int window_right, float softcap, float scale_multiplier, void* out, int64_t out_ts,
+    int64_t out_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
+    void* stream) {
+  return run_call(kModeFwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, nullptr, 0, 0, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, nullptr, 0, 0, nullptr, 0, 0, nullptr,
+                  0, 0, lse, workspace, workspace_bytes, device_status, stream);
+}
+
+extern "C" attn_status attn_varlen_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, const void* out, int64_t out_ts, int64_t out_hs, const float* lse,
+    void* dq, int64_t dq_ts, int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv,
+    int64_t dv_ts, int64_t dv_hs, void* workspace, size_t workspace_bytes,
+    int32_t* device_status, void* stream) {
+  // out and lse are only read on this path
+  return run_call(kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, const_cast<void*>(out), out_ts, out_hs, dq, dq_ts, dq_hs, dk,
+                  dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
+                  workspace_bytes, device_status, stream);
 }

@@ -147,6 +147,60 @@ def test_edge_parity(oracle_mod, case):
     parity(p, oracle_mod)
 
 
+# ------------------------------------------- split forward / backward calls
+
+def _split_cases():
+    return [("tiny", lambda: W.tiny()),
+            ("tiny_causal_win16", lambda: W.tiny(causal=True, window_left=16, window_right=16)),
+            ("ragged_bf16_strided", lambda: W.custom([0, 37, 300, 1], [9, 0, 260, 130], 16,
+                                                     dtype=torch.bfloat16, step=2))]
+
+
+def _split(p, out=None, lse=None):
+    mask = (p.causal, p.window_left, p.window_right, p.softcap, p.scale_multiplier)
+    if out is None:
+        out, lse = BND.attention_varlen_fwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, *mask)
+    dq, dk, dv = BND.attention_varlen_bwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                          out, lse, *mask)
+    torch.cuda.synchronize()
+    return dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+@pytest.mark.parametrize("idx", range(3), ids=[c[0] for c in _split_cases()])
+def test_split_calls_bitwise_equal_fused_and_match_oracle(oracle_mod, idx):
+    """Forward then backward as two calls gives bitwise the fused call's five
+    tensors (the same kernels run), and agrees with the oracle."""
+    p_cpu = _split_cases()[idx][1]()
+    p = p_cpu.to("cuda")
+    fused = run(p)
+    split = _split(p)
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert bits_equal(fused[n], split[n]), n
+    check_all(split, oracle_mod.fvjp(p_cpu), p_cpu.dtype)
+
+
+def test_split_backward_reads_out_and_lse_without_writing_them():
+    p = W.tiny().to("cuda")
+    out, lse = BND.attention_varlen_fwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes)
+    torch.cuda.synchronize()
+    h = [view_bytes_hash(out), view_bytes_hash(lse)]
+    r1 = _split(p, out, lse)
+    r2 = _split(p, out, lse)
+    assert h == [view_bytes_hash(out), view_bytes_hash(lse)]
+    for n in ("dq", "dk", "dv"):
+        assert bits_equal(r1[n], r2[n]), n
+
+
+def test_split_degenerate_sizes():
+    p = W.custom([5, 3], [0, 0], 16).to("cuda")
+    r = _split(p)
+    assert torch.all(r["out"] == 0) and torch.all(r["dq"] == 0)
+    assert torch.all(r["lse"] == -math.inf)
+    p = W.custom([0, 0], [7, 3], 16).to("cuda")
+    r = _split(p)
+    assert torch.all(r["dk"] == 0) and torch.all(r["dv"] == 0)
+
+
 def test_no_cap_large_logits(oracle_mod):
     p = W.custom([50, 20], [300, 90], 16, qk_std=6.0)
     p.softcap = 0.0
