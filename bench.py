@@ -36,17 +36,47 @@ UNIT = "TFLOP/s"
 HEAD_DIM = 160
 
 
+def scored_pairs(p) -> int:
+    """(query, key) pairs the mask admits, summed over sequences: Lq Lk
+    without a mask.  Key j is admissible for query i when
+    i + Lk - Lq - wl <= j <= i + Lk - Lq + wr (causal: wr = 0; a negative
+    window is unbounded)."""
+    import numpy as np
+
+    if not (p.causal or p.window_left >= 0 or p.window_right >= 0):
+        return p.sum_lq_lk()
+    wr = 0 if p.causal else p.window_right
+    total = 0
+    for lq, lk in zip(*p.lengths()):
+        k0 = np.arange(lq, dtype=np.int64) + (lk - lq)
+        lo = np.maximum(0, k0 - p.window_left) if p.window_left >= 0 else np.zeros_like(k0)
+        hi = np.minimum(lk - 1, k0 + wr) if wr >= 0 else np.full_like(k0, lk - 1)
+        total += int(np.clip(hi - lo + 1, 0, None).sum())
+    return total
+
+
 def counted_flops(p) -> float:
-    """4 Lq Lk d (forward) + 10 Lq Lk d (backward) per query head."""
-    return 14.0 * HEAD_DIM * p.Hq * p.sum_lq_lk()
+    """4 d (forward) + 10 d (backward) per admissible (query, key) pair and
+    query head: 14 Lq Lk d per head without a mask."""
+    return 14.0 * HEAD_DIM * p.Hq * scored_pairs(p)
 
 
 def kernel_flops(p) -> dict:
     """Algorithmic flops each kernel contributes to the counted total: the
     forward's two matmuls (4d), dk/dv's four (S^T, dP^T, dV, dK: 8d) and dq's
     dQ = dS K (2d); dq's recompute of S and dP is not counted."""
-    u = HEAD_DIM * p.Hq * p.sum_lq_lk()
+    u = HEAD_DIM * p.Hq * scored_pairs(p)
     return {"forward": 4 * u, "dkdv": 8 * u, "dq": 2 * u, "schedule": 0.0, "preprocess": 0.0}
+
+
+def mask_name(p) -> str:
+    """Suffix naming the mask of a workload ('' without one)."""
+    parts = []
+    if p.causal:
+        parts.append("causal")
+    if p.window_left >= 0 or p.window_right >= 0:
+        parts.append(f"window ({p.window_left}, {p.window_right})")
+    return (", " + " + ".join(parts)) if parts else ""
 
 
 def peaks():
@@ -261,6 +291,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False,
                                 length_scale=args.length_scale)
+    p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
     flops = counted_flops(p)
     kflops = kernel_flops(p)
     out = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
@@ -275,7 +306,8 @@ def run_gpu(args, world, rank, local):
 
     def call():
         binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
-                                      False, -1, -1, p.softcap, p.scale_multiplier, **kw)
+                                      p.causal, p.window_left, p.window_right, p.softcap,
+                                      p.scale_multiplier, **kw)
 
     for _ in range(args.warmup):
         call()
@@ -326,7 +358,8 @@ def run_gpu(args, world, rank, local):
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": dram_traffic(dom) if args.length_scale == 1.0 else None,
+                "traffic": dram_traffic(dom) if args.length_scale == 1.0 and not mask_name(p)
+                           else None,
                 "peak_kind": f"{kind} bf16 sustained"}
     whole_frac = value / world / pk["bf16_tflops"]
 
@@ -340,17 +373,19 @@ def run_gpu(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, generated on device)",
             "config": {"workload": "long_balanced" + (
-                           "" if args.length_scale == 1.0 else f" x{args.length_scale} length"),
+                           "" if args.length_scale == 1.0 else f" x{args.length_scale} length") +
+                           mask_name(p),
                        "B": p.B, "Hq": p.Hq, "Hkv": 1,
                        "head_dim": HEAD_DIM, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
+                       "scored_pairs": scored_pairs(p),
                        "counted_tflop_per_step": flops / 1e12,
                        "l2": "inputs larger than L2 (q view alone is "
                              f"{p.q.numel() * 2 / 1e9:.1f} GB)"},
             "latency_ms": ms, "frac_of_bf16_peak": whole_frac,
             "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
             "clocks": clk, "e2e": e2e}
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and not mask_name(p):
         v, cores, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -378,7 +413,8 @@ def run_e2e(args, p, kw, flops, stream, world):
         for h, d in zip(host_in, dev_in):
             d.copy_(h, non_blocking=True)
         binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
-                                      False, -1, -1, p.softcap, p.scale_multiplier, **kw)
+                                      p.causal, p.window_left, p.window_right, p.softcap,
+                                      p.scale_multiplier, **kw)
         for d, h in zip(dev_out, host_out):
             h.copy_(d, non_blocking=True)
 
@@ -411,6 +447,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--length-scale", type=float, default=1.0,
                     help="scale every sequence length (small cases for profiling)")
+    ap.add_argument("--causal", action="store_true",
+                    help="time the causal variant (flops counted over admissible pairs)")
+    ap.add_argument("--window-left", type=int, default=-1)
+    ap.add_argument("--window-right", type=int, default=-1)
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

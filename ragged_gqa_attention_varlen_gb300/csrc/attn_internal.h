@@ -54,6 +54,9 @@ struct Params {
   int32_t* sched;     // schedule arrays, see sched.cu
 };
 
+// The call has a causal or window mask (selects the masked kernel instances).
+inline bool masked_call(const Params& p) { return p.causal || p.wl >= 0 || p.wr >= 0; }
+
 // Layout of the schedule arrays inside Params::sched (all int32):
 //   [0, B)          fwd/dq sequence order (longest key range first)
 //   [B, 2B+1)       fwd/dq item prefix over that order

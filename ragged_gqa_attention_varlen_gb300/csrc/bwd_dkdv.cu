@@ -91,7 +91,7 @@ struct Pair {
   }
 };
 
-template <bool BF16>
+template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.G;
   const int step_tok = kRowsQ / G;
   const int ngroups = p.Hq / G;
-  auto step_count = [&](const KTile& t) { return ((t.Lq + step_tok - 1) / step_tok) * ngroups; };
+  // steps of a key tile: query blocks t.tb0 .. t.tb0 + t.ntb - 1, each over every head group
+  auto step_count = [&](const KTile& t) { return t.ntb * ngroups; };
 
   // Each role runs inside the branch that set its register budget, so the
   // compiler allocates each branch against its own budget.
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
          ok = ok && (item < 0 || tile_publish(&bars->ring, kpub, p.counters + 1, ntiles,
                                               &item_next, s_abort))) {
       KTile t;
-      ktile_decode(p, item, t);
+      ktile_decode<MASK>(p, item, t);
       const int nsteps = step_count(t);
       const int key = t.k0 + t.key;
       if (nkv > 0 && !(ok = mbar_wait_warp(&bars->kv_empty, (nkv - 1) & 1, s_abort))) break;
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
       if (lane >= 4 && lane < 6) {
         for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
-          const int ptok = t.q0 + (sp / ngroups) * step_tok;
+          const int ptok = t.q0 + (t.tb0 + sp / ngroups) * step_tok;
           const int ph0 = (sp % ngroups) * G;
           if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
           if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++tb;
         }
       };
-      int stb = 0, shg = 0, ptb = kPrefetch / ngroups, phg = kPrefetch % ngroups;
+      int stb = t.tb0, shg = 0, ptb = t.tb0 + kPrefetch / ngroups, phg = kPrefetch % ngroups;
       for (int st = 0; st < nsteps; ++st, ++ndo, advance(stb, shg), advance(ptb, phg)) {
         const int tok = t.q0 + stb * step_tok;
         const int h0 = shg * G;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int item = -1;
         for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
           KTile t;
-          ktile_decode(p, item, t);
+          ktile_decode<MASK>(p, item, t);
           const int nsteps = step_count(t);
           if (!(ok = mbar_wait(&bars->kv_full, tcount & 1, s_abort))) break;
           if (nsteps == 0) {  // no queries: keep every phase count
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int item = -1;
         for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
           KTile t;
-          ktile_decode(p, item, t);
+          ktile_decode<MASK>(p, item, t);
           const int nsteps = step_count(t);
           if (nsteps == 0) {  // no queries: dk = dv = 0
             if (tcount > 0 && !(ok = mbar_wait(&bars->acc_empty, (tcount - 1) & 1, s_abort)))
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // buffer.  The global loads of a step are issued two steps before it is
     // staged.
     const int u = lane;
-    const bool masked = masking(p);
+    constexpr bool masked = MASK;
     const int lgGs = __ffs(G) - 1;  // G is a power of two
     struct Pos {  // a (key tile, query step) of this CTA; st = tb * ngroups + hg
       int item, st, tb, hg, nsteps;
@@ -424,8 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto seek = [&](Pos& q) {
       while (q.item < ntiles) {
-        ktile_decode(p, q.item, q.t);
+        ktile_decode<MASK>(p, q.item, q.t);
         q.nsteps = step_count(q.t);
+        q.tb = q.t.tb0;
         if (q.nsteps > 0) return;
         q.item = take();
       }
@@ -492,8 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         cols->a[b][lc] = fmaf(-m, prel, nl2);
         cols->m[b][lc] = m;
         straddle |= !right && prel < static_cast<float>(kKeys - 1) && i < q0.t.Lq;
+        // the mask is applied per key only on the steps it cuts for some column
+        if (masked && i < q0.t.Lq)
+          straddle |= !all_admissible(p, q0.t.Lq, q0.t.Lk, i, q0.t.key,
+                                      min(q0.t.key + kKeys, q0.t.Lk) - 1);
       }
-      const bool gen = __any_sync(0xffffffffu, straddle) || masked;
+      const bool gen = __any_sync(0xffffffffu, straddle);
       if (lane == 0) {
         cols->general[b][0] = gen ? 1 : 0;
         cols->general[b][1] = 0;
@@ -524,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float rf = static_cast<float>(r);
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
-    const bool masked = masking(p);
+    constexpr bool masked = MASK;
     const int wl = p.wl;
-    const int wr = p.causal ? 0 : p.wr;
+    const int wr = right_window(p);
     const int lgG = __ffs(G) - 1;  // G is a power of two
     uint32_t g = 0;
     int tcount = 0;
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int item = -1;
     for (; (ok = tile_take_warp(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
       KTile t;
-      ktile_decode(p, item, t);
+      ktile_decode<MASK>(p, item, t);
       const int nsteps = step_count(t);
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
@@ -613,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // some column's aligned key lies inside the tile, or a mask applies:
           // prel = i + Lk - Lq - key0 of column c is tok0 + c / G + off,
           // a + m * prel = -lse2 and |m| = slope2
-          const int tok0 = (st / ngroups) * step_tok;
+          const int tok0 = (t.tb0 + st / ngroups) * step_tok;
           const int off = t.Lk - t.Lq - t.key;
 #pragma unroll 1
           for (int q4 = 0; q4 < 16; ++q4) {
@@ -732,15 +738,11 @@ cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorM
                         const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
                         const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
-  if (p.dtype == 1) {
-    auto k = dkdv_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
-  } else {
-    auto k = dkdv_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-    k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
-  }
+  const bool m = masked_call(p);
+  auto k = p.dtype == 1 ? (m ? dkdv_kernel<true, true> : dkdv_kernel<true, false>)
+                        : (m ? dkdv_kernel<false, true> : dkdv_kernel<false, false>);
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
+  k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();
 }
 

@@ -84,7 +84,7 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tdo2,
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
          ok = ok && (item < 0 || tile_publish(&bars->ring, kpub, p.counters + 2, ntiles,
                                               &item_next, s_abort))) {
       QTile t;
-      qtile_decode(p, item, t);
-      const int n = (t.Lk + kKeys - 1) / kKeys;
+      qtile_decode<MASK>(p, item, t);
+      const int n = t.nkt;  // key tiles t.kt0 .. t.kt0 + n - 1
       const int h0 = t.hg * G, tok = t.q0 + t.tok;
       if (tcount > 0 && !(ok = mbar_wait_warp(&bars->q_empty, (tcount - 1) & 1, s_abort))) break;
       if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, kTailed);
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       if (lane == 0) tma_load_4d(sDO, &tdo2, &bars->q_full, 0, h0, tok, 0);
       if (lane == 1) tma_load_3d(sDO + 2 * kTile, &tdot, &bars->q_full, 2 * kChunk, h0, tok);
       for (int j = 0; j < n && ok; ++j, ++g, kr.next()) {
-        const int key = t.k0 + j * kKeys;
+        const int key = t.k0 + (t.kt0 + j) * kKeys;
         if (kr.use > 0 &&
             !(ok = mbar_wait_warp(&bars->k_empty[kr.slot], (kr.use - 1) & 1, s_abort)))
           break;
@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       int item = -1;
       for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
-        qtile_decode(p, item, t);
-        const int n = (t.Lk + kKeys - 1) / kKeys;
+        qtile_decode<MASK>(p, item, t);
+        const int n = t.nkt;  // key tiles t.kt0 .. t.kt0 + n - 1
         if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;   // dO tile
         if (!(ok = mbar_wait(&bars->qt_full, tcount & 1, s_abort))) break;  // Q rows in TMEM
         if (n == 0) {
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       int item = -1;
       for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
-        qtile_decode(p, item, t);
-        const int n = (t.Lk + kKeys - 1) / kKeys;
+        qtile_decode<MASK>(p, item, t);
+        const int n = t.nkt;  // key tiles t.kt0 .. t.kt0 + n - 1
         if (n == 0) {
           if (tcount > 0 && !(ok = mbar_wait(&bars->o_empty, (tcount - 1) & 1, s_abort))) break;
           mbar_arrive(&bars->o_full);
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
-    const bool masked = masking(p);
+    constexpr bool masked = MASK;
     const int lgG = __ffs(G) - 1;  // G is a power of two
     // This lane's Q row of a tile into TMEM: features 80*half..80*half+79 as
     // 40 pair columns (raw 16-bit pairs, the A-operand layout).  Rows outside
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     // completed (the caller has waited for it), then signalled to the S issuer.
     auto load_q = [&](int qitem) -> bool {
       QTile tq;
-      qtile_decode(p, qitem, tq);
+      qtile_decode<MASK>(p, qitem, tq);
       const int il = tq.tok + (r >> lgG);
       const int hq = tq.hg * G + (r & (G - 1));
       uint32_t w[40];
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     if (ok && item >= 0) load_q(item);
     for (int item_next = -1; ok && item >= 0; item = item_next, ++tcount) {
       QTile t;
-      qtile_decode(p, item, t);
-      const int n = (t.Lk + kKeys - 1) / kKeys;
+      qtile_decode<MASK>(p, item, t);
+      const int n = t.nkt;  // key tiles t.kt0 .. t.kt0 + n - 1
       const int i_loc = t.tok + r / G;
       const int h = t.hg * G + r % G;
       const bool row_valid = i_loc < t.Lq;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       }
       for (int j = 0; j < n; ++j) {
         const uint32_t gg = g + j;
-        const int key0 = j * kKeys + half * 64;
+        const int key0 = (t.kt0 + j) * kKeys + half * 64;
         const float pos0 = static_cast<float>(pos_off - key0);
         if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
         tc_fence_after();
@@ -403,7 +403,12 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         if (lane == 0) mbar_arrive(&bars->s_free);  // S may be overwritten now
         // Two batches of 32 columns; within a batch all tanh, then the exponent
         // arguments, then all exp2, so dependent MUFU results are far apart.
-        const bool edge = masked || key0 + 64 > t.Lk;
+        // the mask is applied per key only on the half tiles it cuts for some row
+        const bool edge =
+            key0 + 64 > t.Lk ||
+            (masked && !__all_sync(0xffffffffu, !row_valid ||
+                                                    all_admissible(p, t.Lq, t.Lk, i_loc, key0,
+                                                                   key0 + 63)));
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           float* xb = x + b * 32;
@@ -504,7 +509,9 @@ cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s) {
-  auto k = p.dtype == 1 ? dq_kernel<true> : dq_kernel<false>;
+  const bool m = masked_call(p);
+  auto k = p.dtype == 1 ? (m ? dq_kernel<true, true> : dq_kernel<true, false>)
+                        : (m ? dq_kernel<false, true> : dq_kernel<false, false>);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
   // With `overlap` the launch is a programmatic dependent of the kernel before
   // it (dk/dv, which signals at its start): dq reads nothing dk/dv writes, so

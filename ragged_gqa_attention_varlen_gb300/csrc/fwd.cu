@@ -96,10 +96,11 @@ constexpr float kFixedCapMax = 9.5f;
 
 // The fixed reference of a row whose aligned key is k0 (base 2).  A row with
 // no admissible key gets 0 (every P is then exp2(-inf) = 0).
+template <bool MASK>
 __device__ __forceinline__ float row_bound(const Params& p, int Lk, int k0, float slope2) {
   int64_t lo = 0, hi = static_cast<int64_t>(Lk) - 1;
-  if (masking(p)) {
-    const int wr = p.causal ? 0 : p.wr;
+  if (MASK) {
+    const int wr = right_window(p);
     if (p.wl >= 0) lo = max(lo, static_cast<int64_t>(k0) - p.wl);
     if (wr >= 0) hi = min(hi, static_cast<int64_t>(k0) + wr);
   }
@@ -112,15 +113,22 @@ __device__ __forceinline__ float row_bound(const Params& p, int Lk, int k0, floa
   return -slope2 * static_cast<float>(d);
 }
 
-// First key tile to visit and the tile count for a query tile.
+// The key tiles a query tile visits: the n tiles from t.kt0 on (those that
+// hold a key some query of the tile may attend to), starting at t0, the tile
+// of the key aligned with the tile's first query, and wrapping.
 __device__ __forceinline__ void key_order(const QTile& t, int& n, int& t0) {
-  n = (t.Lk + kKeys - 1) / kKeys;
+  n = t.nkt;
   int k0 = t.tok + t.Lk - t.Lq;  // key aligned with the tile's first query
   k0 = k0 < 0 ? 0 : (k0 >= t.Lk ? t.Lk - 1 : k0);
-  t0 = n > 0 ? k0 / kKeys : 0;
+  t0 = n > 0 ? min(max(k0 / kKeys, t.kt0), t.kt0 + n - 1) : 0;
 }
 
-template <bool BF16>
+// The key tile after kt in the walk of a query tile.
+__device__ __forceinline__ int next_key_tile(const QTile& t, int kt) {
+  return kt + 1 == t.kt0 + t.nkt ? t.kt0 : kt + 1;
+}
+
+template <bool BF16, bool MASK>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk2,
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       int item = -1;
       for (; (ok = take(item)) && item >= 0; ++tcount) {
         QTile t;
-        qtile_decode(p, item, t);
+        qtile_decode<MASK>(p, item, t);
         int n, t0;
         key_order(t, n, t0);
         if (kq) {
@@ -238,8 +246,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           else
             tma_load_3d(sQ + 2 * kTile, &tqt, &bars->q_full, 2 * kChunk, t.hg * G, t.q0 + t.tok);
         }
-        // kt: key tile of step jj, (t0 + jj) mod n
-        for (int jj = 0, kt = t0; jj < n; ++jj, ++g, kt = (kt + 1 == n) ? 0 : kt + 1) {
+        // kt: key tile of step jj
+        for (int jj = 0, kt = t0; jj < n; ++jj, ++g, kt = next_key_tile(t, kt)) {
           const int key = t.k0 + kt * kKeys;
           const int s = g & 1;
           if (g >= 2 && !(ok = __all_sync(gmask, mbar_wait(kq ? &bars->k_empty[s] : &bars->v_empty[s],
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       int item = -1;
       for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
-        qtile_decode(p, item, t);
+        qtile_decode<MASK>(p, item, t);
         int n, t0;
         key_order(t, n, t0);
         if (!(ok = mbar_wait(&bars->q_full, tcount & 1, s_abort))) break;
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       int item = -1;
       for (; (ok = tile_take(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
         QTile t;
-        qtile_decode(p, item, t);
+        qtile_decode<MASK>(p, item, t);
         int n, t0;
         key_order(t, n, t0);
         if (n == 0) {
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
-    const bool masked = masking(p);
+    constexpr bool masked = MASK;
     // With the softcap every logit of a row lies within 2c of a bound known
     // before any key is seen, so P is taken against that bound: no row max,
     // no exchange between the halves, no rescale of O.
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     int item = -1;
     for (; (ok = tile_take_warp(&bars->ring, ktake, &item, s_abort)) && item >= 0; ++tcount) {
       QTile t;
-      qtile_decode(p, item, t);
+      qtile_decode<MASK>(p, item, t);
       int n, t0;
       key_order(t, n, t0);
       const int i_loc = t.tok + r / G;
@@ -399,9 +407,9 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       const int pos_off = i_loc + t.Lk - t.Lq;  // dist(j) = |pos_off - j|
       float m_run = -INFINITY, l = 0.f;          // l: this half's share of the row sum
       uint64_t l2 = f2_make(0.f, 0.f), lu2 = l2;  // fixed reference: row sums as pairs
-      if (fixed) m_run = row_bound(p, t.Lk, pos_off, slope2);
+      if (fixed) m_run = row_bound<MASK>(p, t.Lk, pos_off, slope2);
       const float bref = fixed ? m_run : 0.f;  // subtracted inside the logit
-      for (int jj = 0, kt = t0; jj < n; ++jj, kt = (kt + 1 == n) ? 0 : kt + 1) {
+      for (int jj = 0, kt = t0; jj < n; ++jj, kt = next_key_tile(t, kt)) {
         const uint32_t gg = g + jj;
         const int key0 = kt * kKeys + half * 64;
         const uint32_t sb = tmem + (gg & 1) * 128 + half * 64 + lane_addr;
@@ -415,7 +423,12 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_read[gg & 1]);  // S_gg may be overwritten
         const float pos0 = static_cast<float>(pos_off - key0);
-        const bool edge = masked || key0 + 64 > t.Lk;
+        // the mask is applied per key only on the half tiles it cuts for some row
+        const bool edge =
+            key0 + 64 > t.Lk ||
+            (masked && !__all_sync(0xffffffffu, !row_valid ||
+                                                    all_admissible(p, t.Lq, t.Lk, i_loc, key0,
+                                                                   key0 + 63)));
         // batched: all tanh of a 32-column group, then the logits
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -581,15 +594,11 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
                        const CUtensorMap& tv, int grid, cudaStream_t s) {
-  if (p.dtype == 1) {
-    auto k = fwd_kernel<true>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
-  } else {
-    auto k = fwd_kernel<false>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
-    k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
-  }
+  const bool m = masked_call(p);
+  auto k = p.dtype == 1 ? (m ? fwd_kernel<true, true> : fwd_kernel<true, false>)
+                        : (m ? fwd_kernel<false, true> : fwd_kernel<false, false>);
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
+  k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   return cudaGetLastError();
 }
 

@@ -47,13 +47,26 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
     *p.status = 0;
     for (int i = 0; i < 4; ++i) p.counters[i] = 0;
   }
+  // The work of a sequence's longest forward/dq tile grows with the keys it
+  // visits, of a dk/dv tile with the queries: the whole other length, or
+  // under a window bounded on both sides about the window's span.
+  const int wr = right_window(p);
+  const bool banded = p.wl >= 0 && wr >= 0;
+  const int64_t span_f = banded ? static_cast<int64_t>(p.wl) + wr + kRowsQ / p.G + kKeys : 0;
+  const int64_t span_b = banded ? static_cast<int64_t>(p.wl) + wr + kKeys + kRowsQ / p.G : 0;
+  auto work_f = [&](int c) -> int64_t {
+    const int64_t lk = p.cu_k[c + 1] - p.cu_k[c];
+    return banded ? min(lk, span_f) : lk;
+  };
+  auto work_b = [&](int c) -> int64_t {
+    const int64_t lq = p.cu_q[c + 1] - p.cu_q[c];
+    return banded ? min(lq, span_b) : lq;
+  };
   for (int b = tid; b < B; b += blockDim.x) {
-    int lk = p.cu_k[b + 1] - p.cu_k[b];
-    int lq = p.cu_q[b + 1] - p.cu_q[b];
+    const int64_t lk = work_f(b), lq = work_b(b);
     int rf = 0, rb = 0;
     for (int c = 0; c < B; ++c) {
-      int lkc = p.cu_k[c + 1] - p.cu_k[c];
-      int lqc = p.cu_q[c + 1] - p.cu_q[c];
+      const int64_t lkc = work_f(c), lqc = work_b(c);
       rf += (lkc > lk) || (lkc == lk && c < b);
       rb += (lqc > lq) || (lqc == lq && c < b);
     }

@@ -19,12 +19,76 @@ struct QTile {
   int hg;       // head group (heads hg*G .. hg*G+G-1)
   int Lq, Lk;   // sequence lengths
   int q0, k0;   // packed offsets of the sequence's first query / key
+  int kt0, nkt; // key tiles [kt0, kt0 + nkt) hold every key the tile's queries may attend to
 };
 
 // One dk/dv tile: kKeys keys of one sequence.
 struct KTile {
   int b, key, Lq, Lk, q0, k0;
+  int tb0, ntb;  // query blocks [tb0, tb0 + ntb) (kRowsQ/G tokens each) that may attend to it
 };
+
+__device__ __forceinline__ bool masking(const Params& p) {
+  return p.causal || p.wl >= 0 || p.wr >= 0;
+}
+
+// Right window of the mask (causal caps it at 0); negative = unbounded.
+__device__ __forceinline__ int right_window(const Params& p) { return p.causal ? 0 : p.wr; }
+
+// Key j of local query i is admissible when i + Lk - Lq - wl <= j <= i + Lk - Lq + wr
+// (each bound only where its window is set).  Tiles whose every pair fails
+// this are skipped: they would contribute P = 0 exactly.
+
+// Key tiles [*kt0, *kt0 + *nkt) cover every key that a query of local tokens
+// [qa, qb] may attend to (nkt = 0 when none may attend to any key).
+__device__ __forceinline__ void key_tile_span(const Params& p, int Lq, int Lk, int qa, int qb,
+                                              int& kt0, int& nkt) {
+  int64_t lo = 0, hi = static_cast<int64_t>(Lk) - 1;
+  if (masking(p)) {
+    const int64_t off = static_cast<int64_t>(Lk) - Lq;
+    const int wr = right_window(p);
+    if (p.wl >= 0) lo = max(lo, qa + off - p.wl);
+    if (wr >= 0) hi = min(hi, qb + off + wr);
+  }
+  if (lo > hi) {
+    kt0 = 0;
+    nkt = 0;
+    return;
+  }
+  kt0 = static_cast<int>(lo / kKeys);
+  nkt = static_cast<int>(hi / kKeys) - kt0 + 1;
+}
+
+// Query blocks [*tb0, *tb0 + *ntb) of `blk` tokens cover every query that may
+// attend to a key of local keys [ja, jb].
+__device__ __forceinline__ void query_block_span(const Params& p, int Lq, int Lk, int ja, int jb,
+                                                 int blk, int& tb0, int& ntb) {
+  int64_t lo = 0, hi = static_cast<int64_t>(Lq) - 1;
+  if (masking(p)) {
+    const int64_t off = static_cast<int64_t>(Lk) - Lq;
+    const int wr = right_window(p);
+    if (wr >= 0) lo = max(lo, ja - off - wr);
+    if (p.wl >= 0) hi = min(hi, jb - off + p.wl);
+  }
+  if (lo > hi) {
+    tb0 = 0;
+    ntb = 0;
+    return;
+  }
+  tb0 = static_cast<int>(lo / blk);
+  ntb = static_cast<int>(hi / blk) - tb0 + 1;
+}
+
+// Under a mask whose admissible keys grow with the query (a right bound and
+// no left bound: causal) the query tiles of a sequence are drawn last token
+// block first, and under the mirror case the key tiles last tile first, so
+// the longest tiles of a sequence start first.
+__device__ __forceinline__ bool qtiles_reversed(const Params& p) {
+  return p.wl < 0 && right_window(p) >= 0;
+}
+__device__ __forceinline__ bool ktiles_reversed(const Params& p) {
+  return p.wl >= 0 && right_window(p) < 0;
+}
 
 // Largest r in [0, B) with pre[r] <= n.
 __device__ __forceinline__ int sched_find(const int32_t* pre, int B, int n) {
@@ -44,6 +108,9 @@ __device__ __forceinline__ int ktile_count(const Params& p) {
   return __ldg(p.sched + 4 * p.B + 1);
 }
 
+// MASK: the call has a causal/window mask (kernels are instantiated for both
+// cases, so the unmasked instance carries none of the span arithmetic).
+template <bool MASK>
 __device__ __forceinline__ void qtile_decode(const Params& p, int n, QTile& t) {
   const int32_t* ord = p.sched;
   const int32_t* pre = p.sched + p.B;
@@ -51,26 +118,46 @@ __device__ __forceinline__ void qtile_decode(const Params& p, int n, QTile& t) {
   int b = __ldg(ord + r);
   int local = n - __ldg(pre + r);
   int ngroups = p.Hq / p.G;
+  const int rows_tok = kRowsQ / p.G;
   t.b = b;
-  t.tok = (local / ngroups) * (kRowsQ / p.G);
-  t.hg = local % ngroups;
   t.q0 = __ldg(p.cu_q + b);
   t.k0 = __ldg(p.cu_k + b);
   t.Lq = __ldg(p.cu_q + b + 1) - t.q0;
   t.Lk = __ldg(p.cu_k + b + 1) - t.k0;
+  int blk = local / ngroups;
+  if (MASK && qtiles_reversed(p)) blk = (t.Lq + rows_tok - 1) / rows_tok - 1 - blk;
+  t.tok = blk * rows_tok;
+  t.hg = local % ngroups;
+  if (MASK) {
+    key_tile_span(p, t.Lq, t.Lk, t.tok, min(t.tok + rows_tok, t.Lq) - 1, t.kt0, t.nkt);
+  } else {
+    t.kt0 = 0;
+    t.nkt = (t.Lk + kKeys - 1) / kKeys;
+  }
 }
 
+template <bool MASK>
 __device__ __forceinline__ void ktile_decode(const Params& p, int n, KTile& t) {
   const int32_t* ord = p.sched + 2 * p.B + 1;
   const int32_t* pre = p.sched + 3 * p.B + 1;
   int r = sched_find(pre, p.B, n);
   int b = __ldg(ord + r);
   t.b = b;
-  t.key = (n - __ldg(pre + r)) * kKeys;
   t.q0 = __ldg(p.cu_q + b);
   t.k0 = __ldg(p.cu_k + b);
   t.Lq = __ldg(p.cu_q + b + 1) - t.q0;
   t.Lk = __ldg(p.cu_k + b + 1) - t.k0;
+  int kt = n - __ldg(pre + r);
+  if (MASK && ktiles_reversed(p)) kt = (t.Lk + kKeys - 1) / kKeys - 1 - kt;
+  t.key = kt * kKeys;
+  if (MASK) {
+    query_block_span(p, t.Lq, t.Lk, t.key, min(t.key + kKeys, t.Lk) - 1, kRowsQ / p.G, t.tb0,
+                     t.ntb);
+  } else {
+    const int blk = kRowsQ / p.G;
+    t.tb0 = 0;
+    t.ntb = (t.Lq + blk - 1) / blk;
+  }
 }
 
 // Dynamic tile stream of a persistent CTA.  Warp 0 draws tile numbers from
@@ -138,14 +225,18 @@ __device__ __forceinline__ bool tile_take_warp(TileRing* r, uint32_t& k, int* ou
 // Key j of local query i is admissible under the causal/window mask.
 __device__ __forceinline__ bool admissible(const Params& p, int Lq, int Lk, int i, int j) {
   int k0 = i + Lk - Lq;
-  int wr = p.causal ? 0 : p.wr;
+  int wr = right_window(p);
   if (p.wl >= 0 && j < k0 - p.wl) return false;
   if (wr >= 0 && j > k0 + wr) return false;
   return true;
 }
 
-__device__ __forceinline__ bool masking(const Params& p) {
-  return p.causal || p.wl >= 0 || p.wr >= 0;
+// Every key of local keys [ja, jb] is admissible for local query i.
+__device__ __forceinline__ bool all_admissible(const Params& p, int Lq, int Lk, int i, int ja,
+                                               int jb) {
+  const int64_t k0 = static_cast<int64_t>(i) + Lk - Lq;
+  const int wr = right_window(p);
+  return (p.wl < 0 || ja >= k0 - p.wl) && (wr < 0 || jb <= k0 + wr);
 }
 
 }  // namespace attn

@@ -147,6 +147,47 @@ def test_edge_parity(oracle_mod, case):
     parity(p, oracle_mod)
 
 
+# ------------------------------------------------ masks over many tiles
+# Tiles that no admissible (query, key) pair reaches are skipped; the cases
+# below span many 128-key tiles and query blocks so that skipped, partly cut
+# and fully admissible tiles all occur, in every mask shape.
+
+MASKED = [
+    dict(lq=[1000, 260, 700], lk=[1000, 900, 300], Hq=16, causal=True),
+    dict(lq=[900, 500], lk=[1100, 500], Hq=16, window_left=150, window_right=40,
+         dtype=torch.bfloat16),
+    dict(lq=[800, 90], lk=[800, 600], Hq=16, window_left=200),    # left bound only
+    dict(lq=[600, 64], lk=[900, 700], Hq=16, window_right=100),   # right bound only
+    dict(lq=[700], lk=[700], Hq=32, causal=True, window_left=256, dtype=torch.bfloat16, step=2),
+    dict(lq=[513, 40], lk=[129, 300], Hq=16, window_left=0, window_right=0),  # one diagonal
+    dict(lq=[400, 150], lk=[350, 600], Hq=16, causal=True, softcap=0.0),      # running max
+    dict(lq=[300], lk=[300], Hq=8, causal=True, softcap=30.0),                # wide softcap
+]
+
+
+@pytest.mark.parametrize("case", MASKED, ids=[f"masked{i}" for i in range(len(MASKED))])
+def test_masked_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    softcap = case.pop("softcap", None)
+    p = W.custom(lq, lk, Hq, **case)
+    if softcap is not None:
+        p.softcap = softcap
+    parity(p, oracle_mod)
+
+
+def test_window_wider_than_every_sequence_is_bitwise_unmasked():
+    """A two-sided window that admits every pair takes the unmasked code path
+    on every tile, so the result is bitwise the unmasked call's."""
+    p = W.custom([300, 5, 129], [260, 400, 1], 16, dtype=torch.bfloat16).to("cuda")
+    ref = run(p)
+    ref = {n: ref[n].clone() for n in ("out", "lse", "dq", "dk", "dv")}
+    p.window_left = p.window_right = 10 ** 9
+    wide = run(p)
+    for n, x in ref.items():
+        assert bits_equal(x, wide[n]), n
+
+
 # ------------------------------------------- split forward / backward calls
 
 def _split_cases():
