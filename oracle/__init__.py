@@ -44,7 +44,7 @@ def _load():
         build()
         lib = ctypes.CDLL(_LIB)
         P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        common = [I, I, I, I, P, L, L, P, L, P, L, P, L, L, P, P, P, L, I, I, I, D, D]
+        common = [I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, L, L, P, P, P, L, I, I, I, D, D]
         lib.oracle_fvjp.argtypes = common + [P] + [P] * 8 + [I]
         lib.oracle_fvjp.restype = I
         lib.oracle_rows.argtypes = common + [I, P, P, P, P, P, P, I]
@@ -74,9 +74,11 @@ def _args(p):
     if slopes is not None:
         assert slopes.stride(1) == 1
     keep = (q, k, v, do, cu_q, cu_k, slopes)
-    args = [DTYPE_CODE[p.q.dtype], p.B, p.Hq, p.q.shape[-1],
+    Hkv = p.k.shape[1]
+    assert v.shape[1] == Hkv and p.Hq % Hkv == 0
+    args = [DTYPE_CODE[p.q.dtype], p.B, p.Hq, Hkv, p.q.shape[-1],
             q.data_ptr(), q.stride(0), q.stride(1),
-            k.data_ptr(), k.stride(0), v.data_ptr(), v.stride(0),
+            k.data_ptr(), k.stride(0), k.stride(1), v.data_ptr(), v.stride(0), v.stride(1),
             do.data_ptr(), do.stride(0), do.stride(1),
             cu_q.data_ptr(), cu_k.data_ptr(),
             slopes.data_ptr() if slopes is not None else None,
@@ -89,19 +91,20 @@ def _args(p):
 def fvjp(p, seq_sel=None, nthreads: int = 0, diagnostics: bool = False) -> dict:
     """Forward and full VJP of problem ``p`` (CPU tensors) in fp64.
 
-    Returns float64 tensors out/dq [T_q,Hq,d], lse/D [T_q,Hq], dk/dv [T_k,1,d]
+    Returns float64 tensors out/dq [T_q,Hq,d], lse/D [T_q,Hq], dk/dv [T_k,Hkv,d]
     (plus dz_rowsum, p_rowsum when ``diagnostics``), and the thread count.
     With ``seq_sel`` (iterable of sequence indices) only those sequences are
     computed; other rows hold NaN."""
     lib = _load()
     args, keep = _args(p)
     Tq, Tk, H, d = p.q.shape[0], p.k.shape[0], p.Hq, p.q.shape[-1]
+    Hkv = p.k.shape[1]
     f64 = dict(dtype=torch.float64)
     res = dict(out=torch.full((Tq, H, d), float("nan"), **f64),
                lse=torch.full((Tq, H), float("nan"), **f64),
                dq=torch.full((Tq, H, d), float("nan"), **f64),
-               dk=torch.full((Tk, 1, d), float("nan"), **f64),
-               dv=torch.full((Tk, 1, d), float("nan"), **f64),
+               dk=torch.full((Tk, Hkv, d), float("nan"), **f64),
+               dv=torch.full((Tk, Hkv, d), float("nan"), **f64),
                D=torch.full((Tq, H), float("nan"), **f64))
     if diagnostics:
         res["dz_rowsum"] = torch.full((Tq, H), float("nan"), **f64)

@@ -7,9 +7,11 @@
  * code, header, table or helper with the CUDA path.
  *
  * What it computes (the plain definition; one sequence b, query head h,
- * local query position i in [0, Lq), local key position j in [0, Lk)):
+ * local query position i in [0, Lq), local key position j in [0, Lk); the
+ * Hq query heads share Hkv key/value heads, query head h reading K/V head
+ * g(h) = floor(h / (Hq / Hkv)), so consecutive query heads form a group):
  *
- *   s_ij  = sigma * sum_f q[i,h,f] k[j,f],  sigma = scale_multiplier/sqrt(d)
+ *   s_ij  = sigma * sum_f q[i,h,f] k[j,g(h),f],  sigma = scale_multiplier/sqrt(d)
  *           ("Noncausal Global Extreme-GQA Ragged Attention Full VJP",
  *            section "What You Have": scaled logits use 0.75/sqrt(head_dim))
  *   t_ij  = c * tanh(s_ij / c)   (c = softcap; t = s when c <= 0)
@@ -19,13 +21,18 @@
  *           (same page, "What You Have": the ALiBi distance)
  *   z_ij  = -inf where the mask forbids (i, j)
  *   lse_i = log sum_j exp(z_ij)                (natural log)
- *   P_ij  = exp(z_ij - lse_i);  out_i = sum_j P_ij v_j
+ *   P_ij  = exp(z_ij - lse_i);  out_i = sum_j P_ij v_j,g(h)
  *   D_i   = dO_i . out_i
- *   dP_ij = dO_i . v_j;   dZ_ij = P_ij (dP_ij - D_i)
+ *   dP_ij = dO_i . v_j,g(h);   dZ_ij = P_ij (dP_ij - D_i)
  *   dS_ij = dZ_ij * (1 - (t_ij/c)^2)   (dZ_ij when c <= 0)
- *   dq_i  = sigma sum_j dS_ij k_j
- *   dk_j  = sigma sum_h sum_i dS_ij q_i   (h outer, i inner)
- *   dv_j  = sum_h sum_i P_ij dO_i         (h outer, i inner)
+ *   dq_i  = sigma sum_j dS_ij k_j,g(h)
+ *   dk_j,g = sigma sum_{h: g(h)=g} sum_i dS_ij q_i   (h outer, i inner)
+ *   dv_j,g = sum_{h: g(h)=g} sum_i P_ij dO_i         (h outer, i inner)
+ *
+ * With Hkv = 1 (the pages' case, "Hard Constraints": one K/V head shared by
+ * every query head) g(h) = 0 and dk/dv sum over all heads.  The grouping of
+ * consecutive query heads for Hkv > 1 is the usual grouped-query reading;
+ * the pages fix only Hkv = 1.
  *
  * Rows with no admissible key ("ragged flash attention gradient recompute",
  * "Root causes addressed", empty rows) have lse = -inf, out = 0, and add
@@ -79,13 +86,13 @@ static double bf16_bits_to_double(uint16_t b) {
 
 typedef struct {
   int dtype; /* 0 = fp16, 1 = bf16, 2 = fp64 */
-  int B, Hq, d;
+  int B, Hq, Hkv, d;
   const void *q;
   int64_t q_ts, q_hs;
   const void *k;
-  int64_t k_ts;
+  int64_t k_ts, k_hs;
   const void *v;
-  int64_t v_ts;
+  int64_t v_ts, v_hs;
   const void *dout;
   int64_t do_ts, do_hs;
   const int32_t *cu_q, *cu_k;
@@ -109,8 +116,16 @@ typedef struct {
   int64_t q0, k0;     /* first packed token of the sequence */
   double *Q;          /* [Lq][Hq][d] */
   double *dO;         /* [Lq][Hq][d] */
-  double *K, *V;      /* [Lk][d] */
+  double *K, *V;      /* [Lk][Hkv][d] */
 } seqdata;
+
+/* The K/V head that query head h reads. */
+static int kv_head(const problem *p, int h) { return h / (p->Hq / p->Hkv); }
+
+/* Decoded K (or V) row of key j, K/V head g. */
+static const double *kv_row(const seqdata *s, const double *a, int j, int g) {
+  return a + ((size_t)j * s->p->Hkv + g) * s->p->d;
+}
 
 static void seq_load(const problem *p, int b, seqdata *s) {
   int d = p->d, H = p->Hq;
@@ -122,8 +137,8 @@ static void seq_load(const problem *p, int b, seqdata *s) {
   s->Lk = p->cu_k[b + 1] - p->cu_k[b];
   s->Q = malloc(sizeof(double) * ((size_t)s->Lq * H * d + 1));
   s->dO = malloc(sizeof(double) * ((size_t)s->Lq * H * d + 1));
-  s->K = malloc(sizeof(double) * ((size_t)s->Lk * d + 1));
-  s->V = malloc(sizeof(double) * ((size_t)s->Lk * d + 1));
+  s->K = malloc(sizeof(double) * ((size_t)s->Lk * p->Hkv * d + 1));
+  s->V = malloc(sizeof(double) * ((size_t)s->Lk * p->Hkv * d + 1));
   for (int i = 0; i < s->Lq; i++)
     for (int h = 0; h < H; h++)
       for (int f = 0; f < d; f++) {
@@ -132,11 +147,13 @@ static void seq_load(const problem *p, int b, seqdata *s) {
         s->dO[((size_t)i * H + h) * d + f] = decode(p, p->dout, t * p->do_ts + h * p->do_hs + f);
       }
   for (int j = 0; j < s->Lk; j++)
-    for (int f = 0; f < d; f++) {
-      int64_t t = s->k0 + j;
-      s->K[(size_t)j * d + f] = decode(p, p->k, t * p->k_ts + f);
-      s->V[(size_t)j * d + f] = decode(p, p->v, t * p->v_ts + f);
-    }
+    for (int g = 0; g < p->Hkv; g++)
+      for (int f = 0; f < d; f++) {
+        int64_t t = s->k0 + j;
+        size_t at = ((size_t)j * p->Hkv + g) * d + f;
+        s->K[at] = decode(p, p->k, t * p->k_ts + g * p->k_hs + f);
+        s->V[at] = decode(p, p->v, t * p->v_ts + g * p->v_hs + f);
+      }
 }
 
 static void seq_free(seqdata *s) {
@@ -158,12 +175,13 @@ static double slope_of(const problem *p, int b, int h) {
   return p->slopes ? (double)p->slopes[(int64_t)b * p->slopes_bs + h] : 0.0;
 }
 
-/* Logit of (i, h) against key j before masking: returns z, and the softcap
- * derivative factor 1 - (t/c)^2 through *g. */
-static double logit(const seqdata *s, const double *qi, int i, int j, double slope, double *g) {
+/* Logit of (i, h) against key j of K/V head kh before masking: returns z,
+ * and the softcap derivative factor 1 - (t/c)^2 through *g. */
+static double logit(const seqdata *s, const double *qi, int i, int j, int kh, double slope,
+                    double *g) {
   const problem *p = s->p;
   int d = p->d;
-  const double *kj = s->K + (size_t)j * d;
+  const double *kj = kv_row(s, s->K, j, kh);
   double dot = 0.0;
   for (int f = 0; f < d; f++) dot += qi[f] * kj[f];
   double sigma = p->scale_multiplier / sqrt((double)d);
@@ -186,7 +204,7 @@ static double logit(const seqdata *s, const double *qi, int i, int j, double slo
 typedef struct {
   double *out, *lse, *dq, *Dpre; /* out/dq [T_q][Hq][d]; lse/Dpre [T_q][Hq] */
   double *dz_rowsum, *p_rowsum;  /* optional [T_q][Hq] */
-  double *dk, *dv;               /* [T_k][d] */
+  double *dk, *dv;               /* [T_k][Hkv][d] */
 } outputs;
 
 /* Where one query row's results go. */
@@ -203,9 +221,10 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   const problem *p = s->p;
   int d = p->d, Lk = s->Lk;
   double slope = slope_of(p, s->b, h);
+  int kh = kv_head(p, h);
   double m = -INFINITY;
   for (int j = 0; j < Lk; j++) {
-    z[j] = logit(s, qi, i, j, slope, &gv[j]);
+    z[j] = logit(s, qi, i, j, kh, slope, &gv[j]);
     if (!admissible(p, s->Lq, Lk, i, j)) z[j] = -INFINITY;
     if (z[j] > m) m = z[j];
   }
@@ -230,7 +249,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
     psum += P[j];
   }
   for (int j = 0; j < Lk; j++)
-    for (int f = 0; f < d; f++) o->out[f] += P[j] * s->V[(size_t)j * d + f];
+    for (int f = 0; f < d; f++) o->out[f] += P[j] * kv_row(s, s->V, j, kh)[f];
   double D = 0.0;
   for (int f = 0; f < d; f++) D += dOi[f] * o->out[f];
   *o->D = D;
@@ -238,11 +257,11 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   double sigma = p->scale_multiplier / sqrt((double)d);
   for (int j = 0; j < Lk; j++) {
     double dp = 0.0;
-    for (int f = 0; f < d; f++) dp += dOi[f] * s->V[(size_t)j * d + f];
+    for (int f = 0; f < d; f++) dp += dOi[f] * kv_row(s, s->V, j, kh)[f];
     double dz = P[j] * (dp - D);
     dzsum += dz;
     double ds = dz * gv[j];
-    for (int f = 0; f < d; f++) o->dq[f] += sigma * ds * s->K[(size_t)j * d + f];
+    for (int f = 0; f < d; f++) o->dq[f] += sigma * ds * kv_row(s, s->K, j, kh)[f];
   }
   if (o->dz_sum) *o->dz_sum = dzsum;
   if (o->p_sum) *o->p_sum = psum;
@@ -264,18 +283,20 @@ static void row_pass_packed(const seqdata *s, int h, int i, const outputs *o, do
 
 /* ---- per-key pass: dk, dv (needs every row's lse and D) ---------------- */
 
-static void key_pass(const seqdata *s, int j, const outputs *o) {
+/* Key j of K/V head kh: sums over the query heads of its group. */
+static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
   const problem *p = s->p;
-  int d = p->d, H = p->Hq;
+  int d = p->d, H = p->Hq, R = p->Hq / p->Hkv;
   double sigma = p->scale_multiplier / sqrt((double)d);
-  double *dkrow = o->dk + (s->k0 + j) * (int64_t)d;
-  double *dvrow = o->dv + (s->k0 + j) * (int64_t)d;
+  int64_t at = ((s->k0 + j) * (int64_t)p->Hkv + kh) * d;
+  double *dkrow = o->dk + at;
+  double *dvrow = o->dv + at;
   for (int f = 0; f < d; f++) {
     dkrow[f] = 0.0;
     dvrow[f] = 0.0;
   }
-  const double *vj = s->V + (size_t)j * d;
-  for (int h = 0; h < H; h++) {
+  const double *vj = kv_row(s, s->V, j, kh);
+  for (int h = kh * R; h < (kh + 1) * R; h++) {
     double slope = slope_of(p, s->b, h);
     for (int i = 0; i < s->Lq; i++) {
       int64_t rowid = (s->q0 + i) * (int64_t)H + h;
@@ -285,7 +306,7 @@ static void key_pass(const seqdata *s, int j, const outputs *o) {
       const double *qi = s->Q + ((size_t)i * H + h) * d;
       const double *dOi = s->dO + ((size_t)i * H + h) * d;
       double g;
-      double z = logit(s, qi, i, j, slope, &g);
+      double z = logit(s, qi, i, j, kh, slope, &g);
       double P = exp(z - lse);
       double dp = 0.0;
       for (int f = 0; f < d; f++) dp += dOi[f] * vj[f];
@@ -306,7 +327,7 @@ typedef struct {
   const outputs *o;
   const seqdata *seqs; /* indexed by sequence */
   const int *unit_b;   /* unit -> sequence */
-  const int *unit_a;   /* unit -> head (phase 1) or key (phase 2) */
+  const int *unit_a;   /* unit -> head (phase 1) or key * Hkv + K/V head (phase 2) */
   int n_units;
   int phase;
   int next; /* shared counter */
@@ -332,7 +353,7 @@ static void *worker(void *arg) {
     if (w->phase == 1) {
       for (int i = 0; i < s->Lq; i++) row_pass_packed(s, w->unit_a[u], i, w->o, z, P, g);
     } else {
-      key_pass(s, w->unit_a[u], w->o);
+      key_pass(s, w->unit_a[u] / w->p->Hkv, w->unit_a[u] % w->p->Hkv, w->o);
     }
   }
   free(z);
@@ -362,17 +383,20 @@ static void run_pool(pool *w, int nthreads) {
 /* Full forward + VJP for the sequences with seq_sel[b] != 0 (all of them when
  * seq_sel is NULL).  Output rows of unselected sequences are left untouched.
  * All output arrays are dense fp64: out, dq [T_q][Hq][d]; lse, Dpre [T_q][Hq];
- * dk, dv [T_k][d]; dz_rowsum and p_rowsum [T_q][Hq] are optional (NULL).
- * Returns the number of threads used. */
-int oracle_fvjp(int dtype, int B, int Hq, int d, const void *q, int64_t q_ts, int64_t q_hs,
-                const void *k, int64_t k_ts, const void *v, int64_t v_ts,
+ * dk, dv [T_k][Hkv][d]; dz_rowsum and p_rowsum [T_q][Hq] are optional (NULL).
+ * Hq must be a multiple of Hkv.  Returns the number of threads used (0 for
+ * an invalid head split). */
+int oracle_fvjp(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t q_ts,
+                int64_t q_hs, const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                int64_t v_ts, int64_t v_hs,
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
                 int wr, double softcap, double scale_multiplier, const uint8_t *seq_sel,
                 double *out, double *lse, double *dq, double *dk, double *dv, double *Dpre,
                 double *dz_rowsum, double *p_rowsum, int nthreads) {
-  problem p = {dtype, B, Hq, d, q, q_ts, q_hs, k, k_ts, v, v_ts, dout, do_ts, do_hs,
-               cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
+  if (Hkv < 1 || Hq % Hkv) return 0;
+  problem p = {dtype, B, Hq, Hkv, d, q, q_ts, q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts,
+               do_hs, cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
   outputs o = {out, lse, dq, Dpre, dz_rowsum, p_rowsum, dk, dv};
   int nt = thread_count(nthreads);
   seqdata *seqs = calloc((size_t)B + 1, sizeof(seqdata));
@@ -381,7 +405,7 @@ int oracle_fvjp(int dtype, int B, int Hq, int d, const void *q, int64_t q_ts, in
     if (seq_sel && !seq_sel[b]) continue;
     seq_load(&p, b, &seqs[b]);
     n1 += Hq;
-    n2 += seqs[b].Lk;
+    n2 += seqs[b].Lk * Hkv;
   }
   int *ub = malloc(sizeof(int) * (size_t)(n1 + n2 + 1));
   int *ua = malloc(sizeof(int) * (size_t)(n1 + n2 + 1));
@@ -397,11 +421,11 @@ int oracle_fvjp(int dtype, int B, int Hq, int d, const void *q, int64_t q_ts, in
   }
   pool w1 = {.p = &p, .o = &o, .seqs = seqs, .unit_b = ub, .unit_a = ua, .n_units = n, .phase = 1};
   run_pool(&w1, nt);
-  /* phase 2: one unit per (sequence, key) */
+  /* phase 2: one unit per (sequence, key, K/V head) */
   n = 0;
   for (int b = 0; b < B; b++) {
     if (seq_sel && !seq_sel[b]) continue;
-    for (int j = 0; j < seqs[b].Lk; j++) {
+    for (int j = 0; j < seqs[b].Lk * Hkv; j++) {
       ub[n] = b;
       ua[n] = j;
       n++;
@@ -472,14 +496,16 @@ static void *row_worker(void *arg) {
       qi[f] = decode(p, p->q, t * p->q_ts + (int64_t)h * p->q_hs + f);
       dOi[f] = decode(p, p->dout, t * p->do_ts + (int64_t)h * p->do_hs + f);
     }
-    s.K = malloc(sizeof(double) * ((size_t)s.Lk * d + 1));
-    s.V = malloc(sizeof(double) * ((size_t)s.Lk * d + 1));
+    s.K = malloc(sizeof(double) * ((size_t)s.Lk * p->Hkv * d + 1));
+    s.V = malloc(sizeof(double) * ((size_t)s.Lk * p->Hkv * d + 1));
     for (int j = 0; j < s.Lk; j++)
-      for (int f = 0; f < d; f++) {
-        int64_t tk = s.k0 + j;
-        s.K[(size_t)j * d + f] = decode(p, p->k, tk * p->k_ts + f);
-        s.V[(size_t)j * d + f] = decode(p, p->v, tk * p->v_ts + f);
-      }
+      for (int g = 0; g < p->Hkv; g++)
+        for (int f = 0; f < d; f++) {
+          int64_t tk = s.k0 + j;
+          size_t at = ((size_t)j * p->Hkv + g) * d + f;
+          s.K[at] = decode(p, p->k, tk * p->k_ts + g * p->k_hs + f);
+          s.V[at] = decode(p, p->v, tk * p->v_ts + g * p->v_hs + f);
+        }
     rowdest o = {w->out_r + (int64_t)r * d, w->dq_r + (int64_t)r * d, w->lse_r + r, w->D_r + r,
                  NULL, NULL};
     int Lk1 = s.Lk > 0 ? s.Lk : 1;
@@ -498,15 +524,17 @@ static void *row_worker(void *arg) {
   return NULL;
 }
 
-int oracle_rows(int dtype, int B, int Hq, int d, const void *q, int64_t q_ts, int64_t q_hs,
-                const void *k, int64_t k_ts, const void *v, int64_t v_ts,
+int oracle_rows(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t q_ts,
+                int64_t q_hs, const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                int64_t v_ts, int64_t v_hs,
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
                 int wr, double softcap, double scale_multiplier, int n, const int64_t *tok,
                 const int32_t *head, double *out_r, double *lse_r, double *dq_r, double *D_r,
                 int nthreads) {
-  problem p = {dtype, B, Hq, d, q, q_ts, q_hs, k, k_ts, v, v_ts, dout, do_ts, do_hs,
-               cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
+  if (Hkv < 1 || Hq % Hkv) return 0;
+  problem p = {dtype, B, Hq, Hkv, d, q, q_ts, q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts,
+               do_hs, cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
   rowpool w;
   w.p = &p;
   w.n = n;

@@ -146,15 +146,16 @@ def _alibi_geometric(Hq):
 
 
 def build(name, lq, lk, Hq, dtype, step, pad, slopes, qk_std=1.0, v_std=1.0, do_std=1.0,
-          seed=0, device="cpu", poison=True, **mask) -> Problem:
-    """Draw the values of a problem whose lengths and slopes are already fixed."""
+          seed=0, device="cpu", poison=True, Hkv=1, **mask) -> Problem:
+    """Draw the values of a problem whose lengths and slopes are already fixed
+    (k and v get Hkv heads)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1000003 + 17)
     cu_q, cu_k = _cu(lq), _cu(lk)
     Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
     q = strided_view(Tq, Hq, step, pad, dtype, device, poison)
-    k = strided_view(Tk, 1, step, pad, dtype, device, poison)
-    v = strided_view(Tk, 1, step, pad, dtype, device, poison)
+    k = strided_view(Tk, Hkv, step, pad, dtype, device, poison)
+    v = strided_view(Tk, Hkv, step, pad, dtype, device, poison)
     dout = strided_view(Tq, Hq, step, pad, dtype, device, poison)
     _fill_normal(q, qk_std, gen)
     _fill_normal(k, qk_std, gen)
@@ -230,15 +231,16 @@ def mixed(seed=3, Hq=64, device="cpu", length_scale=1.0):
                  seed=seed, device=device)
 
 
-def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True):
+def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True, Hkv=1):
     """24 sequences with Lq = Lk ~ U[6144, 12288], Hq=96, bf16, dense features,
-    token step 2, N(0,1) values, slopes 2^(-8h/96)."""
+    token step 2, N(0,1) values, slopes 2^(-8h/96); Hkv K/V heads (1 unless
+    asked)."""
     g = torch.Generator().manual_seed(seed)
     B, Hq = 24, 96
     L = _scale(_uniform_int(g, 6144, 12288, B), length_scale)
     slopes = _alibi_geometric(Hq)[None, :].expand(B, Hq).contiguous()
     return build("long_balanced", L, list(L), Hq, torch.bfloat16, 2, HEAD_DIM, slopes,
-                 seed=seed, device=device, poison=poison)
+                 seed=seed, device=device, poison=poison, Hkv=Hkv)
 
 
 def _scale(lengths, s):
@@ -258,9 +260,9 @@ WORKLOADS = {
 
 
 def custom(lq, lk, Hq, dtype=torch.float16, step=1, pad=HEAD_DIM, seed=0, device="cpu",
-           slope_max=0.25, qk_std=1.0, poison=True, **mask) -> Problem:
+           slope_max=0.25, qk_std=1.0, poison=True, Hkv=1, **mask) -> Problem:
     """A small problem with given lengths, for edge cases."""
     g = torch.Generator().manual_seed(seed)
     slopes = torch.rand((len(lq), Hq), generator=g, dtype=torch.float32) * slope_max
     return build("custom", list(lq), list(lk), Hq, dtype, step, pad, slopes, qk_std=qk_std,
-                 seed=seed, device=device, poison=poison, **mask)
+                 seed=seed, device=device, poison=poison, Hkv=Hkv, **mask)

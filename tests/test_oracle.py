@@ -49,33 +49,35 @@ def test_decode_every_16bit_pattern(oracle_mod):
 # ------------------------------------------- library special case: plain SDPA
 
 def _sdpa_reference(p, scale):
-    """Per sequence: torch SDPA in fp64 with K/V expanded over the query heads,
-    and autograd for the VJP (dk/dv sum over heads through the expand)."""
+    """Per sequence: torch SDPA in fp64 with its own grouped-query head
+    mapping (``enable_gqa``: Hq query heads over Hkv K/V heads), and autograd
+    for the VJP (dk/dv sum over the heads of each group)."""
     outs, dqs, dks, dvs, lses = [], [], [], [], []
+    Hkv = p.k.shape[1]
     for b in range(p.B):
         q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
         k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
         q = p.q[q0:q1].double().permute(1, 0, 2).clone().requires_grad_(True)  # [H, Lq, d]
-        k = p.k[k0:k1, 0].double().clone().requires_grad_(True)
-        v = p.v[k0:k1, 0].double().clone().requires_grad_(True)
+        k = p.k[k0:k1].double().permute(1, 0, 2).clone().requires_grad_(True)  # [Hkv, Lk, d]
+        v = p.v[k0:k1].double().permute(1, 0, 2).clone().requires_grad_(True)
         do = p.dout[q0:q1].double().permute(1, 0, 2)
-        kk = k[None].expand(p.Hq, -1, -1)
-        vv = v[None].expand(p.Hq, -1, -1)
-        o = torch.nn.functional.scaled_dot_product_attention(q[None], kk[None], vv[None],
-                                                             scale=scale)[0]
+        o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None],
+                                                             scale=scale, enable_gqa=Hkv > 1)[0]
         gq, gk, gv = torch.autograd.grad(o, (q, k, v), do)
-        lse = torch.logsumexp(scale * q @ kk.transpose(-1, -2), dim=-1)
+        # lse: the logits of each query head against the keys of its group
+        kk = k.detach().repeat_interleave(p.Hq // Hkv, dim=0)
+        lse = torch.logsumexp(scale * q.detach() @ kk.transpose(-1, -2), dim=-1)
         outs.append(o.detach().permute(1, 0, 2))
         dqs.append(gq.permute(1, 0, 2))
-        dks.append(gk[:, None])
-        dvs.append(gv[:, None])
-        lses.append(lse.detach().permute(1, 0))
+        dks.append(gk.permute(1, 0, 2))
+        dvs.append(gv.permute(1, 0, 2))
+        lses.append(lse.permute(1, 0))
     return (torch.cat(outs), torch.cat(lses), torch.cat(dqs), torch.cat(dks), torch.cat(dvs))
 
 
-@pytest.mark.parametrize("softcap", [0.0, 1e7])
-def test_reduces_to_sdpa_without_cap_and_alibi(oracle_mod, softcap):
-    p = f64_problem([3, 7, 1, 12], [5, 2, 9, 12], Hq=4, seed=3)
+@pytest.mark.parametrize("softcap,Hkv", [(0.0, 1), (1e7, 1), (0.0, 2), (0.0, 4)])
+def test_reduces_to_sdpa_without_cap_and_alibi(oracle_mod, softcap, Hkv):
+    p = f64_problem([3, 7, 1, 12], [5, 2, 9, 12], Hq=4, seed=3, Hkv=Hkv)
     p.alibi_slopes.zero_()
     p.softcap = softcap
     r = oracle_mod.fvjp(p)
@@ -293,6 +295,37 @@ def test_empty_rows_contribute_nothing(oracle_mod):
 
 
 # ------------------------------------------------------------- structure
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 3), (4, 4), (8, 2)])
+def test_kv_head_groups_are_independent_problems(oracle_mod, Hq, Hkv):
+    """With Hkv K/V heads, group g (query heads g*R .. g*R+R-1, R = Hq/Hkv,
+    with K/V head g) gives bitwise the results of the one-K/V-head problem
+    made of those heads alone: the head mapping, the per-group dk/dv sums
+    and their order all match the pinned Hkv = 1 case."""
+    R = Hq // Hkv
+    lq, lk = [4, 9, 2], [7, 3, 11]
+    p = W.custom(lq, lk, Hq, seed=21, Hkv=Hkv, causal=True, window_left=5)
+    r = oracle_mod.fvjp(p)
+    for g in range(Hkv):
+        pg = W.custom(lq, lk, R, seed=21, causal=True, window_left=5)
+        pg.q.copy_(p.q[:, g * R:(g + 1) * R])
+        pg.dout.copy_(p.dout[:, g * R:(g + 1) * R])
+        pg.k.copy_(p.k[:, g:g + 1])
+        pg.v.copy_(p.v[:, g:g + 1])
+        pg.alibi_slopes.copy_(p.alibi_slopes[:, g * R:(g + 1) * R])
+        rg = oracle_mod.fvjp(pg)
+        for name in ("out", "dq", "lse", "D"):
+            assert torch.equal(r[name][:, g * R:(g + 1) * R], rg[name]), (name, g)
+        for name in ("dk", "dv"):
+            assert torch.equal(r[name][:, g:g + 1], rg[name]), (name, g)
+    # the row-sampled path maps heads the same way
+    tok, head = [0, 5, 13, 14], [Hq - 1, 0, R, Hq // 2]
+    s = oracle_mod.rows(p, tok, head)
+    for n, (t, h) in enumerate(zip(tok, head)):
+        assert torch.equal(s["out"][n], r["out"][t, h])
+        assert torch.equal(s["dq"][n], r["dq"][t, h])
+        assert float(s["lse"][n]) == float(r["lse"][t, h])
+
 
 def test_sequences_are_independent_and_permutable(oracle_mod):
     p = W.custom([4, 9, 2], [7, 3, 11], Hq=4, seed=13)
