@@ -290,7 +290,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False,
-                                length_scale=args.length_scale)
+                                length_scale=args.length_scale, Hkv=args.hkv)
     p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
     flops = counted_flops(p)
     kflops = kernel_flops(p)
@@ -339,28 +339,36 @@ def run_gpu(args, world, rank, local):
     status = binding.device_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
-    # per-kernel split from separate calls with an event between every two
-    # kernels (the events keep dq from overlapping the tail of dk/dv, so the
-    # timed calls above carry none)
-    for s in range(args.steps):
-        binding.record_events_next_call(ev[s])
-        call()
-    torch.cuda.synchronize()
-    per_kernel = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) /
-                  args.steps for i, name in enumerate(binding.KERNELS)}
     value, ms = aggregate(flops, total_s, args.steps, world)
-    launches = binding.launch_count(p.B, p.Hq, p.total_q, p.total_k) * args.steps
-
-    # ---- roofline of the dominant kernel
+    launches = binding.launch_count(p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * args.steps
     pk, kind = peaks()
-    dom = max(per_kernel, key=per_kernel.get)
-    achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": dram_traffic(dom) if args.length_scale == 1.0 and not mask_name(p)
-                           else None,
-                "peak_kind": f"{kind} bf16 sustained"}
+    if args.hkv == 1:
+        # per-kernel split from separate calls with an event between every two
+        # kernels (the events keep dq from overlapping the tail of dk/dv, so
+        # the timed calls above carry none)
+        for s in range(args.steps):
+            binding.record_events_next_call(ev[s])
+            call()
+        torch.cuda.synchronize()
+        per_kernel = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) /
+                      args.steps for i, name in enumerate(binding.KERNELS)}
+        # ---- roofline of the dominant kernel
+        dom = max(per_kernel, key=per_kernel.get)
+        achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "traffic": dram_traffic(dom) if args.length_scale == 1.0 and not mask_name(p)
+                               else None,
+                    "peak_kind": f"{kind} bf16 sustained"}
+    else:
+        # one call runs a forward, dk/dv and dq per K/V head group: the
+        # roofline is that of the whole call (executed MMA flops: 4d + 8d + 6d)
+        per_kernel = None
+        achieved = 18.0 / 14.0 * flops / (total_s / args.steps) / 1e12
+        roofline = {"bound": "tensor", "kernel": "whole call", "achieved": achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                    "peak_kind": f"{kind} bf16 sustained"}
     whole_frac = value / world / pk["bf16_tflops"]
 
     # ---- end to end: pinned host inputs in, results out, every step
@@ -374,8 +382,8 @@ def run_gpu(args, world, rank, local):
             "data": "synthetic (seeded, generated on device)",
             "config": {"workload": "long_balanced" + (
                            "" if args.length_scale == 1.0 else f" x{args.length_scale} length") +
-                           mask_name(p),
-                       "B": p.B, "Hq": p.Hq, "Hkv": 1,
+                           mask_name(p) + ("" if args.hkv == 1 else f", Hkv={args.hkv}"),
+                       "B": p.B, "Hq": p.Hq, "Hkv": args.hkv,
                        "head_dim": HEAD_DIM, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
                        "scored_pairs": scored_pairs(p),
@@ -385,7 +393,7 @@ def run_gpu(args, world, rank, local):
             "latency_ms": ms, "frac_of_bf16_peak": whole_frac,
             "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
             "clocks": clk, "e2e": e2e}
-    if rank == 0 and world == 1 and not args.no_cpu and not mask_name(p):
+    if rank == 0 and world == 1 and not args.no_cpu and not mask_name(p) and args.hkv == 1:
         v, cores, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -433,7 +441,7 @@ def run_e2e(args, p, kw, flops, stream, world):
     value, ms = aggregate(flops, start.elapsed_time(end) / 1e3, args.steps, world)
     return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "gpu_launches": binding.launch_count(
-                p.B, p.Hq, p.total_q, p.total_k) * args.steps}
+                p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * args.steps}
 
 
 def main():
@@ -451,6 +459,8 @@ def main():
                     help="time the causal variant (flops counted over admissible pairs)")
     ap.add_argument("--window-left", type=int, default=-1)
     ap.add_argument("--window-right", type=int, default=-1)
+    ap.add_argument("--hkv", type=int, default=1,
+                    help="K/V heads (query heads grouped consecutively over them)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

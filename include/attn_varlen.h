@@ -2,22 +2,27 @@
  * attn_varlen.h -- C ABI of the GB300 (sm_103a) ragged GQA attention library.
  *
  * One fused call computes, for packed ragged (cu_seqlens) grouped-query
- * attention with Hq query heads sharing ONE key/value head of dimension 160,
- * the forward output and log-sum-exp and the complete vector-Jacobian product
- * (dq, dk, dv) for a given output cotangent dout.
+ * attention with Hq query heads sharing ONE key/value head of dimension 160
+ * (the pages' case) or, more generally, Hkv key/value heads each shared by
+ * Hq/Hkv consecutive query heads, the forward output and log-sum-exp and the
+ * complete vector-Jacobian product (dq, dk, dv) for a given output cotangent
+ * dout.
  *
  * Operation ("Noncausal Global Extreme-GQA Ragged Attention Full VJP",
  * sections "Hard Constraints" and "What You Have"):
  *   for sequence b with Lq = cu_q[b+1]-cu_q[b] queries and Lk = cu_k[b+1]-cu_k[b]
  *   keys, head h, local query i and key j:
- *     s   = (scale_multiplier / sqrt(160)) * q[i,h,:] . k[j,:]
+ *     s   = (scale_multiplier / sqrt(160)) * q[i,h,:] . k[j,g(h),:]
  *     t   = softcap * tanh(s / softcap)        (t = s when softcap <= 0)
  *     z   = t - alibi_slopes[b,h] * |i + Lk - Lq - j|
  *     z   = -inf where the causal/window mask forbids (i, j)
- *     lse = ln sum_j exp(z),  out[i,h,:] = sum_j exp(z - lse) v[j,:]
- *   and dq, dk, dv are the gradients of <dout, out> with respect to q, k, v;
- *   dk and dv are summed over every query head that shares the K/V head
- *   (same page, "Hard Constraints").
+ *     lse = ln sum_j exp(z),  out[i,h,:] = sum_j exp(z - lse) v[j,g(h),:]
+ *   with g(h) = h / (Hq / Hkv) (0 for the pages' Hkv = 1), and dq, dk, dv
+ *   are the gradients of <dout, out> with respect to q, k, v; dk and dv of
+ *   K/V head g are summed over every query head that reads it (same page,
+ *   "Hard Constraints": all query heads share the single K/V head).  The
+ *   pages fix only Hkv = 1; the consecutive grouping for Hkv > 1 is the
+ *   usual grouped-query reading.
  * The softcap acts on the scaled dot product before ALiBi and masking.  A row
  * with no admissible key ("ragged flash attention gradient recompute",
  * section "Root causes addressed", empty rows) gets out = 0, lse = -inf and
@@ -32,7 +37,9 @@
  * Layouts.  All strides are in ELEMENTS; the feature axis (160 values) is
  * contiguous.  q, dout, out, dq are [total_q, Hq, 160] at
  *   base + token * tok_stride + head * head_stride + feature;
- * k, v, dk, dv are [total_k, 1, 160] at base + token * tok_stride + feature.
+ * k, v, dk, dv are [total_k, Hkv, 160] at
+ *   base + token * tok_stride + head * head_stride + feature
+ * (the head stride is ignored when Hkv = 1).
  * Token and head strides may be non-dense (padded features, token steps).
  * lse is a dense fp32 [total_q, Hq] array.  cu_q, cu_k are int32 [B+1] with
  * cu[0] = 0, non-decreasing, cu[B] = total.  alibi_slopes is fp32 [B, Hq]
@@ -69,8 +76,9 @@ typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype;
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID = -1,     /* a null pointer, negative size, bad cu/total pair */
-  ATTN_ERR_UNSUPPORTED = -2, /* head_dim != 160, Hkv != 1, B too large */
+  ATTN_ERR_INVALID = -1,     /* a null pointer, negative size, bad cu/total pair,
+                                Hkv < 1 or Hq not a multiple of Hkv */
+  ATTN_ERR_UNSUPPORTED = -2, /* head_dim != 160, B too large */
   ATTN_ERR_ALIGNMENT = -3,   /* base not 16-byte aligned, stride not a multiple of 8 */
   ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
   ATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
@@ -98,9 +106,12 @@ size_t attn_varlen_fvjp_workspace_size(int B, int Hq, int64_t total_q, int64_t t
 
 /* Forward + full VJP, fused into one call on `stream` (a cudaStream_t; NULL
  * is the legacy default stream).  `dtype` is the element type of q, k, v,
- * dout, out, dq, dk, dv.  Hkv must be 1 and head_dim 160.  Every base
- * pointer of a 16-bit tensor must be 16-byte aligned and every token/head
- * stride a multiple of 8 elements (the tensors are staged by TMA). */
+ * dout, out, dq, dk, dv.  head_dim must be 160 and Hq a multiple of Hkv.
+ * Every base pointer of a 16-bit tensor must be 16-byte aligned and every
+ * token/head stride a multiple of 8 elements (the tensors are staged by
+ * TMA).  With Hkv > 1 each K/V head group runs as its own problem, one after
+ * the other on `stream` (query heads g*Hq/Hkv .. (g+1)*Hq/Hkv - 1 with K/V
+ * head g), so the call enqueues more kernels (attn_varlen_launch_count). */
 attn_status attn_varlen_fvjp_fwd_bwd(
     attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
     const void *q, int64_t q_tok_stride, int64_t q_head_stride,
@@ -165,8 +176,14 @@ attn_status attn_varlen_bwd(
 const char *attn_status_string(attn_status s);
 
 /* Number of kernel launches one attn_varlen_fvjp_fwd_bwd call enqueues for
- * these sizes (for launch accounting by callers and benchmarks). */
+ * these sizes with one K/V head (for launch accounting by callers and
+ * benchmarks). */
 int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k);
+
+/* The same for any entry point and K/V head count: mode 1 = attn_varlen_fwd,
+ * 2 = attn_varlen_bwd, 3 = the fused call.  0 for an invalid mode or Hkv. */
+int attn_varlen_launch_count(int mode, int B, int Hq, int Hkv, int64_t total_q,
+                             int64_t total_k);
 
 /* Timing hook: the next attn_varlen_fvjp_fwd_bwd call made by THIS host
  * thread records events[0] before its first kernel and events[i] after its
@@ -174,7 +191,8 @@ int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_
  * preprocess, dk/dv, dq), then forgets the events.  `events` holds
  * cudaEvent_t handles owned by the caller; n must be 6 (or 0 to cancel).
  * Returns ATTN_ERR_INVALID for any other n.  Used by benchmarks to time each
- * kernel on the launching stream. */
+ * kernel on the launching stream.  A call with Hkv > 1 records nothing (and
+ * still forgets the events). */
 attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
 
 /* Size of the fixed device scratch array used by

@@ -21,7 +21,8 @@ DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0
 
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
-           "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd")
+           "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
+           "attn_varlen_launch_count")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -46,6 +47,8 @@ def load(path: str = LIB_PATH):
     lib.attn_varlen_fvjp_workspace_size.restype = ctypes.c_size_t
     lib.attn_varlen_fvjp_launch_count.argtypes = [I, I, L, L]
     lib.attn_varlen_fvjp_launch_count.restype = I
+    lib.attn_varlen_launch_count.argtypes = [I, I, I, I, L, L]
+    lib.attn_varlen_launch_count.restype = I
     lib.attn_status_string.argtypes = [I]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_varlen_fvjp_fwd_bwd.argtypes = (
@@ -74,8 +77,9 @@ def workspace_size(B: int, Hq: int, total_q: int, total_k: int) -> int:
     return int(load().attn_varlen_fvjp_workspace_size(B, Hq, total_q, total_k))
 
 
-def launch_count(B: int, Hq: int, total_q: int, total_k: int) -> int:
-    return int(load().attn_varlen_fvjp_launch_count(B, Hq, total_q, total_k))
+def launch_count(B: int, Hq: int, total_q: int, total_k: int, Hkv: int = 1, mode: int = 3) -> int:
+    """Kernel launches of one call (mode 1 forward, 2 backward, 3 fused)."""
+    return int(load().attn_varlen_launch_count(mode, B, Hq, Hkv, total_q, total_k))
 
 
 def record_events_next_call(events):
@@ -92,6 +96,14 @@ def record_events_next_call(events):
 
 def _ptr(t):
     return None if t is None else t.data_ptr()
+
+
+def _kv_heads(q, k):
+    """Hkv of a call: k's head count, which must divide q's."""
+    Hkv = k.shape[1] if k.dim() == 3 else 1
+    if Hkv < 1 or q.shape[1] % Hkv:
+        raise ValueError(f"q's {q.shape[1]} heads are not a multiple of k's {Hkv}")
+    return Hkv
 
 
 def _check_qlike(name, t, dtype, Hq=None):
@@ -127,10 +139,11 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     if dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("q must be fp16 or bf16")
     Hq = q.shape[1]
+    Hkv = _kv_heads(q, k)
     _check_qlike("q", q, dtype)
     _check_qlike("dout", dout, dtype, Hq)
-    _check_qlike("k", k, dtype, 1)
-    _check_qlike("v", v, dtype, 1)
+    _check_qlike("k", k, dtype, Hkv)
+    _check_qlike("v", v, dtype, Hkv)
     if dout.shape[0] != q.shape[0] or v.shape[0] != k.shape[0]:
         raise ValueError("dout must match q and v must match k in length")
     for name, c in (("cu_q", cu_q), ("cu_k", cu_k)):
@@ -148,7 +161,7 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     dq = _like(q) if dq is None else dq
     dk = _like(k) if dk is None else dk
     dv = _like(v) if dv is None else dv
-    for name, t, H in (("out", out, Hq), ("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+    for name, t, H in (("out", out, Hq), ("dq", dq, Hq), ("dk", dk, Hkv), ("dv", dv, Hkv)):
         _check_qlike(name, t, dtype, H)
     if lse is None:
         lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device)
@@ -158,7 +171,7 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fvjp_fwd_bwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -179,9 +192,10 @@ def _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout=None):
     if dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("q must be fp16 or bf16")
     Hq = q.shape[1]
+    Hkv = _kv_heads(q, k)
     _check_qlike("q", q, dtype)
-    _check_qlike("k", k, dtype, 1)
-    _check_qlike("v", v, dtype, 1)
+    _check_qlike("k", k, dtype, Hkv)
+    _check_qlike("v", v, dtype, Hkv)
     if v.shape[0] != k.shape[0]:
         raise ValueError("v must match k in length")
     if dout is not None:
@@ -198,7 +212,7 @@ def _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout=None):
         if (not alibi_slopes.is_cuda or alibi_slopes.dtype != torch.float32 or
                 alibi_slopes.shape != (B, Hq) or alibi_slopes.stride(1) != 1):
             raise ValueError("alibi_slopes must be fp32 [B, Hq] on the device, head stride 1")
-    return dtype, B, Hq
+    return dtype, B, Hq, Hkv
 
 
 def _workspace(workspace, B, Hq, Tq, Tk, device):
@@ -215,7 +229,7 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
     attention_varlen_fvjp; lse is fp32 [T_q, Hq] (natural log), the value the
     backward call reads back.  Asynchronous on ``stream``."""
     lib = load()
-    dtype, B, Hq = _check_common(q, k, v, cu_q, cu_k, alibi_slopes)
+    dtype, B, Hq, Hkv = _check_common(q, k, v, cu_q, cu_k, alibi_slopes)
     Tq, Tk = q.shape[0], k.shape[0]
     out = _like(q) if out is None else out
     _check_qlike("out", out, dtype, Hq)
@@ -226,7 +240,7 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -247,7 +261,7 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
     the same inputs the result is bitwise the one attention_varlen_fvjp gives.
     Asynchronous on ``stream``."""
     lib = load()
-    dtype, B, Hq = _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout)
+    dtype, B, Hq, Hkv = _check_common(q, k, v, cu_q, cu_k, alibi_slopes, dout)
     Tq, Tk = q.shape[0], k.shape[0]
     _check_qlike("out", out, dtype, Hq)
     if out.shape[0] != Tq:
@@ -256,13 +270,13 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
     dq = _like(q) if dq is None else dq
     dk = _like(k) if dk is None else dk
     dv = _like(v) if dv is None else dv
-    for name, t, H in (("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+    for name, t, H in (("dq", dq, Hq), ("dk", dk, Hkv), ("dv", dv, Hkv)):
         _check_qlike(name, t, dtype, H)
     workspace = _workspace(workspace, B, Hq, Tq, Tk, q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_bwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -293,14 +307,15 @@ def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, 
     lib = load()
     dtype = q.dtype
     Hq = q.shape[1]
-    for name, t, H in (("q", q, Hq), ("dout", dout, Hq), ("k", k, 1), ("v", v, 1),
-                       ("out", out, Hq), ("dq", dq, Hq), ("dk", dk, 1), ("dv", dv, 1)):
+    Hkv = _kv_heads(q, k)
+    for name, t, H in (("q", q, Hq), ("dout", dout, Hq), ("k", k, Hkv), ("v", v, Hkv),
+                       ("out", out, Hq), ("dq", dq, Hq), ("dk", dk, Hkv), ("dv", dv, Hkv)):
         _check_qlike(name, t, dtype, H)
     B = cu_q.numel() - 1
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fvjp_fwd_bwd_noalloc(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, 1, HEAD_DIM, q.shape[0],
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, q.shape[0],
         k.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),

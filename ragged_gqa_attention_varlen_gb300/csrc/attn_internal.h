@@ -21,6 +21,11 @@ static_assert(4 * kRegsLow + 8 * kRegsHigh <= 12 * 168, "register split exceeds 
 
 // Query rows of a tile are (token, head) pairs: G consecutive heads of one
 // head group times 128/G consecutive tokens, row r = token*G + head.
+//
+// With Hkv > 1 K/V heads, query heads g*R .. g*R+R-1 (R = Hq/Hkv) read K/V
+// head g, and each such group runs as its own one-K/V-head problem: Params
+// then describe the group (Hq = R, every pointer offset to the group's first
+// head), with lse/D rows still strided by the whole call's head count.
 struct Params {
   int dtype;  // 0 fp16, 1 bf16
   int B, Hq, G;
@@ -47,10 +52,12 @@ struct Params {
   int causal, wl, wr;
   float softcap;  // <= 0: no cap
   float sigma;    // scale_multiplier / sqrt(160)
-  float* lse;     // [total_q, Hq]
-  float* Dbuf;    // [total_q, Hq]
+  float* lse;     // [total_q, lse_rs]
+  float* Dbuf;    // [total_q, lse_rs]
+  int64_t lse_rs; // row stride of lse and D: every query head of the call
   int32_t* status;
-  int32_t* counters;  // [4]: fwd, dkdv, dq tile counters
+  int32_t* counters;  // [3]: fwd, dkdv, dq tile counters (of this K/V head group)
+  int ncounters;      // counters the schedule kernel resets (every group's)
   int32_t* sched;     // schedule arrays, see sched.cu
 };
 

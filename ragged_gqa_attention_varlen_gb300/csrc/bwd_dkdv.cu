@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = q.hg * G + (lc & (G - 1));
         const bool live = q.item < ntiles;
         const bool valid = live && i < q.t.Lq;
-        const int64_t ri = static_cast<int64_t>(q.t.q0 + i) * p.Hq + h;
+        const int64_t ri = static_cast<int64_t>(q.t.q0 + i) * p.lse_rs + h;
         v.lse[hh] = valid ? __ldg(p.lse + ri) : -INFINITY;
         v.sl2[hh] = (live && p.slopes) ? __ldg(p.slopes + q.t.b * p.slopes_bs + h) : 0.f;
         v.D[hh] = valid ? __ldg(p.Dbuf + ri) : 0.f;

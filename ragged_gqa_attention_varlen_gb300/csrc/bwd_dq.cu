@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       const int pos_off = i_loc + t.Lk - t.Lq;
       float lse2 = INFINITY, Drow = 0.f;  // rows outside the sequence get P = 0
       if (row_valid) {
-        const int64_t ri = static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h;
+        const int64_t ri = static_cast<int64_t>(t.q0 + i_loc) * p.lse_rs + h;
         const float lse = p.lse[ri];
         lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
         Drow = p.Dbuf[ri];

@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       const float lnorm = fixed ? lrt : lt;
       const float inv = (lnorm > 0.f) ? 1.f / lnorm : 0.f;
       if (row_valid && half == 0)
-        p.lse[static_cast<int64_t>(t.q0 + i_loc) * p.Hq + h] =
+        p.lse[static_cast<int64_t>(t.q0 + i_loc) * p.lse_rs + h] =
             (lt > 0.f) ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
       const uint32_t ob = tmem + kColO + half * 80 + lane_addr;
       float o[80];

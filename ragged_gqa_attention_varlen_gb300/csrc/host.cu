@@ -40,11 +40,12 @@ struct WsLayout {
   size_t status, counters, sched, dbuf, total;
 };
 
+// Counters: three per K/V head group, and Hkv <= Hq.
 WsLayout ws_layout(int B, int Hq, int64_t total_q) {
   WsLayout w;
   w.status = 0;
   w.counters = 16;
-  w.sched = kAlign;
+  w.sched = align_up(w.counters + sizeof(int32_t) * 3 * static_cast<size_t>(Hq < 2 ? 2 : Hq));
   w.dbuf = w.sched + align_up(sizeof(int32_t) * static_cast<size_t>(sched_words(B)));
   w.total = w.dbuf + align_up(sizeof(float) * static_cast<size_t>(total_q) * Hq);
   return w;
@@ -169,13 +170,21 @@ extern "C" size_t attn_varlen_fvjp_workspace_size(int B, int Hq, int64_t total_q
   return ws_layout(B, Hq, total_q).total;
 }
 
-extern "C" int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k) {
+extern "C" int attn_varlen_launch_count(int mode, int B, int Hq, int Hkv, int64_t total_q,
+                                        int64_t total_k) {
   (void)B;
   (void)Hq;
+  const bool fwd = (mode & 1) != 0, bwd = (mode & 2) != 0;
+  if (Hkv < 1 || (!fwd && !bwd)) return 0;
   if (total_q == 0 && total_k == 0) return 0;
-  if (total_q == 0) return 2;  // dk, dv zero fills
-  if (total_k == 0) return 3;  // out, dq zero fills, lse fill
-  return 5;                    // schedule, forward, preprocess, dk/dv, dq
+  if (total_q == 0) return bwd ? 2 : 0;               // dk, dv zero fills
+  if (total_k == 0) return (fwd ? 2 : 0) + (bwd ? 1 : 0);  // out + lse fills; dq fill
+  // schedule; a forward per K/V head group; preprocess, dk/dv and dq per group
+  return 1 + (fwd ? Hkv : 0) + (bwd ? 1 + 2 * Hkv : 0);
+}
+
+extern "C" int attn_varlen_fvjp_launch_count(int B, int Hq, int64_t total_q, int64_t total_k) {
+  return attn_varlen_launch_count(3, B, Hq, 1, total_q, total_k);
 }
 
 extern "C" attn_status attn_varlen_fvjp_record_events(void* const* events, int n) {
@@ -222,15 +231,12 @@ attn_status run_call(
     int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
     void* stream_ptr) {
   const bool fwd = (mode & kModeFwd) != 0, bwd = (mode & kModeBwd) != 0;
-  (void)k_hs;
-  (void)v_hs;
-  (void)dk_hs;
-  (void)dv_hs;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   // ---- host-side validation (nothing is enqueued on failure)
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
-  if (head_dim != kHeadDim || Hkv != 1) return ATTN_ERR_UNSUPPORTED;
+  if (head_dim != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+  if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
   if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
   if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 && (total_q != 0 || total_k != 0)) return ATTN_ERR_INVALID;
@@ -259,11 +265,17 @@ attn_status run_call(
       if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
     for (int64_t s : {k_ts, v_ts})
       if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (Hkv > 1)  // head strides matter only with several K/V heads
+      for (int64_t s : {k_hs, v_hs})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
     if (bwd) {
       for (const void* ptr : {static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
       for (int64_t s : {dk_ts, dv_ts})
         if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+      if (Hkv > 1)
+        for (int64_t s : {dk_hs, dv_hs})
+          if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
     }
   }
   const WsLayout ws = ws_layout(B, Hq, total_q);
@@ -276,7 +288,7 @@ attn_status run_call(
   p.dtype = dtype;
   p.B = B;
   p.Hq = Hq;
-  p.G = head_group(Hq);
+  p.G = head_group(Hq / (Hkv > 0 ? Hkv : 1));
   p.total_q = total_q;
   p.total_k = total_k;
   p.out = out;
@@ -306,9 +318,11 @@ attn_status run_call(
   p.softcap = softcap;
   p.sigma = static_cast<float>(static_cast<double>(scale_multiplier) / 12.649110640673518);
   p.lse = lse;
+  p.lse_rs = Hq;
   p.Dbuf = reinterpret_cast<float*>(wsb + ws.dbuf);
   p.status = device_status ? device_status : reinterpret_cast<int32_t*>(wsb + ws.status);
   p.counters = reinterpret_cast<int32_t*>(wsb + ws.counters);
+  p.ncounters = 3 * Hkv;
   p.sched = reinterpret_cast<int32_t*>(wsb + ws.sched);
 
   // ---- degenerate sizes: no query or no key at all
@@ -316,8 +330,8 @@ attn_status run_call(
     if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (has_k && bwd) {  // no queries: dk = dv = 0
-      e = launch_zero_fill(dk, total_k, 1, dk_ts, 8, stream);
-      if (e == cudaSuccess) e = launch_zero_fill(dv, total_k, 1, dv_ts, 8, stream);
+      e = launch_zero_fill(dk, total_k, Hkv, dk_ts, Hkv > 1 ? dk_hs : 8, stream);
+      if (e == cudaSuccess) e = launch_zero_fill(dv, total_k, Hkv, dv_ts, Hkv > 1 ? dv_hs : 8, stream);
     }
     if (has_q) {  // no keys: every row is empty
       if (fwd) {
@@ -329,57 +343,99 @@ attn_status run_call(
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
 
-  // ---- TMA tensor maps
+  // ---- TMA tensor maps of one K/V head group (all of them when Hkv = 1)
   if (!encode_fn()) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2, tqf, tdof;
-  if (!encode_q_full(&tqf, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_q_pair(&tq2, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_kv_pair(&tk2, dtype, k, total_k, k_ts) ||
-      !encode_kv_pair(&tv2, dtype, v, total_k, v_ts) ||
-      !encode_q(&tq, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ) ||
-      !encode_q(&tqt, dtype, q, total_q, Hq, q_ts, q_hs, p.G, kRowsQ, true) ||
-      !encode_kv(&tk, dtype, k, total_k, k_ts) || !encode_kv(&tv, dtype, v, total_k, v_ts) ||
-      !encode_kv(&tkt, dtype, k, total_k, k_ts, true) ||
-      !encode_kv(&tvt, dtype, v, total_k, v_ts, true))
-    return ATTN_ERR_ALIGNMENT;
-  if (bwd && (!encode_q_full(&tdof, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
-              !encode_q_pair(&tdo2, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
-              !encode_q(&tdo, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ) ||
-              !encode_q(&tdot, dtype, dout, total_q, Hq, do_ts, do_hs, p.G, kRowsQ, true)))
-    return ATTN_ERR_ALIGNMENT;
+  struct Maps {
+    CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2, tqf, tdof;
+  };
+  const int R = Hq / Hkv;  // query heads per K/V head
+  auto group_params = [&](int g) {
+    Params pg = p;
+    pg.Hq = R;
+    auto off = [](const void* base, int64_t elems) -> const uint16_t* {
+      return base ? static_cast<const uint16_t*>(base) + elems : nullptr;
+    };
+    const int64_t h0 = static_cast<int64_t>(g) * R;
+    pg.q = off(q, h0 * q_hs);
+    pg.out = const_cast<uint16_t*>(off(out, h0 * out_hs));
+    pg.outp = pg.out;
+    pg.dq = const_cast<uint16_t*>(off(dq, h0 * dq_hs));
+    pg.dout = off(dout, h0 * do_hs);
+    pg.dk = const_cast<uint16_t*>(off(dk, static_cast<int64_t>(g) * dk_hs));
+    pg.dv = const_cast<uint16_t*>(off(dv, static_cast<int64_t>(g) * dv_hs));
+    pg.lse = lse + h0;
+    pg.Dbuf = p.Dbuf + h0;
+    pg.slopes = alibi_slopes ? alibi_slopes + h0 : nullptr;
+    pg.counters = p.counters + 3 * g;
+    return pg;
+  };
+  auto encode_group = [&](const Params& pg, int g, Maps& m) -> bool {
+    const void* kg = static_cast<const uint16_t*>(k) + static_cast<int64_t>(g) * k_hs;
+    const void* vg = static_cast<const uint16_t*>(v) + static_cast<int64_t>(g) * v_hs;
+    if (!encode_q_full(&m.tqf, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_q_pair(&m.tq2, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_kv_pair(&m.tk2, dtype, kg, total_k, k_ts) ||
+        !encode_kv_pair(&m.tv2, dtype, vg, total_k, v_ts) ||
+        !encode_q(&m.tq, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_q(&m.tqt, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ, true) ||
+        !encode_kv(&m.tk, dtype, kg, total_k, k_ts) || !encode_kv(&m.tv, dtype, vg, total_k, v_ts) ||
+        !encode_kv(&m.tkt, dtype, kg, total_k, k_ts, true) ||
+        !encode_kv(&m.tvt, dtype, vg, total_k, v_ts, true))
+      return false;
+    if (bwd && (!encode_q_full(&m.tdof, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q_pair(&m.tdo2, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q(&m.tdo, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q(&m.tdot, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ, true)))
+      return false;
+    return true;
+  };
 
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
-  // Upper bounds of the tile counts (the device schedule has the exact ones).
+  // Upper bounds of the tile counts of one group (the device schedule has
+  // the exact ones).
   const int64_t rows_tok = kRowsQ / p.G;
-  const int64_t qtiles_max = (total_q / rows_tok + B) * (Hq / p.G);
+  const int64_t qtiles_max = (total_q / rows_tok + B) * (R / p.G);
   const int64_t ktiles_max = total_k / kKeys + B;
   const int grid_q = static_cast<int>(qtiles_max < sms ? qtiles_max : sms);
   const int grid_k = static_cast<int>(ktiles_max < sms ? ktiles_max : sms);
 
-  // the timing hook applies to the fused call only
-  const int nev = (fwd && bwd) ? g_nevents : 0;
+  // the timing hook applies to the fused call with one K/V head only
+  const int nev = (fwd && bwd && Hkv == 1) ? g_nevents : 0;
   if (fwd && bwd) g_nevents = 0;
   auto mark = [&](int i) {
     if (nev) cudaEventRecord(g_events[i], stream);
   };
+  Params p0 = group_params(0);
+  p0.counters = p.counters;  // the schedule resets every group's counters
   mark(0);
-  if (launch_sched(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_sched(p0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(1);
-  if (fwd && launch_fwd(p, tq2, tqt, tk2, tkt, tv2, tv, grid_q, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  Maps m;
+  if (fwd) {
+    for (int g = 0; g < Hkv; ++g) {
+      const Params pg = group_params(g);
+      if (!encode_group(pg, g, m)) return ATTN_ERR_ALIGNMENT;
+      if (launch_fwd(pg, m.tq2, m.tqt, m.tk2, m.tkt, m.tv2, m.tv, grid_q, stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    }
+  }
   if (!bwd) return ATTN_OK;
   mark(2);
-  if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;  // every head
   mark(3);
-  if (launch_dkdv(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid_k, stream) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
-  mark(4);
-  // dq may overlap the tail of dk/dv (no per-kernel events in between)
-  if (launch_dq(p, tq2, tqt, tdo2, tdot, tk2, tk, tv2, tvt, grid_q, nev == 0, stream) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
+  for (int g = 0; g < Hkv; ++g) {
+    const Params pg = group_params(g);
+    if (!encode_group(pg, g, m)) return ATTN_ERR_ALIGNMENT;
+    if (launch_dkdv(pg, m.tq2, m.tq, m.tdo2, m.tdo, m.tk2, m.tkt, m.tv2, m.tvt, m.tqf, m.tdof,
+                    grid_k, stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    mark(4);
+    // dq may overlap the tail of dk/dv (no per-kernel events in between)
+    if (launch_dq(pg, m.tq2, m.tqt, m.tdo2, m.tdot, m.tk2, m.tk, m.tv2, m.tvt, grid_q, nev == 0,
+                  stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
   mark(5);
   return ATTN_OK;
 }

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
   }
   if (tid == 0) {
     *p.status = 0;
-    for (int i = 0; i < 4; ++i) p.counters[i] = 0;
+    for (int i = 0; i < p.ncounters; ++i) p.counters[i] = 0;
   }
   // The work of a sequence's longest forward/dq tile grows with the keys it
   // visits, of a dk/dv tile with the queries: the whole other length, or
@@ -98,7 +98,8 @@ cudaError_t launch_sched(const Params& p, cudaStream_t s) {
 }
 
 // D[t, h] = sum_f dO[t,h,f] * O[t,h,f] in fp32 over the stored (rounded)
-// output.  One warp per (token, head) row; lanes 0..19 each take 8 features.
+// output, for every head of the call (D row stride = Hq = lse_rs).  One warp
+// per (token, head) row; lanes 0..19 each take 8 features.
 template <typename T>
 __device__ __forceinline__ float dot8(uint4 a, uint4 b);
 

@@ -66,7 +66,11 @@ def _call(lib, **over):
 def test_host_validation_codes(lib):
     assert _call(lib, dtype=7) == -1
     assert _call(lib, hd=128) == -2
-    assert _call(lib, Hkv=2) == -2
+    assert _call(lib, Hkv=3) == -1             # 16 query heads do not split over 3
+    assert _call(lib, Hkv=0) == -1
+    assert _call(lib, Hkv=2, khs=164) == -3     # head strides count once Hkv > 1
+    assert _call(lib, Hkv=1, khs=164) == -4     # ... and are ignored for one K/V head
+    assert _call(lib, Hkv=2) == -4              # a valid split reaches the workspace check
     assert _call(lib, B=20000) == -2
     assert _call(lib, q=0x10008) == -3          # base not 16-byte aligned
     assert _call(lib, qhs=164) == -3            # stride not a multiple of 8 elements
@@ -74,6 +78,15 @@ def test_host_validation_codes(lib):
     assert _call(lib, wsb=16) == -4             # workspace too small
     assert _call(lib, B=0) == -1                # B = 0 with tokens
     assert _call(lib, q=None) == -1
+
+
+def test_launch_counts(lib):
+    f = lib.attn_varlen_launch_count
+    assert f(3, 2, 16, 1, 10, 12) == 5 == lib.attn_varlen_fvjp_launch_count(2, 16, 10, 12)
+    assert f(1, 2, 16, 1, 10, 12) == 2 and f(2, 2, 16, 1, 10, 12) == 4
+    assert f(3, 2, 16, 4, 10, 12) == 1 + 4 + 1 + 2 * 4
+    assert f(3, 2, 16, 4, 0, 12) == 2 and f(1, 2, 16, 4, 0, 12) == 0
+    assert f(3, 2, 16, 1, 10, 0) == 3 and f(0, 2, 16, 1, 10, 12) == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):

@@ -188,6 +188,57 @@ def test_window_wider_than_every_sequence_is_bitwise_unmasked():
         assert bits_equal(x, wide[n]), n
 
 
+# ------------------------------------------------ several K/V heads
+# Query heads g*R .. g*R+R-1 (R = Hq/Hkv) read K/V head g; each group runs
+# as its own one-K/V-head problem.
+
+GQA = [
+    dict(lq=[300, 37, 1, 129], lk=[260, 400, 9, 0], Hq=16, Hkv=2),
+    dict(lq=[200, 64], lk=[333, 90], Hq=48, Hkv=8, dtype=torch.bfloat16, step=2),  # R 6, G 2
+    dict(lq=[150, 20], lk=[140, 300], Hq=12, Hkv=4, causal=True, window_left=40),  # R 3, G 1
+    dict(lq=[90], lk=[130], Hq=8, Hkv=8, pad=192, dtype=torch.bfloat16),            # one head each
+]
+
+
+@pytest.mark.parametrize("case", GQA, ids=[f"gqa{i}" for i in range(len(GQA))])
+def test_gqa_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    p = W.custom(lq, lk, Hq, **case)
+    _, res = parity(p, oracle_mod)
+    # the split calls run the same kernels
+    split = _split(p.to("cuda"))
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert bits_equal(res[n], split[n]), n
+
+
+def test_gqa_call_is_bitwise_its_head_groups_alone():
+    """A call with Hkv = 2 gives bitwise what two one-K/V-head calls give on
+    its two head groups (strided head slices of the same tensors)."""
+    Hq, Hkv = 16, 2
+    R = Hq // Hkv
+    p = W.custom([300, 37, 129], [260, 400, 9], Hq, Hkv=Hkv, dtype=torch.bfloat16).to("cuda")
+    full = run(p)
+    full = {n: full[n].clone() for n in ("out", "lse", "dq", "dk", "dv")}
+    for g in range(Hkv):
+        hs = slice(g * R, (g + 1) * R)
+        r = BND.attention_varlen_fvjp(p.q[:, hs], p.k[:, g:g + 1], p.v[:, g:g + 1], p.cu_q,
+                                      p.cu_k, p.alibi_slopes[:, hs], p.dout[:, hs])
+        torch.cuda.synchronize()
+        assert BND.device_status(r["workspace"]) == 0
+        for n in ("out", "lse", "dq"):
+            assert bits_equal(full[n][:, hs], r[n]), (n, g)
+        for n in ("dk", "dv"):
+            assert bits_equal(full[n][:, g:g + 1], r[n]), (n, g)
+
+
+def test_gqa_rejects_uneven_head_split():
+    p = W.custom([5], [7], 12, Hkv=1).to("cuda")
+    k = torch.zeros((7, 5, 160), dtype=p.k.dtype, device="cuda")
+    with pytest.raises(ValueError):
+        BND.attention_varlen_fvjp(p.q, k, k, p.cu_q, p.cu_k, p.alibi_slopes, p.dout)
+
+
 # ------------------------------------------- split forward / backward calls
 
 def _split_cases():
