@@ -58,14 +58,14 @@ def scored_pairs(p) -> int:
 def counted_flops(p) -> float:
     """4 d (forward) + 10 d (backward) per admissible (query, key) pair and
     query head: 14 Lq Lk d per head without a mask."""
-    return 14.0 * HEAD_DIM * p.Hq * scored_pairs(p)
+    return 14.0 * p.q.shape[-1] * p.Hq * scored_pairs(p)
 
 
 def kernel_flops(p) -> dict:
     """Algorithmic flops each kernel contributes to the counted total: the
     forward's two matmuls (4d), dk/dv's four (S^T, dP^T, dV, dK: 8d) and dq's
     dQ = dS K (2d); dq's recompute of S and dP is not counted."""
-    u = HEAD_DIM * p.Hq * scored_pairs(p)
+    u = p.q.shape[-1] * p.Hq * scored_pairs(p)
     return {"forward": 4 * u, "dkdv": 8 * u, "dq": 2 * u, "schedule": 0.0, "preprocess": 0.0}
 
 
@@ -290,7 +290,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False,
-                                length_scale=args.length_scale, Hkv=args.hkv)
+                                length_scale=args.length_scale, Hkv=args.hkv, d=args.head_dim)
     p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
     flops = counted_flops(p)
     kflops = kernel_flops(p)
@@ -358,8 +358,8 @@ def run_gpu(args, world, rank, local):
         achieved = kflops[dom] / (per_kernel[dom] / 1e3) / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                     "unit": "TFLOP/s", "frac": achieved / peak,
-                    "traffic": dram_traffic(dom) if args.length_scale == 1.0 and not mask_name(p)
-                               else None,
+                    "traffic": dram_traffic(dom) if (args.length_scale == 1.0 and not mask_name(p)
+                                                     and args.head_dim == HEAD_DIM) else None,
                     "peak_kind": f"{kind} bf16 sustained"}
     else:
         # one call runs a forward, dk/dv and dq per K/V head group: the
@@ -382,9 +382,10 @@ def run_gpu(args, world, rank, local):
             "data": "synthetic (seeded, generated on device)",
             "config": {"workload": "long_balanced" + (
                            "" if args.length_scale == 1.0 else f" x{args.length_scale} length") +
-                           mask_name(p) + ("" if args.hkv == 1 else f", Hkv={args.hkv}"),
+                           mask_name(p) + ("" if args.hkv == 1 else f", Hkv={args.hkv}") +
+                           ("" if args.head_dim == HEAD_DIM else f", d={args.head_dim}"),
                        "B": p.B, "Hq": p.Hq, "Hkv": args.hkv,
-                       "head_dim": HEAD_DIM, "token_step": 2, "total_q": p.total_q,
+                       "head_dim": args.head_dim, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
                        "scored_pairs": scored_pairs(p),
                        "counted_tflop_per_step": flops / 1e12,
@@ -393,7 +394,8 @@ def run_gpu(args, world, rank, local):
             "latency_ms": ms, "frac_of_bf16_peak": whole_frac,
             "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
             "clocks": clk, "e2e": e2e}
-    if rank == 0 and world == 1 and not args.no_cpu and not mask_name(p) and args.hkv == 1:
+    if (rank == 0 and world == 1 and not args.no_cpu and not mask_name(p) and args.hkv == 1
+            and args.head_dim == HEAD_DIM):
         v, cores, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -459,6 +461,7 @@ def main():
                     help="time the causal variant (flops counted over admissible pairs)")
     ap.add_argument("--window-left", type=int, default=-1)
     ap.add_argument("--window-right", type=int, default=-1)
+    ap.add_argument("--head-dim", type=int, default=HEAD_DIM, choices=(64, 128, 160))
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
     args = ap.parse_args()

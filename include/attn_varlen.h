@@ -12,7 +12,7 @@
  * sections "Hard Constraints" and "What You Have"):
  *   for sequence b with Lq = cu_q[b+1]-cu_q[b] queries and Lk = cu_k[b+1]-cu_k[b]
  *   keys, head h, local query i and key j:
- *     s   = (scale_multiplier / sqrt(160)) * q[i,h,:] . k[j,g(h),:]
+ *     s   = (scale_multiplier / sqrt(head_dim)) * q[i,h,:] . k[j,g(h),:]
  *     t   = softcap * tanh(s / softcap)        (t = s when softcap <= 0)
  *     z   = t - alibi_slopes[b,h] * |i + Lk - Lq - j|
  *     z   = -inf where the causal/window mask forbids (i, j)
@@ -34,10 +34,10 @@
  *   (window_left < 0 or j >= k0 - window_left) and
  *   (wr < 0 or j <= k0 + wr), where wr = 0 if causal else window_right.
  *
- * Layouts.  All strides are in ELEMENTS; the feature axis (160 values) is
- * contiguous.  q, dout, out, dq are [total_q, Hq, 160] at
+ * Layouts.  All strides are in ELEMENTS; the feature axis (head_dim values,
+ * 160 in the pages' workload) is contiguous.  q, dout, out, dq are [total_q, Hq, head_dim] at
  *   base + token * tok_stride + head * head_stride + feature;
- * k, v, dk, dv are [total_k, Hkv, 160] at
+ * k, v, dk, dv are [total_k, Hkv, head_dim] at
  *   base + token * tok_stride + head * head_stride + feature
  * (the head stride is ignored when Hkv = 1).
  * Token and head strides may be non-dense (padded features, token steps).
@@ -78,7 +78,7 @@ typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID = -1,     /* a null pointer, negative size, bad cu/total pair,
                                 Hkv < 1 or Hq not a multiple of Hkv */
-  ATTN_ERR_UNSUPPORTED = -2, /* head_dim != 160, B too large */
+  ATTN_ERR_UNSUPPORTED = -2, /* head_dim not 64, 128 or 160; B too large */
   ATTN_ERR_ALIGNMENT = -3,   /* base not 16-byte aligned, stride not a multiple of 8 */
   ATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
   ATTN_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
@@ -96,7 +96,7 @@ typedef enum {
 
 /* Largest batch (number of sequences) accepted. */
 #define ATTN_MAX_BATCH 16384
-/* The only head dimension implemented. */
+/* The pages' head dimension; 128 and 64 are accepted too. */
 #define ATTN_HEAD_DIM 160
 
 /* Bytes of device workspace a call with these sizes needs (256-byte aligned
@@ -106,7 +106,9 @@ size_t attn_varlen_fvjp_workspace_size(int B, int Hq, int64_t total_q, int64_t t
 
 /* Forward + full VJP, fused into one call on `stream` (a cudaStream_t; NULL
  * is the legacy default stream).  `dtype` is the element type of q, k, v,
- * dout, out, dq, dk, dv.  head_dim must be 160 and Hq a multiple of Hkv.
+ * dout, out, dq, dk, dv.  head_dim must be 160 (the pages' case), 128 or 64
+ * (run on the same 160-feature tiles with the features past head_dim read
+ * as zeros and never written), and Hq a multiple of Hkv.
  * Every base pointer of a 16-bit tensor must be 16-byte aligned and every
  * token/head stride a multiple of 8 elements (the tensors are staged by
  * TMA).  With Hkv > 1 each K/V head group runs as its own problem, one after

@@ -13,7 +13,8 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn_varlen.so")
-HEAD_DIM = 160
+HEAD_DIM = 160            # the pages' head dimension
+HEAD_DIMS = (64, 128, 160)  # head dimensions the library accepts
 _lib = None
 
 ATTN_F16, ATTN_BF16 = 0, 1
@@ -99,10 +100,13 @@ def _ptr(t):
 
 
 def _kv_heads(q, k):
-    """Hkv of a call: k's head count, which must divide q's."""
+    """Hkv of a call: k's head count, which must divide q's (and k's head
+    dimension must be q's)."""
     Hkv = k.shape[1] if k.dim() == 3 else 1
     if Hkv < 1 or q.shape[1] % Hkv:
         raise ValueError(f"q's {q.shape[1]} heads are not a multiple of k's {Hkv}")
+    if k.shape[-1] != q.shape[-1]:
+        raise ValueError("q and k must have the same head dimension")
     return Hkv
 
 
@@ -111,8 +115,9 @@ def _check_qlike(name, t, dtype, Hq=None):
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
-    if t.dim() != 3 or t.shape[-1] != HEAD_DIM or t.stride(-1) != 1:
-        raise ValueError(f"{name} must be [tokens, heads, 160] with a contiguous feature axis")
+    if t.dim() != 3 or t.shape[-1] not in HEAD_DIMS or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be [tokens, heads, d] (d in {HEAD_DIMS}) with a "
+                         "contiguous feature axis")
     if Hq is not None and t.shape[1] != Hq:
         raise ValueError(f"{name} must have {Hq} heads")
 
@@ -171,7 +176,7 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fvjp_fwd_bwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -240,7 +245,7 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -276,7 +281,7 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_bwd(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, Tq, Tk,
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
@@ -315,7 +320,7 @@ def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, 
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     code = lib.attn_varlen_fvjp_fwd_bwd_noalloc(
-        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, HEAD_DIM, q.shape[0],
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], q.shape[0],
         k.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),

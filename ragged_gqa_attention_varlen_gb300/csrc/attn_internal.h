@@ -29,6 +29,9 @@ static_assert(4 * kRegsLow + 8 * kRegsHigh <= 12 * 168, "register split exceeds 
 struct Params {
   int dtype;  // 0 fp16, 1 bf16
   int B, Hq, G;
+  int d;      // head dimension: 160, 128 or 64 (the kernels' tiles hold 160
+              // features; the TMA maps fill features >= d with zeros and
+              // every other load or store stops at d)
   int64_t total_q, total_k;
   // outputs (element strides)
   void* out;
@@ -61,6 +64,13 @@ struct Params {
   int32_t* sched;     // schedule arrays, see sched.cu
 };
 
+// 16-byte units (8 features) of a row's features [80*half, 80*half + 80)
+// that lie below the head dimension.
+__host__ __device__ inline int feature_units(int d, int half) {
+  const int u = (d - 80 * half) / 8;
+  return u < 0 ? 0 : (u > 10 ? 10 : u);
+}
+
 // The call has a causal or window mask (selects the masked kernel instances).
 inline bool masked_call(const Params& p) { return p.causal || p.wl >= 0 || p.wr >= 0; }
 
@@ -88,7 +98,7 @@ cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s);
-cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
+cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs, int d,
                              cudaStream_t s);
 cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s);
 

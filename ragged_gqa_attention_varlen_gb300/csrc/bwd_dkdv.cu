@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : static_cast<uint16_t*>(p.dv) + static_cast<int64_t>(t.k0 + j) * p.dv_ts;
       const uint32_t acc = tmem + (half ? kColDK : kColDV) + lane_addr;
 #pragma unroll 1
-      for (int c = 0; c < kHeadDim / 32; ++c) {
+      for (int c = 0; c < p.d / 32; ++c) {  // d is a multiple of 32
         float a[32];
         tmem_ld32(acc + c * 32, a);
         tmem_wait_ld();

@@ -343,9 +343,10 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         const uint4* src = reinterpret_cast<const uint4*>(
             static_cast<const uint16_t*>(p.q) + static_cast<int64_t>(tq.q0 + il) * p.q_ts +
             static_cast<int64_t>(hq) * p.q_hs + half * 80);
+        const int nu = feature_units(p.d, half);  // features past d read as 0
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
-          const uint4 v = __ldg(src + u);
+          const uint4 v = u < nu ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
           w[4 * u] = v.x;
           w[4 * u + 1] = v.y;
           w[4 * u + 2] = v.z;
@@ -487,12 +488,13 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_empty);
       if (row_valid) {
+        const int nu = feature_units(p.d, half);
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
           float w[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) w[i] = n > 0 ? o[8 * u + i] * p.sigma : 0.f;
-          *reinterpret_cast<uint4*>(qrow + u * 8) = pack8<BF16>(w);
+          if (u < nu) *reinterpret_cast<uint4*>(qrow + u * 8) = pack8<BF16>(w);
         }
       }
     }

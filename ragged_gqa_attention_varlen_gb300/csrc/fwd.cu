@@ -573,12 +573,13 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         uint16_t* orow = static_cast<uint16_t*>(p.out) +
                          static_cast<int64_t>(t.q0 + i_loc) * p.out_ts +
                          static_cast<int64_t>(h) * p.out_hs + half * 80;
+        const int nu = feature_units(p.d, half);
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
           float w[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) w[i] = n > 0 ? o[8 * u + i] * inv : 0.f;
-          *reinterpret_cast<uint4*>(orow + u * 8) = pack8<BF16>(w);
+          if (u < nu) *reinterpret_cast<uint4*>(orow + u * 8) = pack8<BF16>(w);
         }
       }
     }

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstring>
 
 #include "../../include/attn_varlen.h"
@@ -54,12 +55,16 @@ WsLayout ws_layout(int B, int Hq, int64_t total_q) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
 
-// [T, H, 160] view -> 3-D map (feature, head, token) with a box of
+// Every map's feature extent is the head dimension d (160, 128 or 64); the
+// kernels' tiles always span 160 features, and a box part past d is filled
+// with zeros by the TMA unit (it contributes nothing to any product).
+//
+// [T, H, d] view -> 3-D map (feature, head, token) with a box of
 // 64 features x G heads x (rows/G) tokens and the 128-byte swizzle, or (tail)
 // 32 features (128..159) with the 64-byte swizzle.
-bool encode_q(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
+bool encode_q(CUtensorMap* m, int dtype, int d, const void* base, int64_t T, int H, int64_t ts,
               int64_t hs, int G, int rows, bool tail = false) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(tail ? kHeadDim - 2 * kChunk : kChunk),
@@ -73,12 +78,12 @@ bool encode_q(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [T, 1, 160] view -> 2-D map (feature, token), box 64 x 128 keys with the
-// 128-byte swizzle, or (tail) 32 x 128 with the 64-byte swizzle for features
-// 128..159.
-bool encode_kv(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t ts,
+// [T, d] view of one K/V head -> 2-D map (feature, token), box 64 x 128 keys
+// with the 128-byte swizzle, or (tail) 32 x 128 with the 64-byte swizzle for
+// features 128..159.
+bool encode_kv(CUtensorMap* m, int dtype, int d, const void* base, int64_t T, int64_t ts,
                bool tail = false) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ts) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(tail ? kHeadDim - 2 * kChunk : kChunk),
                        static_cast<cuuint32_t>(kKeys)};
@@ -95,11 +100,14 @@ bool encode_kv(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t t
 // outer axis (stride 128 bytes): one box then loads both 128-byte-swizzled
 // chunks of a tile, in the layout of two separate chunk boxes (chunk c at
 // c * 16 KB).  A TMA operation costs about the same time whatever its size,
-// so fewer, larger boxes raise the load rate.
-bool encode_q_pair(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
-                   int64_t hs, int G, int rows) {
+// so fewer, larger boxes raise the load rate.  With d = 64 the chunk axis has
+// extent 1, so the second chunk of the box reads as zeros.
+cuuint64_t chunk_count(int d) { return d >= 2 * kChunk ? 2 : 1; }
+
+bool encode_q_pair(CUtensorMap* m, int dtype, int d, const void* base, int64_t T, int H,
+                   int64_t ts, int64_t hs, int G, int rows) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(kChunk), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(T), 2};
+                        static_cast<cuuint64_t>(T), chunk_count(d)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2,
                            static_cast<cuuint64_t>(kChunk) * 2};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(G),
@@ -112,8 +120,10 @@ bool encode_q_pair(CUtensorMap* m, int dtype, const void* base, int64_t T, int H
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_kv_pair(CUtensorMap* m, int dtype, const void* base, int64_t T, int64_t ts) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunk), static_cast<cuuint64_t>(T), 2};
+bool encode_kv_pair(CUtensorMap* m, int dtype, int d, const void* base, int64_t T,
+                    int64_t ts) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kChunk), static_cast<cuuint64_t>(T),
+                        chunk_count(d)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ts) * 2, static_cast<cuuint64_t>(kChunk) * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kKeys), 2};
   cuuint32_t estr[3] = {1, 1, 1};
@@ -124,14 +134,14 @@ bool encode_kv_pair(CUtensorMap* m, int dtype, const void* base, int64_t T, int6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A whole query tile (160 features x G heads x rows/G tokens) as one
+// A whole query tile (d features x G heads x rows/G tokens) as one
 // unswizzled box, for L2 prefetches only.
-bool encode_q_full(CUtensorMap* m, int dtype, const void* base, int64_t T, int H, int64_t ts,
-                   int64_t hs, int G, int rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+bool encode_q_full(CUtensorMap* m, int dtype, int d, const void* base, int64_t T, int H,
+                   int64_t ts, int64_t hs, int G, int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(G),
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(G),
                        static_cast<cuuint32_t>(rows / G)};
   cuuint32_t estr[3] = {1, 1, 1};
   return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -235,7 +245,7 @@ attn_status run_call(
   // ---- host-side validation (nothing is enqueued on failure)
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
-  if (head_dim != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+  if (head_dim != 160 && head_dim != 128 && head_dim != 64) return ATTN_ERR_UNSUPPORTED;
   if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
   if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
   if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
@@ -289,6 +299,7 @@ attn_status run_call(
   p.B = B;
   p.Hq = Hq;
   p.G = head_group(Hq / (Hkv > 0 ? Hkv : 1));
+  p.d = head_dim;
   p.total_q = total_q;
   p.total_k = total_k;
   p.out = out;
@@ -316,7 +327,8 @@ attn_status run_call(
   p.wl = window_left;
   p.wr = window_right;
   p.softcap = softcap;
-  p.sigma = static_cast<float>(static_cast<double>(scale_multiplier) / 12.649110640673518);
+  p.sigma = static_cast<float>(static_cast<double>(scale_multiplier) /
+                               std::sqrt(static_cast<double>(head_dim)));
   p.lse = lse;
   p.lse_rs = Hq;
   p.Dbuf = reinterpret_cast<float*>(wsb + ws.dbuf);
@@ -330,15 +342,18 @@ attn_status run_call(
     if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (has_k && bwd) {  // no queries: dk = dv = 0
-      e = launch_zero_fill(dk, total_k, Hkv, dk_ts, Hkv > 1 ? dk_hs : 8, stream);
-      if (e == cudaSuccess) e = launch_zero_fill(dv, total_k, Hkv, dv_ts, Hkv > 1 ? dv_hs : 8, stream);
+      e = launch_zero_fill(dk, total_k, Hkv, dk_ts, Hkv > 1 ? dk_hs : 8, head_dim, stream);
+      if (e == cudaSuccess)
+        e = launch_zero_fill(dv, total_k, Hkv, dv_ts, Hkv > 1 ? dv_hs : 8, head_dim, stream);
     }
     if (has_q) {  // no keys: every row is empty
       if (fwd) {
-        if (e == cudaSuccess) e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, stream);
+        if (e == cudaSuccess)
+          e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, head_dim, stream);
         if (e == cudaSuccess) e = launch_fill_f32(lse, total_q * Hq, -INFINITY, stream);
       }
-      if (bwd && e == cudaSuccess) e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, stream);
+      if (bwd && e == cudaSuccess)
+        e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, head_dim, stream);
     }
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
@@ -372,20 +387,20 @@ attn_status run_call(
   auto encode_group = [&](const Params& pg, int g, Maps& m) -> bool {
     const void* kg = static_cast<const uint16_t*>(k) + static_cast<int64_t>(g) * k_hs;
     const void* vg = static_cast<const uint16_t*>(v) + static_cast<int64_t>(g) * v_hs;
-    if (!encode_q_full(&m.tqf, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
-        !encode_q_pair(&m.tq2, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
-        !encode_kv_pair(&m.tk2, dtype, kg, total_k, k_ts) ||
-        !encode_kv_pair(&m.tv2, dtype, vg, total_k, v_ts) ||
-        !encode_q(&m.tq, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
-        !encode_q(&m.tqt, dtype, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ, true) ||
-        !encode_kv(&m.tk, dtype, kg, total_k, k_ts) || !encode_kv(&m.tv, dtype, vg, total_k, v_ts) ||
-        !encode_kv(&m.tkt, dtype, kg, total_k, k_ts, true) ||
-        !encode_kv(&m.tvt, dtype, vg, total_k, v_ts, true))
+    if (!encode_q_full(&m.tqf, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_q_pair(&m.tq2, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_kv_pair(&m.tk2, dtype, head_dim, kg, total_k, k_ts) ||
+        !encode_kv_pair(&m.tv2, dtype, head_dim, vg, total_k, v_ts) ||
+        !encode_q(&m.tq, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+        !encode_q(&m.tqt, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ, true) ||
+        !encode_kv(&m.tk, dtype, head_dim, kg, total_k, k_ts) || !encode_kv(&m.tv, dtype, head_dim, vg, total_k, v_ts) ||
+        !encode_kv(&m.tkt, dtype, head_dim, kg, total_k, k_ts, true) ||
+        !encode_kv(&m.tvt, dtype, head_dim, vg, total_k, v_ts, true))
       return false;
-    if (bwd && (!encode_q_full(&m.tdof, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
-                !encode_q_pair(&m.tdo2, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
-                !encode_q(&m.tdo, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
-                !encode_q(&m.tdot, dtype, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ, true)))
+    if (bwd && (!encode_q_full(&m.tdof, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q_pair(&m.tdo2, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q(&m.tdo, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+                !encode_q(&m.tdot, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ, true)))
       return false;
     return true;
   };

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Params p) {
     const int64_t t = row / p.Hq;
     const int h = static_cast<int>(row - t * p.Hq);
     float acc = 0.f;
-    if (lane < kHeadDim / 8) {
+    if (lane < p.d / 8) {
       uint4 a = *reinterpret_cast<const uint4*>(o + t * p.out_ts + h * p.out_hs + lane * 8);
       uint4 b = *reinterpret_cast<const uint4*>(d + t * p.do_ts + h * p.do_hs + lane * 8);
       acc = dot8<T>(a, b);
@@ -167,23 +167,25 @@ cudaError_t launch_preprocess(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Zero a strided [T, H, 160] 16-bit tensor, 16 bytes per thread.
-__global__ void zero_fill_kernel(uint16_t* base, int64_t T, int H, int64_t ts, int64_t hs) {
-  const int64_t units = T * H * (kHeadDim / 8);
+// Zero a strided [T, H, d] 16-bit tensor, 16 bytes per thread.
+__global__ void zero_fill_kernel(uint16_t* base, int64_t T, int H, int64_t ts, int64_t hs,
+                                 int d) {
+  const int per_row = d / 8;
+  const int64_t units = T * H * per_row;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int64_t row = u / (kHeadDim / 8);
-    int c = static_cast<int>(u - row * (kHeadDim / 8));
+    int64_t row = u / per_row;
+    int c = static_cast<int>(u - row * per_row);
     int64_t t = row / H;
     int h = static_cast<int>(row - t * H);
     *reinterpret_cast<uint4*>(base + t * ts + h * hs + c * 8) = make_uint4(0, 0, 0, 0);
   }
 }
 
-cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs,
+cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs, int d,
                              cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  zero_fill_kernel<<<152 * 8, 256, 0, s>>>(static_cast<uint16_t*>(base), T, H, ts, hs);
+  zero_fill_kernel<<<152 * 8, 256, 0, s>>>(static_cast<uint16_t*>(base), T, H, ts, hs, d);
   return cudaGetLastError();
 }
 

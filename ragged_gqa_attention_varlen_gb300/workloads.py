@@ -98,15 +98,16 @@ def _copy_view(x: torch.Tensor, device) -> torch.Tensor:
     return y
 
 
-def strided_view(T: int, H: int, step: int, pad: int, dtype, device, poison: bool = True):
-    """An uninitialised [T, H, 160] view into a [step*T, H, pad] buffer.
+def strided_view(T: int, H: int, step: int, pad: int, dtype, device, poison: bool = True,
+                 d: int = HEAD_DIM):
+    """An uninitialised [T, H, d] view into a [step*T, H, pad] buffer.
 
-    The gaps (token rows skipped by the step, features 160..pad-1) hold NaN
+    The gaps (token rows skipped by the step, features d..pad-1) hold NaN
     when ``poison`` is set, so a kernel that reads them shows it."""
     base = torch.empty((max(step * T, 1), H, pad), dtype=dtype, device=device)
-    if poison and (step > 1 or pad > HEAD_DIM):
+    if poison and (step > 1 or pad > d):
         base.fill_(float("nan"))
-    return base[: step * T: step, :, :HEAD_DIM] if T > 0 else base[:0, :, :HEAD_DIM]
+    return base[: step * T: step, :, :d] if T > 0 else base[:0, :, :d]
 
 
 def _fill_normal(view: torch.Tensor, std: float, gen: torch.Generator, chunk_tokens: int = 4096):
@@ -146,17 +147,18 @@ def _alibi_geometric(Hq):
 
 
 def build(name, lq, lk, Hq, dtype, step, pad, slopes, qk_std=1.0, v_std=1.0, do_std=1.0,
-          seed=0, device="cpu", poison=True, Hkv=1, **mask) -> Problem:
+          seed=0, device="cpu", poison=True, Hkv=1, d=HEAD_DIM, **mask) -> Problem:
     """Draw the values of a problem whose lengths and slopes are already fixed
-    (k and v get Hkv heads)."""
+    (k and v get Hkv heads; every row has d features)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed * 1000003 + 17)
     cu_q, cu_k = _cu(lq), _cu(lk)
     Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
-    q = strided_view(Tq, Hq, step, pad, dtype, device, poison)
-    k = strided_view(Tk, Hkv, step, pad, dtype, device, poison)
-    v = strided_view(Tk, Hkv, step, pad, dtype, device, poison)
-    dout = strided_view(Tq, Hq, step, pad, dtype, device, poison)
+    pad = max(pad, d)
+    q = strided_view(Tq, Hq, step, pad, dtype, device, poison, d)
+    k = strided_view(Tk, Hkv, step, pad, dtype, device, poison, d)
+    v = strided_view(Tk, Hkv, step, pad, dtype, device, poison, d)
+    dout = strided_view(Tq, Hq, step, pad, dtype, device, poison, d)
     _fill_normal(q, qk_std, gen)
     _fill_normal(k, qk_std, gen)
     _fill_normal(v, v_std, gen)
@@ -231,7 +233,7 @@ def mixed(seed=3, Hq=64, device="cpu", length_scale=1.0):
                  seed=seed, device=device)
 
 
-def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True, Hkv=1):
+def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True, Hkv=1, d=HEAD_DIM):
     """24 sequences with Lq = Lk ~ U[6144, 12288], Hq=96, bf16, dense features,
     token step 2, N(0,1) values, slopes 2^(-8h/96); Hkv K/V heads (1 unless
     asked)."""
@@ -239,8 +241,8 @@ def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True, Hkv=1):
     B, Hq = 24, 96
     L = _scale(_uniform_int(g, 6144, 12288, B), length_scale)
     slopes = _alibi_geometric(Hq)[None, :].expand(B, Hq).contiguous()
-    return build("long_balanced", L, list(L), Hq, torch.bfloat16, 2, HEAD_DIM, slopes,
-                 seed=seed, device=device, poison=poison, Hkv=Hkv)
+    return build("long_balanced", L, list(L), Hq, torch.bfloat16, 2, d, slopes,
+                 seed=seed, device=device, poison=poison, Hkv=Hkv, d=d)
 
 
 def _scale(lengths, s):
@@ -260,9 +262,9 @@ WORKLOADS = {
 
 
 def custom(lq, lk, Hq, dtype=torch.float16, step=1, pad=HEAD_DIM, seed=0, device="cpu",
-           slope_max=0.25, qk_std=1.0, poison=True, Hkv=1, **mask) -> Problem:
+           slope_max=0.25, qk_std=1.0, poison=True, Hkv=1, d=HEAD_DIM, **mask) -> Problem:
     """A small problem with given lengths, for edge cases."""
     g = torch.Generator().manual_seed(seed)
     slopes = torch.rand((len(lq), Hq), generator=g, dtype=torch.float32) * slope_max
     return build("custom", list(lq), list(lk), Hq, dtype, step, pad, slopes, qk_std=qk_std,
-                 seed=seed, device=device, poison=poison, Hkv=Hkv, **mask)
+                 seed=seed, device=device, poison=poison, Hkv=Hkv, d=d, **mask)

@@ -65,7 +65,8 @@ def _call(lib, **over):
 
 def test_host_validation_codes(lib):
     assert _call(lib, dtype=7) == -1
-    assert _call(lib, hd=128) == -2
+    assert _call(lib, hd=96) == -2              # head dims: 64, 128 and 160
+    assert _call(lib, hd=128) == -4 and _call(lib, hd=64) == -4
     assert _call(lib, Hkv=3) == -1             # 16 query heads do not split over 3
     assert _call(lib, Hkv=0) == -1
     assert _call(lib, Hkv=2, khs=164) == -3     # head strides count once Hkv > 1

@@ -75,13 +75,14 @@ def _sdpa_reference(p, scale):
     return (torch.cat(outs), torch.cat(lses), torch.cat(dqs), torch.cat(dks), torch.cat(dvs))
 
 
-@pytest.mark.parametrize("softcap,Hkv", [(0.0, 1), (1e7, 1), (0.0, 2), (0.0, 4)])
-def test_reduces_to_sdpa_without_cap_and_alibi(oracle_mod, softcap, Hkv):
-    p = f64_problem([3, 7, 1, 12], [5, 2, 9, 12], Hq=4, seed=3, Hkv=Hkv)
+@pytest.mark.parametrize("softcap,Hkv,d", [(0.0, 1, 160), (1e7, 1, 160), (0.0, 2, 160),
+                                           (0.0, 4, 160), (0.0, 1, 128), (0.0, 2, 64)])
+def test_reduces_to_sdpa_without_cap_and_alibi(oracle_mod, softcap, Hkv, d):
+    p = f64_problem([3, 7, 1, 12], [5, 2, 9, 12], Hq=4, seed=3, Hkv=Hkv, d=d)
     p.alibi_slopes.zero_()
     p.softcap = softcap
     r = oracle_mod.fvjp(p)
-    out, lse, dq, dk, dv = _sdpa_reference(p, sigma())
+    out, lse, dq, dk, dv = _sdpa_reference(p, 0.75 / math.sqrt(d))
     tol = dict(rtol=1e-9, atol=1e-11)
     torch.testing.assert_close(r["out"], out, **tol)
     torch.testing.assert_close(r["lse"], lse, **tol)

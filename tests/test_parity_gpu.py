@@ -239,6 +239,45 @@ def test_gqa_rejects_uneven_head_split():
         BND.attention_varlen_fvjp(p.q, k, k, p.cu_q, p.cu_k, p.alibi_slopes, p.dout)
 
 
+# ------------------------------------------------ head dimensions 128 and 64
+# The tiles span 160 features; the TMA maps fill features past d with zeros
+# and every other load and store stops at d.
+
+HEAD_DIMS = [
+    dict(lq=[300, 37, 1, 129], lk=[260, 400, 9, 0], Hq=16, d=128),
+    dict(lq=[200, 64], lk=[333, 90], Hq=48, d=64, dtype=torch.bfloat16, step=2),
+    dict(lq=[150, 20], lk=[140, 300], Hq=12, Hkv=4, d=128, causal=True, window_left=40,
+         dtype=torch.bfloat16),
+    dict(lq=[90, 500], lk=[130, 450], Hq=8, d=64, pad=192),  # NaN past feature 64
+    dict(lq=[1000], lk=[1000], Hq=16, d=128, dtype=torch.bfloat16, step=3, pad=136),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_DIMS, ids=[f"d{c['d']}_{i}" for i, c in enumerate(HEAD_DIMS)])
+def test_head_dim_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    parity(W.custom(lq, lk, Hq, **case), oracle_mod)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_dim_outputs_written_exactly(d):
+    """Padded NaN-filled output views with d features: exactly the d
+    features of every row are written (the padding past d stays NaN), and
+    the values equal those of dense outputs bit for bit."""
+    p = W.custom([70, 5, 300], [40, 260, 0], 16, d=d, dtype=torch.bfloat16, step=2,
+                 pad=192).to("cuda")
+    dense = run(p)
+    outs = dict(out=nan_like_strided(p.q), dq=nan_like_strided(p.dout), dk=nan_like_strided(p.k),
+                dv=nan_like_strided(p.v))
+    strided = run(p, **outs)
+    for n in ("out", "dq", "dk", "dv"):
+        assert torch.equal(strided[n].contiguous(), dense[n]), n
+        raw = torch.empty(0, dtype=strided[n].dtype, device="cuda").set_(
+            strided[n].untyped_storage())
+        assert int(torch.isnan(raw).sum()) == raw.numel() - strided[n].numel(), n
+
+
 # ------------------------------------------- split forward / backward calls
 
 def _split_cases():
