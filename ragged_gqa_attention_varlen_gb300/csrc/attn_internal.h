@@ -66,9 +66,8 @@ struct Params {
 
 // 16-byte units (8 features) of a row's features [80*half, 80*half + 80)
 // that lie below the head dimension.
-__host__ __device__ inline int feature_units(int d, int half) {
-  const int u = (d - 80 * half) / 8;
-  return u < 0 ? 0 : (u > 10 ? 10 : u);
+__host__ __device__ constexpr int feature_units(int d, int half) {
+  return (d - 80 * half) / 8 < 0 ? 0 : ((d - 80 * half) / 8 > 10 ? 10 : (d - 80 * half) / 8);
 }
 
 // The call has a causal or window mask (selects the masked kernel instances).

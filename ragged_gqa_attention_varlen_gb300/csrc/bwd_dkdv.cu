@@ -91,7 +91,9 @@ struct Pair {
   }
 };
 
-template <bool BF16, bool MASK>
+// HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
+// follow it; the shared-memory and TMEM layouts are those of 160 features.
+template <bool BF16, bool MASK, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
@@ -280,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // would hold back the next step's S^T and dP^T (and the reverse).
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t kIdG = idesc_f16(128, kHeadDim, BF16, false, true);
+      // N = d: features past the head dimension are neither multiplied nor stored
+      constexpr uint32_t kIdG = idesc_f16(128, HD, BF16, false, true);
+      constexpr int nk = HD / 16;  // K steps of S^T and dP^T over the features
       const uint32_t kb = smem_addr(sK), vb = smem_addr(sV), db = smem_addr(sDO);
       // A = K or V: features 0..127 in 128-byte-swizzled chunks, 128..159 in a
       // 64-byte-swizzled chunk.  B = Q or dO, three 128-byte-swizzled chunks,
@@ -301,10 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-          umma_ss_off(d, a, off, b, off, kIdS, k > 0);
+          if (k < nk) umma_ss_off(d, a, off, b, off, kIdS, k > 0);
         }
-        umma_ss_off(d, at, 0, b, 2 * kTile, kIdS, 1);
-        umma_ss_off(d, at, 32, b, 2 * kTile + 32, kIdS, 1);
+        if (nk > 8) {
+          umma_ss_off(d, at, 0, b, 2 * kTile, kIdS, 1);
+          umma_ss_off(d, at, 32, b, 2 * kTile + 32, kIdS, 1);
+        }
       };
       // D (+)= X^T B over the step's 128 query rows; rows 16k..16k+15 are the
       // pair columns 448 + 32*(k/4) + 8*(k%4)
@@ -708,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : static_cast<uint16_t*>(p.dv) + static_cast<int64_t>(t.k0 + j) * p.dv_ts;
       const uint32_t acc = tmem + (half ? kColDK : kColDV) + lane_addr;
 #pragma unroll 1
-      for (int c = 0; c < p.d / 32; ++c) {  // d is a multiple of 32
+      for (int c = 0; c < HD / 32; ++c) {
         float a[32];
         tmem_ld32(acc + c * 32, a);
         tmem_wait_ld();
@@ -734,13 +740,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool B, bool M>
+auto dkdv_for_d(int d) {
+  return d == 128 ? dkdv_kernel<B, M, 128>
+                  : (d == 64 ? dkdv_kernel<B, M, 64> : dkdv_kernel<B, M, 160>);
+}
+
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                         const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
                         const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? dkdv_kernel<true, true> : dkdv_kernel<true, false>)
-                        : (m ? dkdv_kernel<false, true> : dkdv_kernel<false, false>);
+  auto k = p.dtype == 1 ? (m ? dkdv_for_d<true, true>(p.d) : dkdv_for_d<true, false>(p.d))
+                        : (m ? dkdv_for_d<false, true>(p.d) : dkdv_for_d<false, false>(p.d));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
   k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();

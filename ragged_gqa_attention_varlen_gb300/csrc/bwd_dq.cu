@@ -84,7 +84,9 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <bool BF16, bool MASK>
+// HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
+// follow it; the shared-memory and TMEM layouts are those of 160 features.
+template <bool BF16, bool MASK, int HD>
 __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tdo2,
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     // ------------------------------------------------------------ S, dP issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
+      constexpr int nk = HD / 16;  // K steps of S and dP below the head dimension
       const uint32_t db = smem_addr(sDO), vb = smem_addr(sV);
       // K-major operand stored as two 128-byte-swizzled chunks + a 64-byte tail
       auto tailed = [&](uint32_t base, int k) -> uint64_t {
@@ -253,8 +256,9 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           // features 16k..16k+15 of Q: pair columns 8k..8k+7 of its region
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ts(tmem + kColS, tmem + kColQt + k * 8,
-                    sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
+            if (k < nk)
+              umma_ts(tmem + kColS, tmem + kColQt + k * 8,
+                      sdesc_sw128(kb + (k >> 2) * kTile + (k & 3) * 32, 16, 1024), kIdS, k > 0);
           umma_commit(&bars->s_full);
           // dP = dO V^T once dQ of the previous key tile has read dS (written
           // over the previous dP, after it was read)
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
+            if (k < nk) umma_ss(tmem + kColP, tailed(db, k), tailed(vb, k), kIdS, k > 0);
           umma_commit(&bars->dp_full);
           umma_commit(&bars->v_empty);
           if (j + 1 == n) umma_commit(&bars->q_empty);  // last dP of this tile issued
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     // busy, so the wait for dS_j must not sit behind the S and dP products
     // of the next key tile.
     if (lane == 0) {
-      constexpr uint32_t kIdQ = idesc_f16(128, kHeadDim, BF16, false, true);
+      constexpr uint32_t kIdQ = idesc_f16(128, HD, BF16, false, true);  // N = d
       uint32_t g = 0;
       Ring3 kr;
       int tcount = 0;
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         const uint4* src = reinterpret_cast<const uint4*>(
             static_cast<const uint16_t*>(p.q) + static_cast<int64_t>(tq.q0 + il) * p.q_ts +
             static_cast<int64_t>(hq) * p.q_hs + half * 80);
-        const int nu = feature_units(p.d, half);  // features past d read as 0
+        const int nu = feature_units(HD, half);  // features past d read as 0
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
           const uint4 v = u < nu ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_empty);
       if (row_valid) {
-        const int nu = feature_units(p.d, half);
+        const int nu = feature_units(HD, half);
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
           float w[8];
@@ -507,13 +511,18 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool B, bool M>
+auto dq_for_d(int d) {
+  return d == 128 ? dq_kernel<B, M, 128> : (d == 64 ? dq_kernel<B, M, 64> : dq_kernel<B, M, 160>);
+}
+
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? dq_kernel<true, true> : dq_kernel<true, false>)
-                        : (m ? dq_kernel<false, true> : dq_kernel<false, false>);
+  auto k = p.dtype == 1 ? (m ? dq_for_d<true, true>(p.d) : dq_for_d<true, false>(p.d))
+                        : (m ? dq_for_d<false, true>(p.d) : dq_for_d<false, false>(p.d));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
   // With `overlap` the launch is a programmatic dependent of the kernel before
   // it (dk/dv, which signals at its start): dq reads nothing dk/dv writes, so

@@ -128,7 +128,9 @@ __device__ __forceinline__ int next_key_tile(const QTile& t, int kt) {
   return kt + 1 == t.kt0 + t.nkt ? t.kt0 : kt + 1;
 }
 
-template <bool BF16, bool MASK>
+// HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
+// follow it; the shared-memory and TMEM layouts are those of 160 features.
+template <bool BF16, bool MASK, int HD>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk2,
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
+      constexpr int nk = HD / 16;
       uint32_t g = 0;  // global key-step counter of this CTA
       int tcount = 0;
       bool ok = true;
@@ -313,8 +316,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           const uint32_t kb = smem_addr(sK + (gs & 1) * kTailed);
           const uint32_t qb = smem_addr(sQ);
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            umma_ss(tmem + (gs & 1) * 128, tailed(qb, k), tailed(kb, k), kIdS, k > 0);
+          for (int k = 0; k < kHeadDim / 16; ++k)  // K steps below the head dimension
+            if (k < nk) umma_ss(tmem + (gs & 1) * 128, tailed(qb, k), tailed(kb, k), kIdS, k > 0);
           umma_commit(&bars->s_full[gs & 1]);
           umma_commit(&bars->k_empty[gs & 1]);
           if (jj == n - 1) umma_commit(&bars->q_empty);
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     // A second issuing thread, so that the wait for P_j and the bookkeeping
     // between groups overlap the S products queued by warp 1.
     if (lane == 0) {
-      constexpr uint32_t kIdO = idesc_f16(128, kHeadDim, BF16, false, true);
+      constexpr uint32_t kIdO = idesc_f16(128, HD, BF16, false, true);  // N = d
       uint32_t g = 0;
       int tcount = 0;
       bool ok = true;
@@ -573,7 +576,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         uint16_t* orow = static_cast<uint16_t*>(p.out) +
                          static_cast<int64_t>(t.q0 + i_loc) * p.out_ts +
                          static_cast<int64_t>(h) * p.out_hs + half * 80;
-        const int nu = feature_units(p.d, half);
+        const int nu = feature_units(HD, half);
 #pragma unroll
         for (int u = 0; u < 10; ++u) {
           float w[8];
@@ -592,12 +595,17 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool B, bool M>
+auto fwd_for_d(int d) {
+  return d == 128 ? fwd_kernel<B, M, 128> : (d == 64 ? fwd_kernel<B, M, 64> : fwd_kernel<B, M, 160>);
+}
+
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
                        const CUtensorMap& tv, int grid, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? fwd_kernel<true, true> : fwd_kernel<true, false>)
-                        : (m ? fwd_kernel<false, true> : fwd_kernel<false, false>);
+  auto k = p.dtype == 1 ? (m ? fwd_for_d<true, true>(p.d) : fwd_for_d<true, false>(p.d))
+                        : (m ? fwd_for_d<false, true>(p.d) : fwd_for_d<false, false>(p.d));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
   k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   return cudaGetLastError();
