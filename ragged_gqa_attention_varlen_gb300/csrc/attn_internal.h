@@ -39,9 +39,10 @@ struct Params {
   void* dq;
   int64_t dq_ts, dq_hs;
   void* dk;
-  int64_t dk_ts;
+  int64_t dk_ts, dk_hs;
   void* dv;
-  int64_t dv_ts;
+  int64_t dv_ts, dv_hs;
+  int Hkv;  // K/V heads of the call (the preprocess zeroes dk/dv rows of all of them)
   // inputs read outside TMA
   const void* outp;  // = out, read back by the preprocess kernel
   const void* dout;
@@ -77,8 +78,10 @@ inline bool masked_call(const Params& p) { return p.causal || p.wl >= 0 || p.wr 
 //   [0, B)          fwd/dq sequence order (longest key range first)
 //   [B, 2B+1)       fwd/dq item prefix over that order
 //   [2B+1, 3B+1)    dk/dv sequence order (longest query range first)
-//   [3B+1, 4B+2)    dk/dv item prefix over that order
-inline int sched_words(int B) { return 4 * B + 2; }
+//   [3B+1, 4B+2)    dk/dv item prefix over that order (key tiles that some
+//                   query may attend to: a contiguous run per sequence)
+//   [4B+2, 5B+2)    first such key tile of each order position
+inline int sched_words(int B) { return 5 * B + 2; }
 
 cudaError_t launch_sched(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,

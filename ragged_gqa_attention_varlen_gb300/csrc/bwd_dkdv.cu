@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  // (the rows of keys outside every scheduled tile were zeroed by the
+  // preprocess kernel)
   if (*s_status != 0 || static_cast<int>(blockIdx.x) >= ntiles) return;
 
   if (tid == 0) {

@@ -310,8 +310,11 @@ attn_status run_call(
   p.dq_hs = dq_hs;
   p.dk = dk;
   p.dk_ts = dk_ts;
+  p.dk_hs = Hkv > 1 ? dk_hs : 0;
   p.dv = dv;
   p.dv_ts = dv_ts;
+  p.dv_hs = Hkv > 1 ? dv_hs : 0;
+  p.Hkv = Hkv;
   p.outp = out;
   p.dout = dout;
   p.q = q;

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
   int32_t* pre_f = p.sched + B;
   int32_t* ord_b = p.sched + 2 * B + 1;
   int32_t* pre_b = p.sched + 3 * B + 1;
+  int32_t* kt0_b = p.sched + 4 * B + 2;
   if (bad) {
     // No tiles: every later kernel finds nothing to do.
     for (int b = tid; b <= B; b += blockDim.x) {
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
       if (b < B) {
         ord_f[b] = 0;
         ord_b[b] = 0;
+        kt0_b[b] = 0;
       }
     }
     if (tid == 0) *p.status = ATTN_DEV_BAD_CU;
@@ -83,9 +85,11 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
       pre_b[r] = acc_b;
       int bf = ord_f[r], bb = ord_b[r];
       int lq = p.cu_q[bf + 1] - p.cu_q[bf];
-      int lk = p.cu_k[bb + 1] - p.cu_k[bb];
       acc_f += ((lq + rows_tok - 1) / rows_tok) * ngroups;
-      acc_b += (lk + kKeys - 1) / kKeys;
+      int kt0, nkt;
+      dkdv_key_span(p, p.cu_q[bb + 1] - p.cu_q[bb], p.cu_k[bb + 1] - p.cu_k[bb], kt0, nkt);
+      kt0_b[r] = kt0;
+      acc_b += nkt;
     }
     pre_f[B] = acc_f;
     pre_b[B] = acc_b;
@@ -153,11 +157,42 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Params p) {
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) p.Dbuf[row] = acc;
   }
+  // dk = dv = 0 (every K/V head) for the keys outside every scheduled dk/dv
+  // tile: keys of sequences without queries and keys the mask leaves
+  // unreached.  The dk/dv kernel writes every other key row.
+  const int64_t kstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t krow = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       krow < p.total_k; krow += kstride) {
+    int lo = 0, hi = p.B - 1;  // the last sequence with cu_k[b] <= krow
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cu_k[mid] <= krow)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int k0 = p.cu_k[lo];
+    const int Lk = p.cu_k[lo + 1] - k0;
+    const int j = static_cast<int>(krow - k0);
+    int kt0, nkt;
+    dkdv_key_span(p, p.cu_q[lo + 1] - p.cu_q[lo], Lk, kt0, nkt);
+    if (j >= Lk || (nkt > 0 && j >= kt0 * kKeys && j < (kt0 + nkt) * kKeys)) continue;
+    for (int g = 0; g < p.Hkv; ++g) {
+      uint4* dk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + krow * p.dk_ts +
+                                           g * p.dk_hs);
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + krow * p.dv_ts +
+                                           g * p.dv_hs);
+      for (int u = 0; u < p.d / 8; ++u) {
+        dk[u] = make_uint4(0u, 0u, 0u, 0u);
+        dv[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
 }
 
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s) {
   const int64_t rows = p.total_q * p.Hq;
-  if (rows == 0) return cudaSuccess;
+  if (rows == 0 && p.total_k == 0) return cudaSuccess;
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 152 * 64) blocks = 152 * 64;
   if (p.dtype == 1)

@@ -79,6 +79,29 @@ __device__ __forceinline__ void query_block_span(const Params& p, int Lq, int Lk
   ntb = static_cast<int>(hi / blk) - tb0 + 1;
 }
 
+// Key tiles [*kt0, *kt0 + *nkt) of a sequence hold every key that some query
+// may attend to (the admissible keys form one run: j >= Lk - Lq - wl and
+// j <= Lq - 1 + Lk - Lq + wr where the windows are set).  The dk/dv schedule
+// holds only these tiles, so no dk/dv tile is without queries; the rows of
+// the other keys are zeroed by the dk/dv kernel's prologue.
+__device__ __forceinline__ void dkdv_key_span(const Params& p, int Lq, int Lk, int& kt0,
+                                              int& nkt) {
+  int64_t lo = 0, hi = static_cast<int64_t>(Lk) - 1;
+  if (masking(p)) {
+    const int64_t off = static_cast<int64_t>(Lk) - Lq;
+    const int wr = right_window(p);
+    if (p.wl >= 0) lo = max(lo, off - p.wl);
+    if (wr >= 0) hi = min(hi, static_cast<int64_t>(Lq) - 1 + off + wr);
+  }
+  if (Lq == 0 || lo > hi) {
+    kt0 = 0;
+    nkt = 0;
+    return;
+  }
+  kt0 = static_cast<int>(lo / kKeys);
+  nkt = static_cast<int>(hi / kKeys) - kt0 + 1;
+}
+
 // Under a mask whose admissible keys grow with the query (a right bound and
 // no left bound: causal) the query tiles of a sequence are drawn last token
 // block first, and under the mirror case the key tiles last tile first, so
@@ -148,7 +171,8 @@ __device__ __forceinline__ void ktile_decode(const Params& p, int n, KTile& t) {
   t.Lq = __ldg(p.cu_q + b + 1) - t.q0;
   t.Lk = __ldg(p.cu_k + b + 1) - t.k0;
   int kt = n - __ldg(pre + r);
-  if (MASK && ktiles_reversed(p)) kt = (t.Lk + kKeys - 1) / kKeys - 1 - kt;
+  if (MASK && ktiles_reversed(p)) kt = __ldg(pre + r + 1) - __ldg(pre + r) - 1 - kt;
+  kt += __ldg(p.sched + 4 * p.B + 2 + r);  // the sequence's first scheduled key tile
   t.key = kt * kKeys;
   if (MASK) {
     query_block_span(p, t.Lq, t.Lk, t.key, min(t.key + kKeys, t.Lk) - 1, kRowsQ / p.G, t.tb0,

@@ -136,6 +136,8 @@ EDGE = [
     dict(lq=[40, 300], lk=[200, 140], Hq=16, window_left=5, window_right=60),
     dict(lq=[40, 300], lk=[200, 140], Hq=16, causal=True, window_left=70),
     dict(lq=[30, 12], lk=[200, 40], Hq=16, qk_std=100.0),           # saturated softcap
+    dict(lq=[0, 5], lk=[7, 0], Hq=16),            # no dk/dv tile at all, keys still zeroed
+    dict(lq=[0, 5, 0], lk=[7, 0, 300], Hq=16, Hkv=4, d=128),
 ]
 
 
@@ -162,6 +164,16 @@ MASKED = [
     dict(lq=[513, 40], lk=[129, 300], Hq=16, window_left=0, window_right=0),  # one diagonal
     dict(lq=[400, 150], lk=[350, 600], Hq=16, causal=True, softcap=0.0),      # running max
     dict(lq=[300], lk=[300], Hq=8, causal=True, softcap=30.0),                # wide softcap
+]
+
+
+# Key tiles that no query may attend to are left out of the dk/dv schedule
+# (their rows are zeroed up front): runs of such tiles, drawn back to back by
+# one CTA, once stalled the lookahead of the column-scalar warp.
+MASKED += [
+    dict(lq=[90, 40], lk=[2000, 1500], Hq=16, window_left=200),          # 13 + 11 empty tiles
+    dict(lq=[0, 300, 0, 64], lk=[900, 400, 700, 1300], Hq=16, causal=True),
+    dict(lq=[0, 0, 37], lk=[1000, 600, 40], Hq=16),                      # empty query sets
 ]
 
 
