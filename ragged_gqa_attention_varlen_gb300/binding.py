@@ -133,8 +133,9 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
                           stream=None):
     """Forward + full VJP in one library call.
 
-    q, dout: [T_q, Hq, 160]; k, v: [T_k, 1, 160] CUDA views (fp16 or bf16, any
-    token/head strides that are multiples of 8 elements).  cu_q, cu_k: int32
+    q, dout: [T_q, Hq, d]; k, v: [T_k, Hkv, d] CUDA views (fp16 or bf16,
+    d in 64/128/160 -- 160 is the pages' case, as is Hkv = 1 -- Hq a multiple
+    of Hkv, any token/head strides that are multiples of 8 elements).  cu_q, cu_k: int32
     [B+1] on the device.  alibi_slopes: fp32 [B, Hq] or None.  Outputs may be
     passed in (any strides of the same rules); otherwise dense ones are
     allocated.  Returns dict(out, dq, dk, dv, lse, workspace).  The call is

@@ -55,7 +55,7 @@ struct Params {
   int64_t slopes_bs;
   int causal, wl, wr;
   float softcap;  // <= 0: no cap
-  float sigma;    // scale_multiplier / sqrt(160)
+  float sigma;    // scale_multiplier / sqrt(d)
   float* lse;     // [total_q, lse_rs]
   float* Dbuf;    // [total_q, lse_rs]
   int64_t lse_rs; // row stride of lse and D: every query head of the call

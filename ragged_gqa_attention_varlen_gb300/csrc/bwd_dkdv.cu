@@ -1,9 +1,11 @@
 // bwd_dkdv.cu -- backward pass, dk and dv.
 //
 // dv_j = sum_h sum_i P_ij dO_i and dk_j = sigma * sum_h sum_i dS_ij q_i, the
-// sums running over every query head that shares the single K/V head
-// ("Noncausal Global Extreme-GQA Ragged Attention Full VJP", "Hard
-// Constraints") and every query of the sequence.  P is recomputed from the
+// sums running over every query head that shares the K/V head (all of them
+// in the pages' case of one K/V head: "Noncausal Global Extreme-GQA Ragged
+// Attention Full VJP", "Hard Constraints"; the query heads of one group when
+// the host runs K/V head groups one after the other) and every query of the
+// sequence.  P is recomputed from the
 // stored lse ("ragged flash attention gradient recompute", "Root causes
 // addressed").
 //

@@ -8,11 +8,12 @@
 // repeated calls are bitwise identical.
 //
 // Tile: the forward's 128 query rows.  Per key tile j:
-//   S_j  = Q K_j^T    M=128 N=128 K=160, Q from TMEM, K from shared memory
-//   dP_j = dO V_j^T   M=128 N=128 K=160, both from shared memory
+//   S_j  = Q K_j^T    M=128 N=128 K=d, Q from TMEM, K from shared memory
+//   dP_j = dO V_j^T   M=128 N=128 K=d, both from shared memory
 //   dS_j              elementwise warps; written as 16-bit pairs over the
 //                     columns of dP_j they have read
-//   dQ  += dS_j K_j   M=128 N=160 K=128, A operand from TMEM
+//   dQ  += dS_j K_j   M=128 N=d K=128, A operand from TMEM
+// (d = 160 in the pages' workload; the layouts below are those of 160.)
 //
 // Warp roles (384 threads, 12 warps): warp 0 loads with TMA (dO once per
 // tile; K through three slots, V through one; each tile as two boxes from two

@@ -7,8 +7,8 @@
 // only O and L = m + log l are stored.
 //
 // Tile: 128 query rows = (128/G tokens) x (G heads of one head group); all
-// heads share the single K/V head, so every row of a tile reads the same
-// 128-key K and V tiles.  Per key tile j:
+// heads of the call (of one K/V head group) share one K/V head, so every row
+// of a tile reads the same 128-key K and V tiles.  Per key tile j:
 //   S_j = Q K_j^T         tcgen05.mma (Q, K from shared memory), fp32 in TMEM
 //   P_j = exp2(z - m)     softmax warps, one thread per row (TMEM lane); P_j
 //                         goes to its own TMEM region as 16-bit pairs
