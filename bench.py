@@ -269,19 +269,6 @@ def dram_traffic(kernel: str):
         return None
 
 
-def pinned_copy(x: torch.Tensor) -> torch.Tensor:
-    """Pinned host copy of a device tensor's whole storage (its padded base)."""
-    st = x.untyped_storage()
-    n = st.nbytes()
-    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
-    h.copy_(torch.empty(0, dtype=torch.uint8, device=x.device).set_(st))
-    return h
-
-
-def storage_bytes_view(x: torch.Tensor) -> torch.Tensor:
-    return torch.empty(0, dtype=torch.uint8, device=x.device).set_(x.untyped_storage())
-
-
 def run_gpu(args, world, rank, local):
     from ragged_gqa_attention_varlen_gb300 import _build, binding
 
@@ -403,34 +390,63 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def pinned_like(x: torch.Tensor) -> torch.Tensor:
+    """A pinned host tensor with x's shape, strides and values (its whole
+    storage copied, so padding keeps its place)."""
+    n = x.untyped_storage().nbytes() // x.element_size()
+    base = torch.empty(n, dtype=x.dtype, pin_memory=True)
+    src = torch.empty(0, dtype=x.dtype, device=x.device).set_(x.untyped_storage())
+    base.copy_(src)
+    return base.as_strided(x.shape, x.stride(), x.storage_offset())
+
+
 def run_e2e(args, p, kw, flops, stream, world):
-    """Same call with the inputs in pinned host memory: every step copies the
-    inputs' storage host->device, runs the call, and copies every result
-    device->host, all inside the timed region."""
+    """The same call through the host-buffer entry point: inputs in pinned
+    host memory, results back in pinned host memory, every step.  The library
+    cuts the batch into chunks of whole sequences and overlaps each chunk's
+    copies over the host link with the kernels of the others; all of it lies
+    inside the timed region."""
     from ragged_gqa_attention_varlen_gb300 import binding
 
-    ins = [p.q, p.k, p.v, p.dout, p.cu_q, p.cu_k, p.alibi_slopes]
-    host_in = [pinned_copy(x) for x in ins]
-    dev_in = [storage_bytes_view(x) for x in ins]
-    outs = [kw["out"], kw["dq"], kw["dk"], kw["dv"], kw["lse"]]
-    host_out = [torch.empty(x.numel() * x.element_size(), dtype=torch.uint8, pin_memory=True)
-                for x in outs]
-    dev_out = [storage_bytes_view(x) for x in outs]
-    h2d = sum(h.numel() for h in host_in)
-    d2h = sum(h.numel() for h in host_out)
+    hq, hk, hv, hdo = (pinned_like(x) for x in (p.q, p.k, p.v, p.dout))
+    hcu_q, hcu_k = p.cu_q.cpu(), p.cu_k.cpu()
+    hsl = p.alibi_slopes.cpu() if p.alibi_slopes is not None else None
+    d = p.q.shape[-1]
+    chunks = args.e2e_chunks
+    outs = dict(out=torch.empty(p.q.shape, dtype=p.q.dtype, pin_memory=True),
+                dq=torch.empty(p.q.shape, dtype=p.q.dtype, pin_memory=True),
+                dk=torch.empty(p.k.shape, dtype=p.k.dtype, pin_memory=True),
+                dv=torch.empty(p.v.shape, dtype=p.v.dtype, pin_memory=True),
+                lse=torch.empty((p.total_q, p.Hq), dtype=torch.float32, pin_memory=True),
+                host_status=torch.zeros(chunks, dtype=torch.int32, pin_memory=True))
+    buf = torch.empty(binding.host_buffer_size(p.B, p.Hq, args.hkv, d, p.total_q, p.total_k,
+                                               chunks), dtype=torch.uint8, device=p.q.device)
+    # bytes the call moves: the elements of every input and output (padding
+    # between heads or tokens is not copied), the rebased cu arrays, slopes
+    h2d = (2 * p.q.numel() + 2 * p.k.numel()) * p.q.element_size() + \
+        8 * (p.B + chunks) + (4 * p.alibi_slopes.numel() if hsl is not None else 0)
+    d2h = (2 * p.q.numel() + 2 * p.k.numel()) * p.q.element_size() + \
+        4 * p.total_q * p.Hq + 4 * chunks
 
     def step():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
-                                      p.causal, p.window_left, p.window_right, p.softcap,
-                                      p.scale_multiplier, **kw)
-        for d, h in zip(dev_out, host_out):
-            h.copy_(d, non_blocking=True)
+        binding.attention_varlen_fvjp_host(hq, hk, hv, hcu_q, hcu_k, hsl, hdo, p.causal,
+                                           p.window_left, p.window_right, p.softcap,
+                                           p.scale_multiplier, chunks=chunks, device_buffer=buf,
+                                           stream=stream, **outs)
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     torch.cuda.synchronize()
+    if int(outs["host_status"].abs().sum()) != 0:
+        raise RuntimeError(f"device status {outs['host_status'].tolist()}")
+    # the results equal the device-resident call's (dk, dv, lse whole; out and
+    # dq on their first and last 4096 tokens)
+    for n in ("out", "dq", "dk", "dv", "lse"):
+        h, g = outs[n], kw[n]
+        sl = [slice(None)] if n in ("dk", "dv", "lse") else [slice(0, 4096), slice(-4096, None)]
+        for s_ in sl:
+            if not torch.equal(h[s_], g[s_].cpu()):
+                raise RuntimeError(f"end-to-end {n} differs from the device call")
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -441,9 +457,10 @@ def run_e2e(args, p, kw, flops, stream, world):
     torch.cuda.synchronize()
     barrier(world)
     value, ms = aggregate(flops, start.elapsed_time(end) / 1e3, args.steps, world)
+    nc = min(chunks, max(p.B, 1))
     return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "gpu_launches": binding.launch_count(
-                p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * args.steps}
+            "d2h_bytes_per_step": d2h, "chunks": chunks, "gpu_launches": binding.launch_count(
+                p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * nc * args.steps}
 
 
 def main():
@@ -462,6 +479,8 @@ def main():
     ap.add_argument("--window-left", type=int, default=-1)
     ap.add_argument("--window-right", type=int, default=-1)
     ap.add_argument("--head-dim", type=int, default=HEAD_DIM, choices=(64, 128, 160))
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="sequence chunks of the end-to-end leg (copies overlap compute)")
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
     args = ap.parse_args()

@@ -197,6 +197,54 @@ int attn_varlen_launch_count(int mode, int B, int Hq, int Hkv, int64_t total_q,
  * still forgets the events). */
 attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
 
+/* Forward + full VJP with every input and output in HOST memory, for
+ * callers whose data lives on the host (the transfers over the host link are
+ * then part of the call).  The pages have no counterpart; it serves the
+ * end-to-end path.
+ *
+ * The batch is cut into `chunks` runs of whole sequences of about equal
+ * sum Lq*Lk.  Chunk c's inputs are copied to the device on one internal
+ * stream while chunk c - 1 computes on `stream` and chunk c - 2's results
+ * are copied back on another internal stream, so copies overlap the kernels.
+ * Sequences are independent, so each sequence's out, lse, dq, dk, dv are
+ * bitwise those of attn_varlen_fvjp_fwd_bwd on device copies of the inputs,
+ * whatever the chunking.
+ *
+ * Arguments: those of attn_varlen_fvjp_fwd_bwd with HOST pointers for q, k,
+ * v, dout, cu_q, cu_k, alibi_slopes (or NULL), out, dq, dk, dv and lse (same
+ * shapes and stride rules; host memory should be page-locked for the copies
+ * to run asynchronously), plus `device_buffer` (a DEVICE array of at least
+ * attn_varlen_fvjp_host_buffer_size bytes, 256-byte aligned, owned by the
+ * caller; it holds dense device copies and the workspace) and `host_status`
+ * (HOST, `chunks` int32 words: the device status word of each chunk, 0 when
+ * clean; written when the stream reaches the end of the call).  The call
+ * reads the host cu arrays before it returns (to cut the chunks); the other
+ * host arrays are read and written asynchronously, so they must stay valid
+ * until `stream` has passed the call.  Host rows are copied one token at a
+ * time when their heads are dense (head stride = head_dim), else one
+ * (token, head) row at a time; feature padding is neither read nor written.
+ * Errors as for attn_varlen_fvjp_fwd_bwd; ATTN_ERR_WORKSPACE when the device
+ * buffer is too small; ATTN_ERR_INVALID when chunks < 1. */
+attn_status attn_varlen_fvjp_fwd_bwd_host(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    float *lse, void *device_buffer, size_t device_buffer_bytes, int chunks,
+    int32_t *host_status, void *stream);
+
+/* Bytes of device buffer attn_varlen_fvjp_fwd_bwd_host needs. */
+size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim, int64_t total_q,
+                                          int64_t total_k, int chunks);
+
 /* Size of the fixed device scratch array used by
  * attn_varlen_fvjp_fwd_bwd_noalloc (64 MiB). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)

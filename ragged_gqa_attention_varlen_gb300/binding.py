@@ -23,7 +23,8 @@ DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
            "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
-           "attn_varlen_launch_count")
+           "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
+           "attn_varlen_fvjp_host_buffer_size")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -68,6 +69,12 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L, P] +
         [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
     lib.attn_varlen_bwd.restype = I
+    lib.attn_varlen_fvjp_fwd_bwd_host.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + [P, L, L] * 4 +
+        [P, P, ctypes.c_size_t, I, P, P])
+    lib.attn_varlen_fvjp_fwd_bwd_host.restype = I
+    lib.attn_varlen_fvjp_host_buffer_size.argtypes = [I, I, I, I, L, L, I]
+    lib.attn_varlen_fvjp_host_buffer_size.restype = ctypes.c_size_t
     lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
     lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
@@ -301,6 +308,86 @@ def _check_lse(lse, Tq, Hq):
     if (not lse.is_cuda or lse.dtype != torch.float32 or lse.shape != (Tq, Hq) or
             not lse.is_contiguous()):
         raise ValueError(f"lse must be a contiguous fp32 [{Tq}, {Hq}] CUDA tensor")
+
+
+def host_buffer_size(B: int, Hq: int, Hkv: int, d: int, total_q: int, total_k: int,
+                     chunks: int) -> int:
+    return int(load().attn_varlen_fvjp_host_buffer_size(B, Hq, Hkv, d, total_q, total_k, chunks))
+
+
+def _check_host(name, t, dtype, H):
+    if t.is_cuda or t.dtype != dtype or t.dim() != 3 or t.shape[1] != H or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be a host [tokens, {H}, d] {dtype} tensor with a "
+                         "contiguous feature axis")
+
+
+def attention_varlen_fvjp_host(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
+                               window_left=-1, window_right=-1, softcap=3.0,
+                               scale_multiplier=0.75, chunks=4, out=None, dq=None, dk=None,
+                               dv=None, lse=None, device_buffer=None, host_status=None,
+                               device=None, stream=None):
+    """The fused call on HOST tensors (pinned for asynchronous copies): the
+    library copies ``chunks`` runs of whole sequences to the device, computes
+    and copies the results back, overlapping the copies with the kernels.
+    cu_q, cu_k (int32) and alibi_slopes (fp32 [B, Hq] or None) are host
+    tensors too.  Outputs (host) may be passed in; otherwise pinned ones are
+    allocated.  Returns dict(out, dq, dk, dv, lse, status, device_buffer); the
+    results are complete once ``stream`` has passed the call (synchronise
+    before reading them), and ``status`` then holds one device status word per
+    chunk."""
+    lib = load()
+    dtype = q.dtype
+    if dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("q must be fp16 or bf16")
+    Hq, Hkv, d = q.shape[1], k.shape[1], q.shape[-1]
+    if d not in HEAD_DIMS or Hq % Hkv or k.shape[-1] != d:
+        raise ValueError("bad head dimension or head split")
+    for name, t, H in (("q", q, Hq), ("dout", dout, Hq), ("k", k, Hkv), ("v", v, Hkv)):
+        _check_host(name, t, dtype, H)
+    for name, c in (("cu_q", cu_q), ("cu_k", cu_k)):
+        if c.is_cuda or c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 host vector")
+    B = cu_q.numel() - 1
+    Tq, Tk = q.shape[0], k.shape[0]
+    if alibi_slopes is not None and (alibi_slopes.is_cuda or alibi_slopes.dtype != torch.float32
+                                     or alibi_slopes.shape != (B, Hq)
+                                     or alibi_slopes.stride(1) != 1):
+        raise ValueError("alibi_slopes must be a host fp32 [B, Hq] tensor, head stride 1")
+    pin = dict(dtype=dtype, pin_memory=True)
+    out = torch.empty(q.shape, **pin) if out is None else out
+    dq = torch.empty(q.shape, **pin) if dq is None else dq
+    dk = torch.empty(k.shape, **pin) if dk is None else dk
+    dv = torch.empty(v.shape, **pin) if dv is None else dv
+    for name, t, H in (("out", out, Hq), ("dq", dq, Hq), ("dk", dk, Hkv), ("dv", dv, Hkv)):
+        _check_host(name, t, dtype, H)
+    if lse is None:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, pin_memory=True)
+    if lse.is_cuda or lse.dtype != torch.float32 or lse.shape != (Tq, Hq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous host fp32 [T_q, Hq] tensor")
+    if host_status is None:
+        host_status = torch.zeros(chunks, dtype=torch.int32, pin_memory=True)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    nbytes = host_buffer_size(B, Hq, Hkv, d, Tq, Tk, chunks)
+    if device_buffer is None:
+        device_buffer = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    code = lib.attn_varlen_fvjp_fwd_bwd_host(
+        ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, d, Tq, Tk,
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
+        _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
+        _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+        alibi_slopes.stride(0) if alibi_slopes is not None else 0,
+        int(bool(causal)), int(window_left), int(window_right), float(softcap),
+        float(scale_multiplier),
+        _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
+        _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
+        _ptr(lse), _ptr(device_buffer), device_buffer.numel(), int(chunks), _ptr(host_status),
+        stream.cuda_stream)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+    return dict(out=out, dq=dq, dk=dk, dv=dv, lse=lse, status=host_status,
+                device_buffer=device_buffer)
 
 
 def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv, lse,

@@ -102,3 +102,39 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
             fake, None, None]
     assert lib.attn_varlen_fvjp_fwd_bwd_noalloc(*args) == -8
     assert b"scratch" in lib.attn_status_string(-8)
+
+
+def test_host_entry_point_validates_before_touching_the_device(lib):
+    """The host-buffer entry point checks its arguments (and reads the host cu
+    arrays) before any CUDA call: these all fail on a machine without a GPU
+    with the documented codes."""
+    import ctypes
+
+    import numpy as np
+
+    cu_q = np.array([0, 5, 9], dtype=np.int32)
+    cu_k = np.array([0, 7, 12], dtype=np.int32)
+    fake = 0x10000  # host pointers that the failing calls never dereference
+    status = np.zeros(4, dtype=np.int32)
+
+    def call(**over):
+        a = dict(dtype=0, B=2, Hq=16, Hkv=1, hd=160, tq=9, tk=12,
+                 q=fake, qts=16 * 160, qhs=160, k=fake, kts=160, khs=160, v=fake, vts=160,
+                 vhs=160, do=fake, dts=16 * 160, dhs=160, cuq=cu_q.ctypes.data,
+                 cuk=cu_k.ctypes.data, sl=None, slb=16, causal=0, wl=-1, wr=-1, cap=3.0,
+                 sm=0.75, out=fake, ots=16 * 160, ohs=160, dq=fake, dqts=16 * 160, dqhs=160,
+                 dk=fake, dkts=160, dkhs=160, dv=fake, dvts=160, dvhs=160, lse=fake,
+                 buf=None, bufb=0, chunks=2, st=status.ctypes.data, stream=None)
+        a.update(over)
+        return lib.attn_varlen_fvjp_fwd_bwd_host(*a.values())
+
+    assert call(chunks=0) == -1
+    assert call(Hkv=3) == -1
+    assert call(hd=96) == -2
+    assert call(qts=100) == -3                 # a token pitch shorter than its heads
+    bad = np.array([0, 6, 9], dtype=np.int32)
+    assert call(cuk=bad.ctypes.data) == -1     # cu_k[B] != total_k
+    assert call() == -4                        # no device buffer
+    need = lib.attn_varlen_fvjp_host_buffer_size(2, 16, 1, 160, 9, 12, 2)
+    assert need > lib.attn_varlen_fvjp_workspace_size(2, 16, 9, 12)
+    assert call(buf=0x100000, bufb=need - 1) == -4

@@ -290,6 +290,46 @@ def test_head_dim_outputs_written_exactly(d):
         assert int(torch.isnan(raw).sum()) == raw.numel() - strided[n].numel(), n
 
 
+# --------------------------------------------- host-resident inputs/outputs
+
+def _host_cases():
+    return [("tiny", lambda: W.tiny()),
+            ("ragged_bf16_padded", lambda: W.custom([0, 37, 300, 1, 80], [9, 0, 260, 130, 75],
+                                                    16, dtype=torch.bfloat16, step=2, pad=192)),
+            ("gqa_d128_causal", lambda: W.custom([150, 20, 64], [140, 300, 64], 12, Hkv=4,
+                                                 d=128, causal=True))]
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3, 9])
+@pytest.mark.parametrize("idx", range(3), ids=[c[0] for c in _host_cases()])
+def test_host_buffers_bitwise_equal_device_call(idx, chunks):
+    """The host-buffer entry point (chunked copies overlapped with the
+    kernels) gives bitwise the device call's results for every chunking,
+    including host layouts with padded heads (copied one head at a time)."""
+    p_cpu = _host_cases()[idx][1]()
+    dev = run(p_cpu.to("cuda"))
+    r = BND.attention_varlen_fvjp_host(p_cpu.q, p_cpu.k, p_cpu.v, p_cpu.cu_q, p_cpu.cu_k,
+                                       p_cpu.alibi_slopes, p_cpu.dout, p_cpu.causal,
+                                       p_cpu.window_left, p_cpu.window_right, p_cpu.softcap,
+                                       p_cpu.scale_multiplier, chunks=chunks)
+    torch.cuda.synchronize()
+    assert torch.all(r["status"] == 0), r["status"]
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert bits_equal(dev[n].cpu(), r[n]), n
+
+
+def test_host_buffers_leave_output_padding_alone():
+    p_cpu = W.custom([40, 3], [20, 70], 16, dtype=torch.bfloat16, step=2, pad=192)
+    outs = dict(out=nan_like_strided(p_cpu.q), dq=nan_like_strided(p_cpu.dout),
+                dk=nan_like_strided(p_cpu.k), dv=nan_like_strided(p_cpu.v))
+    r = BND.attention_varlen_fvjp_host(p_cpu.q, p_cpu.k, p_cpu.v, p_cpu.cu_q, p_cpu.cu_k,
+                                       p_cpu.alibi_slopes, p_cpu.dout, chunks=2, **outs)
+    torch.cuda.synchronize()
+    for n in ("out", "dq", "dk", "dv"):
+        raw = torch.empty(0, dtype=r[n].dtype).set_(r[n].untyped_storage())
+        assert int(torch.isnan(raw).sum()) == raw.numel() - r[n].numel(), n
+
+
 # ------------------------------------------- split forward / backward calls
 
 def _split_cases():
