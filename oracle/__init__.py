@@ -44,13 +44,19 @@ def _load():
         build()
         lib = ctypes.CDLL(_LIB)
         P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        common = [I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, L, L, P, P, P, L, I, I, I, D, D]
+        U64, F32 = ctypes.c_uint64, ctypes.c_float
+        common = ([I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, L, L, P, P, P, L, I, I, I, D, D] +
+                  [I, U64, F32, P])
         lib.oracle_fvjp.argtypes = common + [P] + [P] * 8 + [I]
         lib.oracle_fvjp.restype = I
         lib.oracle_rows.argtypes = common + [I, P, P, P, P, P, P, I]
         lib.oracle_rows.restype = I
         lib.oracle_decode.argtypes = [I, ctypes.c_uint16]
         lib.oracle_decode.restype = D
+        lib.oracle_splitmix64.argtypes = [U64]
+        lib.oracle_splitmix64.restype = U64
+        lib.oracle_drop_factor.argtypes = [U64, F32, I, I, I, I]
+        lib.oracle_drop_factor.restype = D
         _lib = lib
     return _lib
 
@@ -73,7 +79,12 @@ def _args(p):
     slopes = None if p.alibi_slopes is None else p.alibi_slopes.float().cpu()
     if slopes is not None:
         assert slopes.stride(1) == 1
-    keep = (q, k, v, do, cu_q, cu_k, slopes)
+    seed = getattr(p, "dropout_seed", None)
+    rates = getattr(p, "dropout_rates", None)
+    if rates is not None:
+        rates = rates.float().cpu().contiguous()
+        assert rates.shape == (p.q.shape[0],)
+    keep = (q, k, v, do, cu_q, cu_k, slopes, rates)
     Hkv = p.k.shape[1]
     assert v.shape[1] == Hkv and p.Hq % Hkv == 0
     args = [DTYPE_CODE[p.q.dtype], p.B, p.Hq, Hkv, p.q.shape[-1],
@@ -84,7 +95,9 @@ def _args(p):
             slopes.data_ptr() if slopes is not None else None,
             slopes.stride(0) if slopes is not None else 0,
             int(bool(p.causal)), int(p.window_left), int(p.window_right),
-            float(p.softcap), float(p.scale_multiplier)]
+            float(p.softcap), float(p.scale_multiplier),
+            int(seed is not None), int(seed or 0) & 0xFFFFFFFFFFFFFFFF,
+            float(getattr(p, "dropout_rate", 0.0)), rates.data_ptr() if rates is not None else None]
     return args, keep
 
 
@@ -144,6 +157,16 @@ def rows(p, tok, head, nthreads: int = 0) -> dict:
 def decode(dtype: torch.dtype, bits: int) -> float:
     """The oracle's own decoding of one 16-bit pattern."""
     return _load().oracle_decode(DTYPE_CODE[dtype], bits & 0xFFFF)
+
+
+def splitmix64(x: int) -> int:
+    """The oracle's SplitMix64 output function of one 64-bit value."""
+    return int(_load().oracle_splitmix64(x & 0xFFFFFFFFFFFFFFFF))
+
+
+def drop_factor(seed: int, rate: float, b: int, h: int, i: int, j: int) -> float:
+    """The oracle's dropout factor (keep * 1/(1-rate), or 0) of one element."""
+    return float(_load().oracle_drop_factor(seed & 0xFFFFFFFFFFFFFFFF, rate, b, h, i, j))
 
 
 def cores() -> int:

@@ -34,6 +34,18 @@
  * consecutive query heads for Hkv > 1 is the usual grouped-query reading;
  * the pages fix only Hkv = 1.
  *
+ * Dropout (optional; "ragged flash attention gradient recompute", "Root
+ * causes addressed": a counter-based splitmix64 hash of (seed, b, h, row,
+ * col), independent of tiling, with one rate or one rate per row):
+ *   K_bh   = splitmix64(splitmix64(seed ^ b) ^ h)
+ *   x_ij   = splitmix64(K_bh ^ (i << 32 | j))          (i, j local positions)
+ *   keep   = (x_ij >> 40) >= T,  T = (uint32)(rate * 2^24) in fp32 (2^24 when
+ *            rate >= 1),  scale = 1 / (1 - rate)  (0 when rate >= 1)
+ *   with rate = the call's rate, or rates[token] per query token when given.
+ *   out_i  = sum_j P_ij keep_ij scale v_j     (lse and P undropped)
+ *   dZ_ij  = P_ij (keep_ij scale dP_ij - D_i),  dv_j += P_ij keep_ij scale dO_i
+ *   (D_i = dO_i . out_i of the dropped out, as above).
+ *
  * Rows with no admissible key ("ragged flash attention gradient recompute",
  * "Root causes addressed", empty rows) have lse = -inf, out = 0, and add
  * nothing to any gradient.
@@ -100,7 +112,52 @@ typedef struct {
   int64_t slopes_bs;
   int causal, wl, wr;
   double softcap, scale_multiplier;
+  int dropout;               /* 0: none */
+  uint64_t seed;
+  float rate;                /* used when rates is NULL */
+  const float *rates;        /* per query token [total_q], or NULL */
 } problem;
+
+/* ---- counter-based dropout ------------------------------------------- */
+
+/* SplitMix64's output function (Steele, Lea and Flood, "Fast splittable
+ * pseudorandom number generators", OOPSLA 2014): a Weyl increment, then two
+ * xor-shift-multiply rounds and a final xor-shift. */
+static uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+/* Threshold and scale of a dropout rate (fp32 rate, as the caller gives it). */
+static void drop_params(float rate, uint32_t *T, double *scale) {
+  if (!(rate < 1.0f)) {
+    *T = 1u << 24;
+    *scale = 0.0;
+    return;
+  }
+  if (!(rate > 0.0f)) {
+    *T = 0;
+    *scale = 1.0;
+    return;
+  }
+  *T = (uint32_t)(rate * 16777216.0f);
+  *scale = 1.0 / (1.0 - (double)rate);
+}
+
+/* The dropout factor keep * scale of element (b, h, i, j); 1 without dropout.
+ * `token` is the packed query token (for per-token rates). */
+static double drop_factor(const problem *p, int b, int h, int64_t token, int i, int j) {
+  if (!p->dropout) return 1.0;
+  const float rate = p->rates ? p->rates[token] : p->rate;
+  uint32_t T;
+  double scale;
+  drop_params(rate, &T, &scale);
+  const uint64_t kbh = splitmix64(splitmix64(p->seed ^ (uint64_t)b) ^ (uint64_t)h);
+  const uint64_t x = splitmix64(kbh ^ (((uint64_t)(uint32_t)i << 32) | (uint64_t)(uint32_t)j));
+  return (uint32_t)(x >> 40) >= T ? scale : 0.0;
+}
 
 /* Element idx (in elements, strides already applied) of input array a. */
 static double decode(const problem *p, const void *a, int64_t idx) {
@@ -248,8 +305,11 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
     P[j] = exp(z[j] - lse);
     psum += P[j];
   }
-  for (int j = 0; j < Lk; j++)
-    for (int f = 0; f < d; f++) o->out[f] += P[j] * kv_row(s, s->V, j, kh)[f];
+  const int64_t token = s->q0 + i;
+  for (int j = 0; j < Lk; j++) {
+    const double pd = P[j] * drop_factor(p, s->b, h, token, i, j);
+    for (int f = 0; f < d; f++) o->out[f] += pd * kv_row(s, s->V, j, kh)[f];
+  }
   double D = 0.0;
   for (int f = 0; f < d; f++) D += dOi[f] * o->out[f];
   *o->D = D;
@@ -258,7 +318,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   for (int j = 0; j < Lk; j++) {
     double dp = 0.0;
     for (int f = 0; f < d; f++) dp += dOi[f] * kv_row(s, s->V, j, kh)[f];
-    double dz = P[j] * (dp - D);
+    double dz = P[j] * (drop_factor(p, s->b, h, token, i, j) * dp - D);
     dzsum += dz;
     double ds = dz * gv[j];
     for (int f = 0; f < d; f++) o->dq[f] += sigma * ds * kv_row(s, s->K, j, kh)[f];
@@ -310,9 +370,10 @@ static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
       double P = exp(z - lse);
       double dp = 0.0;
       for (int f = 0; f < d; f++) dp += dOi[f] * vj[f];
-      double ds = P * (dp - o->Dpre[rowid]) * g;
+      const double fd = drop_factor(p, s->b, h, s->q0 + i, i, j);
+      double ds = P * (fd * dp - o->Dpre[rowid]) * g;
       for (int f = 0; f < d; f++) {
-        dvrow[f] += P * dOi[f];
+        dvrow[f] += P * fd * dOi[f];
         dkrow[f] += ds * qi[f];
       }
     }
@@ -391,12 +452,15 @@ int oracle_fvjp(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
                 int64_t v_ts, int64_t v_hs,
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
-                int wr, double softcap, double scale_multiplier, const uint8_t *seq_sel,
+                int wr, double softcap, double scale_multiplier, int dropout, uint64_t seed,
+                float rate, const float *rates, const uint8_t *seq_sel,
                 double *out, double *lse, double *dq, double *dk, double *dv, double *Dpre,
                 double *dz_rowsum, double *p_rowsum, int nthreads) {
   if (Hkv < 1 || Hq % Hkv) return 0;
-  problem p = {dtype, B, Hq, Hkv, d, q, q_ts, q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts,
-               do_hs, cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
+  problem p = {dtype, B,     Hq,    Hkv,  d,     q,  q_ts,  q_hs,    k,
+               k_ts,  k_hs,  v,     v_ts, v_hs,  dout, do_ts, do_hs,  cu_q,
+               cu_k,  slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier,
+               dropout, seed, rate, rates};
   outputs o = {out, lse, dq, Dpre, dz_rowsum, p_rowsum, dk, dv};
   int nt = thread_count(nthreads);
   seqdata *seqs = calloc((size_t)B + 1, sizeof(seqdata));
@@ -529,12 +593,15 @@ int oracle_rows(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
                 int64_t v_ts, int64_t v_hs,
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
-                int wr, double softcap, double scale_multiplier, int n, const int64_t *tok,
+                int wr, double softcap, double scale_multiplier, int dropout, uint64_t seed,
+                float rate, const float *rates, int n, const int64_t *tok,
                 const int32_t *head, double *out_r, double *lse_r, double *dq_r, double *D_r,
                 int nthreads) {
   if (Hkv < 1 || Hq % Hkv) return 0;
-  problem p = {dtype, B, Hq, Hkv, d, q, q_ts, q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts,
-               do_hs, cu_q, cu_k, slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier};
+  problem p = {dtype, B,     Hq,    Hkv,  d,     q,  q_ts,  q_hs,    k,
+               k_ts,  k_hs,  v,     v_ts, v_hs,  dout, do_ts, do_hs,  cu_q,
+               cu_k,  slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier,
+               dropout, seed, rate, rates};
   rowpool w;
   w.p = &p;
   w.n = n;
@@ -553,6 +620,18 @@ int oracle_rows(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
   pthread_mutex_destroy(&w.mu);
   free(tid);
   return nt;
+}
+
+/* Exposed for the dropout pins in the test-suite. */
+uint64_t oracle_splitmix64(uint64_t x) { return splitmix64(x); }
+
+double oracle_drop_factor(uint64_t seed, float rate, int b, int h, int i, int j) {
+  problem p;
+  memset(&p, 0, sizeof p);
+  p.dropout = 1;
+  p.seed = seed;
+  p.rate = rate;
+  return drop_factor(&p, b, h, 0, i, j);
 }
 
 /* Exposed for the decoder pins in the test-suite. */

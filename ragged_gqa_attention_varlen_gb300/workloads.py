@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field
+from typing import Optional
 
 import torch
 
@@ -43,6 +44,11 @@ class Problem:
     window_right: int = -1
     softcap: float = 3.0
     scale_multiplier: float = 0.75
+    # counter-based dropout: off when dropout_seed is None; one rate, or one
+    # per query token (fp32 [total_q]) when dropout_rates is given
+    dropout_seed: Optional[int] = None
+    dropout_rate: float = 0.0
+    dropout_rates: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
 
     @property
@@ -70,10 +76,14 @@ class Problem:
         out.cu_q = self.cu_q.to(device)
         out.cu_k = self.cu_k.to(device)
         out.alibi_slopes = self.alibi_slopes.to(device)
+        if self.dropout_rates is not None:
+            out.dropout_rates = self.dropout_rates.to(device)
         return out
 
     def sequence(self, b: int) -> "Problem":
-        """Sequence b alone, as a B=1 problem with dense CPU copies."""
+        """Sequence b alone, as a B=1 problem with dense CPU copies (without
+        dropout: its hash depends on the sequence index)."""
+        assert self.dropout_seed is None, "a dropout problem cannot be cut into sequences"
         q0, q1 = int(self.cu_q[b]), int(self.cu_q[b + 1])
         k0, k1 = int(self.cu_k[b]), int(self.cu_k[b + 1])
         return Problem(

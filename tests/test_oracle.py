@@ -405,3 +405,114 @@ def test_extreme_logits_stay_finite(oracle_mod, softcap, std):
     for n in ("out", "lse", "dq", "dk", "dv"):
         assert torch.isfinite(r[n]).all(), n
     torch.testing.assert_close(r["p_rowsum"], torch.ones_like(r["p_rowsum"]), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ dropout
+
+def test_splitmix64_matches_the_generators_first_outputs(oracle_mod):
+    """SplitMix64 started from state 0 produces 0xE220A8397B1DCDAF,
+    0x6E789E6AA1B965F4, 0x06C45D188009454F: its output function of the state
+    after one, two and three Weyl increments (the function adds the
+    increment itself, so it is applied to 0, phi and 2 phi)."""
+    phi = 0x9E3779B97F4A7C15
+    got = [oracle_mod.splitmix64((n * phi) & 0xFFFFFFFFFFFFFFFF) for n in range(3)]
+    assert got == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_dropout_factors_are_zero_or_the_scale_at_the_rate(oracle_mod):
+    rate = 0.3
+    f = torch.tensor([oracle_mod.drop_factor(1234, rate, b, h, i, j)
+                      for b in range(2) for h in range(3) for i in range(40) for j in range(50)],
+                     dtype=torch.float64)
+    scale = 1.0 / (1.0 - float(torch.tensor(rate, dtype=torch.float32)))
+    assert torch.all((f == 0) | (f == scale))
+    n, kept = f.numel(), int((f > 0).sum())
+    p_keep = 1.0 - int(rate * 2 ** 24) / 2 ** 24
+    assert abs(kept - n * p_keep) < 5 * math.sqrt(n * p_keep * (1 - p_keep))
+    # rate 0 keeps everything at scale 1; rate 1 drops everything
+    assert oracle_mod.drop_factor(7, 0.0, 0, 0, 3, 4) == 1.0
+    assert oracle_mod.drop_factor(7, 1.0, 0, 0, 3, 4) == 0.0
+    # the factor depends on (seed, b, h, i, j) alone
+    assert oracle_mod.drop_factor(5, rate, 1, 2, 3, 4) == oracle_mod.drop_factor(5, rate, 1, 2, 3, 4)
+    assert len({oracle_mod.drop_factor(s, 0.5, 0, 0, 0, 0) for s in range(64)}) == 2
+
+
+def test_dropout_rate_zero_is_no_dropout(oracle_mod):
+    p = f64_problem([7, 3], [5, 9], Hq=4, seed=2, causal=True)
+    r0 = oracle_mod.fvjp(p)
+    p.dropout_seed, p.dropout_rate = 99, 0.0
+    r1 = oracle_mod.fvjp(p)
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.equal(r0[n], r1[n]), n
+
+
+def _dropout_reference(oracle_mod, p):
+    """torch fp64 autograd of the definition with an explicit keep mask built
+    from the oracle's per-element factors: z = softcap(sigma q.k) - ALiBi,
+    P = softmax(z), out = (P * M) v, grads of <dout, out>."""
+    outs, dqs, dks, dvs = [], [], [], []
+    sm = p.scale_multiplier / math.sqrt(p.q.shape[-1])
+    for b in range(p.B):
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+        Lq, Lk = q1 - q0, k1 - k0
+        q = p.q[q0:q1].double().permute(1, 0, 2).clone().requires_grad_(True)
+        k = p.k[k0:k1, 0].double().clone().requires_grad_(True)
+        v = p.v[k0:k1, 0].double().clone().requires_grad_(True)
+        do = p.dout[q0:q1].double().permute(1, 0, 2)
+        s = sm * q @ k.T
+        t = p.softcap * torch.tanh(s / p.softcap)
+        i = torch.arange(Lq, dtype=torch.float64)[:, None]
+        j = torch.arange(Lk, dtype=torch.float64)[None, :]
+        dist = (i + Lk - Lq - j).abs()
+        z = t - p.alibi_slopes[b].double()[:, None, None] * dist
+        P = torch.softmax(z, dim=-1)
+        M = torch.tensor([[[oracle_mod.drop_factor(p.dropout_seed, p.dropout_rate, b, h, ii, jj)
+                            for jj in range(Lk)] for ii in range(Lq)] for h in range(p.Hq)],
+                         dtype=torch.float64)
+        o = (P * M) @ v
+        gq, gk, gv = torch.autograd.grad(o, (q, k, v), do)
+        outs.append(o.detach().permute(1, 0, 2))
+        dqs.append(gq.permute(1, 0, 2))
+        dks.append(gk[:, None])
+        dvs.append(gv[:, None])
+    return torch.cat(outs), torch.cat(dqs), torch.cat(dks), torch.cat(dvs)
+
+
+def test_dropout_forward_and_vjp_match_autograd_of_the_definition(oracle_mod):
+    p = f64_problem([6, 9], [8, 5], Hq=3, seed=4, qk_std=2.0)
+    p.dropout_seed, p.dropout_rate = 2024, 0.25
+    r = oracle_mod.fvjp(p, diagnostics=True)
+    out, dq, dk, dv = _dropout_reference(oracle_mod, p)
+    tol = dict(rtol=1e-10, atol=1e-12)
+    torch.testing.assert_close(r["out"], out, **tol)
+    torch.testing.assert_close(r["dq"], dq, **tol)
+    torch.testing.assert_close(r["dk"], dk, **tol)
+    torch.testing.assert_close(r["dv"], dv, **tol)
+    # lse stays the undropped one, and the softmax-input gradient still sums to 0
+    p.dropout_seed = None
+    r0 = oracle_mod.fvjp(p)
+    assert torch.equal(r["lse"], r0["lse"])
+    assert float(r["dz_rowsum"].abs().max()) < 1e-12
+
+
+def test_dropout_per_token_rates(oracle_mod):
+    """A per-token rate of 0 leaves that token's rows exactly as without
+    dropout; the others follow their own rate."""
+    p = f64_problem([6, 5], [7, 4], Hq=2, seed=8)
+    base = oracle_mod.fvjp(p)
+    rates = torch.zeros(11, dtype=torch.float32)
+    rates[[1, 4, 7]] = 0.5
+    p.dropout_seed, p.dropout_rates = 77, rates
+    r = oracle_mod.fvjp(p)
+    for t in range(11):
+        same = torch.equal(r["out"][t], base["out"][t]) and torch.equal(r["dq"][t], base["dq"][t])
+        assert same == (float(rates[t]) == 0.0) or float(rates[t]) > 0, t
+    assert not torch.equal(r["dk"], base["dk"])
+    # equal to a scalar rate where every token has that rate
+    p2 = f64_problem([6, 5], [7, 4], Hq=2, seed=8)
+    p2.dropout_seed, p2.dropout_rate = 77, 0.5
+    p.dropout_rates = torch.full((11,), 0.5, dtype=torch.float32)
+    ra, rb = oracle_mod.fvjp(p), oracle_mod.fvjp(p2)
+    for n in ("out", "dq", "dk", "dv"):
+        assert torch.equal(ra[n], rb[n]), n
