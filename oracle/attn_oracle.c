@@ -37,8 +37,9 @@
  * Dropout (optional; "ragged flash attention gradient recompute", "Root
  * causes addressed": a counter-based splitmix64 hash of (seed, b, h, row,
  * col), independent of tiling, with one rate or one rate per row):
- *   K_bh   = splitmix64(splitmix64(seed ^ b) ^ h)
- *   x_ij   = splitmix64(K_bh ^ (i << 32 | j))          (i, j local positions)
+ *   K_b    = splitmix64(seed ^ b)
+ *   x_hij  = splitmix64(K_b ^ (h << 48 | i << 24 | j))  (i, j local positions
+ *            below 2^24, h below 2^16: one hash per element)
  *   keep   = (x_ij >> 40) >= T,  T = (uint32)(rate * 2^24) in fp32 (2^24 when
  *            rate >= 1),  scale = 1 / (1 - rate)  (0 when rate >= 1)
  *   with rate = the call's rate, or rates[token] per query token when given.
@@ -154,8 +155,9 @@ static double drop_factor(const problem *p, int b, int h, int64_t token, int i, 
   uint32_t T;
   double scale;
   drop_params(rate, &T, &scale);
-  const uint64_t kbh = splitmix64(splitmix64(p->seed ^ (uint64_t)b) ^ (uint64_t)h);
-  const uint64_t x = splitmix64(kbh ^ (((uint64_t)(uint32_t)i << 32) | (uint64_t)(uint32_t)j));
+  const uint64_t kb = splitmix64(p->seed ^ (uint64_t)b);
+  const uint64_t x = splitmix64(kb ^ (((uint64_t)h << 48) | ((uint64_t)(uint32_t)i << 24) |
+                                      (uint64_t)(uint32_t)j));
   return (uint32_t)(x >> 40) >= T ? scale : 0.0;
 }
 
