@@ -279,6 +279,7 @@ def run_gpu(args, world, rank, local):
     p = workloads.long_balanced(seed=5 + rank, device=dev, poison=False,
                                 length_scale=args.length_scale, Hkv=args.hkv, d=args.head_dim)
     p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
+    drop = {} if args.dropout is None else dict(dropout_seed=1234, dropout_rate=args.dropout)
     flops = counted_flops(p)
     kflops = kernel_flops(p)
     out = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
@@ -294,7 +295,7 @@ def run_gpu(args, world, rank, local):
     def call():
         binding.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
                                       p.causal, p.window_left, p.window_right, p.softcap,
-                                      p.scale_multiplier, **kw)
+                                      p.scale_multiplier, **kw, **drop)
 
     for _ in range(args.warmup):
         call()
@@ -346,7 +347,8 @@ def run_gpu(args, world, rank, local):
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "traffic": dram_traffic(dom) if (args.length_scale == 1.0 and not mask_name(p)
-                                                     and args.head_dim == HEAD_DIM) else None,
+                                                     and args.head_dim == HEAD_DIM
+                                                     and args.dropout is None) else None,
                     "peak_kind": f"{kind} bf16 sustained"}
     else:
         # one call runs a forward, dk/dv and dq per K/V head group: the
@@ -360,7 +362,7 @@ def run_gpu(args, world, rank, local):
 
     # ---- end to end: pinned host inputs in, results out, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.dropout is None:
         e2e = run_e2e(args, p, kw, flops, stream, world)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -370,7 +372,8 @@ def run_gpu(args, world, rank, local):
             "config": {"workload": "long_balanced" + (
                            "" if args.length_scale == 1.0 else f" x{args.length_scale} length") +
                            mask_name(p) + ("" if args.hkv == 1 else f", Hkv={args.hkv}") +
-                           ("" if args.head_dim == HEAD_DIM else f", d={args.head_dim}"),
+                           ("" if args.head_dim == HEAD_DIM else f", d={args.head_dim}") +
+                           ("" if args.dropout is None else f", dropout {args.dropout}"),
                        "B": p.B, "Hq": p.Hq, "Hkv": args.hkv,
                        "head_dim": args.head_dim, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
@@ -382,7 +385,7 @@ def run_gpu(args, world, rank, local):
             "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
             "clocks": clk, "e2e": e2e}
     if (rank == 0 and world == 1 and not args.no_cpu and not mask_name(p) and args.hkv == 1
-            and args.head_dim == HEAD_DIM):
+            and args.head_dim == HEAD_DIM and args.dropout is None):
         v, cores, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -481,6 +484,8 @@ def main():
     ap.add_argument("--head-dim", type=int, default=HEAD_DIM, choices=(64, 128, 160))
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="sequence chunks of the end-to-end leg (copies overlap compute)")
+    ap.add_argument("--dropout", type=float, default=None,
+                    help="time with counter-based dropout at this rate")
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
     args = ap.parse_args()

@@ -197,6 +197,70 @@ int attn_varlen_launch_count(int mode, int B, int Hq, int Hkv, int64_t total_q,
  * still forgets the events). */
 attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
 
+/* The fused, forward and backward calls with counter-based dropout on the
+ * attention weights ("ragged flash attention gradient recompute", "Root
+ * causes addressed": a splitmix64 hash of (seed, b, h, row, col), independent
+ * of tiling, with a scalar or a per-row rate).  Arguments are those of
+ * attn_varlen_fvjp_fwd_bwd / attn_varlen_fwd / attn_varlen_bwd plus, after
+ * scale_multiplier: dropout_seed, dropout_rate (used when dropout_rates is
+ * NULL) and dropout_rates (DEVICE fp32 [total_q]: one rate per query token,
+ * shared by its heads, or NULL).
+ *
+ * Element (sequence b, query head h, local query i, local key j) is kept when
+ * the top 24 bits of splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | j))
+ * are at least T = (uint32)(rate * 2^24) (computed in fp32; 2^24, dropping
+ * everything, when rate >= 1), and kept weights are scaled by 1 / (1 - rate).
+ * out = sum_j P_ij keep_ij scale v_j with the undropped softmax P (lse is the
+ * undropped one); the backward pass regenerates the same keep bits.  Local
+ * positions must stay below 2^24 and head indices below 2^16.  Dropout runs
+ * with head_dim 160 only (ATTN_ERR_UNSUPPORTED otherwise); a NaN rate is
+ * ATTN_ERR_INVALID.  Results are bitwise repeatable for a fixed seed. */
+attn_status attn_varlen_fvjp_fwd_bwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+attn_status attn_varlen_fwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+attn_status attn_varlen_bwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    const void *out, int64_t out_tok_stride, int64_t out_head_stride, const float *lse,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
+
 /* Forward + full VJP with every input and output in HOST memory, for
  * callers whose data lives on the host (the transfers over the host link are
  * then part of the call).  The pages have no counterpart; it serves the

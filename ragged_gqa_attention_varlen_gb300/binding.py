@@ -24,7 +24,8 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
            "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
            "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
-           "attn_varlen_fvjp_host_buffer_size")
+           "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_fwd_bwd_dropout",
+           "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -75,6 +76,19 @@ def load(path: str = LIB_PATH):
     lib.attn_varlen_fvjp_fwd_bwd_host.restype = I
     lib.attn_varlen_fvjp_host_buffer_size.argtypes = [I, I, I, I, L, L, I]
     lib.attn_varlen_fvjp_host_buffer_size.restype = ctypes.c_size_t
+    DR = [ctypes.c_uint64, F, P]  # dropout seed, rate, per-token rates
+    lib.attn_varlen_fvjp_fwd_bwd_dropout.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
+        [P, L, L] * 4 + [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fvjp_fwd_bwd_dropout.restype = I
+    lib.attn_varlen_fwd_dropout.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 3 + [P, P, P, L, I, I, I, F, F] + DR + [P, L, L] +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fwd_dropout.restype = I
+    lib.attn_varlen_bwd_dropout.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
+        [P, L, L, P] + [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_bwd_dropout.restype = I
     lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
     lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
@@ -104,6 +118,16 @@ def record_events_next_call(events):
 
 def _ptr(t):
     return None if t is None else t.data_ptr()
+
+
+def _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq):
+    """(seed, rate, rates pointer) for the dropout entry points; rates is an
+    fp32 CUDA vector of one rate per query token, or None."""
+    if dropout_rates is not None:
+        if (not dropout_rates.is_cuda or dropout_rates.dtype != torch.float32 or
+                dropout_rates.shape != (Tq,) or not dropout_rates.is_contiguous()):
+            raise ValueError("dropout_rates must be a contiguous fp32 CUDA vector [T_q]")
+    return [int(dropout_seed) & 0xFFFFFFFFFFFFFFFF, float(dropout_rate), _ptr(dropout_rates)]
 
 
 def _kv_heads(q, k):
@@ -137,7 +161,7 @@ def _like(x: torch.Tensor) -> torch.Tensor:
 def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
                           window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
                           out=None, dq=None, dk=None, dv=None, lse=None, workspace=None,
-                          stream=None):
+                          stream=None, dropout_seed=None, dropout_rate=0.0, dropout_rates=None):
     """Forward + full VJP in one library call.
 
     q, dout: [T_q, Hq, d]; k, v: [T_k, Hkv, d] CUDA views (fp16 or bf16,
@@ -146,7 +170,9 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     [B+1] on the device.  alibi_slopes: fp32 [B, Hq] or None.  Outputs may be
     passed in (any strides of the same rules); otherwise dense ones are
     allocated.  Returns dict(out, dq, dk, dv, lse, workspace).  The call is
-    asynchronous on ``stream`` (default: the current stream)."""
+    asynchronous on ``stream`` (default: the current stream).  With a
+    ``dropout_seed`` the attention weights get counter-based dropout at
+    ``dropout_rate`` (or per query token from ``dropout_rates``)."""
     lib = load()
     dtype = q.dtype
     if dtype not in (torch.float16, torch.bfloat16):
@@ -183,14 +209,17 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
         workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    code = lib.attn_varlen_fvjp_fwd_bwd(
+    drop = ([] if dropout_seed is None else
+            _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
+    fn = lib.attn_varlen_fvjp_fwd_bwd_dropout if drop else lib.attn_varlen_fvjp_fwd_bwd
+    code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
         alibi_slopes.stride(0) if alibi_slopes is not None else 0,
         int(bool(causal)), int(window_left), int(window_right), float(softcap),
-        float(scale_multiplier),
+        float(scale_multiplier), *drop,
         _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
         _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
         _ptr(lse), _ptr(workspace), workspace.numel(), None, stream.cuda_stream)
@@ -237,7 +266,8 @@ def _workspace(workspace, B, Hq, Tq, Tk, device):
 
 def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window_left=-1,
                          window_right=-1, softcap=3.0, scale_multiplier=0.75, out=None, lse=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, dropout_seed=None, dropout_rate=0.0,
+                         dropout_rates=None):
     """Forward only: returns (out, lse).  Same argument rules as
     attention_varlen_fvjp; lse is fp32 [T_q, Hq] (natural log), the value the
     backward call reads back.  Asynchronous on ``stream``."""
@@ -252,14 +282,17 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
     workspace = _workspace(workspace, B, Hq, Tq, Tk, q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    code = lib.attn_varlen_fwd(
+    drop = ([] if dropout_seed is None else
+            _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
+    fn = lib.attn_varlen_fwd_dropout if drop else lib.attn_varlen_fwd
+    code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
         alibi_slopes.stride(0) if alibi_slopes is not None else 0,
         int(bool(causal)), int(window_left), int(window_right), float(softcap),
-        float(scale_multiplier), _ptr(out), out.stride(0), out.stride(1),
+        float(scale_multiplier), *drop, _ptr(out), out.stride(0), out.stride(1),
         _ptr(lse), _ptr(workspace), workspace.numel(), None, stream.cuda_stream)
     if code != 0:
         raise AttnError(code, lib.attn_status_string(code).decode())
@@ -268,7 +301,8 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
 
 def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, causal=False,
                          window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
-                         dq=None, dk=None, dv=None, workspace=None, stream=None):
+                         dq=None, dk=None, dv=None, workspace=None, stream=None,
+                         dropout_seed=None, dropout_rate=0.0, dropout_rates=None):
     """Backward only: given the forward's out and lse for the same inputs and
     options, returns (dq, dk, dv).  out and lse are read, not modified.  For
     the same inputs the result is bitwise the one attention_varlen_fvjp gives.
@@ -288,14 +322,17 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
     workspace = _workspace(workspace, B, Hq, Tq, Tk, q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    code = lib.attn_varlen_bwd(
+    drop = ([] if dropout_seed is None else
+            _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
+    fn = lib.attn_varlen_bwd_dropout if drop else lib.attn_varlen_bwd
+    code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
         _ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
         alibi_slopes.stride(0) if alibi_slopes is not None else 0,
         int(bool(causal)), int(window_left), int(window_right), float(softcap),
-        float(scale_multiplier), _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
+        float(scale_multiplier), *drop, _ptr(out), out.stride(0), out.stride(1), _ptr(lse),
         _ptr(dq), dq.stride(0), dq.stride(1), _ptr(dk), dk.stride(0), dk.stride(1),
         _ptr(dv), dv.stride(0), dv.stride(1),
         _ptr(workspace), workspace.numel(), None, stream.cuda_stream)

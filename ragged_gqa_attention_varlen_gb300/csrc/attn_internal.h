@@ -59,6 +59,17 @@ struct Params {
   float* lse;     // [total_q, lse_rs]
   float* Dbuf;    // [total_q, lse_rs]
   int64_t lse_rs; // row stride of lse and D: every query head of the call
+  // counter-based dropout ("ragged flash attention gradient recompute", "Root
+  // causes addressed"): element (b, h, i, j) is kept when the top 24 bits of
+  // splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | j)) reach the
+  // rate's threshold T = rate * 2^24, and then scaled by 1 / (1 - rate)
+  int dropout;
+  uint64_t drop_seed;
+  uint32_t drop_T;           // threshold of the call's rate (when drop_tab is null)
+  float drop_scale;
+  const float* drop_rates;   // per query token [total_q], or null
+  uint2* drop_tab;           // per query token (T, scale bits), made by the schedule kernel
+  int head0;                 // first query head of this K/V head group (hash input h)
   int32_t* status;
   int32_t* counters;  // [3]: fwd, dkdv, dq tile counters (of this K/V head group)
   int ncounters;      // counters the schedule kernel resets (every group's)

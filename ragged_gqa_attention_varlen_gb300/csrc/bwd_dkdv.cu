@@ -95,7 +95,7 @@ struct Pair {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD>
+template <bool BF16, bool MASK, int HD, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
@@ -553,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       KTile t;
       ktile_decode<MASK>(p, item, t);
       const int nsteps = step_count(t);
+      const uint64_t dkb = DROP ? splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b)) : 0;
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
         const int b = gg & 1;
@@ -590,13 +591,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* pa = reinterpret_cast<const float4*>(cols->a[b] + half * 64);
         const float4* pm = reinterpret_cast<const float4*>(cols->m[b] + half * 64);
         uint32_t pk[32];
+        // dropout: column c (query token, head) of this thread's key; P^T for
+        // dV is P * keep * scale and dS uses keep * scale * dP (keep bits kept)
+        uint64_t kbits = 0;
+        const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
+        const int dh0 = DROP ? p.head0 + (st % ngroups) * G : 0;
+        auto dcol = [&](int c, float& sc) -> bool {
+          const int lc = half * 64 + c;
+          const int it = dtok0 + (lc >> lgG);
+          sc = 0.f;
+          if (it >= t.Lq) return false;
+          uint32_t T;
+          drop_row(p, static_cast<int64_t>(t.q0) + it, T, sc);
+          return drop_keep(dkb, drop_hi(dh0 + (lc & (G - 1)), it), t.key + r, T);
+        };
+        auto pack_p = [&](int c, float a, float bb) -> uint32_t {  // columns c, c + 1
+          if (DROP) {
+            float s0, s1;
+            const bool k0 = dcol(c, s0), k1 = dcol(c + 1, s1);
+            kbits |= (static_cast<uint64_t>(k0) << c) | (static_cast<uint64_t>(k1) << (c + 1));
+            a = k0 ? a * s0 : 0.f;
+            bb = k1 ? bb * s1 : 0.f;
+          }
+          return Pack<BF16>::two(a, bb);
+        };
         auto p_group = [&](int q4, float b0, float b1, float b2, float b3) {
           const uint64_t z0 = f2_fma(t2[2 * q4], lm.capped ? os2 : is2, f2_make(b0, b1));
           const uint64_t z1 = f2_fma(t2[2 * q4 + 1], lm.capped ? os2 : is2, f2_make(b2, b3));
           const uint64_t p0 = f2_make(ex2_approx(f2_lo(z0)), ex2_approx(f2_hi(z0)));
           const uint64_t p1 = f2_make(ex2_approx(f2_lo(z1)), ex2_approx(f2_hi(z1)));
-          pk[2 * q4] = Pack<BF16>::two(f2_lo(p0), f2_hi(p0));
-          pk[2 * q4 + 1] = Pack<BF16>::two(f2_lo(p1), f2_hi(p1));
+          pk[2 * q4] = pack_p(4 * q4, f2_lo(p0), f2_hi(p0));
+          pk[2 * q4 + 1] = pack_p(4 * q4 + 2, f2_lo(p1), f2_hi(p1));
           // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
           t2[2 * q4] = lm.capped ? f2_mul(p0, f2_fma(t2[2 * q4], t2[2 * q4], m12)) : f2_mul(p0, m12);
           t2[2 * q4 + 1] =
@@ -621,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             z[i] = f2_make(ex2_approx(f2_lo(z[i])), ex2_approx(f2_hi(z[i])));
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            pk[i] = Pack<BF16>::two(f2_lo(z[i]), f2_hi(z[i]));
+            pk[i] = pack_p(2 * i, f2_lo(z[i]), f2_hi(z[i]));
             // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
             t2[i] = lm.capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
           }
@@ -679,6 +704,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dp_read);
+        if (DROP) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            float sc = p.drop_scale;
+            if (p.drop_tab) {  // per-token rates: the column's own scale
+              const int it = dtok0 + ((half * 64 + c) >> lgG);
+              sc = it < t.Lq ? __uint_as_float(__ldg(p.drop_tab + t.q0 + it).y) : 0.f;
+            }
+            d[c] = ((kbits >> c) & 1) ? d[c] * sc : 0.f;
+          }
+        }
         // dS^T = P (1 - tanh^2) (dP - D) = t2 (D - dP), D per group of 4 columns
         if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) break;
         {
@@ -744,10 +780,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool B, bool M>
+template <bool B, bool M, bool DR>
 auto dkdv_for_d(int d) {
-  return d == 128 ? dkdv_kernel<B, M, 128>
-                  : (d == 64 ? dkdv_kernel<B, M, 64> : dkdv_kernel<B, M, 160>);
+  if constexpr (DR) {
+    return dkdv_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
+  } else {
+    return d == 128 ? dkdv_kernel<B, M, 128, false>
+                    : (d == 64 ? dkdv_kernel<B, M, 64, false> : dkdv_kernel<B, M, 160, false>);
+  }
 }
 
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
@@ -755,8 +795,11 @@ cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorM
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
                         const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? dkdv_for_d<true, true>(p.d) : dkdv_for_d<true, false>(p.d))
-                        : (m ? dkdv_for_d<false, true>(p.d) : dkdv_for_d<false, false>(p.d));
+  auto k = p.dropout
+               ? (p.dtype == 1 ? (m ? dkdv_for_d<true, true, true>(p.d) : dkdv_for_d<true, false, true>(p.d))
+                               : (m ? dkdv_for_d<false, true, true>(p.d) : dkdv_for_d<false, false, true>(p.d)))
+               : (p.dtype == 1 ? (m ? dkdv_for_d<true, true, false>(p.d) : dkdv_for_d<true, false, false>(p.d))
+                               : (m ? dkdv_for_d<false, true, false>(p.d) : dkdv_for_d<false, false, false>(p.d)));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
   k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();

@@ -87,7 +87,7 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD>
+template <bool BF16, bool MASK, int HD, bool DROP>
 __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tdo2,
@@ -393,6 +393,15 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
         Drow = p.Dbuf[ri];
       }
+      // dropout of this row: dS = P (1 - tanh^2) (keep * scale * dP - D)
+      uint64_t dkb = 0, dhi = 0;
+      uint32_t dT = 0;
+      float dsc = 1.f;
+      if (DROP) {
+        dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b));
+        dhi = drop_hi(p.head0 + h, i_loc);
+        if (row_valid) drop_row(p, static_cast<int64_t>(t.q0) + i_loc, dT, dsc);
+      }
       for (int j = 0; j < n; ++j) {
         const uint32_t gg = g + j;
         const int key0 = (t.kt0 + j) * kKeys + half * 64;
@@ -445,6 +454,12 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
             for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);  // P (1 - tanh^2)
           }
         }
+        uint64_t kbits = 0;  // dropout keep bit of each of this half's 64 keys
+        if (DROP) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            kbits |= static_cast<uint64_t>(drop_keep(dkb, dhi, key0 + c, dT)) << c;
+        }
         if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
         tc_fence_after();
         const uint32_t pbuf = tmem + kColP + half * 64 + lane_addr;
@@ -454,6 +469,10 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           float d[32];
           tmem_ld32(pbuf + cc * 32, d);
           tmem_wait_ld();
+          if (DROP) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) d[c] = ((kbits >> (cc * 32 + c)) & 1) ? d[c] * dsc : 0.f;
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
             pk[cc * 16 + (c >> 1)] = Pack<BF16>::two(x[cc * 32 + c] * (d[c] - Drow),
@@ -512,9 +531,14 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool B, bool M>
+template <bool B, bool M, bool DR>
 auto dq_for_d(int d) {
-  return d == 128 ? dq_kernel<B, M, 128> : (d == 64 ? dq_kernel<B, M, 64> : dq_kernel<B, M, 160>);
+  if constexpr (DR) {
+    return dq_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
+  } else {
+    return d == 128 ? dq_kernel<B, M, 128, false>
+                    : (d == 64 ? dq_kernel<B, M, 64, false> : dq_kernel<B, M, 160, false>);
+  }
 }
 
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
@@ -522,8 +546,11 @@ cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? dq_for_d<true, true>(p.d) : dq_for_d<true, false>(p.d))
-                        : (m ? dq_for_d<false, true>(p.d) : dq_for_d<false, false>(p.d));
+  auto k = p.dropout
+               ? (p.dtype == 1 ? (m ? dq_for_d<true, true, true>(p.d) : dq_for_d<true, false, true>(p.d))
+                               : (m ? dq_for_d<false, true, true>(p.d) : dq_for_d<false, false, true>(p.d)))
+               : (p.dtype == 1 ? (m ? dq_for_d<true, true, false>(p.d) : dq_for_d<true, false, false>(p.d))
+                               : (m ? dq_for_d<false, true, false>(p.d) : dq_for_d<false, false, false>(p.d)));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
   // With `overlap` the launch is a programmatic dependent of the kernel before
   // it (dk/dv, which signals at its start): dq reads nothing dk/dv writes, so

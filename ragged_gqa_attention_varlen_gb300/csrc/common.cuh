@@ -13,6 +13,50 @@ namespace attn {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// SplitMix64's output function (Steele, Lea and Flood, OOPSLA 2014): a Weyl
+// increment, two xor-shift-multiply rounds and a final xor-shift.
+__host__ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Threshold and scale of a dropout rate: keep when the hash's top 24 bits
+// are >= T (probability 1 - T / 2^24), and scale kept values by 1/(1 - rate).
+__host__ __device__ __forceinline__ void drop_params(float rate, uint32_t& T, float& scale) {
+  if (!(rate < 1.f)) {
+    T = 1u << 24;
+    scale = 0.f;
+  } else if (!(rate > 0.f)) {
+    T = 0u;
+    scale = 1.f;
+  } else {
+    T = static_cast<uint32_t>(rate * 16777216.0f);
+    scale = 1.f / (1.f - rate);
+  }
+}
+
+// Dropout of one element: `kb` = splitmix64(seed ^ b), `hi` = h << 48 | i << 24.
+__device__ __forceinline__ bool drop_keep(uint64_t kb, uint64_t hi, int j, uint32_t T) {
+  return static_cast<uint32_t>(splitmix64(kb ^ (hi | static_cast<uint32_t>(j))) >> 40) >= T;
+}
+__device__ __forceinline__ uint64_t drop_hi(int h, int i) {
+  return (static_cast<uint64_t>(h) << 48) | (static_cast<uint64_t>(static_cast<uint32_t>(i)) << 24);
+}
+
+// Threshold and scale of query token `tok` (packed index).
+__device__ __forceinline__ void drop_row(const Params& p, int64_t tok, uint32_t& T, float& scale) {
+  if (p.drop_tab) {
+    const uint2 e = __ldg(p.drop_tab + tok);
+    T = e.x;
+    scale = __uint_as_float(e.y);
+  } else {
+    T = p.drop_T;
+    scale = p.drop_scale;
+  }
+}
+
 // Constants of the logit map z2 = log2(e) * (c*tanh(sigma*x/c) - slope*dist)
 // (or log2(e) * (sigma*x - slope*dist) without a cap), where x is the raw
 // q.k accumulator.

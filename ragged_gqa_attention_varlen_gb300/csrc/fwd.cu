@@ -130,7 +130,7 @@ __device__ __forceinline__ int next_key_tile(const QTile& t, int kt) {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD>
+template <bool BF16, bool MASK, int HD, bool DROP>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk2,
@@ -412,6 +412,18 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint64_t l2 = f2_make(0.f, 0.f), lu2 = l2;  // fixed reference: row sums as pairs
       if (fixed) m_run = row_bound<MASK>(p, t.Lk, pos_off, slope2);
       const float bref = fixed ? m_run : 0.f;  // subtracted inside the logit
+      // dropout of this row: P V uses P * keep * scale, the sums plain P
+      uint64_t dkb = 0, dhi = 0;
+      uint32_t dT = 0;
+      float dsc = 1.f;
+      if (DROP) {
+        dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b));
+        dhi = drop_hi(p.head0 + h, i_loc);
+        if (row_valid) drop_row(p, static_cast<int64_t>(t.q0) + i_loc, dT, dsc);
+      }
+      auto dropped = [&](float pv, int j) -> float {
+        return drop_keep(dkb, dhi, j, dT) ? pv * dsc : 0.f;
+      };
       for (int jj = 0, kt = t0; jj < n; ++jj, kt = next_key_tile(t, kt)) {
         const uint32_t gg = g + jj;
         const int key0 = kt * kKeys + half * 64;
@@ -466,10 +478,16 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
           for (int c = 0; c < 64; c += 2) {
             x[c] = ex2_approx(x[c]);  // the reference is inside the logit
             x[c + 1] = ex2_approx(x[c + 1]);
+            if (DROP) {
+              pk[c >> 1] = Pack<BF16>::two(dropped(x[c], key0 + c), dropped(x[c + 1], key0 + c + 1));
+              lu2 = f2_add(lu2, f2_make(x[c], x[c + 1]));
+              continue;
+            }
             pk[c >> 1] = Pack<BF16>::two(x[c], x[c + 1]);
             // two row sums: of P (for lse) and of the rounded P that
             // multiplies V (for out, which is then exactly a weighted mean of
-            // V rows: one key gives out = v)
+            // V rows: one key gives out = v; with dropout out is normalised by
+            // the plain sum)
             lu2 = f2_add(lu2, f2_make(x[c], x[c + 1]));
             l2 = f2_add(l2, Pack<BF16>::unpack(pk[c >> 1]));
           }
@@ -525,7 +543,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           l += x[c] + x[c + 1];
-          pk[c >> 1] = Pack<BF16>::two(x[c], x[c + 1]);
+          pk[c >> 1] = DROP ? Pack<BF16>::two(dropped(x[c], key0 + c), dropped(x[c + 1], key0 + c + 1))
+                            : Pack<BF16>::two(x[c], x[c + 1]);
         }
         // this half's 64 keys -> 32 pair columns of the P region
         const uint32_t pb = tmem + kColP + half * 32 + lane_addr;
@@ -553,7 +572,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       const float lrt = fixed ? lr + lrs[(half ^ 1) * 128 + r] : 0.f;
       if (!(ok = mbar_wait_warp(&bars->o_full, tcount & 1, s_abort))) break;
       tc_fence_after();
-      const float lnorm = fixed ? lrt : lt;
+      const float lnorm = (fixed && !DROP) ? lrt : lt;
       const float inv = (lnorm > 0.f) ? 1.f / lnorm : 0.f;
       if (row_valid && half == 0)
         p.lse[static_cast<int64_t>(t.q0 + i_loc) * p.lse_rs + h] =
@@ -595,17 +614,25 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool B, bool M>
+template <bool B, bool M, bool DR>
 auto fwd_for_d(int d) {
-  return d == 128 ? fwd_kernel<B, M, 128> : (d == 64 ? fwd_kernel<B, M, 64> : fwd_kernel<B, M, 160>);
+  if constexpr (DR) {
+    return fwd_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
+  } else {
+    return d == 128 ? fwd_kernel<B, M, 128, false>
+                    : (d == 64 ? fwd_kernel<B, M, 64, false> : fwd_kernel<B, M, 160, false>);
+  }
 }
 
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
                        const CUtensorMap& tv, int grid, cudaStream_t s) {
   const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? fwd_for_d<true, true>(p.d) : fwd_for_d<true, false>(p.d))
-                        : (m ? fwd_for_d<false, true>(p.d) : fwd_for_d<false, false>(p.d));
+  auto k = p.dropout
+               ? (p.dtype == 1 ? (m ? fwd_for_d<true, true, true>(p.d) : fwd_for_d<true, false, true>(p.d))
+                               : (m ? fwd_for_d<false, true, true>(p.d) : fwd_for_d<false, false, true>(p.d)))
+               : (p.dtype == 1 ? (m ? fwd_for_d<true, true, false>(p.d) : fwd_for_d<true, false, false>(p.d))
+                               : (m ? fwd_for_d<false, true, false>(p.d) : fwd_for_d<false, false, false>(p.d)));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
   k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   return cudaGetLastError();

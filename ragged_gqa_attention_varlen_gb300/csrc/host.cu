@@ -9,6 +9,7 @@
 
 #include "../../include/attn_varlen.h"
 #include "attn_internal.h"
+#include "common.cuh"
 
 namespace attn {
 namespace {
@@ -38,7 +39,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace layout: [status + counters | schedule | D].
 struct WsLayout {
-  size_t status, counters, sched, dbuf, total;
+  size_t status, counters, sched, dbuf, droptab, total;
 };
 
 // Counters: three per K/V head group, and Hkv <= Hq.
@@ -48,7 +49,8 @@ WsLayout ws_layout(int B, int Hq, int64_t total_q) {
   w.counters = 16;
   w.sched = align_up(w.counters + sizeof(int32_t) * 3 * static_cast<size_t>(Hq < 2 ? 2 : Hq));
   w.dbuf = w.sched + align_up(sizeof(int32_t) * static_cast<size_t>(sched_words(B)));
-  w.total = w.dbuf + align_up(sizeof(float) * static_cast<size_t>(total_q) * Hq);
+  w.droptab = w.dbuf + align_up(sizeof(float) * static_cast<size_t>(total_q) * Hq);
+  w.total = w.droptab + align_up(sizeof(uint2) * static_cast<size_t>(total_q));
   return w;
 }
 
@@ -228,6 +230,14 @@ namespace {
 constexpr int kModeFwd = 1;  // out, lse
 constexpr int kModeBwd = 2;  // dq, dk, dv from out and lse
 
+// Dropout arguments of a call (off by default).
+struct Dropout {
+  bool on = false;
+  uint64_t seed = 0;
+  float rate = 0.f;
+  const float* rates = nullptr;  // per query token, device
+};
+
 // The three entry points share one body: host-side validation, the tensor
 // maps, and the launches of the requested passes.
 attn_status run_call(
@@ -239,13 +249,15 @@ attn_status run_call(
     float scale_multiplier, void* out, int64_t out_ts, int64_t out_hs, void* dq, int64_t dq_ts,
     int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts,
     int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
-    void* stream_ptr) {
+    void* stream_ptr, const Dropout& drop = Dropout()) {
   const bool fwd = (mode & kModeFwd) != 0, bwd = (mode & kModeBwd) != 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   // ---- host-side validation (nothing is enqueued on failure)
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
   if (head_dim != 160 && head_dim != 128 && head_dim != 64) return ATTN_ERR_UNSUPPORTED;
+  if (drop.on && head_dim != 160) return ATTN_ERR_UNSUPPORTED;
+  if (drop.on && !(drop.rate == drop.rate)) return ATTN_ERR_INVALID;
   if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
   if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
   if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
@@ -338,6 +350,13 @@ attn_status run_call(
   p.status = device_status ? device_status : reinterpret_cast<int32_t*>(wsb + ws.status);
   p.counters = reinterpret_cast<int32_t*>(wsb + ws.counters);
   p.ncounters = 3 * Hkv;
+  if (drop.on) {
+    p.dropout = 1;
+    p.drop_seed = drop.seed;
+    drop_params(drop.rate, p.drop_T, p.drop_scale);
+    p.drop_rates = drop.rates;
+    p.drop_tab = drop.rates ? reinterpret_cast<uint2*>(wsb + ws.droptab) : nullptr;
+  }
   p.sched = reinterpret_cast<int32_t*>(wsb + ws.sched);
 
   // ---- degenerate sizes: no query or no key at all
@@ -385,6 +404,7 @@ attn_status run_call(
     pg.Dbuf = p.Dbuf + h0;
     pg.slopes = alibi_slopes ? alibi_slopes + h0 : nullptr;
     pg.counters = p.counters + 3 * g;
+    pg.head0 = static_cast<int>(h0);
     return pg;
   };
   auto encode_group = [&](const Params& pg, int g, Maps& m) -> bool {
@@ -509,4 +529,71 @@ extern "C" attn_status attn_varlen_bwd(
                   scale_multiplier, const_cast<void*>(out), out_ts, out_hs, dq, dq_ts, dq_hs, dk,
                   dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
                   workspace_bytes, device_status, stream);
+}
+
+extern "C" attn_status attn_varlen_fvjp_fwd_bwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, uint64_t dropout_seed, float dropout_rate,
+    const float* dropout_rates, void* out, int64_t out_ts, int64_t out_hs, void* dq,
+    int64_t dq_ts, int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv,
+    int64_t dv_ts, int64_t dv_hs, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  return run_call(kModeFwd | kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts,
+                  q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k,
+                  alibi_slopes, slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, dq, dq_ts, dq_hs, dk, dk_ts, dk_hs, dv,
+                  dv_ts, dv_hs, lse, workspace, workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" attn_status attn_varlen_fwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const int32_t* cu_q, const int32_t* cu_k,
+    const float* alibi_slopes, int64_t slopes_batch_stride, int causal, int window_left,
+    int window_right, float softcap, float scale_multiplier, uint64_t dropout_seed,
+    float dropout_rate, const float* dropout_rates, void* out, int64_t out_ts, int64_t out_hs,
+    float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  return run_call(kModeFwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, nullptr, 0, 0, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, nullptr, 0, 0, nullptr, 0, 0, nullptr,
+                  0, 0, lse, workspace, workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" attn_status attn_varlen_bwd_dropout(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, uint64_t dropout_seed, float dropout_rate,
+    const float* dropout_rates, const void* out, int64_t out_ts, int64_t out_hs,
+    const float* lse, void* dq, int64_t dq_ts, int64_t dq_hs, void* dk, int64_t dk_ts,
+    int64_t dk_hs, void* dv, int64_t dv_ts, int64_t dv_hs, void* workspace,
+    size_t workspace_bytes, int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  return run_call(kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, const_cast<void*>(out), out_ts, out_hs, dq, dq_ts, dq_hs, dk,
+                  dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
+                  workspace_bytes, device_status, stream, dr);
 }

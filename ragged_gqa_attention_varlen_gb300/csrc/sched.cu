@@ -5,6 +5,7 @@
 
 #include "../../include/attn_varlen.h"
 #include "attn_internal.h"
+#include "common.cuh"
 #include "sched.cuh"
 
 namespace attn {
@@ -49,6 +50,14 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
     *p.status = 0;
     for (int i = 0; i < p.ncounters; ++i) p.counters[i] = 0;
   }
+  // per-token dropout thresholds and scales
+  if (p.drop_tab)
+    for (int64_t t = tid; t < p.total_q; t += blockDim.x) {
+      uint32_t T;
+      float sc;
+      drop_params(p.drop_rates[t], T, sc);
+      p.drop_tab[t] = make_uint2(T, __float_as_uint(sc));
+    }
   // The work of a sequence's longest forward/dq tile grows with the keys it
   // visits, of a dk/dv tile with the queries: the whole other length, or
   // under a window bounded on both sides about the window's span.

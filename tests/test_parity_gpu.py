@@ -330,6 +330,71 @@ def test_host_buffers_leave_output_padding_alone():
         assert int(torch.isnan(raw).sum()) == raw.numel() - r[n].numel(), n
 
 
+# ------------------------------------------------------------------ dropout
+# Counter-based dropout: the keep decisions are integer hashes of (seed,
+# sequence, head, row, column) on both sides, so the GPU and the oracle drop
+# the same elements.
+
+DROPOUT = [
+    dict(lq=[70, 300, 1], lk=[90, 260, 40], Hq=16, rate=0.2),
+    dict(lq=[200, 64], lk=[333, 90], Hq=48, dtype=torch.bfloat16, step=2, rate=0.5, causal=True),
+    dict(lq=[150, 20], lk=[140, 300], Hq=12, Hkv=4, rate=None),   # per-token rates
+    dict(lq=[40, 7], lk=[50, 30], Hq=16, rate=0.0),               # keeps everything
+]
+
+
+def _with_dropout(case, seed=4321):
+    case = dict(case)
+    lq, lk, Hq, rate = case.pop("lq"), case.pop("lk"), case.pop("Hq"), case.pop("rate")
+    p = W.custom(lq, lk, Hq, **case)
+    p.dropout_seed = seed
+    if rate is None:
+        g = torch.Generator().manual_seed(3)
+        p.dropout_rates = torch.rand(sum(lq), generator=g) * 0.6
+    else:
+        p.dropout_rate = rate
+    return p
+
+
+def _run_dropout(p, **kw):
+    r = BND.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                  p.causal, p.window_left, p.window_right, p.softcap,
+                                  p.scale_multiplier, dropout_seed=p.dropout_seed,
+                                  dropout_rate=p.dropout_rate, dropout_rates=p.dropout_rates, **kw)
+    torch.cuda.synchronize()
+    assert BND.device_status(r["workspace"]) == 0
+    return r
+
+
+@pytest.mark.parametrize("idx", range(len(DROPOUT)), ids=[f"drop{i}" for i in range(len(DROPOUT))])
+def test_dropout_parity(oracle_mod, idx):
+    p_cpu = _with_dropout(DROPOUT[idx])
+    p = p_cpu.to("cuda")
+    res = _run_dropout(p)
+    check_all(res, oracle_mod.fvjp(p_cpu), p_cpu.dtype)
+    # repeatable, and the split calls regenerate the same keep bits
+    again = _run_dropout(p)
+    mask = (p.causal, p.window_left, p.window_right, p.softcap, p.scale_multiplier)
+    drop = dict(dropout_seed=p.dropout_seed, dropout_rate=p.dropout_rate,
+                dropout_rates=p.dropout_rates)
+    out, lse = BND.attention_varlen_fwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, *mask,
+                                        **drop)
+    dq, dk, dv = BND.attention_varlen_bwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                          out, lse, *mask, **drop)
+    torch.cuda.synchronize()
+    for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert bits_equal(res[n], again[n]), n
+        assert bits_equal(res[n], x), n
+
+
+def test_dropout_seed_changes_the_result():
+    p = _with_dropout(DROPOUT[0]).to("cuda")
+    a = {n: x.clone() for n, x in _run_dropout(p).items() if n != "workspace"}
+    p.dropout_seed = 4322
+    b = _run_dropout(p)
+    assert not bits_equal(a["out"], b["out"]) and bits_equal(a["lse"], b["lse"])
+
+
 # ------------------------------------------- split forward / backward calls
 
 def _split_cases():
