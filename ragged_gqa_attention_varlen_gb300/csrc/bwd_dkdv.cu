@@ -557,6 +557,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
         const int b = gg & 1;
+        // dropout keep bits of this step's 64 columns (query token, head) for
+        // this thread's key, hashed while S^T is computed
+        const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
+        uint64_t kbits = 0;
+        if (DROP) {
+          const int dh0 = p.head0 + (st % ngroups) * G;
+#pragma unroll 4
+          for (int c = 0; c < 64; ++c) {
+            const int lc = half * 64 + c;
+            const int it = dtok0 + (lc >> lgG);
+            bool keep = false;
+            if (it < t.Lq) {
+              uint32_t T;
+              float sc;
+              drop_row(p, static_cast<int64_t>(t.q0) + it, T, sc);
+              keep = drop_keep(dkb, drop_hi(dh0 + (lc & (G - 1)), it), t.key + r, T);
+            }
+            kbits |= static_cast<uint64_t>(keep) << c;
+          }
+        }
         // S^T: read it and release SP for dP^T
         if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
         tc_fence_after();
@@ -591,27 +611,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* pa = reinterpret_cast<const float4*>(cols->a[b] + half * 64);
         const float4* pm = reinterpret_cast<const float4*>(cols->m[b] + half * 64);
         uint32_t pk[32];
-        // dropout: column c (query token, head) of this thread's key; P^T for
-        // dV is P * keep * scale and dS uses keep * scale * dP (keep bits kept)
-        uint64_t kbits = 0;
-        const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
-        const int dh0 = DROP ? p.head0 + (st % ngroups) * G : 0;
-        auto dcol = [&](int c, float& sc) -> bool {
-          const int lc = half * 64 + c;
-          const int it = dtok0 + (lc >> lgG);
-          sc = 0.f;
-          if (it >= t.Lq) return false;
-          uint32_t T;
-          drop_row(p, static_cast<int64_t>(t.q0) + it, T, sc);
-          return drop_keep(dkb, drop_hi(dh0 + (lc & (G - 1)), it), t.key + r, T);
+        // dropout: P^T for dV is P * keep * scale and dS uses keep * scale * dP
+        // (keep bits hashed at the start of the step)
+        auto dscale = [&](int c) -> float {  // the scale of column c (its query token)
+          if (!p.drop_tab) return p.drop_scale;
+          const int it = dtok0 + ((half * 64 + c) >> lgG);
+          return it < t.Lq ? __uint_as_float(__ldg(p.drop_tab + t.q0 + it).y) : 0.f;
         };
         auto pack_p = [&](int c, float a, float bb) -> uint32_t {  // columns c, c + 1
           if (DROP) {
-            float s0, s1;
-            const bool k0 = dcol(c, s0), k1 = dcol(c + 1, s1);
-            kbits |= (static_cast<uint64_t>(k0) << c) | (static_cast<uint64_t>(k1) << (c + 1));
-            a = k0 ? a * s0 : 0.f;
-            bb = k1 ? bb * s1 : 0.f;
+            a = ((kbits >> c) & 1) ? a * dscale(c) : 0.f;
+            bb = ((kbits >> (c + 1)) & 1) ? bb * dscale(c + 1) : 0.f;
           }
           return Pack<BF16>::two(a, bb);
         };
@@ -706,14 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->dp_read);
         if (DROP) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            float sc = p.drop_scale;
-            if (p.drop_tab) {  // per-token rates: the column's own scale
-              const int it = dtok0 + ((half * 64 + c) >> lgG);
-              sc = it < t.Lq ? __uint_as_float(__ldg(p.drop_tab + t.q0 + it).y) : 0.f;
-            }
-            d[c] = ((kbits >> c) & 1) ? d[c] * sc : 0.f;
-          }
+          for (int c = 0; c < 64; ++c) d[c] = ((kbits >> c) & 1) ? d[c] * dscale(c) : 0.f;
         }
         // dS^T = P (1 - tanh^2) (dP - D) = t2 (D - dP), D per group of 4 columns
         if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) break;

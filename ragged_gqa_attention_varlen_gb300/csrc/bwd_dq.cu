@@ -406,6 +406,13 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         const uint32_t gg = g + j;
         const int key0 = (t.kt0 + j) * kKeys + half * 64;
         const float pos0 = static_cast<float>(pos_off - key0);
+        // dropout keep bits of this half's 64 keys, hashed while S is computed
+        uint64_t kbits = 0;
+        if (DROP) {
+#pragma unroll 8
+          for (int c = 0; c < 64; ++c)
+            kbits |= static_cast<uint64_t>(drop_keep(dkb, dhi, key0 + c, dT)) << c;
+        }
         if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
         tc_fence_after();
         float x[64];
@@ -453,12 +460,6 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);  // P (1 - tanh^2)
           }
-        }
-        uint64_t kbits = 0;  // dropout keep bit of each of this half's 64 keys
-        if (DROP) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            kbits |= static_cast<uint64_t>(drop_keep(dkb, dhi, key0 + c, dT)) << c;
         }
         if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
         tc_fence_after();

@@ -421,13 +421,19 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         dhi = drop_hi(p.head0 + h, i_loc);
         if (row_valid) drop_row(p, static_cast<int64_t>(t.q0) + i_loc, dT, dsc);
       }
-      auto dropped = [&](float pv, int j) -> float {
-        return drop_keep(dkb, dhi, j, dT) ? pv * dsc : 0.f;
-      };
+
       for (int jj = 0, kt = t0; jj < n; ++jj, kt = next_key_tile(t, kt)) {
         const uint32_t gg = g + jj;
         const int key0 = kt * kKeys + half * 64;
         const uint32_t sb = tmem + (gg & 1) * 128 + half * 64 + lane_addr;
+        // dropout keep bits of this half's 64 keys, hashed while S is computed
+        uint64_t kbits = 0;
+        if (DROP) {
+#pragma unroll 8
+          for (int c = 0; c < 64; ++c)
+            kbits |= static_cast<uint64_t>(drop_keep(dkb, dhi, key0 + c, dT)) << c;
+        }
+        auto dropped = [&](float pv, int c) -> float { return ((kbits >> c) & 1) ? pv * dsc : 0.f; };
         if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;
         tc_fence_after();
         float x[64];
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
             x[c] = ex2_approx(x[c]);  // the reference is inside the logit
             x[c + 1] = ex2_approx(x[c + 1]);
             if (DROP) {
-              pk[c >> 1] = Pack<BF16>::two(dropped(x[c], key0 + c), dropped(x[c + 1], key0 + c + 1));
+              pk[c >> 1] = Pack<BF16>::two(dropped(x[c], c), dropped(x[c + 1], c + 1));
               lu2 = f2_add(lu2, f2_make(x[c], x[c + 1]));
               continue;
             }
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           l += x[c] + x[c + 1];
-          pk[c >> 1] = DROP ? Pack<BF16>::two(dropped(x[c], key0 + c), dropped(x[c + 1], key0 + c + 1))
+          pk[c >> 1] = DROP ? Pack<BF16>::two(dropped(x[c], c), dropped(x[c + 1], c + 1))
                             : Pack<BF16>::two(x[c], x[c + 1]);
         }
         // this half's 64 keys -> 32 pair columns of the P region
