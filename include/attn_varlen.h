@@ -305,6 +305,15 @@ attn_status attn_varlen_fvjp_fwd_bwd_host(
     float *lse, void *device_buffer, size_t device_buffer_bytes, int chunks,
     int32_t *host_status, void *stream);
 
+/* The chunking attn_varlen_fvjp_fwd_bwd_host uses: writes the sequence
+ * boundaries 0 = cuts[0] < cuts[1] < ... < cuts[n] = B of n <= chunks runs of
+ * whole sequences (HOST cu arrays; sequence b weighs Lq*Lk + 1, and run c
+ * ends at the first sequence where the running weight reaches c/chunks of the
+ * total) and returns n (0 for invalid arguments; 1 when B = 0, with
+ * cuts = {0, 0}).  `cuts` holds chunks + 1 entries. */
+int attn_varlen_host_chunks(int B, const int32_t *cu_q, const int32_t *cu_k, int chunks,
+                            int32_t *cuts);
+
 /* Bytes of device buffer attn_varlen_fvjp_fwd_bwd_host needs. */
 size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim, int64_t total_q,
                                           int64_t total_k, int chunks);

@@ -25,7 +25,7 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
            "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
            "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_fwd_bwd_dropout",
-           "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout")
+           "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH):
     lib.attn_varlen_fvjp_fwd_bwd_host.restype = I
     lib.attn_varlen_fvjp_host_buffer_size.argtypes = [I, I, I, I, L, L, I]
     lib.attn_varlen_fvjp_host_buffer_size.restype = ctypes.c_size_t
+    lib.attn_varlen_host_chunks.argtypes = [I, P, P, I, P]
+    lib.attn_varlen_host_chunks.restype = I
     DR = [ctypes.c_uint64, F, P]  # dropout seed, rate, per-token rates
     lib.attn_varlen_fvjp_fwd_bwd_dropout.argtypes = (
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
@@ -350,6 +352,15 @@ def _check_lse(lse, Tq, Hq):
 def host_buffer_size(B: int, Hq: int, Hkv: int, d: int, total_q: int, total_k: int,
                      chunks: int) -> int:
     return int(load().attn_varlen_fvjp_host_buffer_size(B, Hq, Hkv, d, total_q, total_k, chunks))
+
+
+def host_chunks(cu_q, cu_k, chunks: int):
+    """Sequence boundaries of the host-buffer entry point's chunks (host int32
+    cu tensors)."""
+    B = cu_q.numel() - 1
+    cuts = torch.zeros(chunks + 1, dtype=torch.int32)
+    n = load().attn_varlen_host_chunks(B, _ptr(cu_q), _ptr(cu_k), chunks, _ptr(cuts))
+    return cuts[:n + 1].tolist()
 
 
 def _check_host(name, t, dtype, H):

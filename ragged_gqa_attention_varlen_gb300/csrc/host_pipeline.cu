@@ -112,6 +112,24 @@ struct Resources {
 
 }  // namespace
 
+extern "C" int attn_varlen_host_chunks(int B, const int32_t* cu_q, const int32_t* cu_k,
+                                       int chunks, int32_t* cuts) {
+  if (B < 0 || chunks < 1 || !cuts || (B > 0 && (!cu_q || !cu_k))) return 0;
+  // each sequence weighs Lq*Lk + 1, so empty ones still spread over the chunks
+  double total = 0;
+  for (int b = 0; b < B; ++b)
+    total += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
+  int n = 0;
+  cuts[0] = 0;
+  double acc = 0;
+  for (int b = 0; b < B; ++b) {
+    acc += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
+    if (n + 1 < chunks && b + 1 < B && acc >= total * (n + 1) / chunks) cuts[++n] = b + 1;
+  }
+  cuts[++n] = B;
+  return n;
+}
+
 extern "C" size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim,
                                                      int64_t total_q, int64_t total_k,
                                                      int chunks) {
@@ -161,20 +179,8 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
     return ATTN_ERR_WORKSPACE;
 
   // ---- chunks: runs of whole sequences of about equal sum Lq*Lk
-  std::vector<int> cut(1, 0);  // sequence boundaries
-  {
-    double total = 0;
-    for (int b = 0; b < B; ++b)
-      total += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
-    double acc = 0;
-    for (int b = 0; b < B; ++b) {
-      acc += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
-      const int c = static_cast<int>(cut.size());
-      if (c < chunks && b + 1 < B && acc >= total * c / chunks) cut.push_back(b + 1);
-    }
-    cut.push_back(B);
-  }
-  const int nc = static_cast<int>(cut.size()) - 1;
+  std::vector<int> cut(static_cast<size_t>(chunks) + 1);
+  const int nc = attn_varlen_host_chunks(B, cu_q, cu_k, chunks, cut.data());
   // rebased cu arrays of every chunk: chunk c's cu_q at [cut[c] + c], its cu_k
   // B + chunks entries later
   std::vector<int32_t> cus(2 * static_cast<size_t>(B + chunks), 0);

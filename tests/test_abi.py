@@ -138,3 +138,29 @@ def test_host_entry_point_validates_before_touching_the_device(lib):
     need = lib.attn_varlen_fvjp_host_buffer_size(2, 16, 1, 160, 9, 12, 2)
     assert need > lib.attn_varlen_fvjp_workspace_size(2, 16, 9, 12)
     assert call(buf=0x100000, bufb=need - 1) == -4
+
+
+def test_host_chunks_cut_whole_sequences_of_balanced_work(lib):
+    """The host-buffer entry point's chunking: strictly increasing sequence
+    boundaries from 0 to B, at most `chunks` runs, and every run's weight
+    (sum of Lq*Lk + 1) within one sequence's weight of an equal share."""
+    import torch
+
+    from ragged_gqa_attention_varlen_gb300 import binding
+
+    g = torch.Generator().manual_seed(1)
+    for trial in range(200):
+        B = int(torch.randint(0, 40, (1,), generator=g))
+        lq = torch.randint(0, 500, (B,), generator=g)
+        lk = torch.randint(0, 500, (B,), generator=g)
+        cu_q = torch.cat([torch.zeros(1, dtype=torch.int64), lq.cumsum(0)]).to(torch.int32)
+        cu_k = torch.cat([torch.zeros(1, dtype=torch.int64), lk.cumsum(0)]).to(torch.int32)
+        chunks = int(torch.randint(1, 9, (1,), generator=g))
+        cuts = binding.host_chunks(cu_q, cu_k, chunks)
+        assert cuts[0] == 0 and cuts[-1] == B
+        assert 1 <= len(cuts) - 1 <= max(1, min(chunks, B))
+        assert all(a < b for a, b in zip(cuts, cuts[1:])) or B == 0
+        w = (lq * lk + 1).double()
+        share, wmax = float(w.sum()) / chunks, float(w.max()) if B else 0.0
+        for a, b in zip(cuts, cuts[1:]):
+            assert float(w[a:b].sum()) <= share + wmax + 1e-6
