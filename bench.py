@@ -9,7 +9,13 @@ forward and 10 Lq Lk d backward flops per head (TFLOP/s); latency is
 ms_per_step.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
-on a bounded sample of the same workload instead.
+on a bounded sample of the same workload instead.  The end-to-end leg runs
+the same call through the host-buffer entry point (``--e2e-chunks``).
+
+Variants of the workload (each a separate line, named in config.workload):
+``--causal`` / ``--window-left`` / ``--window-right`` (flops counted over the
+admissible pairs only), ``--hkv`` (K/V heads), ``--head-dim`` (128 or 64),
+``--dropout RATE``, ``--length-scale`` (small cases for profiling).
 """
 from __future__ import annotations
 
