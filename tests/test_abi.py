@@ -164,3 +164,41 @@ def test_host_chunks_cut_whole_sequences_of_balanced_work(lib):
         share, wmax = float(w.sum()) / chunks, float(w.max()) if B else 0.0
         for a, b in zip(cuts, cuts[1:]):
             assert float(w[a:b].sum()) <= share + wmax + 1e-6
+
+
+def test_python_entry_points_refuse_host_tensors(lib):
+    """There is no CPU fallback: the device entry points reject host tensors
+    before calling the library (and the library needs a GPU to compute)."""
+    import torch
+
+    from ragged_gqa_attention_varlen_gb300 import binding, workloads
+
+    p = workloads.tiny()
+    for fn, args in (
+            (binding.attention_varlen_fvjp, (p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout)),
+            (binding.attention_varlen_fwd, (p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes)),
+            (binding.attention_varlen_bwd, (p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                            p.q, torch.zeros(p.q.shape[:2])))):
+        try:
+            fn(*args)
+        except ValueError as e:
+            assert "CUDA" in str(e)
+        else:
+            raise AssertionError(f"{fn.__name__} accepted host tensors")
+
+
+def test_python_host_entry_point_rejects_device_layout_errors(lib):
+    """The host-buffer wrapper checks its tensors on the host side too."""
+    import pytest
+    import torch
+
+    from ragged_gqa_attention_varlen_gb300 import binding, workloads
+
+    p = workloads.tiny()
+    with pytest.raises(ValueError):  # cu arrays must be int32
+        binding.attention_varlen_fvjp_host(p.q, p.k, p.v, p.cu_q.long(), p.cu_k, p.alibi_slopes,
+                                           p.dout)
+    with pytest.raises(ValueError):  # 7 query heads over 2 K/V heads
+        q = torch.zeros((p.q.shape[0], 7, 160), dtype=p.q.dtype)
+        k = torch.zeros((p.k.shape[0], 2, 160), dtype=p.q.dtype)
+        binding.attention_varlen_fvjp_host(q, k, k, p.cu_q, p.cu_k, None, q)
