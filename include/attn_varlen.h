@@ -46,8 +46,10 @@
  * with the given batch stride and head stride 1, or NULL for no ALiBi.
  *
  * Ownership and execution.  Every pointer argument except the scalar
- * arguments is a DEVICE pointer owned by the caller; the library allocates
- * nothing and keeps no pointer after the call returns.  The call validates
+ * arguments is a DEVICE pointer owned by the caller (the host-buffer entry
+ * point below takes host pointers instead, and creates two streams and a few
+ * events per call); the library allocates no memory and keeps no pointer
+ * after the call returns.  The call validates
  * its arguments on the host, enqueues its kernels on `stream` and returns
  * without synchronising.  Inputs are read-only; out, dq, dk, dv and lse are
  * fully overwritten (dk/dv rows of keys that no query attends get 0).  For a
