@@ -154,7 +154,7 @@ def test_alibi_distance_tables(oracle_mod, shape):
 
 
 def test_alibi_equal_lengths_is_abs_i_minus_j(oracle_mod):
-    """North-star identity: Lq = Lk makes the distance |i - j|."""
+    """Equal lengths: Lq = Lk makes the distance |i - j|."""
     L = 7
     p = f64_problem([L], [L], Hq=1, seed=2)
     p.q.zero_()
