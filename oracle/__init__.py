@@ -46,8 +46,8 @@ def _load():
         P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         U64, F32 = ctypes.c_uint64, ctypes.c_float
         common = ([I, I, I, I, I, P, L, L, P, L, L, P, L, L, P, L, L, P, P, P, L, I, I, I, D, D] +
-                  [I, U64, F32, P])
-        lib.oracle_fvjp.argtypes = common + [P] + [P] * 8 + [I]
+                  [I, U64, F32, P] + [I, P, L, L, P, L, L])
+        lib.oracle_fvjp.argtypes = common + [P] + [P] * 10 + [I]
         lib.oracle_fvjp.restype = I
         lib.oracle_rows.argtypes = common + [I, P, P, P, P, P, P, I]
         lib.oracle_rows.restype = I
@@ -84,7 +84,13 @@ def _args(p):
     if rates is not None:
         rates = rates.float().cpu().contiguous()
         assert rates.shape == (p.q.shape[0],)
-    keep = (q, k, v, do, cu_q, cu_k, slopes, rates)
+    qg, kg = getattr(p, "q_gate", None), getattr(p, "k_gate", None)
+    R = 0
+    if qg is not None:
+        qg, kg = _raw(qg), _raw(kg)
+        R = qg.shape[-1]
+        assert kg.shape[-1] == R and qg.stride(-1) == 1 and kg.stride(-1) == 1
+    keep = (q, k, v, do, cu_q, cu_k, slopes, rates, qg, kg)
     Hkv = p.k.shape[1]
     assert v.shape[1] == Hkv and p.Hq % Hkv == 0
     args = [DTYPE_CODE[p.q.dtype], p.B, p.Hq, Hkv, p.q.shape[-1],
@@ -97,7 +103,9 @@ def _args(p):
             int(bool(p.causal)), int(p.window_left), int(p.window_right),
             float(p.softcap), float(p.scale_multiplier),
             int(seed is not None), int(seed or 0) & 0xFFFFFFFFFFFFFFFF,
-            float(getattr(p, "dropout_rate", 0.0)), rates.data_ptr() if rates is not None else None]
+            float(getattr(p, "dropout_rate", 0.0)), rates.data_ptr() if rates is not None else None,
+            R, qg.data_ptr() if R else None, qg.stride(0) if R else 0, qg.stride(1) if R else 0,
+            kg.data_ptr() if R else None, kg.stride(0) if R else 0, kg.stride(1) if R else 0]
     return args, keep
 
 
@@ -122,6 +130,10 @@ def fvjp(p, seq_sel=None, nthreads: int = 0, diagnostics: bool = False) -> dict:
     if diagnostics:
         res["dz_rowsum"] = torch.full((Tq, H), float("nan"), **f64)
         res["p_rowsum"] = torch.full((Tq, H), float("nan"), **f64)
+    if getattr(p, "q_gate", None) is not None:
+        R = p.q_gate.shape[-1]
+        res["dq_gate"] = torch.full((Tq, H, R), float("nan"), **f64)
+        res["dk_gate"] = torch.full((Tk, Hkv, R), float("nan"), **f64)
     sel = None
     if seq_sel is not None:
         mask = np.zeros(p.B, dtype=np.uint8)
@@ -130,14 +142,18 @@ def fvjp(p, seq_sel=None, nthreads: int = 0, diagnostics: bool = False) -> dict:
     ptr = lambda name: res[name].data_ptr() if name in res else None
     nt = lib.oracle_fvjp(*args, sel.data_ptr() if sel is not None else None,
                          ptr("out"), ptr("lse"), ptr("dq"), ptr("dk"), ptr("dv"), ptr("D"),
-                         ptr("dz_rowsum"), ptr("p_rowsum"), int(nthreads))
+                         ptr("dz_rowsum"), ptr("p_rowsum"), ptr("dq_gate"), ptr("dk_gate"),
+                         int(nthreads))
     del keep
     res["threads"] = nt
     return res
 
 
 def rows(p, tok, head, nthreads: int = 0) -> dict:
-    """out, lse, D and dq of the sampled packed rows (tok[r], head[r])."""
+    """out, lse, D and dq of the sampled packed rows (tok[r], head[r])
+    (ungated problems)."""
+    if getattr(p, "q_gate", None) is not None:
+        raise NotImplementedError("the row sampler serves ungated problems")
     lib = _load()
     args, keep = _args(p)
     tok = torch.as_tensor(tok, dtype=torch.int64).contiguous()

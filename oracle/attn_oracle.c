@@ -47,6 +47,16 @@
  *   dZ_ij  = P_ij (keep_ij scale dP_ij - D_i),  dv_j += P_ij keep_ij scale dO_i
  *   (D_i = dO_i . out_i of the dropped out, as above).
  *
+ * Gate (optional; "b300-attention-engine", "Why it is hard": each
+ * query-key pair also gets a sigmoid gate from separate low-dimensional
+ * projections that scales the softmax weight after normalisation):
+ *   G_ij = 1 / (1 + exp(-qg_i . kg_j,g(h) / sqrt(R)))    (qg, kg of width R)
+ *   out_i = sum_j P_ij G_ij (keep scale)_ij v_j
+ *   dW_ij = dO_i . v_j;  dZ_ij = P_ij (G_ij (keep scale)_ij dW_ij - D_i)
+ *   dg_ij = dW_ij P_ij (keep scale)_ij G_ij (1 - G_ij)
+ *   dqg_i = sum_j dg_ij kg_j / sqrt(R);  dkg_j = sum_h sum_i dg_ij qg_i / sqrt(R)
+ *   dv_j += P_ij G_ij (keep scale)_ij dO_i;  D_i = dO_i . out_i as before.
+ *
  * Rows with no admissible key ("ragged flash attention gradient recompute",
  * "Root causes addressed", empty rows) have lse = -inf, out = 0, and add
  * nothing to any gradient.
@@ -117,6 +127,11 @@ typedef struct {
   uint64_t seed;
   float rate;                /* used when rates is NULL */
   const float *rates;        /* per query token [total_q], or NULL */
+  int R;                     /* gate width; 0: no gate */
+  const void *qg;            /* [T_q][Hq][R] with strides */
+  int64_t qg_ts, qg_hs;
+  const void *kg;            /* [T_k][Hkv][R] with strides */
+  int64_t kg_ts, kg_hs;
 } problem;
 
 /* ---- counter-based dropout ------------------------------------------- */
@@ -176,6 +191,7 @@ typedef struct {
   double *Q;          /* [Lq][Hq][d] */
   double *dO;         /* [Lq][Hq][d] */
   double *K, *V;      /* [Lk][Hkv][d] */
+  double *Qg, *Kg;    /* [Lq][Hq][R], [Lk][Hkv][R] (NULL without a gate) */
 } seqdata;
 
 /* The K/V head that query head h reads. */
@@ -213,6 +229,34 @@ static void seq_load(const problem *p, int b, seqdata *s) {
         s->K[at] = decode(p, p->k, t * p->k_ts + g * p->k_hs + f);
         s->V[at] = decode(p, p->v, t * p->v_ts + g * p->v_hs + f);
       }
+  s->Qg = s->Kg = NULL;
+  if (p->R > 0) {
+    const int R = p->R;
+    s->Qg = malloc(sizeof(double) * ((size_t)s->Lq * H * R + 1));
+    s->Kg = malloc(sizeof(double) * ((size_t)s->Lk * p->Hkv * R + 1));
+    for (int i = 0; i < s->Lq; i++)
+      for (int h = 0; h < H; h++)
+        for (int f = 0; f < R; f++)
+          s->Qg[((size_t)i * H + h) * R + f] =
+              decode(p, p->qg, (s->q0 + i) * p->qg_ts + h * p->qg_hs + f);
+    for (int j = 0; j < s->Lk; j++)
+      for (int g = 0; g < p->Hkv; g++)
+        for (int f = 0; f < R; f++)
+          s->Kg[((size_t)j * p->Hkv + g) * R + f] =
+              decode(p, p->kg, (s->k0 + j) * p->kg_ts + g * p->kg_hs + f);
+  }
+}
+
+/* The gate of query row (i, h) and key j of K/V head kh (1 without a gate). */
+static double gate_of(const seqdata *s, int h, int i, int j, int kh) {
+  const problem *p = s->p;
+  if (p->R == 0) return 1.0;
+  const double *qg = s->Qg + ((size_t)i * p->Hq + h) * p->R;
+  const double *kg = s->Kg + ((size_t)j * p->Hkv + kh) * p->R;
+  double g = 0.0;
+  for (int f = 0; f < p->R; f++) g += qg[f] * kg[f];
+  g /= sqrt((double)p->R);
+  return 1.0 / (1.0 + exp(-g));
 }
 
 static void seq_free(seqdata *s) {
@@ -220,6 +264,8 @@ static void seq_free(seqdata *s) {
   free(s->dO);
   free(s->K);
   free(s->V);
+  free(s->Qg);
+  free(s->Kg);
 }
 
 static int admissible(const problem *p, int Lq, int Lk, int i, int j) {
@@ -264,6 +310,7 @@ typedef struct {
   double *out, *lse, *dq, *Dpre; /* out/dq [T_q][Hq][d]; lse/Dpre [T_q][Hq] */
   double *dz_rowsum, *p_rowsum;  /* optional [T_q][Hq] */
   double *dk, *dv;               /* [T_k][Hkv][d] */
+  double *dqg, *dkg;             /* [T_q][Hq][R], [T_k][Hkv][R] with a gate */
 } outputs;
 
 /* Where one query row's results go. */
@@ -271,6 +318,7 @@ typedef struct {
   double *out, *dq; /* [d] each */
   double *lse, *D;
   double *dz_sum, *p_sum; /* optional */
+  double *dqg;            /* [R] with a gate, else NULL */
 } rowdest;
 
 /* One query row (i, h) of sequence s, whose decoded q and dO rows are qi and
@@ -291,6 +339,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
     o->out[f] = 0.0;
     o->dq[f] = 0.0;
   }
+  for (int f = 0; o->dqg && f < p->R; f++) o->dqg[f] = 0.0;
   if (m == -INFINITY) { /* empty row */
     *o->lse = -INFINITY;
     *o->D = 0.0;
@@ -309,7 +358,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   }
   const int64_t token = s->q0 + i;
   for (int j = 0; j < Lk; j++) {
-    const double pd = P[j] * drop_factor(p, s->b, h, token, i, j);
+    const double pd = P[j] * gate_of(s, h, i, j, kh) * drop_factor(p, s->b, h, token, i, j);
     for (int f = 0; f < d; f++) o->out[f] += pd * kv_row(s, s->V, j, kh)[f];
   }
   double D = 0.0;
@@ -320,10 +369,17 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   for (int j = 0; j < Lk; j++) {
     double dp = 0.0;
     for (int f = 0; f < d; f++) dp += dOi[f] * kv_row(s, s->V, j, kh)[f];
-    double dz = P[j] * (drop_factor(p, s->b, h, token, i, j) * dp - D);
+    const double fd = drop_factor(p, s->b, h, token, i, j);
+    const double G = gate_of(s, h, i, j, kh);
+    double dz = P[j] * (G * fd * dp - D);
     dzsum += dz;
     double ds = dz * gv[j];
     for (int f = 0; f < d; f++) o->dq[f] += sigma * ds * kv_row(s, s->K, j, kh)[f];
+    if (o->dqg) {
+      const double dg = dp * P[j] * fd * G * (1.0 - G) / sqrt((double)p->R);
+      const double *kg = s->Kg + ((size_t)j * p->Hkv + kh) * p->R;
+      for (int f = 0; f < p->R; f++) o->dqg[f] += dg * kg[f];
+    }
   }
   if (o->dz_sum) *o->dz_sum = dzsum;
   if (o->p_sum) *o->p_sum = psum;
@@ -337,7 +393,8 @@ static void row_pass_packed(const seqdata *s, int h, int i, const outputs *o, do
   int64_t rowid = (s->q0 + i) * (int64_t)H + h;
   rowdest r = {o->out + rowid * d, o->dq + rowid * d, o->lse + rowid, o->Dpre + rowid,
                o->dz_rowsum ? o->dz_rowsum + rowid : NULL,
-               o->p_rowsum ? o->p_rowsum + rowid : NULL};
+               o->p_rowsum ? o->p_rowsum + rowid : NULL,
+               o->dqg ? o->dqg + rowid * s->p->R : NULL};
   const double *qi = s->Q + ((size_t)i * H + h) * d;
   const double *dOi = s->dO + ((size_t)i * H + h) * d;
   row_pass(s, h, i, qi, dOi, &r, z, P, gv);
@@ -358,6 +415,8 @@ static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
     dvrow[f] = 0.0;
   }
   const double *vj = kv_row(s, s->V, j, kh);
+  double *dkgrow = o->dkg ? o->dkg + ((s->k0 + j) * (int64_t)p->Hkv + kh) * p->R : NULL;
+  for (int f = 0; dkgrow && f < p->R; f++) dkgrow[f] = 0.0;
   for (int h = kh * R; h < (kh + 1) * R; h++) {
     double slope = slope_of(p, s->b, h);
     for (int i = 0; i < s->Lq; i++) {
@@ -373,10 +432,16 @@ static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
       double dp = 0.0;
       for (int f = 0; f < d; f++) dp += dOi[f] * vj[f];
       const double fd = drop_factor(p, s->b, h, s->q0 + i, i, j);
-      double ds = P * (fd * dp - o->Dpre[rowid]) * g;
+      const double G = gate_of(s, h, i, j, kh);
+      double ds = P * (G * fd * dp - o->Dpre[rowid]) * g;
       for (int f = 0; f < d; f++) {
-        dvrow[f] += P * fd * dOi[f];
+        dvrow[f] += P * G * fd * dOi[f];
         dkrow[f] += ds * qi[f];
+      }
+      if (dkgrow) {
+        const double dg = dp * P * fd * G * (1.0 - G) / sqrt((double)p->R);
+        const double *qg = s->Qg + ((size_t)i * H + h) * p->R;
+        for (int f = 0; f < p->R; f++) dkgrow[f] += dg * qg[f];
       }
     }
   }
@@ -455,15 +520,18 @@ int oracle_fvjp(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
                 int wr, double softcap, double scale_multiplier, int dropout, uint64_t seed,
-                float rate, const float *rates, const uint8_t *seq_sel,
-                double *out, double *lse, double *dq, double *dk, double *dv, double *Dpre,
-                double *dz_rowsum, double *p_rowsum, int nthreads) {
+                float rate, const float *rates, int R, const void *qg, int64_t qg_ts,
+                int64_t qg_hs, const void *kg, int64_t kg_ts, int64_t kg_hs,
+                const uint8_t *seq_sel, double *out, double *lse, double *dq, double *dk,
+                double *dv, double *Dpre, double *dz_rowsum, double *p_rowsum, double *dqg,
+                double *dkg, int nthreads) {
   if (Hkv < 1 || Hq % Hkv) return 0;
   problem p = {dtype, B,     Hq,    Hkv,  d,     q,  q_ts,  q_hs,    k,
                k_ts,  k_hs,  v,     v_ts, v_hs,  dout, do_ts, do_hs,  cu_q,
                cu_k,  slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier,
-               dropout, seed, rate, rates};
-  outputs o = {out, lse, dq, Dpre, dz_rowsum, p_rowsum, dk, dv};
+               dropout, seed, rate, rates, R, qg, qg_ts, qg_hs, kg, kg_ts, kg_hs};
+  if (R < 0 || (R > 0 && (!qg || !kg || !dqg || !dkg))) return 0;
+  outputs o = {out, lse, dq, Dpre, dz_rowsum, p_rowsum, dk, dv, dqg, dkg};
   int nt = thread_count(nthreads);
   seqdata *seqs = calloc((size_t)B + 1, sizeof(seqdata));
   int n1 = 0, n2 = 0;
@@ -555,6 +623,7 @@ static void *row_worker(void *arg) {
     s.Lq = p->cu_q[b + 1] - p->cu_q[b];
     s.Lk = p->cu_k[b + 1] - p->cu_k[b];
     s.Q = s.dO = NULL;
+    s.Qg = s.Kg = NULL;
     int i = (int)(t - s.q0);
     double *qi = malloc(sizeof(double) * d);
     double *dOi = malloc(sizeof(double) * d);
@@ -573,7 +642,7 @@ static void *row_worker(void *arg) {
           s.V[at] = decode(p, p->v, tk * p->v_ts + g * p->v_hs + f);
         }
     rowdest o = {w->out_r + (int64_t)r * d, w->dq_r + (int64_t)r * d, w->lse_r + r, w->D_r + r,
-                 NULL, NULL};
+                 NULL, NULL, NULL};
     int Lk1 = s.Lk > 0 ? s.Lk : 1;
     double *z = malloc(sizeof(double) * Lk1), *P = malloc(sizeof(double) * Lk1);
     double *g = malloc(sizeof(double) * Lk1);
@@ -596,14 +665,17 @@ int oracle_rows(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
                 const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
                 const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
                 int wr, double softcap, double scale_multiplier, int dropout, uint64_t seed,
-                float rate, const float *rates, int n, const int64_t *tok,
+                float rate, const float *rates, int R, const void *qg, int64_t qg_ts,
+                int64_t qg_hs, const void *kg, int64_t kg_ts, int64_t kg_hs, int n,
+                const int64_t *tok,
                 const int32_t *head, double *out_r, double *lse_r, double *dq_r, double *D_r,
                 int nthreads) {
   if (Hkv < 1 || Hq % Hkv) return 0;
   problem p = {dtype, B,     Hq,    Hkv,  d,     q,  q_ts,  q_hs,    k,
                k_ts,  k_hs,  v,     v_ts, v_hs,  dout, do_ts, do_hs,  cu_q,
                cu_k,  slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier,
-               dropout, seed, rate, rates};
+               dropout, seed, rate, rates, R, qg, qg_ts, qg_hs, kg, kg_ts, kg_hs};
+  if (R != 0) return 0; /* the row sampler serves the ungated path */
   rowpool w;
   w.p = &p;
   w.n = n;

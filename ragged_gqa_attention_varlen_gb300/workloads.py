@@ -49,6 +49,9 @@ class Problem:
     dropout_seed: Optional[int] = None
     dropout_rate: float = 0.0
     dropout_rates: Optional[torch.Tensor] = None
+    # sigmoid gate projections (the gated variant): [T_q, Hq, R], [T_k, Hkv, R]
+    q_gate: Optional[torch.Tensor] = None
+    k_gate: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
 
     @property

@@ -516,3 +516,82 @@ def test_dropout_per_token_rates(oracle_mod):
     ra, rb = oracle_mod.fvjp(p), oracle_mod.fvjp(p2)
     for n in ("out", "dq", "dk", "dv"):
         assert torch.equal(ra[n], rb[n]), n
+
+
+# ------------------------------------------------------- gated variant (f4)
+
+def _gated_problem(lq, lk, Hq, Hkv, R, seed, **mask):
+    p = f64_problem(lq, lk, Hq=Hq, seed=seed, qk_std=1.5, Hkv=Hkv, **mask)
+    g = torch.Generator().manual_seed(seed + 100)
+    p.q_gate = torch.randn((sum(lq), Hq, R), generator=g, dtype=torch.float64)
+    p.k_gate = torch.randn((sum(lk), Hkv, R), generator=g, dtype=torch.float64)
+    return p
+
+
+def _gated_reference(p):
+    """torch fp64 autograd of the gated definition: out = (softmax(z) * G) v
+    with z = softcap(sigma q.k) - ALiBi (masked), G = sigmoid(qg.kg / sqrt(R)),
+    K/V and gate-key heads shared by consecutive query heads."""
+    Hkv, R = p.k.shape[1], p.q_gate.shape[-1]
+    rep = p.Hq // Hkv
+    sm = p.scale_multiplier / math.sqrt(p.q.shape[-1])
+    res = {n: [] for n in ("out", "dq", "dk", "dv", "dq_gate", "dk_gate")}
+    for b in range(p.B):
+        q0, q1 = int(p.cu_q[b]), int(p.cu_q[b + 1])
+        k0, k1 = int(p.cu_k[b]), int(p.cu_k[b + 1])
+        Lq, Lk = q1 - q0, k1 - k0
+        q = p.q[q0:q1].permute(1, 0, 2).clone().requires_grad_(True)
+        k = p.k[k0:k1].permute(1, 0, 2).clone().requires_grad_(True)
+        v = p.v[k0:k1].permute(1, 0, 2).clone().requires_grad_(True)
+        qg = p.q_gate[q0:q1].permute(1, 0, 2).clone().requires_grad_(True)
+        kg = p.k_gate[k0:k1].permute(1, 0, 2).clone().requires_grad_(True)
+        do = p.dout[q0:q1].permute(1, 0, 2)
+        kk, vv, kkg = (x.repeat_interleave(rep, dim=0) for x in (k, v, kg))
+        t = p.softcap * torch.tanh(sm * q @ kk.transpose(1, 2) / p.softcap)
+        i = torch.arange(Lq, dtype=torch.float64)[:, None]
+        j = torch.arange(Lk, dtype=torch.float64)[None, :]
+        z = t - p.alibi_slopes[b][:, None, None] * (i + Lk - Lq - j).abs()
+        k0_ = i + Lk - Lq
+        ok = torch.ones(Lq, Lk, dtype=torch.bool)
+        wr = 0 if p.causal else p.window_right
+        if p.window_left >= 0:
+            ok &= j >= k0_ - p.window_left
+        if wr >= 0:
+            ok &= j <= k0_ + wr
+        z = z.masked_fill(~ok, -math.inf)
+        P = torch.softmax(z, dim=-1).nan_to_num(0.0)
+        G = torch.sigmoid(qg @ kkg.transpose(1, 2) / math.sqrt(R))
+        o = (P * G) @ vv
+        grads = torch.autograd.grad(o, (q, k, v, qg, kg), do)
+        res["out"].append(o.detach().permute(1, 0, 2))
+        for n, gr in zip(("dq", "dk", "dv", "dq_gate", "dk_gate"), grads):
+            res[n].append(gr.permute(1, 0, 2))
+    return {n: torch.cat(x) for n, x in res.items()}
+
+
+@pytest.mark.parametrize("Hq,Hkv,R,mask", [(4, 1, 8, dict()), (6, 2, 4, dict(causal=True)),
+                                           (4, 4, 16, dict(window_left=2, window_right=1))])
+def test_gated_forward_and_five_gradients_match_autograd(oracle_mod, Hq, Hkv, R, mask):
+    p = _gated_problem([5, 8, 1], [6, 3, 4], Hq, Hkv, R, seed=31, **mask)
+    r = oracle_mod.fvjp(p, diagnostics=True)
+    ref = _gated_reference(p)
+    tol = dict(rtol=1e-10, atol=1e-12)
+    for n in ("out", "dq", "dk", "dv", "dq_gate", "dk_gate"):
+        torch.testing.assert_close(r[n], ref[n], **tol, msg=n)
+    # the softmax-input gradient still sums to zero over each row
+    assert float(r["dz_rowsum"].abs().max()) < 1e-12
+
+
+def test_constant_gate_halves_the_ungated_results(oracle_mod):
+    """qg = 0 makes every gate sigmoid(0) = 1/2: out and dq, dk, dv are half
+    the ungated ones, and nothing reaches the gate keys."""
+    p = _gated_problem([4, 6], [5, 3], 4, 2, 8, seed=5)
+    p.q_gate.zero_()
+    r = oracle_mod.fvjp(p)
+    p0 = _gated_problem([4, 6], [5, 3], 4, 2, 8, seed=5)
+    p0.q_gate = p0.k_gate = None
+    r0 = oracle_mod.fvjp(p0)
+    for n in ("out", "dq", "dk", "dv"):
+        torch.testing.assert_close(r[n], 0.5 * r0[n], rtol=1e-13, atol=1e-15, msg=n)
+    assert torch.equal(r["dk_gate"], torch.zeros_like(r["dk_gate"]))
+    assert torch.equal(r["lse"], r0["lse"])
