@@ -47,7 +47,7 @@
  *   dZ_ij  = P_ij (keep_ij scale dP_ij - D_i),  dv_j += P_ij keep_ij scale dO_i
  *   (D_i = dO_i . out_i of the dropped out, as above).
  *
- * Gate (optional; "b300-attention-engine", "Why it is hard": each
+ * Gate (optional; "Pairwise-Gated Attention Engine", "Why it is hard": each
  * query-key pair also gets a sigmoid gate from separate low-dimensional
  * projections that scales the softmax weight after normalisation):
  *   G_ij = 1 / (1 + exp(-qg_i . kg_j,g(h) / sqrt(R)))    (qg, kg of width R)
