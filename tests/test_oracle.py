@@ -520,6 +520,9 @@ def test_dropout_per_token_rates(oracle_mod):
 
 # ------------------------------------------------------- gated variant (f4)
 
+import oracle as _oracle  # noqa: E402  (the helper below needs its keep factors)
+
+
 def _gated_problem(lq, lk, Hq, Hkv, R, seed, **mask):
     p = f64_problem(lq, lk, Hq=Hq, seed=seed, qk_std=1.5, Hkv=Hkv, **mask)
     g = torch.Generator().manual_seed(seed + 100)
@@ -561,6 +564,11 @@ def _gated_reference(p):
         z = z.masked_fill(~ok, -math.inf)
         P = torch.softmax(z, dim=-1).nan_to_num(0.0)
         G = torch.sigmoid(qg @ kkg.transpose(1, 2) / math.sqrt(R))
+        if p.dropout_seed is not None:  # the oracle's own keep factors, as an explicit mask
+            G = G * torch.tensor(
+                [[[_oracle.drop_factor(p.dropout_seed, p.dropout_rate, b, h, ii, jj)
+                   for jj in range(Lk)] for ii in range(Lq)] for h in range(p.Hq)],
+                dtype=torch.float64)
         o = (P * G) @ vv
         grads = torch.autograd.grad(o, (q, k, v, qg, kg), do)
         res["out"].append(o.detach().permute(1, 0, 2))
@@ -580,6 +588,16 @@ def test_gated_forward_and_five_gradients_match_autograd(oracle_mod, Hq, Hkv, R,
         torch.testing.assert_close(r[n], ref[n], **tol, msg=n)
     # the softmax-input gradient still sums to zero over each row
     assert float(r["dz_rowsum"].abs().max()) < 1e-12
+
+
+def test_gate_with_dropout_matches_autograd(oracle_mod):
+    """Gate and dropout compose: out = (P * G * keep * scale) v."""
+    p = _gated_problem([6, 4], [5, 7], 4, 2, 8, seed=17, causal=True)
+    p.dropout_seed, p.dropout_rate = 99, 0.3
+    r = oracle_mod.fvjp(p)
+    ref = _gated_reference(p)
+    for n in ("out", "dq", "dk", "dv", "dq_gate", "dk_gate"):
+        torch.testing.assert_close(r[n], ref[n], rtol=1e-10, atol=1e-12, msg=n)
 
 
 def test_constant_gate_halves_the_ungated_results(oracle_mod):
