@@ -98,6 +98,18 @@ bool host_strides_ok(int64_t ts, int64_t hs, int H, int d) {
 struct Resources {
   cudaStream_t in = nullptr, out = nullptr;
   std::vector<cudaEvent_t> events;
+  // On an error part-way, the caller's stream still waits for the work the
+  // call has enqueued on its own streams, so the caller can free its buffers
+  // once it has synchronised that stream.
+  void join(cudaStream_t caller) {
+    for (cudaStream_t s : {in, out}) {
+      cudaEvent_t e;
+      if (s && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) {
+        if (cudaEventRecord(e, s) == cudaSuccess) cudaStreamWaitEvent(caller, e, 0);
+        cudaEventDestroy(e);
+      }
+    }
+  }
   ~Resources() {
     for (cudaEvent_t e : events) cudaEventDestroy(e);
     if (in) cudaStreamDestroy(in);
@@ -200,9 +212,12 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
   float* lse_dev = reinterpret_cast<float*>(base + L.lse);
   Resources r;
   cudaEvent_t entry, done;
-#define ATTN_TRY(x)                              \
-  do {                                           \
-    if ((x) != cudaSuccess) return ATTN_ERR_CUDA; \
+#define ATTN_TRY(x)                 \
+  do {                              \
+    if ((x) != cudaSuccess) {       \
+      r.join(stream);               \
+      return ATTN_ERR_CUDA;         \
+    }                               \
   } while (0)
   ATTN_TRY(cudaStreamCreateWithFlags(&r.in, cudaStreamNonBlocking));
   ATTN_TRY(cudaStreamCreateWithFlags(&r.out, cudaStreamNonBlocking));
@@ -247,7 +262,10 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
         Hq, causal, window_left, window_right, softcap, scale_multiplier, at(L.out, t0, qts), qts,
         d, at(L.dq, t0, qts), qts, d, at(L.dk, u0, kts), kts, d, at(L.dv, u0, kts), kts, d,
         lse_dev + t0 * Hq, base + L.ws, L.ws_bytes, status_dev + c, stream);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK) {
+      r.join(stream);
+      return st;
+    }
     ATTN_TRY(cudaEventRecord(comp_done, stream));
     // results of chunk c
     ATTN_TRY(cudaStreamWaitEvent(r.out, comp_done, 0));
