@@ -258,6 +258,26 @@ def long_balanced(seed=5, device="cpu", length_scale=1.0, poison=True, Hkv=1, d=
                  seed=seed, device=device, poison=poison, Hkv=Hkv, d=d)
 
 
+def gated(seed=6, device="cpu", length_scale=1.0, d=128, R=64, Hq=32, Hkv=8, poison=True):
+    """The gated variant's training shape family ("Pairwise-Gated Attention
+    Engine", "The task": head sizes 64 and 128, gate sizes 32 and 64,
+    grouped K/V heads, sequences up to 16,384 tokens): 8 causal sequences with
+    Lq = Lk ~ U[1024, 16384], bf16, dense layouts, no softcap and no ALiBi
+    (the page's plain softmax), q/k/v/dout and the gate projections N(0,1)."""
+    g = torch.Generator().manual_seed(seed)
+    B = 8
+    L = _scale(_uniform_int(g, 1024, 16384, B), length_scale)
+    p = build("gated", L, list(L), Hq, torch.bfloat16, 1, d, torch.zeros(B, Hq), seed=seed,
+              device=device, poison=poison, Hkv=Hkv, d=d, causal=True)
+    p.softcap = 0.0
+    gg = torch.Generator(device=device).manual_seed(seed * 7 + 1)
+    p.q_gate = torch.randn((sum(L), Hq, R), generator=gg, dtype=torch.float32,
+                           device=device).to(torch.bfloat16)
+    p.k_gate = torch.randn((sum(L), Hkv, R), generator=gg, dtype=torch.float32,
+                           device=device).to(torch.bfloat16)
+    return p
+
+
 def _scale(lengths, s):
     if s == 1.0:
         return list(lengths)

@@ -613,3 +613,17 @@ def test_constant_gate_halves_the_ungated_results(oracle_mod):
         torch.testing.assert_close(r[n], 0.5 * r0[n], rtol=1e-13, atol=1e-15, msg=n)
     assert torch.equal(r["dk_gate"], torch.zeros_like(r["dk_gate"]))
     assert torch.equal(r["lse"], r0["lse"])
+
+
+def test_gated_bf16_inputs_decode_like_torch(oracle_mod):
+    """16-bit gate projections are decoded exactly: the oracle on a bf16 gated
+    problem equals the oracle on its fp64 copy."""
+    p = W.gated(length_scale=1 / 1024, d=64, R=32, Hq=4, Hkv=2)
+    r = oracle_mod.fvjp(p)
+    p64 = W.gated(length_scale=1 / 1024, d=64, R=32, Hq=4, Hkv=2)
+    for n in ("q", "k", "v", "dout", "q_gate", "k_gate"):
+        setattr(p64, n, getattr(p, n).double())
+    r64 = oracle_mod.fvjp(p64)
+    for n in ("out", "lse", "dq", "dk", "dv", "dq_gate", "dk_gate"):
+        assert torch.equal(r[n], r64[n]), n
+        assert torch.isfinite(r[n]).all(), n

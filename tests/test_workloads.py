@@ -61,3 +61,12 @@ def test_options_shape_the_views():
     assert p.k.shape == (13, 4, 128) and p.q.shape == (9, 12, 128)
     p = W.long_balanced(length_scale=1 / 256, Hkv=8, d=64)
     assert p.k.shape[1:] == (8, 64) and p.q.shape[1:] == (96, 64)
+
+
+def test_gated_family_follows_its_page():
+    p = W.gated(length_scale=1 / 256, d=64, R=32, Hq=16, Hkv=4)
+    assert p.q.shape[1:] == (16, 64) and p.k.shape[1:] == (4, 64)
+    assert p.q_gate.shape == (p.q.shape[0], 16, 32) and p.k_gate.shape == (p.k.shape[0], 4, 32)
+    assert p.causal and p.softcap == 0.0 and float(p.alibi_slopes.abs().max()) == 0.0
+    lq, lk = p.lengths()
+    assert lq == lk and all(4 <= x <= 64 for x in lq)
