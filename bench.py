@@ -75,6 +75,34 @@ def kernel_flops(p) -> dict:
     return {"forward": 4 * u, "dkdv": 8 * u, "dq": 2 * u, "schedule": 0.0, "preprocess": 0.0}
 
 
+# Transcendental (MUFU) operations per (head, query, key) unit in each kernel:
+# the forward, dk/dv and dq each take one tanh (softcap) and one exp2 (P)
+# per element; without a softcap there is no tanh.  Issue rates measured on
+# this GPU with one CTA of eight elementwise warps per SM (tanh.approx.f32 16,
+# ex2.approx 32 per clock per SM).
+MUFU_RATE = {"tanh": 16.0, "ex2": 32.0}
+
+
+def mufu_bound(p, call_ms, kernel_ms, sm_mhz, sms):
+    """Time the MUFU alone needs for the call's transcendentals at the
+    measured issue rates and the sampled SM clock, next to the measured
+    times: the co-bound of the tensor-core roofline."""
+    units = p.Hq * scored_pairs(p)
+    per = {"tanh": 1.0 if p.softcap > 0 else 0.0, "ex2": 1.0}
+    clk_per_unit = sum(per[k] / MUFU_RATE[k] for k in per)  # SM clocks per unit per kernel
+    mhz = sm_mhz or 2070.0
+    one_kernel_ms = units * clk_per_unit / sms / (mhz * 1e6) * 1e3
+    out = {"ops_per_unit_per_kernel": per, "rate_per_clk_per_sm": MUFU_RATE,
+           "rate_source": "measured issue rate (probe, 8 warps per SM)", "sms": sms,
+           "sm_mhz": mhz, "units": units, "bound_ms": 3 * one_kernel_ms, "call_ms": call_ms,
+           "frac": 3 * one_kernel_ms / call_ms}
+    if kernel_ms:
+        out["per_kernel"] = {k: {"bound_ms": one_kernel_ms, "kernel_ms": kernel_ms[k],
+                                 "frac": one_kernel_ms / kernel_ms[k]}
+                             for k in ("forward", "dkdv", "dq") if k in kernel_ms}
+    return out
+
+
 def mask_name(p) -> str:
     """Suffix naming the mask of a workload ('' without one)."""
     parts = []
@@ -371,6 +399,13 @@ def run_gpu(args, world, rank, local):
     if not args.no_e2e and args.dropout is None:
         e2e = run_e2e(args, p, kw, flops, stream, world)
 
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mufu = mufu_bound(p, ms, per_kernel, clk.get("sm_mhz"), sms)
+    executed = None
+    if per_kernel:  # executed MMA flops per kernel (dq's recompute included)
+        u = p.q.shape[-1] * p.Hq * scored_pairs(p)
+        executed = {k: {"tflops": f * u / (per_kernel[k] / 1e3) / 1e12, "ms": per_kernel[k]}
+                    for k, f in (("forward", 4), ("dkdv", 8), ("dq", 6))}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -388,13 +423,111 @@ def run_gpu(args, world, rank, local):
                        "l2": "inputs larger than L2 (q view alone is "
                              f"{p.q.numel() * 2 / 1e9:.1f} GB)"},
             "latency_ms": ms, "frac_of_bf16_peak": whole_frac,
-            "kernel_ms": per_kernel, "roofline": roofline, "gpu_launches": launches,
-            "clocks": clk, "e2e": e2e}
+            "kernel_ms": per_kernel, "executed_mma": executed, "roofline": roofline,
+            "mufu": mufu, "gpu_launches": launches, "clocks": clk, "e2e": e2e}
     if (rank == 0 and world == 1 and not args.no_cpu and not mask_name(p) and args.hkv == 1
             and args.head_dim == HEAD_DIM and args.dropout is None):
         v, cores, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample,
+                                "extrapolated_full_s": flops / (v * 1e12),
+                                "extrapolated_note": "the full workload's counted flops at "
+                                                     "the sample's rate (extrapolation, not "
+                                                     "a run)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_shard(args, world, rank, local):
+    """Strong scaling of ONE batch over the ranks with the library's shard
+    plan: every rank builds the same long balanced batch, takes its share
+    (whole sequences, longest processing time first; head parts of a
+    dominant sequence), and a step is the share's calls plus the exchange of
+    partial dk/dv (point-to-point to the rank holding part 0, then the
+    library's fixed-order sum).  Gathering a rank's sequences into its own
+    packed copy happens once, before timing."""
+    from ragged_gqa_attention_varlen_gb300 import _build, binding, shard
+
+    _build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = workloads.long_balanced(seed=5, device=dev, poison=False,
+                                length_scale=args.length_scale, Hkv=args.hkv, d=args.head_dim)
+    p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
+    flops = counted_flops(p)
+    plan = shard.make_plan(p, world)
+    mine = shard.shares(p, plan, rank)
+    stream = torch.cuda.current_stream(dev)
+    bufs = []
+    for s_ in mine:
+        q = s_.problem
+        bufs.append(dict(out=torch.empty(q.q.shape, dtype=q.q.dtype, device=dev),
+                         dq=torch.empty(q.q.shape, dtype=q.q.dtype, device=dev),
+                         dk=torch.empty(q.k.shape, dtype=q.k.dtype, device=dev),
+                         dv=torch.empty(q.v.shape, dtype=q.v.dtype, device=dev),
+                         lse=torch.empty((q.total_q, q.Hq), dtype=torch.float32, device=dev),
+                         workspace=torch.empty(binding.workspace_size(q.B, q.Hq, q.total_q,
+                                                                      q.total_k),
+                                               dtype=torch.uint8, device=dev),
+                         stream=stream))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def reduce(parts):
+        out = torch.empty_like(parts[0])
+        binding.sum_partials(parts, out, stream=stream)
+        return out
+
+    def step():
+        results = []
+        for s_, kw in zip(mine, bufs):
+            q = s_.problem
+            results.append(binding.attention_varlen_fvjp(
+                q.q, q.k, q.v, q.cu_q, q.cu_k, q.alibi_slopes, q.dout, q.causal, q.window_left,
+                q.window_right, q.softcap, q.scale_multiplier, **kw))
+        return shard.exchange(p, plan, rank, mine, results, reduce, dist)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for kw in bufs:
+        st = binding.device_status(kw["workspace"])
+        if st != 0:
+            raise RuntimeError(f"device status {st:#x}")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    t = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    value, ms = flops * args.steps / t / 1e12, t / args.steps * 1e3
+    pk, kind = peaks()
+    launches = sum(binding.launch_count(s_.problem.B, s_.problem.Hq, s_.problem.total_q,
+                                        s_.problem.total_k, Hkv=s_.problem.k.shape[1])
+                   for s_ in mine) * args.steps
+    mean = sum(plan.work) / max(len(plan.work), 1)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, generated on device)",
+            "config": {"workload": f"long_balanced, one batch sharded over {world} rank(s)" +
+                                   mask_name(p), "B": p.B, "Hq": p.Hq, "Hkv": args.hkv,
+                       "head_dim": args.head_dim, "units": len(plan.units),
+                       "cut_sequences": sum(1 for b in range(p.B) if len(plan.parts(b)) > 1),
+                       "rank_work_max_over_mean": max(plan.work) / mean if mean else None,
+                       "counted_tflop_per_step": flops / 1e12,
+                       "l2": "inputs larger than L2"},
+            "latency_ms": ms, "frac_of_bf16_peak": value / world / pk["bf16_tflops"],
+            "gpu_launches": launches, "clocks": clk}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -494,12 +627,17 @@ def main():
                     help="time with counter-based dropout at this rate")
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
+    ap.add_argument("--shard", action="store_true",
+                    help="strong scaling: one batch split over the ranks by the shard plan")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.shard:
+        run_shard(args, world, rank, local)
+        return 0
     run_gpu(args, world, rank, local)
     return 0
 

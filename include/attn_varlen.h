@@ -316,6 +316,45 @@ attn_status attn_varlen_fvjp_fwd_bwd_host(
 int attn_varlen_host_chunks(int B, const int32_t *cu_q, const int32_t *cu_k, int chunks,
                             int32_t *cuts);
 
+/* Shard plan of one batch over `nranks` processes (1..16), one GPU each.
+ * Sequences are independent problems, so the batch shards by sequence with
+ * no exchange of data.  Each sequence weighs Hq times its admissible
+ * (query, key) pairs under the mask; a sequence weighing more than 1/nranks
+ * of the batch is cut into k = min(nranks, ceil(weight / (total/nranks)))
+ * parts by query head (one K/V head: heads [e*Hq/k, (e+1)*Hq/k)) or by
+ * whole K/V head groups (Hkv > 1: at most Hkv parts), and every unit (a
+ * whole sequence or a part) goes, heaviest first, to the least loaded rank
+ * (lowest on ties), the parts of one sequence to different ranks.  With one
+ * K/V head each part's call yields a partial dk/dv of the sequence's keys
+ * (summed over the part's heads only); the rank holding part 0 adds the
+ * parts in part order (attn_varlen_sum_partials).  Parts of Hkv > 1 cover
+ * disjoint K/V heads and need no sum.  Partitioning follows the sequence
+ * independence of "Noncausal Global Extreme-GQA Ragged Attention Full VJP",
+ * "Hard Constraints" (each sequence attends only within itself); the pages
+ * describe no multi-GPU split, so this plan is this library's own.
+ *
+ * cu_q, cu_k are HOST int32 [B+1] arrays.  Writes, for units u = 0..n-1 in
+ * order of (sequence, first head), unit_seq[u], the head range
+ * [unit_h0[u], unit_h1[u]) and unit_rank[u], and the work of each rank in
+ * rank_work[nranks].  Returns n (at most B + (nranks - 1)^2, and max_units
+ * must be at least n), or -1 for invalid arguments. */
+int attn_varlen_shard_plan(int B, const int32_t *cu_q, const int32_t *cu_k, int Hq, int Hkv,
+                           int causal, int window_left, int window_right, int nranks,
+                           int max_units, int32_t *unit_seq, int32_t *unit_h0,
+                           int32_t *unit_h1, int32_t *unit_rank, double *rank_work);
+
+/* Fixed-order sum of partial key gradients (the exchange step of the shard
+ * plan above): out[r, :] = part[0][r, :] + part[1][r, :] + ... in part order,
+ * accumulated in fp32 and rounded once to `dtype`.  `parts` is a HOST array
+ * of nparts (1..16) DEVICE pointers to [rows, d] 16-bit arrays with row
+ * stride part_row_stride (elements); out has row stride out_row_stride.  d
+ * and both strides must be multiples of 8 elements and every pointer 16-byte
+ * aligned (ATTN_ERR_ALIGNMENT otherwise).  Asynchronous on `stream`; the
+ * result is the same bits on every call. */
+attn_status attn_varlen_sum_partials(attn_dtype dtype, int nparts, const void *const *parts,
+                                     int64_t rows, int d, int64_t part_row_stride, void *out,
+                                     int64_t out_row_stride, void *stream);
+
 /* Bytes of device buffer attn_varlen_fvjp_fwd_bwd_host needs. */
 size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim, int64_t total_q,
                                           int64_t total_k, int chunks);
@@ -337,17 +376,22 @@ size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim, i
  * The call allocates nothing (no cudaMalloc, no allocating library routine).
  *
  * Limits and sharing:
- *  - Problems whose attn_varlen_fvjp_workspace_size exceeds the array (about
- *    16.7 million query rows total_q * Hq, with the schedule of up to
- *    ATTN_MAX_BATCH sequences) are rejected with ATTN_ERR_SCRATCH_LIMIT
- *    before anything is enqueued.
+ *  - The call needs A(16 + 12 * max(Hq, 2)) + A(4 * (5 * B + 2)) +
+ *    A(4 * total_q * Hq) bytes of the array, A() rounding up to a multiple
+ *    of 256 (status word and tile counters, the tile schedule, the fp32 D
+ *    term): at most ATTN_NOALLOC_SCRATCH_BYTES, so total_q * Hq up to about
+ *    16.7 million query rows.  Larger problems are rejected with
+ *    ATTN_ERR_SCRATCH_LIMIT before anything is enqueued.
  *  - Every call on a device uses the same array, which keeps the last call's
  *    contents.  The call resets what must start at zero itself.  Calls whose
  *    work overlaps on the GPU (other streams, other host threads) race on the
  *    array and give wrong results; serialise them.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - The current device must be the one that owns `stream` and every
+ *    pointer: the array used is the current device's.
+ *  - The first call on each device, and the first after that device's
+ *    context was destroyed and created again (cudaDeviceReset), looks up the
+ *    array's device address (cudaGetSymbolAddress) with that device current;
+ *    make such a call before any stream capture.
  *  - With device_status NULL the status word is the first int32 of the
  *    array, which the caller cannot read; pass a device_status pointer to
  *    see device-side errors. */

@@ -51,6 +51,8 @@ def _load():
         lib.oracle_fvjp.restype = I
         lib.oracle_rows.argtypes = common + [I, P, P, P, P, P, P, I]
         lib.oracle_rows.restype = I
+        lib.oracle_keys.argtypes = common + [I, P, P, P, P, I]
+        lib.oracle_keys.restype = I
         lib.oracle_decode.argtypes = [I, ctypes.c_uint16]
         lib.oracle_decode.restype = D
         lib.oracle_splitmix64.argtypes = [U64]
@@ -166,6 +168,29 @@ def rows(p, tok, head, nthreads: int = 0) -> dict:
                          res["lse"].data_ptr(), res["dq"].data_ptr(), res["D"].data_ptr(),
                          int(nthreads))
     del keep
+    res["threads"] = nt
+    return res
+
+
+def keys(p, tok, head, nthreads: int = 0) -> dict:
+    """dk and dv of the sampled packed keys (tok[r], K/V head head[r])
+    (ungated problems), equal bit for bit to ``fvjp``'s rows: every sequence
+    holding a sampled key takes the row pass without its dq part, then each
+    sampled key the key pass."""
+    if getattr(p, "q_gate", None) is not None:
+        raise NotImplementedError("the key sampler serves ungated problems")
+    lib = _load()
+    args, keep = _args(p)
+    tok = torch.as_tensor(tok, dtype=torch.int64).contiguous()
+    head = torch.as_tensor(head, dtype=torch.int32).contiguous()
+    n, d = tok.numel(), p.q.shape[-1]
+    f64 = dict(dtype=torch.float64)
+    res = dict(dk=torch.empty((n, d), **f64), dv=torch.empty((n, d), **f64))
+    nt = lib.oracle_keys(*args, n, tok.data_ptr(), head.data_ptr(), res["dk"].data_ptr(),
+                         res["dv"].data_ptr(), int(nthreads))
+    del keep
+    if nt == 0:
+        raise ValueError("oracle_keys rejected its arguments")
     res["threads"] = nt
     return res
 

@@ -319,6 +319,7 @@ typedef struct {
   double *lse, *D;
   double *dz_sum, *p_sum; /* optional */
   double *dqg;            /* [R] with a gate, else NULL */
+  int stats_only;         /* stop after lse, out and D (no dq): feeds a key pass */
 } rowdest;
 
 /* One query row (i, h) of sequence s, whose decoded q and dO rows are qi and
@@ -337,7 +338,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   }
   for (int f = 0; f < d; f++) {
     o->out[f] = 0.0;
-    o->dq[f] = 0.0;
+    if (o->dq) o->dq[f] = 0.0;
   }
   for (int f = 0; o->dqg && f < p->R; f++) o->dqg[f] = 0.0;
   if (m == -INFINITY) { /* empty row */
@@ -364,6 +365,7 @@ static void row_pass(const seqdata *s, int h, int i, const double *qi, const dou
   double D = 0.0;
   for (int f = 0; f < d; f++) D += dOi[f] * o->out[f];
   *o->D = D;
+  if (o->stats_only) return;
   double dzsum = 0.0;
   double sigma = p->scale_multiplier / sqrt((double)d);
   for (int j = 0; j < Lk; j++) {
@@ -391,10 +393,11 @@ static void row_pass_packed(const seqdata *s, int h, int i, const outputs *o, do
                             double *P, double *gv) {
   int d = s->p->d, H = s->p->Hq;
   int64_t rowid = (s->q0 + i) * (int64_t)H + h;
-  rowdest r = {o->out + rowid * d, o->dq + rowid * d, o->lse + rowid, o->Dpre + rowid,
+  rowdest r = {o->out + rowid * d, o->dq ? o->dq + rowid * d : NULL, o->lse + rowid,
+               o->Dpre + rowid,
                o->dz_rowsum ? o->dz_rowsum + rowid : NULL,
                o->p_rowsum ? o->p_rowsum + rowid : NULL,
-               o->dqg ? o->dqg + rowid * s->p->R : NULL};
+               o->dqg ? o->dqg + rowid * s->p->R : NULL, o->dq == NULL};
   const double *qi = s->Q + ((size_t)i * H + h) * d;
   const double *dOi = s->dO + ((size_t)i * H + h) * d;
   row_pass(s, h, i, qi, dOi, &r, z, P, gv);
@@ -402,20 +405,18 @@ static void row_pass_packed(const seqdata *s, int h, int i, const outputs *o, do
 
 /* ---- per-key pass: dk, dv (needs every row's lse and D) ---------------- */
 
-/* Key j of K/V head kh: sums over the query heads of its group. */
-static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
+/* Key j of K/V head kh: sums over the query heads of its group, into the
+ * rows dkrow, dvrow (and dkgrow with a gate). */
+static void key_pass_to(const seqdata *s, int j, int kh, const outputs *o, double *dkrow,
+                        double *dvrow, double *dkgrow) {
   const problem *p = s->p;
   int d = p->d, H = p->Hq, R = p->Hq / p->Hkv;
   double sigma = p->scale_multiplier / sqrt((double)d);
-  int64_t at = ((s->k0 + j) * (int64_t)p->Hkv + kh) * d;
-  double *dkrow = o->dk + at;
-  double *dvrow = o->dv + at;
   for (int f = 0; f < d; f++) {
     dkrow[f] = 0.0;
     dvrow[f] = 0.0;
   }
   const double *vj = kv_row(s, s->V, j, kh);
-  double *dkgrow = o->dkg ? o->dkg + ((s->k0 + j) * (int64_t)p->Hkv + kh) * p->R : NULL;
   for (int f = 0; dkgrow && f < p->R; f++) dkgrow[f] = 0.0;
   for (int h = kh * R; h < (kh + 1) * R; h++) {
     double slope = slope_of(p, s->b, h);
@@ -448,6 +449,14 @@ static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
   for (int f = 0; f < d; f++) dkrow[f] *= sigma;
 }
 
+/* Key j of K/V head kh into the packed dk, dv (and dkg) outputs. */
+static void key_pass(const seqdata *s, int j, int kh, const outputs *o) {
+  const problem *p = s->p;
+  int64_t at = ((s->k0 + j) * (int64_t)p->Hkv + kh) * p->d;
+  double *dkgrow = o->dkg ? o->dkg + ((s->k0 + j) * (int64_t)p->Hkv + kh) * p->R : NULL;
+  key_pass_to(s, j, kh, o, o->dk + at, o->dv + at, dkgrow);
+}
+
 /* ---- a tiny thread pool over a fixed unit list ------------------------- */
 
 typedef struct {
@@ -457,7 +466,8 @@ typedef struct {
   const int *unit_b;   /* unit -> sequence */
   const int *unit_a;   /* unit -> head (phase 1) or key * Hkv + K/V head (phase 2) */
   int n_units;
-  int phase;
+  int phase; /* 1: rows of (sequence, head); 2: keys; 3: sampled keys into dk_r/dv_r */
+  double *dk_r, *dv_r; /* phase 3: [n_units][d] */
   int next; /* shared counter */
   pthread_mutex_t mu;
 } pool;
@@ -480,8 +490,12 @@ static void *worker(void *arg) {
     const seqdata *s = &w->seqs[w->unit_b[u]];
     if (w->phase == 1) {
       for (int i = 0; i < s->Lq; i++) row_pass_packed(s, w->unit_a[u], i, w->o, z, P, g);
-    } else {
+    } else if (w->phase == 2) {
       key_pass(s, w->unit_a[u] / w->p->Hkv, w->unit_a[u] % w->p->Hkv, w->o);
+    } else {
+      const int64_t d = w->p->d;
+      key_pass_to(s, w->unit_a[u] / w->p->Hkv, w->unit_a[u] % w->p->Hkv, w->o,
+                  w->dk_r + u * d, w->dv_r + u * d, NULL);
     }
   }
   free(z);
@@ -693,6 +707,93 @@ int oracle_rows(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t
   for (int t = 0; t < nt; t++) pthread_join(tid[t], NULL);
   pthread_mutex_destroy(&w.mu);
   free(tid);
+  return nt;
+}
+
+/* Key-sampled dk and dv: for each sampled key (packed key token key_tok[r],
+ * K/V head key_head[r]) its dk and dv rows, written densely at index r of
+ * dk_r/dv_r [n][d].  Every sequence holding a sampled key first takes the
+ * row pass of oracle_fvjp with the dq part left out (lse and D are computed
+ * the same way, operation for operation), then each sampled key takes
+ * oracle_fvjp's key pass: the rows equal oracle_fvjp's dk and dv bit for
+ * bit, at about a quarter of its cost per sequence.  Ungated problems only.
+ * Returns the number of threads used (0 for invalid arguments). */
+int oracle_keys(int dtype, int B, int Hq, int Hkv, int d, const void *q, int64_t q_ts,
+                int64_t q_hs, const void *k, int64_t k_ts, int64_t k_hs, const void *v,
+                int64_t v_ts, int64_t v_hs,
+                const void *dout, int64_t do_ts, int64_t do_hs, const int32_t *cu_q,
+                const int32_t *cu_k, const float *slopes, int64_t slopes_bs, int causal, int wl,
+                int wr, double softcap, double scale_multiplier, int dropout, uint64_t seed,
+                float rate, const float *rates, int R, const void *qg, int64_t qg_ts,
+                int64_t qg_hs, const void *kg, int64_t kg_ts, int64_t kg_hs, int n,
+                const int64_t *key_tok, const int32_t *key_head, double *dk_r, double *dv_r,
+                int nthreads) {
+  if (Hkv < 1 || Hq % Hkv || R != 0 || n < 0) return 0;
+  problem p = {dtype, B,     Hq,    Hkv,  d,     q,  q_ts,  q_hs,    k,
+               k_ts,  k_hs,  v,     v_ts, v_hs,  dout, do_ts, do_hs,  cu_q,
+               cu_k,  slopes, slopes_bs, causal, wl, wr, softcap, scale_multiplier,
+               dropout, seed, rate, rates, R, qg, qg_ts, qg_hs, kg, kg_ts, kg_hs};
+  int64_t Tq = B > 0 ? cu_q[B] : 0;
+  for (int r = 0; r < n; r++) {
+    if (key_head[r] < 0 || key_head[r] >= Hkv || key_tok[r] < 0 || key_tok[r] >= cu_k[B])
+      return 0;
+  }
+  /* the sequence of each sampled key (last b with cu_k[b] <= t, non-empty) */
+  int *kb = malloc(sizeof(int) * ((size_t)n + 1));
+  uint8_t *need = calloc((size_t)B + 1, 1);
+  for (int r = 0; r < n; r++) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) / 2;
+      if (cu_k[mid] <= key_tok[r])
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    while (lo < B && cu_k[lo + 1] <= key_tok[r]) lo++;
+    kb[r] = lo;
+    need[lo] = 1;
+  }
+  double *out = malloc(sizeof(double) * ((size_t)Tq * Hq * d + 1));
+  double *lse = malloc(sizeof(double) * ((size_t)Tq * Hq + 1));
+  double *Dpre = malloc(sizeof(double) * ((size_t)Tq * Hq + 1));
+  outputs o = {out, lse, NULL, Dpre, NULL, NULL, NULL, NULL, NULL, NULL};
+  int nt = thread_count(nthreads);
+  seqdata *seqs = calloc((size_t)B + 1, sizeof(seqdata));
+  int n1 = 0;
+  for (int b = 0; b < B; b++)
+    if (need[b]) {
+      seq_load(&p, b, &seqs[b]);
+      n1 += Hq;
+    }
+  int *ub = malloc(sizeof(int) * (size_t)(n1 + n + 1));
+  int *ua = malloc(sizeof(int) * (size_t)(n1 + n + 1));
+  int m = 0;
+  for (int b = 0; b < B; b++)
+    for (int h = 0; need[b] && h < Hq; h++) {
+      ub[m] = b;
+      ua[m] = h;
+      m++;
+    }
+  pool w1 = {.p = &p, .o = &o, .seqs = seqs, .unit_b = ub, .unit_a = ua, .n_units = m, .phase = 1};
+  run_pool(&w1, nt);
+  for (int r = 0; r < n; r++) {
+    ub[r] = kb[r];
+    ua[r] = (int)(key_tok[r] - cu_k[kb[r]]) * Hkv + key_head[r];
+  }
+  pool w3 = {.p = &p, .o = &o, .seqs = seqs, .unit_b = ub, .unit_a = ua, .n_units = n,
+             .phase = 3, .dk_r = dk_r, .dv_r = dv_r};
+  run_pool(&w3, nt);
+  for (int b = 0; b < B; b++)
+    if (need[b]) seq_free(&seqs[b]);
+  free(seqs);
+  free(ub);
+  free(ua);
+  free(kb);
+  free(need);
+  free(out);
+  free(lse);
+  free(Dpre);
   return nt;
 }
 

@@ -25,7 +25,8 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
            "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
            "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_fwd_bwd_dropout",
-           "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks")
+           "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks",
+           "attn_varlen_shard_plan", "attn_varlen_sum_partials")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -91,6 +92,10 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
         [P, L, L, P] + [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
     lib.attn_varlen_bwd_dropout.restype = I
+    lib.attn_varlen_shard_plan.argtypes = [I, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
+    lib.attn_varlen_shard_plan.restype = I
+    lib.attn_varlen_sum_partials.argtypes = [I, I, P, L, I, L, P, L, P]
+    lib.attn_varlen_sum_partials.restype = I
     lib.attn_varlen_fvjp_record_events.argtypes = [P, I]
     lib.attn_varlen_fvjp_record_events.restype = I
     _lib = lib
@@ -455,7 +460,19 @@ def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, 
     B = cu_q.numel() - 1
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    code = lib.attn_varlen_fvjp_fwd_bwd_noalloc(
+    # the library uses the scratch array of the current device
+    with torch.cuda.device(q.device):
+        code = _noalloc_call(lib, q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv, lse,
+                             device_status, causal, window_left, window_right, softcap,
+                             scale_multiplier, stream, dtype, B, Hq, Hkv)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+
+
+def _noalloc_call(lib, q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv, lse,
+                  device_status, causal, window_left, window_right, softcap, scale_multiplier,
+                  stream, dtype, B, Hq, Hkv):
+    return lib.attn_varlen_fvjp_fwd_bwd_noalloc(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], q.shape[0],
         k.shape[0], _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
         _ptr(v), v.stride(0), v.stride(1), _ptr(dout), dout.stride(0), dout.stride(1),
@@ -466,6 +483,47 @@ def attention_varlen_fvjp_noalloc(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, 
         _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
         _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
         _ptr(lse), _ptr(device_status), stream.cuda_stream)
+
+
+def shard_plan(cu_q, cu_k, Hq: int, Hkv: int, nranks: int, causal=False, window_left=-1,
+               window_right=-1):
+    """The library's shard plan of one batch over ``nranks`` processes: a list
+    of units (sequence, first head, end head, rank) in (sequence, head) order
+    and the work of each rank.  cu arrays may live on any device (read on the
+    host)."""
+    lib = load()
+    cq = cu_q.detach().to("cpu", torch.int32).contiguous()
+    ck = cu_k.detach().to("cpu", torch.int32).contiguous()
+    B = cq.numel() - 1
+    cap = B + (nranks - 1) ** 2 + 1
+    bufs = [torch.empty(cap, dtype=torch.int32) for _ in range(4)]
+    work = torch.empty(max(nranks, 1), dtype=torch.float64)
+    n = lib.attn_varlen_shard_plan(B, _ptr(cq), _ptr(ck), Hq, Hkv, int(bool(causal)),
+                                   int(window_left), int(window_right), nranks, cap,
+                                   *[_ptr(b) for b in bufs], _ptr(work))
+    if n < 0:
+        raise ValueError("attn_varlen_shard_plan rejected its arguments")
+    units = [tuple(int(b[u]) for b in bufs) for u in range(n)]
+    return units, work.tolist()
+
+
+def sum_partials(parts, out, stream=None):
+    """out = parts[0] + parts[1] + ... (in this order, fp32 accumulation, one
+    rounding): 16-bit [rows, (1,) d] tensors with a contiguous feature axis."""
+    lib = load()
+    d = out.shape[-1]
+    rows = out.shape[0]
+    assert out.dim() == 2 or (out.dim() == 3 and out.shape[1] == 1), "one K/V head"
+    for t in parts:
+        assert t.dtype == out.dtype and t.shape == out.shape and t.device == out.device
+        assert t.stride(-1) == 1
+    assert out.stride(-1) == 1
+    if stream is None:
+        stream = torch.cuda.current_stream(out.device)
+    arr = (ctypes.c_void_p * len(parts))(*[t.data_ptr() for t in parts])
+    code = lib.attn_varlen_sum_partials(
+        ATTN_BF16 if out.dtype == torch.bfloat16 else ATTN_F16, len(parts), arr, rows, d,
+        parts[0].stride(0), _ptr(out), out.stride(0), stream.cuda_stream)
     if code != 0:
         raise AttnError(code, lib.attn_status_string(code).decode())
 

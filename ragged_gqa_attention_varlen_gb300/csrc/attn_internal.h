@@ -94,6 +94,11 @@ inline bool masked_call(const Params& p) { return p.causal || p.wl >= 0 || p.wr 
 //   [4B+2, 5B+2)    first such key tile of each order position
 inline int sched_words(int B) { return 5 * B + 2; }
 
+// Workspace bytes a call uses (host.cu): the status word, tile counters,
+// schedule and D, plus the per-token dropout rate table when `rate_table`.
+// attn_varlen_fvjp_workspace_size reports the size with the table.
+size_t workspace_bytes_needed(int B, int Hq, int64_t total_q, bool rate_table);
+
 cudaError_t launch_sched(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,

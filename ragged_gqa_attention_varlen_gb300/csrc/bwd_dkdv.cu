@@ -498,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float prel = static_cast<float>(i + q0.t.Lk - q0.t.Lq - q0.t.key);
         // bias(r) = -sl2 * |prel - r| + nl2 = a + m * r for every key r of the
         // tile when prel >= 127 (m = sl2) or prel <= 0 (m = -sl2).  In every
-        // case nl2 = a + m * prel and sl2 = |m|, which the general form uses.
+        // case nl2 = a + m * prel, and the general form recovers sl2 from m
+        // and the sign of prel (a slope may be negative).
         const bool right = prel <= 0.f;  // every key at or right of i
         const float m = right ? -sl2 : sl2;
         cols->a[b][lc] = fmaf(-m, prel, nl2);
@@ -663,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:
           // prel = i + Lk - Lq - key0 of column c is tok0 + c / G + off,
-          // a + m * prel = -lse2 and |m| = slope2
+          // a + m * prel = -lse2, and the column's slope2 is m where its
+          // scalars were staged for keys left of prel (prel > 0), else -m
           const int tok0 = (t.tb0 + st / ngroups) * step_tok;
           const int off = t.Lk - t.Lq - t.key;
 #pragma unroll 1
@@ -676,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v = 0; v < 4; ++v) {
               const int c = half * 64 + q4 * 4 + v;
               const float prel = static_cast<float>(tok0 + (c >> lgG) + off);
-              bv[v] = fmaf(-fabsf(mv[v]), fabsf(prel - rf), fmaf(mv[v], prel, av[v]));
+              const float sl = prel <= 0.f ? -mv[v] : mv[v];
+              bv[v] = fmaf(-sl, fabsf(prel - rf), fmaf(mv[v], prel, av[v]));
               if (masked) {
                 const bool adm = (wl < 0 || rf >= prel - static_cast<float>(wl)) &&
                                  (wr < 0 || rf <= prel + static_cast<float>(wr));

@@ -1,6 +1,5 @@
 // common.cuh -- per-element arithmetic shared by the attention kernels:
-// logits with softcap and ALiBi in the base-2 domain, 16-bit packing, and
-// swizzled shared-memory row writes.
+// the logit map's constants, counter-based dropout and 16-bit packing.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -74,31 +73,6 @@ __device__ __forceinline__ LogitMap make_logit_map(const Params& p) {
   return m;
 }
 
-// tanh(x) = sign(x) * (1 - 2 / (exp(2|x|) + 1)).  Only the absolute error
-// matters here (the logit is c * tanh), and it stays near 2e-7 on the whole
-// line: the exponential's relative error scales a term that is at most 1.
-// |x| is clamped at 15, where tanh already rounds to 1 in fp32.
-__device__ __forceinline__ float tanh_acc(float x) {
-  float ax = fminf(fabsf(x), 15.f);
-  float e = ex2_approx(2.f * kLog2e * ax);
-  return copysignf(1.f - __fdividef(2.f, e + 1.f), x);
-}
-
-// Base-2 logit and, through *th, the tanh value (for the chain rule).
-__device__ __forceinline__ float logit2(const LogitMap& m, float acc, float slope2, float dist,
-                                        float* th) {
-  float z;
-  if (m.capped) {
-    float t = tanh_acc(acc * m.in_scale);
-    *th = t;
-    z = t * m.out_scale;
-  } else {
-    *th = 0.f;
-    z = acc * m.in_scale;
-  }
-  return fmaf(-slope2, dist, z);
-}
-
 template <bool BF16>
 struct Pack;
 
@@ -131,21 +105,6 @@ template <bool BF16>
 __device__ __forceinline__ uint4 pack8(const float* v) {
   return make_uint4(Pack<BF16>::two(v[0], v[1]), Pack<BF16>::two(v[2], v[3]),
                     Pack<BF16>::two(v[4], v[5]), Pack<BF16>::two(v[6], v[7]));
-}
-
-// Write 32 consecutive values v[0..31] of row r, starting at element col
-// (a multiple of 32) of a K-major swizzled tile made of 64-wide chunks that
-// are chunk_bytes apart.
-template <bool BF16>
-__device__ __forceinline__ void store_row32_sw128(uint8_t* tile, uint32_t chunk_bytes, int r,
-                                                  int col, const float* v) {
-  uint8_t* base = tile + (col >> 6) * chunk_bytes;
-  const int u0 = (col & 63) >> 3;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    uint4 w = pack8<BF16>(v + 8 * u);
-    *reinterpret_cast<uint4*>(base + sw128_offset(r, u0 + u)) = w;
-  }
 }
 
 }  // namespace attn

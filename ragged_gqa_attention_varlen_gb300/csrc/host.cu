@@ -54,6 +54,17 @@ WsLayout ws_layout(int B, int Hq, int64_t total_q) {
   return w;
 }
 
+}  // namespace
+
+// Bytes of workspace a call uses: everything up to the per-token dropout
+// rate table, plus the table when the call has per-token rates.
+size_t workspace_bytes_needed(int B, int Hq, int64_t total_q, bool rate_table) {
+  const WsLayout w = ws_layout(B, Hq, total_q);
+  return rate_table ? w.total : w.droptab;
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s > 0 && (s % 8) == 0; }
 
@@ -301,7 +312,10 @@ attn_status run_call(
     }
   }
   const WsLayout ws = ws_layout(B, Hq, total_q);
-  if (!workspace || workspace_bytes < ws.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  // the per-token dropout rate table (the layout's last part) is used only
+  // by calls with per-token rates
+  const size_t ws_need = (drop.on && drop.rates) ? ws.total : ws.droptab;
+  if (!workspace || workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_WORKSPACE;
 
   uint8_t* wsb = static_cast<uint8_t*>(workspace);

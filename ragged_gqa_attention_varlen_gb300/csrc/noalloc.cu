@@ -7,11 +7,14 @@
 // synchronise the device) once it is serving.  The ordinary entry point needs
 // a caller-provided workspace; this one uses a fixed scratch array compiled
 // into the library instead, so such a caller only passes inputs and outputs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/attn_varlen.h"
+#include "attn_internal.h"
 
 namespace {
 
@@ -20,24 +23,71 @@ namespace {
 // ATTN_NOALLOC_SCRATCH_BYTES until the process exits.
 __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
+// The array's device address belongs to the context the library's module is
+// loaded in.  It is looked up once per device and context: a new context on
+// the same device (after cudaDeviceReset, or once the primary context was
+// released and created again) loads the module again, and the array may then
+// live elsewhere.  Contexts are told apart by their process-unique id.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, std::atomic<Fn>& slot) {
+  Fn f = slot.load();
+  if (f) return f;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  f = reinterpret_cast<Fn>(ptr);
+  slot.store(f);
+  return f;
+}
+
+// Id of the context current on this thread; false when there is none yet or
+// the driver functions are unavailable.
+bool current_context_id(unsigned long long* id) {
+  static std::atomic<CtxGetCurrentFn> get_current{nullptr};
+  static std::atomic<CtxGetIdFn> get_id{nullptr};
+  CtxGetCurrentFn cur = driver_fn("cuCtxGetCurrent", get_current);
+  CtxGetIdFn gid = driver_fn("cuCtxGetId", get_id);
+  if (!cur || !gid) return false;
+  CUcontext ctx = nullptr;
+  if (cur(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return gid(ctx, id) == CUDA_SUCCESS;
+}
+
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
-std::mutex g_scratch_mu;
+struct Entry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+Entry g_entry[kMaxDevices];
+std::mutex g_entry_mu;
 
 // In host code the array's name is only a host-side stand-in; its device
-// address comes from the runtime, looked up once per device with that device
-// current.
+// address comes from the runtime, with the device current.
 attn_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(g_entry_mu);
+  if (have_id && g_entry[dev].addr && g_entry[dev].ctx_id == id) {
+    *out = g_entry[dev].addr;
+    return ATTN_OK;
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+  // the lookup makes the device's primary context current if none was; the
+  // address is kept only when the context it belongs to is known
+  if (have_id || current_context_id(&id))
+    g_entry[dev] = Entry{id, p};
+  else
+    g_entry[dev] = Entry{0, nullptr};
+  *out = p;
   return ATTN_OK;
 }
 
@@ -53,7 +103,8 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_noalloc(
     int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts,
     int64_t dv_hs, float* lse, int32_t* device_status, void* stream) {
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
-  if (attn_varlen_fvjp_workspace_size(B, Hq, total_q, total_k) > ATTN_NOALLOC_SCRATCH_BYTES)
+  // no dropout here, so the workspace's per-token rate table is not needed
+  if (attn::workspace_bytes_needed(B, Hq, total_q, false) > ATTN_NOALLOC_SCRATCH_BYTES)
     return ATTN_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   attn_status s = scratch_address(&scratch);

@@ -297,55 +297,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Warp-collective load of 16 consecutive fp32 columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Warp-collective load of 16 lanes x 64 columns (shape 16x256b, 8 repeats):
-// for every 8-column block j, thread t receives lanes (base + t/4, base + 8 +
-// t/4) x columns (8j + 2(t%4), 8j + 2(t%4) + 1), in the register order
-// v[4j] = (t/4, 2u), v[4j+1] = (t/4, 2u+1), v[4j+2] = (t/4+8, 2u),
-// v[4j+3] = (t/4+8, 2u+1) with u = t%4.
-__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Warp-collective store of 16 lanes x 32 columns (shape 16x128b, 8 repeats):
-// for every 4-column block j, thread t writes v[2j] to (base + t/4, 4j + t%4)
-// and v[2j+1] to (base + 8 + t/4, 4j + t%4).
-__device__ __forceinline__ void tmem_st16x128_x8(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
-}
-
 // Warp-collective store of 32 consecutive fp32 columns of this thread's lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -461,29 +412,10 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Elementwise operations on two fp32 values (kept as scalar operations: the
-// packed f32x2 forms constrain register pairing enough to cause spills in the
-// elementwise warps).
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                     float c0, float c1) {
-  d0 = fmaf(a0, b0, c0);
-  d1 = fmaf(a1, b1, c1);
-}
-__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  d0 = a0 * b0;
-  d1 = a1 * b1;
-}
-
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Byte offset of 16-byte unit `u` (0..7) of row `r` inside a 128-byte
-// swizzled tile whose 8-row groups are 1024 bytes apart.
-__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {
-  return (r >> 3) * 1024u + (r & 7u) * 128u + ((u ^ (r & 7u)) << 4);
 }
 
 }  // namespace attn

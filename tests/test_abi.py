@@ -104,6 +104,37 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     assert b"scratch" in lib.attn_status_string(-8)
 
 
+def test_noalloc_scratch_limit_is_the_documented_formula(lib):
+    """The header's size formula for the no-allocation call (status and
+    counters, schedule, fp32 D; no dropout rate table) decides acceptance:
+    the largest total_q that fits passes the size check, one more token is
+    refused.  A misaligned q makes the accepted call stop at the host checks,
+    so nothing is launched on any machine."""
+    A = lambda x: (x + 255) // 256 * 256
+    B, Hq, cap = 2, 96, 64 << 20
+
+    def need(tq):
+        return A(16 + 12 * max(Hq, 2)) + A(4 * (5 * B + 2)) + A(4 * tq * Hq)
+
+    tq = (cap - need(0)) // (4 * Hq)
+    while need(tq + 1) <= cap:
+        tq += 1
+    assert need(tq) <= cap < need(tq + 1)
+    fake, bad = 0x10000, 0x10008
+
+    def call(total_q):
+        args = [0, 2, Hq, 1, 160, total_q, 12,
+                bad, 96 * 160, 160, fake, 160, 160, fake, 160, 160, fake, 96 * 160, 160,
+                fake, fake, fake, 96, 0, -1, -1, 3.0, 0.75,
+                fake, 96 * 160, 160, fake, 96 * 160, 160, fake, 160, 160, fake, 160, 160,
+                fake, None, None]
+        return lib.attn_varlen_fvjp_fwd_bwd_noalloc(*args)
+
+    assert call(tq + 1) == -8
+    # past the size check: ALIGNMENT (-3) where a device exists, CUDA (-5) here
+    assert call(tq) in (-3, -5)
+
+
 def test_host_entry_point_validates_before_touching_the_device(lib):
     """The host-buffer entry point checks its arguments (and reads the host cu
     arrays) before any CUDA call: these all fail on a machine without a GPU

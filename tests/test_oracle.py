@@ -153,6 +153,26 @@ def test_alibi_distance_tables(oracle_mod, shape):
         torch.testing.assert_close(r["lse"][:, h], torch.from_numpy(lse), rtol=1e-13, atol=1e-14)
 
 
+@pytest.mark.parametrize("shape", sorted(ALIBI_TABLES))
+def test_alibi_negative_slope_favours_far_keys(oracle_mod, shape):
+    """A negative slope enters with its sign: with q = 0 the weights are
+    exp(|slope| * distance) normalised, largest at the farthest key."""
+    Lq, Lk = shape
+    p = f64_problem([Lq], [Lk], Hq=2, seed=3)
+    p.q.zero_()
+    p.alibi_slopes.copy_(torch.tensor([[-0.7, -0.05]]))
+    r = oracle_mod.fvjp(p)
+    dist = np.array(ALIBI_TABLES[shape], dtype=np.float64)
+    for h, slope in enumerate((-0.7, -0.05)):
+        w = np.exp(-f32(slope) * dist)
+        lse = np.log(w.sum(1))
+        w = w / w.sum(1, keepdims=True)
+        assert (w.argmax(1) == dist.argmax(1)).all()
+        expect = torch.from_numpy(w) @ p.v[:, 0]
+        torch.testing.assert_close(r["out"][:, h], expect, rtol=1e-13, atol=1e-14)
+        torch.testing.assert_close(r["lse"][:, h], torch.from_numpy(lse), rtol=1e-13, atol=1e-14)
+
+
 def test_alibi_equal_lengths_is_abs_i_minus_j(oracle_mod):
     """Equal lengths: Lq = Lk makes the distance |i - j|."""
     L = 7
@@ -382,6 +402,20 @@ def test_row_sampler_matches_full_pass(oracle_mod):
         assert torch.equal(s["out"][n], r["out"][t, h])
         assert torch.equal(s["dq"][n], r["dq"][t, h])
         assert float(s["lse"][n]) == float(r["lse"][t, h])
+
+
+@pytest.mark.parametrize("mask", [dict(), dict(causal=True), dict(window_left=3, window_right=1)])
+def test_key_sampler_matches_full_pass(oracle_mod, mask):
+    """The key sampler's dk/dv rows are the full pass's, bit for bit (it runs
+    the same row arithmetic without dq, then the same key pass), with several
+    K/V heads and empty sequences among the sampled ones."""
+    p = W.custom([5, 0, 9, 4], [7, 3, 12, 1], 8, seed=5, Hkv=2, **mask)
+    ref = oracle_mod.fvjp(p)
+    tok = torch.tensor([0, 6, 7, 9, 11, 21, 10, 22])
+    head = torch.tensor([0, 1, 1, 0, 1, 0, 0, 1], dtype=torch.int32)
+    r = oracle_mod.keys(p, tok, head)
+    for n in ("dk", "dv"):
+        assert torch.equal(r[n], ref[n][tok, head.long()]), n
 
 
 def test_strided_poisoned_views_match_dense(oracle_mod):

@@ -188,6 +188,35 @@ def test_masked_parity(oracle_mod, case):
     parity(p, oracle_mod)
 
 
+# ------------------------------------------------ negative ALiBi slopes
+# A negative slope makes the ALiBi term grow with the distance: the forward's
+# fixed softmax reference then sits at the row's farthest admissible key, and
+# dk/dv's per-key bias of a tile that straddles a column's aligned key takes
+# the slope's sign from the staged scalars.  Slopes here are drawn in
+# U(-0.25, 0.25) per (sequence, head), both signs in every sequence.
+
+NEG_SLOPES = [
+    dict(lq=[300, 129, 40], lk=[257, 400, 170], Hq=8),
+    dict(lq=[260, 90], lk=[300, 600], Hq=16, dtype=torch.bfloat16, causal=True),
+    dict(lq=[200, 300], lk=[350, 300], Hq=16, window_left=100, window_right=30),
+    dict(lq=[150, 64], lk=[400, 200], Hq=16, softcap=0.0),             # running max path
+    dict(lq=[130, 70], lk=[260, 500], Hq=16, Hkv=2, d=128, dtype=torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("case", NEG_SLOPES, ids=[f"neg{i}" for i in range(len(NEG_SLOPES))])
+def test_negative_slope_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    softcap = case.pop("softcap", None)
+    p = W.custom(lq, lk, Hq, slope_max=0.5, **case)
+    p.alibi_slopes = p.alibi_slopes - 0.25
+    assert (p.alibi_slopes < 0).any() and (p.alibi_slopes > 0).any()
+    if softcap is not None:
+        p.softcap = softcap
+    parity(p, oracle_mod)
+
+
 def test_window_wider_than_every_sequence_is_bitwise_unmasked():
     """A two-sided window that admits every pair takes the unmasked code path
     on every tile, so the result is bitwise the unmasked call's."""
@@ -541,9 +570,23 @@ def test_full_size_sampled(oracle_mod, name):
     check_tensor("out(sampled)", torch.stack(got_out), torch.stack(ref_out), p.dtype)
     check_tensor("dq(sampled)", torch.stack(got_dq), torch.stack(ref_dq), p.dtype)
     check_lse(torch.stack(got_lse), torch.stack(ref_lse))
-    # dk/dv in full on the cheapest sequences (by Lq*Lk), except for the
-    # balanced long case where every sequence is too large for the oracle
-    if name != "long_balanced":
+    # dk/dv: in full on the two cheapest sequences (by Lq*Lk); in the balanced
+    # long case, where every sequence is long, on 64 sampled keys of the
+    # cheapest one (their lse and D come from the oracle's own row pass over
+    # every head of that sequence)
+    if name == "long_balanced":
+        b = min(range(p.B), key=lambda i: lq[i] * lk[i])
+        L = lk[b]
+        kg = torch.Generator().manual_seed(7)
+        keys = sorted(set([0, 1, 127, 128, 129, L // 2, L - 129, L - 128, L - 2, L - 1] +
+                          torch.randint(0, L, (54,), generator=kg).tolist()))
+        sp = p.sequence(b)
+        ref = oracle_mod.keys(sp, keys, [0] * len(keys))
+        k0 = int(p.cu_k[b])
+        rows = torch.tensor(keys) + k0
+        check_tensor(f"dk(seq {b}, sampled keys)", r1["dk"][rows.cuda(), 0].cpu(), ref["dk"], p.dtype)
+        check_tensor(f"dv(seq {b}, sampled keys)", r1["dv"][rows.cuda(), 0].cpu(), ref["dv"], p.dtype)
+    else:
         work = sorted(range(p.B), key=lambda b: lq[b] * lk[b])
         for b in [w for w in work if lq[w] > 0 and lk[w] > 0][:2]:
             sp = p.sequence(b)

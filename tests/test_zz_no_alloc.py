@@ -10,7 +10,6 @@ never hides the rest of the suite.
 import pytest
 import torch
 
-from helpers import LSE_ATOL, MAX_ABS_FRAC, REL_FRO, rel_fro
 from ragged_gqa_attention_varlen_gb300 import binding as BND
 from ragged_gqa_attention_varlen_gb300 import workloads as W
 
@@ -26,19 +25,17 @@ def lib():
     return BND.load()
 
 
-def _close(name, x, ref, dtype):
-    x, ref = x.double().cpu(), ref.double().cpu()
-    assert torch.isfinite(x).all(), name
-    amax = float(ref.abs().max())
-    assert rel_fro(x, ref) <= REL_FRO[dtype], name
-    assert float((x - ref).abs().max()) <= MAX_ABS_FRAC * amax, name
+def _bits(x):
+    return x.contiguous().view(torch.int16 if x.element_size() == 2 else torch.int32)
 
 
 @pytest.mark.parametrize("order", ["large_then_small", "small_then_large"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(order):
     """Two calls in a row through the no-allocation entry point (different
     problem sizes, so the second inherits the first's scratch contents), each
-    matching the ordinary entry point on the same inputs."""
+    bitwise equal to the ordinary entry point on the same inputs: both run the
+    same kernels on the same schedule, so any difference (a counter or status
+    word left over from the previous call) shows."""
     probs = [W.q_short(length_scale=0.25).to("cuda"), W.tiny().to("cuda")]
     if order == "small_then_large":
         probs.reverse()
@@ -58,8 +55,5 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(order):
                                           p.scale_multiplier)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        for name, x in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv)):
-            _close(name, x, ref[name], p.dtype)
-        assert torch.equal(torch.isinf(lse), torch.isinf(ref["lse"]))
-        fin = torch.isfinite(ref["lse"])
-        assert float((lse[fin] - ref["lse"][fin]).abs().max()) <= LSE_ATOL
+        for name, x in (("out", out), ("dq", dq), ("dk", dk), ("dv", dv), ("lse", lse)):
+            assert torch.equal(_bits(x), _bits(ref[name])), name
