@@ -532,6 +532,89 @@ def run_shard(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_gated(args, world, rank, local):
+    """The sigmoid-gated variant on its own training-shape workload (8 causal
+    sequences, Lq = Lk ~ U[1024, 16384], Hq 32 over 8 K/V heads, bf16, head
+    size 128 and gate width 64 by default).  Counted flops per admissible
+    (query, key) pair and head: 4d + 2R forward (S, W V, gate logits) and
+    10d + 4R backward (the ungated 10d plus dq_g and dk_g); the roofline is
+    the whole call's executed MMA flops (18d + 10R: dq recomputes S, dP and
+    the gate logits, dk/dv recomputes S^T, dP^T and the gate logits) over its
+    time."""
+    from ragged_gqa_attention_varlen_gb300 import _build, binding
+
+    _build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = 128 if args.head_dim == HEAD_DIM else args.head_dim
+    R = args.gate_dim
+    p = workloads.gated(seed=6 + rank, device=dev, poison=False, length_scale=args.length_scale,
+                        d=d, R=R)
+    pairs = scored_pairs(p)
+    flops = (14.0 * d + 6.0 * R) * p.Hq * pairs
+    executed = (18.0 * d + 10.0 * R) * p.Hq * pairs
+    kw = dict(out=torch.empty(p.q.shape, dtype=p.q.dtype, device=dev),
+              dq=torch.empty(p.q.shape, dtype=p.q.dtype, device=dev),
+              dk=torch.empty(p.k.shape, dtype=p.k.dtype, device=dev),
+              dv=torch.empty(p.v.shape, dtype=p.v.dtype, device=dev),
+              dq_gate=torch.empty(p.q_gate.shape, dtype=p.q.dtype, device=dev),
+              dk_gate=torch.empty(p.k_gate.shape, dtype=p.q.dtype, device=dev),
+              lse=torch.empty((p.total_q, p.Hq), dtype=torch.float32, device=dev),
+              workspace=torch.empty(binding.workspace_size(p.B, p.Hq, p.total_q, p.total_k),
+                                    dtype=torch.uint8, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        binding.attention_varlen_gated(p.q, p.k, p.v, p.q_gate, p.k_gate, p.cu_q, p.cu_k,
+                                       p.alibi_slopes, p.dout, p.causal, p.window_left,
+                                       p.window_right, p.scale_multiplier, stream=stream, **kw)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    st = binding.device_status(kw["workspace"])
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x}")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        call()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    value, ms = aggregate(flops, start.elapsed_time(end) / 1e3, args.steps, world)
+    pk, kind = peaks()
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved = executed / (ms / 1e3) / 1e12
+    Hkv = p.k.shape[1]
+    line = {"metric": "gated fwd+full-VJP TFLOP/s & latency (pairwise sigmoid gate)",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, generated on device)",
+            "config": {"workload": "gated" + ("" if args.length_scale == 1.0
+                                               else f" x{args.length_scale} length"),
+                       "B": p.B, "Hq": p.Hq, "Hkv": Hkv, "head_dim": d, "gate_dim": R,
+                       "causal": True, "total_q": p.total_q, "scored_pairs": pairs,
+                       "counted_flops_per_pair_head": 14 * d + 6 * R,
+                       "counted_tflop_per_step": flops / 1e12},
+            "latency_ms": ms,
+            "roofline": {"bound": "tensor", "kernel": "whole call", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": None, "peak_kind": f"{kind} bf16 sustained"},
+            "gpu_launches": binding.launch_count(p.B, p.Hq, p.total_q, p.total_k,
+                                                 Hkv=Hkv) * args.steps,
+            "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def pinned_like(x: torch.Tensor) -> torch.Tensor:
     """A pinned host tensor with x's shape, strides and values (its whole
     storage copied, so padding keeps its place)."""
@@ -627,6 +710,9 @@ def main():
                     help="time with counter-based dropout at this rate")
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
+    ap.add_argument("--gated", action="store_true",
+                    help="time the sigmoid-gated variant on its own workload")
+    ap.add_argument("--gate-dim", type=int, default=64, help="gate width of --gated")
     ap.add_argument("--shard", action="store_true",
                     help="strong scaling: one batch split over the ranks by the shard plan")
     args = ap.parse_args()
@@ -637,6 +723,9 @@ def main():
         return run_reference(args, world, rank)
     if args.shard:
         run_shard(args, world, rank, local)
+        return 0
+    if args.gated:
+        run_gated(args, world, rank, local)
         return 0
     run_gpu(args, world, rank, local)
     return 0

@@ -316,6 +316,64 @@ attn_status attn_varlen_fvjp_fwd_bwd_host(
 int attn_varlen_host_chunks(int B, const int32_t *cu_q, const int32_t *cu_k, int chunks,
                             int32_t *cuts);
 
+/* The sigmoid-gated variant ("Pairwise-Gated Attention Engine", "Why it is
+ * hard"): each query-key pair also gets a gate from separate projections
+ * q_gate [total_q, Hq, gate_dim] and k_gate [total_k, Hkv, gate_dim],
+ *   G_ij = sigmoid(q_gate[i,h,:] . k_gate[j,g(h),:] / sqrt(gate_dim)),
+ * which scales the normalised attention weight:
+ *   out[i,h,:] = sum_j exp(z_ij - lse_ih) G_ij v[j,g(h),:],
+ * with z = (scale_multiplier / sqrt(head_dim)) q.k - ALiBi, masked as in
+ * the ungated call, and lse the ungated log-sum-exp (the gate sits outside
+ * the normalisation).  The page's attention is the plain softmax: there is
+ * no softcap argument (the logits are not capped) and no dropout.  The
+ * backward pass writes dq, dk, dv and the gate gradients dq_gate
+ * [total_q, Hq, gate_dim] and dk_gate [total_k, Hkv, gate_dim] (dk, dv and
+ * dk_gate summed over the query heads of each K/V head).
+ *
+ * head_dim must be 64 or 128 and gate_dim a multiple of 8 up to 64
+ * (ATTN_ERR_UNSUPPORTED otherwise); the gate tensors follow the layout and
+ * alignment rules of q and k (16-byte base, strides multiples of 8
+ * elements).  Other arguments, the workspace (attn_varlen_fvjp_workspace_size)
+ * and the error behaviour are those of attn_varlen_fvjp_fwd_bwd; every
+ * output, dk_gate rows of keys no query attends included, is fully
+ * overwritten, and repeated calls are bitwise identical. */
+attn_status attn_varlen_gated_fvjp_fwd_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int gate_dim,
+    int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const void *q_gate, int64_t qg_tok_stride, int64_t qg_head_stride,
+    const void *k_gate, int64_t kg_tok_stride, int64_t kg_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    void *dq_gate, int64_t dqg_tok_stride, int64_t dqg_head_stride,
+    void *dk_gate, int64_t dkg_tok_stride, int64_t dkg_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+/* The forward half of the gated call: out and lse only. */
+attn_status attn_varlen_gated_fwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int gate_dim,
+    int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *q_gate, int64_t qg_tok_stride, int64_t qg_head_stride,
+    const void *k_gate, int64_t kg_tok_stride, int64_t kg_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float scale_multiplier,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
 /* Shard plan of one batch over `nranks` processes (1..16), one GPU each.
  * Sequences are independent problems, so the batch shards by sequence with
  * no exchange of data.  Each sequence weighs Hq times its admissible

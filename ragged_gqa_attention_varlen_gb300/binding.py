@@ -26,7 +26,8 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
            "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_fwd_bwd_dropout",
            "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks",
-           "attn_varlen_shard_plan", "attn_varlen_sum_partials")
+           "attn_varlen_shard_plan", "attn_varlen_sum_partials",
+           "attn_varlen_gated_fvjp_fwd_bwd", "attn_varlen_gated_fwd")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -92,6 +93,14 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
         [P, L, L, P] + [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
     lib.attn_varlen_bwd_dropout.restype = I
+    lib.attn_varlen_gated_fvjp_fwd_bwd.argtypes = (
+        [I, I, I, I, I, I, L, L] + [P, L, L] * 6 + [P, P, P, L, I, I, I, F] + [P, L, L] * 6 +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_gated_fvjp_fwd_bwd.restype = I
+    lib.attn_varlen_gated_fwd.argtypes = (
+        [I, I, I, I, I, I, L, L] + [P, L, L] * 5 + [P, P, P, L, I, I, I, F] + [P, L, L] +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_gated_fwd.restype = I
     lib.attn_varlen_shard_plan.argtypes = [I, P, P, I, I, I, I, I, I, I, P, P, P, P, P]
     lib.attn_varlen_shard_plan.restype = I
     lib.attn_varlen_sum_partials.argtypes = [I, I, P, L, I, L, P, L, P]
@@ -483,6 +492,68 @@ def _noalloc_call(lib, q, k, v, cu_q, cu_k, alibi_slopes, dout, out, dq, dk, dv,
         _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
         _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
         _ptr(lse), _ptr(device_status), stream.cuda_stream)
+
+
+def attention_varlen_gated(q, k, v, q_gate, k_gate, cu_q, cu_k, alibi_slopes, dout=None,
+                           causal=False, window_left=-1, window_right=-1, scale_multiplier=1.0,
+                           out=None, dq=None, dk=None, dv=None, dq_gate=None, dk_gate=None,
+                           lse=None, workspace=None, stream=None):
+    """The sigmoid-gated call: with ``dout`` the fused forward and backward
+    (returns out, lse, dq, dk, dv, dq_gate, dk_gate, workspace), without it
+    the forward only (out, lse, workspace).  Head dimension 64 or 128, gate
+    width a multiple of 8 up to 64; no softcap (the gated page's plain
+    softmax)."""
+    lib = load()
+    dtype = q.dtype
+    Hq, R = q.shape[1], q_gate.shape[-1]
+    Hkv = _kv_heads(q, k)
+    for name, t, H in (("q", q, Hq), ("k", k, Hkv), ("v", v, Hkv)):
+        _check_qlike(name, t, dtype, H)
+    for name, t, H in (("q_gate", q_gate, Hq), ("k_gate", k_gate, Hkv)):
+        if not t.is_cuda or t.dtype != dtype or t.dim() != 3 or t.shape[1] != H or \
+                t.stride(-1) != 1 or t.shape[-1] != R:
+            raise ValueError(f"{name} must be a CUDA [tokens, {H}, R] tensor of {dtype} with a "
+                             "contiguous last axis")
+    B = cu_q.numel() - 1
+    Tq, Tk, d = q.shape[0], k.shape[0], q.shape[-1]
+    out = _like(q) if out is None else out
+    lse = torch.empty((Tq, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(B, Hq, Tq, Tk), 256), dtype=torch.uint8,
+                                device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    code_dt = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
+    head = [code_dt, B, Hq, Hkv, d, R, Tq, Tk, _ptr(q), q.stride(0), q.stride(1), _ptr(k),
+            k.stride(0), k.stride(1), _ptr(v), v.stride(0), v.stride(1)]
+    gates = [_ptr(q_gate), q_gate.stride(0), q_gate.stride(1), _ptr(k_gate), k_gate.stride(0),
+             k_gate.stride(1)]
+    mid = [_ptr(cu_q), _ptr(cu_k), _ptr(alibi_slopes),
+           alibi_slopes.stride(0) if alibi_slopes is not None else 0, int(bool(causal)),
+           int(window_left), int(window_right), float(scale_multiplier)]
+    tail = [_ptr(lse), _ptr(workspace), workspace.numel(), None, stream.cuda_stream]
+    if dout is None:
+        code = lib.attn_varlen_gated_fwd(*head, *gates, *mid, _ptr(out), out.stride(0),
+                                         out.stride(1), *tail)
+        if code != 0:
+            raise AttnError(code, lib.attn_status_string(code).decode())
+        return dict(out=out, lse=lse, workspace=workspace)
+    _check_qlike("dout", dout, dtype, Hq)
+    dq = _like(q) if dq is None else dq
+    dk = _like(k) if dk is None else dk
+    dv = _like(v) if dv is None else dv
+    dq_gate = _like(q_gate) if dq_gate is None else dq_gate
+    dk_gate = _like(k_gate) if dk_gate is None else dk_gate
+    code = lib.attn_varlen_gated_fvjp_fwd_bwd(
+        *head, _ptr(dout), dout.stride(0), dout.stride(1), *gates, *mid,
+        _ptr(out), out.stride(0), out.stride(1), _ptr(dq), dq.stride(0), dq.stride(1),
+        _ptr(dk), dk.stride(0), dk.stride(1), _ptr(dv), dv.stride(0), dv.stride(1),
+        _ptr(dq_gate), dq_gate.stride(0), dq_gate.stride(1),
+        _ptr(dk_gate), dk_gate.stride(0), dk_gate.stride(1), *tail)
+    if code != 0:
+        raise AttnError(code, lib.attn_status_string(code).decode())
+    return dict(out=out, lse=lse, dq=dq, dk=dk, dv=dv, dq_gate=dq_gate, dk_gate=dk_gate,
+                workspace=workspace)
 
 
 def shard_plan(cu_q, cu_k, Hq: int, Hkv: int, nranks: int, causal=False, window_left=-1,

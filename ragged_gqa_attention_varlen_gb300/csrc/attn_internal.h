@@ -74,6 +74,16 @@ struct Params {
   int32_t* counters;  // [3]: fwd, dkdv, dq tile counters (of this K/V head group)
   int ncounters;      // counters the schedule kernel resets (every group's)
   int32_t* sched;     // schedule arrays, see sched.cu
+  // sigmoid gate ("Pairwise-Gated Attention Engine", "Why it is hard"):
+  // G_ij = sigmoid(qg_i . kg_j / sqrt(R)) scales the normalised weight
+  const void* qg;     // [total_q, Hq, R] (null: no gate)
+  int64_t qg_ts, qg_hs;
+  void* dqg;
+  int64_t dqg_ts, dqg_hs;
+  void* dkg;          // [total_k, Hkv, R]
+  int64_t dkg_ts, dkg_hs;
+  int R;              // gate width (32 or 64)
+  float gscale;       // 1 / sqrt(R)
 };
 
 // 16-byte units (8 features) of a row's features [80*half, 80*half + 80)
@@ -116,6 +126,19 @@ cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s);
+// Gated kernels (gate.cu): head dimension 64 or 128, gate width padded to
+// 64 by the tensor maps.  Maps: *2 cover a whole 128-row tile (both 64-wide
+// chunks when d = 128), *g the gate projections.
+cudaError_t launch_gate_fwd(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqg,
+                            const CUtensorMap& tk, const CUtensorMap& tkg, const CUtensorMap& tv,
+                            int grid, cudaStream_t s);
+cudaError_t launch_gate_dq(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqg,
+                           const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tkg,
+                           const CUtensorMap& tv, int grid, cudaStream_t s);
+cudaError_t launch_gate_dkdv(const Params& p, const CUtensorMap& tq, const CUtensorMap& tqg,
+                             const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tkg,
+                             const CUtensorMap& tv, int grid, cudaStream_t s);
+
 cudaError_t launch_zero_fill(void* base, int64_t T, int H, int64_t ts, int64_t hs, int d,
                              cudaStream_t s);
 cudaError_t launch_fill_f32(float* base, int64_t n, float value, cudaStream_t s);

@@ -611,3 +611,285 @@ extern "C" attn_status attn_varlen_bwd_dropout(
                   dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
                   workspace_bytes, device_status, stream, dr);
 }
+
+// ------------------------------------------------------------------ gated
+
+namespace {
+
+// The sigmoid-gated call ("Pairwise-Gated Attention Engine", "Why it is
+// hard"): validation, tensor maps per K/V head group and the launches of the
+// requested passes (forward: schedule, forward per group; backward:
+// schedule, preprocess, dk/dv and dq per group).
+attn_status run_gated(
+    int mode, attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int gate_dim,
+    int64_t total_q, int64_t total_k, const void* q, int64_t q_ts, int64_t q_hs, const void* k,
+    int64_t k_ts, int64_t k_hs, const void* v, int64_t v_ts, int64_t v_hs, const void* dout,
+    int64_t do_ts, int64_t do_hs, const void* qg, int64_t qg_ts, int64_t qg_hs, const void* kg,
+    int64_t kg_ts, int64_t kg_hs, const int32_t* cu_q, const int32_t* cu_k,
+    const float* alibi_slopes, int64_t slopes_batch_stride, int causal, int window_left,
+    int window_right, float scale_multiplier, void* out, int64_t out_ts, int64_t out_hs,
+    void* dq, int64_t dq_ts, int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv,
+    int64_t dv_ts, int64_t dv_hs, void* dqg, int64_t dqg_ts, int64_t dqg_hs, void* dkg,
+    int64_t dkg_ts, int64_t dkg_hs, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* device_status, void* stream_ptr) {
+  const bool fwd = (mode & kModeFwd) != 0, bwd = (mode & kModeBwd) != 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
+  if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
+  if (head_dim != 128 && head_dim != 64) return ATTN_ERR_UNSUPPORTED;
+  if (gate_dim < 8 || gate_dim > 64 || gate_dim % 8) return ATTN_ERR_UNSUPPORTED;
+  if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
+  if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
+  if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 && (total_q != 0 || total_k != 0)) return ATTN_ERR_INVALID;
+  if (!(scale_multiplier == scale_multiplier)) return ATTN_ERR_INVALID;
+  if (B > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID;
+  if (alibi_slopes && slopes_batch_stride < Hq && B > 1) return ATTN_ERR_INVALID;
+  const bool has_q = total_q > 0, has_k = total_k > 0;
+  if (has_q && (!q || !qg || !out || !lse)) return ATTN_ERR_INVALID;
+  if (has_q && bwd && (!dout || !dq || !dqg)) return ATTN_ERR_INVALID;
+  if (has_k && (!k || !v || !kg)) return ATTN_ERR_INVALID;
+  if (has_k && bwd && (!dk || !dv || !dkg)) return ATTN_ERR_INVALID;
+  if (has_q) {
+    for (const void* ptr : {q, qg, static_cast<const void*>(out)})
+      if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+    for (int64_t s : {q_ts, q_hs, qg_ts, qg_hs, out_ts, out_hs})
+      if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (bwd) {
+      for (const void* ptr : {dout, static_cast<const void*>(dq), static_cast<const void*>(dqg)})
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+      for (int64_t s : {do_ts, do_hs, dq_ts, dq_hs, dqg_ts, dqg_hs})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    }
+  }
+  if (has_k) {
+    for (const void* ptr : {k, v, kg})
+      if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+    for (int64_t s : {k_ts, v_ts, kg_ts})
+      if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (Hkv > 1)
+      for (int64_t s : {k_hs, v_hs, kg_hs})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    if (bwd) {
+      for (const void* ptr : {static_cast<const void*>(dk), static_cast<const void*>(dv),
+                              static_cast<const void*>(dkg)})
+        if (!aligned16(ptr)) return ATTN_ERR_ALIGNMENT;
+      for (int64_t s : {dk_ts, dv_ts, dkg_ts})
+        if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+      if (Hkv > 1)
+        for (int64_t s : {dk_hs, dv_hs, dkg_hs})
+          if (!stride_ok(s)) return ATTN_ERR_ALIGNMENT;
+    }
+  }
+  const WsLayout ws = ws_layout(B, Hq, total_q);
+  if (!workspace || workspace_bytes < ws.droptab ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_WORKSPACE;
+
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  p.dtype = dtype;
+  p.B = B;
+  p.Hq = Hq;
+  p.G = head_group(Hq / Hkv);
+  p.d = head_dim;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.out = out;
+  p.out_ts = out_ts;
+  p.out_hs = out_hs;
+  p.dq = dq;
+  p.dq_ts = dq_ts;
+  p.dq_hs = dq_hs;
+  p.dk = dk;
+  p.dk_ts = dk_ts;
+  p.dk_hs = Hkv > 1 ? dk_hs : 0;
+  p.dv = dv;
+  p.dv_ts = dv_ts;
+  p.dv_hs = Hkv > 1 ? dv_hs : 0;
+  p.Hkv = Hkv;
+  p.outp = out;
+  p.dout = dout;
+  p.q = q;
+  p.q_ts = q_ts;
+  p.q_hs = q_hs;
+  p.do_ts = do_ts;
+  p.do_hs = do_hs;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.slopes = alibi_slopes;
+  p.slopes_bs = slopes_batch_stride;
+  p.causal = causal ? 1 : 0;
+  p.wl = window_left;
+  p.wr = window_right;
+  p.softcap = 0.f;
+  p.sigma = static_cast<float>(static_cast<double>(scale_multiplier) /
+                               std::sqrt(static_cast<double>(head_dim)));
+  p.lse = lse;
+  p.lse_rs = Hq;
+  p.Dbuf = reinterpret_cast<float*>(wsb + ws.dbuf);
+  p.status = device_status ? device_status : reinterpret_cast<int32_t*>(wsb + ws.status);
+  p.counters = reinterpret_cast<int32_t*>(wsb + ws.counters);
+  p.ncounters = 3 * Hkv;
+  p.sched = reinterpret_cast<int32_t*>(wsb + ws.sched);
+  p.qg = qg;
+  p.qg_ts = qg_ts;
+  p.qg_hs = qg_hs;
+  p.dqg = dqg;
+  p.dqg_ts = dqg_ts;
+  p.dqg_hs = dqg_hs;
+  p.dkg = bwd ? dkg : nullptr;
+  p.dkg_ts = dkg_ts;
+  p.dkg_hs = Hkv > 1 ? dkg_hs : 0;
+  p.R = gate_dim;
+  p.gscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(gate_dim)));
+
+  if (!has_q || !has_k) {
+    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (has_k && bwd) {  // no queries: dk = dv = dk_g = 0
+      e = launch_zero_fill(dk, total_k, Hkv, dk_ts, Hkv > 1 ? dk_hs : 8, head_dim, stream);
+      if (e == cudaSuccess)
+        e = launch_zero_fill(dv, total_k, Hkv, dv_ts, Hkv > 1 ? dv_hs : 8, head_dim, stream);
+      if (e == cudaSuccess)
+        e = launch_zero_fill(dkg, total_k, Hkv, dkg_ts, Hkv > 1 ? dkg_hs : 8, gate_dim, stream);
+    }
+    if (has_q) {  // no keys: every row is empty
+      if (fwd) {
+        if (e == cudaSuccess)
+          e = launch_zero_fill(out, total_q, Hq, out_ts, out_hs, head_dim, stream);
+        if (e == cudaSuccess) e = launch_fill_f32(lse, total_q * Hq, -INFINITY, stream);
+      }
+      if (bwd && e == cudaSuccess)
+        e = launch_zero_fill(dq, total_q, Hq, dq_ts, dq_hs, head_dim, stream);
+      if (bwd && e == cudaSuccess)
+        e = launch_zero_fill(dqg, total_q, Hq, dqg_ts, dqg_hs, gate_dim, stream);
+    }
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+
+  if (!encode_fn()) return ATTN_ERR_CUDA;
+  const int R = Hq / Hkv;
+  auto off = [](const void* base, int64_t elems) -> uint16_t* {
+    return base ? const_cast<uint16_t*>(static_cast<const uint16_t*>(base)) + elems : nullptr;
+  };
+  auto group_params = [&](int g) {
+    Params pg = p;
+    pg.Hq = R;
+    const int64_t h0 = static_cast<int64_t>(g) * R;
+    pg.q = off(q, h0 * q_hs);
+    pg.out = off(out, h0 * out_hs);
+    pg.outp = pg.out;
+    pg.dq = off(dq, h0 * dq_hs);
+    pg.dout = off(dout, h0 * do_hs);
+    pg.dk = off(dk, static_cast<int64_t>(g) * dk_hs);
+    pg.dv = off(dv, static_cast<int64_t>(g) * dv_hs);
+    pg.qg = off(qg, h0 * qg_hs);
+    pg.dqg = off(dqg, h0 * dqg_hs);
+    pg.dkg = off(dkg, static_cast<int64_t>(g) * dkg_hs);
+    pg.lse = lse + h0;
+    pg.Dbuf = p.Dbuf + h0;
+    pg.slopes = alibi_slopes ? alibi_slopes + h0 : nullptr;
+    pg.counters = p.counters + 3 * g;
+    pg.head0 = static_cast<int>(h0);
+    return pg;
+  };
+  struct Maps {
+    CUtensorMap tq, tqg, tdo, tk, tkg, tv;
+  };
+  // a 128-row tile of head_dim features: both 64-wide chunks in one box
+  // when head_dim = 128; the gate projections as one 64-wide box (zeros
+  // past gate_dim)
+  auto encode_group = [&](const Params& pg, int g, Maps& m) -> bool {
+    const void* kgrp = static_cast<const uint16_t*>(k) + static_cast<int64_t>(g) * k_hs;
+    const void* vgrp = static_cast<const uint16_t*>(v) + static_cast<int64_t>(g) * v_hs;
+    const void* kggrp = static_cast<const uint16_t*>(kg) + static_cast<int64_t>(g) * kg_hs;
+    const bool two = head_dim == 128;
+    bool ok = two ? encode_q_pair(&m.tq, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ)
+                  : encode_q(&m.tq, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ);
+    ok = ok && encode_q(&m.tqg, dtype, gate_dim, pg.qg, total_q, R, qg_ts, qg_hs, p.G, kRowsQ);
+    ok = ok && (two ? encode_kv_pair(&m.tk, dtype, head_dim, kgrp, total_k, k_ts)
+                    : encode_kv(&m.tk, dtype, head_dim, kgrp, total_k, k_ts));
+    ok = ok && (two ? encode_kv_pair(&m.tv, dtype, head_dim, vgrp, total_k, v_ts)
+                    : encode_kv(&m.tv, dtype, head_dim, vgrp, total_k, v_ts));
+    ok = ok && encode_kv(&m.tkg, dtype, gate_dim, kggrp, total_k, kg_ts);
+    if (bwd)
+      ok = ok && (two ? encode_q_pair(&m.tdo, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs,
+                                      p.G, kRowsQ)
+                      : encode_q(&m.tdo, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs,
+                                 p.G, kRowsQ));
+    return ok;
+  };
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int64_t rows_tok = kRowsQ / p.G;
+  const int64_t qtiles_max = (total_q / rows_tok + B) * (R / p.G);
+  const int64_t ktiles_max = total_k / kKeys + B;
+  const int grid_q = static_cast<int>(qtiles_max < sms ? qtiles_max : sms);
+  const int grid_k = static_cast<int>(ktiles_max < sms ? ktiles_max : sms);
+  Params p0 = group_params(0);
+  p0.counters = p.counters;
+  if (launch_sched(p0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  Maps m;
+  if (fwd) {
+    for (int g = 0; g < Hkv; ++g) {
+      const Params pg = group_params(g);
+      if (!encode_group(pg, g, m)) return ATTN_ERR_ALIGNMENT;
+      if (launch_gate_fwd(pg, m.tq, m.tqg, m.tk, m.tkg, m.tv, grid_q, stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    }
+  }
+  if (!bwd) return ATTN_OK;
+  if (launch_preprocess(p, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  for (int g = 0; g < Hkv; ++g) {
+    const Params pg = group_params(g);
+    if (!encode_group(pg, g, m)) return ATTN_ERR_ALIGNMENT;
+    if (launch_gate_dkdv(pg, m.tq, m.tqg, m.tdo, m.tk, m.tkg, m.tv, grid_k, stream) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (launch_gate_dq(pg, m.tq, m.tqg, m.tdo, m.tk, m.tkg, m.tv, grid_q, stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_varlen_gated_fvjp_fwd_bwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int gate_dim, int64_t total_q,
+    int64_t total_k, const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts,
+    int64_t k_hs, const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts,
+    int64_t do_hs, const void* q_gate, int64_t qg_ts, int64_t qg_hs, const void* k_gate,
+    int64_t kg_ts, int64_t kg_hs, const int32_t* cu_q, const int32_t* cu_k,
+    const float* alibi_slopes, int64_t slopes_batch_stride, int causal, int window_left,
+    int window_right, float scale_multiplier, void* out, int64_t out_ts, int64_t out_hs,
+    void* dq, int64_t dq_ts, int64_t dq_hs, void* dk, int64_t dk_ts, int64_t dk_hs, void* dv,
+    int64_t dv_ts, int64_t dv_hs, void* dq_gate, int64_t dqg_ts, int64_t dqg_hs, void* dk_gate,
+    int64_t dkg_ts, int64_t dkg_hs, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* device_status, void* stream) {
+  return run_gated(kModeFwd | kModeBwd, dtype, B, Hq, Hkv, head_dim, gate_dim, total_q, total_k,
+                   q, q_ts, q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, q_gate, qg_ts,
+                   qg_hs, k_gate, kg_ts, kg_hs, cu_q, cu_k, alibi_slopes, slopes_batch_stride,
+                   causal, window_left, window_right, scale_multiplier, out, out_ts, out_hs, dq,
+                   dq_ts, dq_hs, dk, dk_ts, dk_hs, dv, dv_ts, dv_hs, dq_gate, dqg_ts, dqg_hs,
+                   dk_gate, dkg_ts, dkg_hs, lse, workspace, workspace_bytes, device_status,
+                   stream);
+}
+
+extern "C" attn_status attn_varlen_gated_fwd(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int gate_dim, int64_t total_q,
+    int64_t total_k, const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts,
+    int64_t k_hs, const void* v, int64_t v_ts, int64_t v_hs, const void* q_gate, int64_t qg_ts,
+    int64_t qg_hs, const void* k_gate, int64_t kg_ts, int64_t kg_hs, const int32_t* cu_q,
+    const int32_t* cu_k, const float* alibi_slopes, int64_t slopes_batch_stride, int causal,
+    int window_left, int window_right, float scale_multiplier, void* out, int64_t out_ts,
+    int64_t out_hs, float* lse, void* workspace, size_t workspace_bytes, int32_t* device_status,
+    void* stream) {
+  return run_gated(kModeFwd, dtype, B, Hq, Hkv, head_dim, gate_dim, total_q, total_k, q, q_ts,
+                   q_hs, k, k_ts, k_hs, v, v_ts, v_hs, nullptr, 0, 0, q_gate, qg_ts, qg_hs,
+                   k_gate, kg_ts, kg_hs, cu_q, cu_k, alibi_slopes, slopes_batch_stride, causal,
+                   window_left, window_right, scale_multiplier, out, out_ts, out_hs, nullptr, 0,
+                   0, nullptr, 0, 0, nullptr, 0, 0, nullptr, 0, 0, nullptr, 0, 0, lse,
+                   workspace, workspace_bytes, device_status, stream);
+}

@@ -195,6 +195,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Params p) {
         dk[u] = make_uint4(0u, 0u, 0u, 0u);
         dv[u] = make_uint4(0u, 0u, 0u, 0u);
       }
+      if (p.dkg) {  // the gate's key projections (gated calls)
+        uint4* dg = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dkg) + krow * p.dkg_ts +
+                                             g * p.dkg_hs);
+        for (int u = 0; u < p.R / 8; ++u) dg[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 }

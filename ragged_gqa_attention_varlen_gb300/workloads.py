@@ -76,6 +76,9 @@ class Problem:
         out = Problem(**{**self.__dict__})
         for name in ("q", "k", "v", "dout"):
             out.__dict__[name] = _copy_view(getattr(self, name), device)
+        for name in ("q_gate", "k_gate"):
+            if getattr(self, name) is not None:
+                out.__dict__[name] = _copy_view(getattr(self, name), device)
         out.cu_q = self.cu_q.to(device)
         out.cu_k = self.cu_k.to(device)
         out.alibi_slopes = self.alibi_slopes.to(device)
@@ -263,13 +266,15 @@ def gated(seed=6, device="cpu", length_scale=1.0, d=128, R=64, Hq=32, Hkv=8, poi
     Engine", "The task": head sizes 64 and 128, gate sizes 32 and 64,
     grouped K/V heads, sequences up to 16,384 tokens): 8 causal sequences with
     Lq = Lk ~ U[1024, 16384], bf16, dense layouts, no softcap and no ALiBi
-    (the page's plain softmax), q/k/v/dout and the gate projections N(0,1)."""
+    (the page's plain softmax with logits q.k / sqrt(d): scale multiplier 1),
+    q/k/v/dout and the gate projections N(0,1)."""
     g = torch.Generator().manual_seed(seed)
     B = 8
     L = _scale(_uniform_int(g, 1024, 16384, B), length_scale)
     p = build("gated", L, list(L), Hq, torch.bfloat16, 1, d, torch.zeros(B, Hq), seed=seed,
               device=device, poison=poison, Hkv=Hkv, d=d, causal=True)
     p.softcap = 0.0
+    p.scale_multiplier = 1.0
     gg = torch.Generator(device=device).manual_seed(seed * 7 + 1)
     p.q_gate = torch.randn((sum(L), Hq, R), generator=gg, dtype=torch.float32,
                            device=device).to(torch.bfloat16)

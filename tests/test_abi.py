@@ -233,3 +233,31 @@ def test_python_host_entry_point_rejects_device_layout_errors(lib):
         q = torch.zeros((p.q.shape[0], 7, 160), dtype=p.q.dtype)
         k = torch.zeros((p.k.shape[0], 2, 160), dtype=p.q.dtype)
         binding.attention_varlen_fvjp_host(q, k, k, p.cu_q, p.cu_k, None, q)
+
+
+def _gated_call(lib, **over):
+    """A gated call whose arguments fail host validation (fake pointers are
+    never dereferenced)."""
+    fake = 0x10000
+    a = dict(dtype=1, B=2, Hq=8, Hkv=2, hd=128, R=64, tq=10, tk=12,
+             q=fake, qts=8 * 128, qhs=128, k=fake, kts=2 * 128, khs=128, v=fake, vts=2 * 128,
+             vhs=128, do=fake, dts=8 * 128, dhs=128, qg=fake, qgts=8 * 64, qghs=64, kg=fake,
+             kgts=2 * 64, kghs=64, cuq=fake, cuk=fake, sl=None, slb=0, causal=1, wl=-1, wr=-1,
+             sm=1.0, out=fake, ots=8 * 128, ohs=128, dq=fake, dqts=8 * 128, dqhs=128,
+             dk=fake, dkts=2 * 128, dkhs=128, dv=fake, dvts=2 * 128, dvhs=128,
+             dqg=fake, dqgts=8 * 64, dqghs=64, dkg=fake, dkgts=2 * 64, dkghs=64,
+             lse=fake, ws=fake, wsb=0, st=None, stream=None)
+    a.update(over)
+    return lib.attn_varlen_gated_fvjp_fwd_bwd(*a.values())
+
+
+def test_gated_host_validation_codes(lib):
+    assert _gated_call(lib) == -4                 # valid up to the missing workspace
+    assert _gated_call(lib, hd=160) == -2         # head dimensions 64 and 128 only
+    assert _gated_call(lib, R=72) == -2           # gate width up to 64
+    assert _gated_call(lib, R=20) == -2           # ... in multiples of 8
+    assert _gated_call(lib, hd=64, R=32) == -4
+    assert _gated_call(lib, qg=0x10008) == -3     # gate base not 16-byte aligned
+    assert _gated_call(lib, kgts=2 * 64 + 4) == -3
+    assert _gated_call(lib, dkg=None) == -1       # the backward needs both gate gradients
+    assert _gated_call(lib, Hkv=3) == -1
