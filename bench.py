@@ -644,8 +644,8 @@ def run_e2e(args, p, kw, flops, stream, world):
                 dv=torch.empty(p.v.shape, dtype=p.v.dtype, pin_memory=True),
                 lse=torch.empty((p.total_q, p.Hq), dtype=torch.float32, pin_memory=True),
                 host_status=torch.zeros(chunks, dtype=torch.int32, pin_memory=True))
-    buf = torch.empty(binding.host_buffer_size(p.B, p.Hq, args.hkv, d, p.total_q, p.total_k,
-                                               chunks), dtype=torch.uint8, device=p.q.device)
+    buf = torch.empty(binding.host_buffer_size_for(p.cu_q, p.cu_k, p.Hq, args.hkv, d, chunks),
+                      dtype=torch.uint8, device=p.q.device)
     # bytes the call moves: the elements of every input and output (padding
     # between heads or tokens is not copied), the rebased cu arrays, slopes
     h2d = (2 * p.q.numel() + 2 * p.k.numel()) * p.q.element_size() + \
@@ -684,7 +684,10 @@ def run_e2e(args, p, kw, flops, stream, world):
     value, ms = aggregate(flops, start.elapsed_time(end) / 1e3, args.steps, world)
     nc = min(chunks, max(p.B, 1))
     return {"value": value, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "chunks": chunks, "gpu_launches": binding.launch_count(
+            "d2h_bytes_per_step": d2h, "chunks": chunks,
+            "device_buffer_gb": buf.numel() / 1e9,
+            "link_gbs_average": (h2d + d2h) / (ms / 1e3) / 1e9,
+            "gpu_launches": binding.launch_count(
                 p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * nc * args.steps}
 
 

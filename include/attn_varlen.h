@@ -269,19 +269,23 @@ attn_status attn_varlen_bwd_dropout(
  * end-to-end path.
  *
  * The batch is cut into `chunks` runs of whole sequences of about equal
- * sum Lq*Lk.  Chunk c's inputs are copied to the device on one internal
- * stream while chunk c - 1 computes on `stream` and chunk c - 2's results
- * are copied back on another internal stream, so copies overlap the kernels.
- * Sequences are independent, so each sequence's out, lse, dq, dk, dv are
- * bitwise those of attn_varlen_fvjp_fwd_bwd on device copies of the inputs,
- * whatever the chunking.
+ * sum Lq*Lk.  Each chunk goes through one of up to four slots of the device
+ * buffer: its inputs are copied in on one internal stream (once the slot's
+ * previous chunk has been copied out), it computes on one of two internal
+ * compute streams (chunks alternate between them, so one chunk's first
+ * kernels overlap the last kernels of the one before), and its results are
+ * copied back on another internal stream.  Sequences are independent, so
+ * each sequence's out, lse, dq, dk, dv are bitwise those of
+ * attn_varlen_fvjp_fwd_bwd on device copies of the inputs, whatever the
+ * chunking.
  *
  * Arguments: those of attn_varlen_fvjp_fwd_bwd with HOST pointers for q, k,
  * v, dout, cu_q, cu_k, alibi_slopes (or NULL), out, dq, dk, dv and lse (same
  * shapes and stride rules; host memory should be page-locked for the copies
  * to run asynchronously), plus `device_buffer` (a DEVICE array of at least
- * attn_varlen_fvjp_host_buffer_size bytes, 256-byte aligned, owned by the
- * caller; it holds dense device copies and the workspace) and `host_status`
+ * attn_varlen_fvjp_host_buffer_size_for bytes, 256-byte aligned, owned by the
+ * caller; its slots hold dense device copies of one chunk each and its
+ * workspace) and `host_status`
  * (HOST, `chunks` int32 words: the device status word of each chunk, 0 when
  * clean; written when the stream reaches the end of the call).  The call
  * reads the host cu arrays before it returns (to cut the chunks); the other
@@ -290,7 +294,11 @@ attn_status attn_varlen_bwd_dropout(
  * time when their heads are dense (head stride = head_dim), else one
  * (token, head) row at a time; feature padding is neither read nor written.
  * Errors as for attn_varlen_fvjp_fwd_bwd; ATTN_ERR_WORKSPACE when the device
- * buffer is too small; ATTN_ERR_INVALID when chunks < 1. */
+ * buffer is too small; ATTN_ERR_INVALID when chunks < 1.  An error found
+ * after the first chunk was enqueued (a failed CUDA call) returns with the
+ * caller's stream waiting for the work already enqueued: the output host
+ * arrays may then hold the results of the earlier chunks, and host_status
+ * is not written (its copy is enqueued last). */
 attn_status attn_varlen_fvjp_fwd_bwd_host(
     attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
     const void *q, int64_t q_tok_stride, int64_t q_head_stride,
@@ -413,7 +421,16 @@ attn_status attn_varlen_sum_partials(attn_dtype dtype, int nparts, const void *c
                                      int64_t rows, int d, int64_t part_row_stride, void *out,
                                      int64_t out_row_stride, void *stream);
 
-/* Bytes of device buffer attn_varlen_fvjp_fwd_bwd_host needs. */
+/* Bytes of device buffer attn_varlen_fvjp_fwd_bwd_host needs for these
+ * lengths (HOST cu arrays): the status words, cu arrays and slopes, and
+ * min(4, number of chunks) slots sized for the largest chunk -- about
+ * min(4, chunks)/chunks of the batch's dense copies.  0 for invalid
+ * arguments. */
+size_t attn_varlen_fvjp_host_buffer_size_for(int B, const int32_t *cu_q, const int32_t *cu_k,
+                                              int Hq, int Hkv, int head_dim, int chunks);
+
+/* An upper bound of attn_varlen_fvjp_host_buffer_size_for over every length
+ * split with these totals (each slot sized for the whole batch). */
 size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim, int64_t total_q,
                                           int64_t total_k, int chunks);
 

@@ -24,7 +24,8 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
            "attn_varlen_fvjp_fwd_bwd_noalloc", "attn_varlen_fwd", "attn_varlen_bwd",
            "attn_varlen_launch_count", "attn_varlen_fvjp_fwd_bwd_host",
-           "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_fwd_bwd_dropout",
+           "attn_varlen_fvjp_host_buffer_size", "attn_varlen_fvjp_host_buffer_size_for",
+           "attn_varlen_fvjp_fwd_bwd_dropout",
            "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks",
            "attn_varlen_shard_plan", "attn_varlen_sum_partials",
            "attn_varlen_gated_fvjp_fwd_bwd", "attn_varlen_gated_fwd")
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
     lib.attn_varlen_fvjp_fwd_bwd_host.restype = I
     lib.attn_varlen_fvjp_host_buffer_size.argtypes = [I, I, I, I, L, L, I]
     lib.attn_varlen_fvjp_host_buffer_size.restype = ctypes.c_size_t
+    lib.attn_varlen_fvjp_host_buffer_size_for.argtypes = [I, P, P, I, I, I, I]
+    lib.attn_varlen_fvjp_host_buffer_size_for.restype = ctypes.c_size_t
     lib.attn_varlen_host_chunks.argtypes = [I, P, P, I, P]
     lib.attn_varlen_host_chunks.restype = I
     DR = [ctypes.c_uint64, F, P]  # dropout seed, rate, per-token rates
@@ -363,6 +366,15 @@ def _check_lse(lse, Tq, Hq):
         raise ValueError(f"lse must be a contiguous fp32 [{Tq}, {Hq}] CUDA tensor")
 
 
+def host_buffer_size_for(cu_q, cu_k, Hq: int, Hkv: int, d: int, chunks: int) -> int:
+    """Device buffer bytes of the host-buffer call for these lengths (host
+    int32 cu arrays)."""
+    cq = cu_q.detach().to("cpu", torch.int32).contiguous()
+    ck = cu_k.detach().to("cpu", torch.int32).contiguous()
+    return int(load().attn_varlen_fvjp_host_buffer_size_for(cq.numel() - 1, _ptr(cq), _ptr(ck),
+                                                            Hq, Hkv, d, chunks))
+
+
 def host_buffer_size(B: int, Hq: int, Hkv: int, d: int, total_q: int, total_k: int,
                      chunks: int) -> int:
     return int(load().attn_varlen_fvjp_host_buffer_size(B, Hq, Hkv, d, total_q, total_k, chunks))
@@ -429,7 +441,7 @@ def attention_varlen_fvjp_host(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=F
     if host_status is None:
         host_status = torch.zeros(chunks, dtype=torch.int32, pin_memory=True)
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    nbytes = host_buffer_size(B, Hq, Hkv, d, Tq, Tk, chunks)
+    nbytes = host_buffer_size_for(cu_q, cu_k, Hq, Hkv, d, chunks)
     if device_buffer is None:
         device_buffer = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
     if stream is None:

@@ -19,14 +19,21 @@ namespace {
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+constexpr int kMaxSlots = 4;   // chunks in flight: copies in, two computing, copies out
+constexpr int kCompStreams = 2;
 
-// Offsets in the caller's device buffer.  Device copies are dense:
-// [T, H, d] with token stride H*d and head stride d.
+// Offsets in the caller's device buffer: the shared part (status words of
+// every chunk, rebased cu arrays, slopes), then `slots` ring slots, each
+// holding one chunk's workspace and dense device copies [T, H, d] (token
+// stride H*d, head stride d) sized for the largest chunk.
 struct Layout {
-  size_t ws, ws_bytes, status, cu, slopes, q, dout, out, dq, k, v, dk, dv, lse, total;
+  size_t status, cu, slopes, slot0, slot_bytes, total;
+  size_t ws, ws_bytes, q, dout, out, dq, k, v, dk, dv, lse;  // offsets within a slot
+  int slots;
 };
 
-Layout layout(int B, int Hq, int Hkv, int d, int64_t Tq, int64_t Tk, int chunks) {
+Layout layout(int B, int Hq, int Hkv, int d, int chunks, int nslots, int Bc, int64_t Tq,
+              int64_t Tk) {
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -34,11 +41,13 @@ Layout layout(int B, int Hq, int Hkv, int d, int64_t Tq, int64_t Tk, int chunks)
     off = align_up(off + bytes);
     return at;
   };
-  L.ws_bytes = attn_varlen_fvjp_workspace_size(B, Hq, Tq, Tk);
-  L.ws = take(L.ws_bytes);
   L.status = take(sizeof(int32_t) * static_cast<size_t>(chunks));
   L.cu = take(sizeof(int32_t) * 2 * static_cast<size_t>(B + chunks));  // cu_q, then cu_k
   L.slopes = take(sizeof(float) * static_cast<size_t>(B) * Hq);
+  L.slot0 = off;
+  off = 0;
+  L.ws_bytes = attn_varlen_fvjp_workspace_size(Bc, Hq, Tq, Tk);
+  L.ws = take(L.ws_bytes);
   const size_t qbytes = static_cast<size_t>(Tq) * Hq * d * 2;
   const size_t kbytes = static_cast<size_t>(Tk) * Hkv * d * 2;
   L.q = take(qbytes);
@@ -50,13 +59,26 @@ Layout layout(int B, int Hq, int Hkv, int d, int64_t Tq, int64_t Tk, int chunks)
   L.dk = take(kbytes);
   L.dv = take(kbytes);
   L.lse = take(sizeof(float) * static_cast<size_t>(Tq) * Hq);
-  L.total = off;
+  L.slot_bytes = off;
+  L.slots = nslots;
+  L.total = L.slot0 + static_cast<size_t>(nslots) * L.slot_bytes;
   return L;
 }
 
+// The chunking of these lengths and the layout its largest chunk needs.
+struct Plan {
+  std::vector<int32_t> cut;
+  int nc;
+  Layout L;
+};
+
+Plan plan_of(int B, const int32_t* cu_q, const int32_t* cu_k, int Hq, int Hkv, int d,
+             int chunks);
+
 // Rows [r0, r1) of a 16-bit [T, H, d] tensor between host (strides ts, hs in
-// elements) and a dense device copy.  One 2-D copy when the host heads are
-// dense, else one per head; feature padding is never touched.
+// elements) and a dense device copy whose first row is r0.  One 2-D copy
+// when the host heads are dense, else one per head; feature padding is never
+// touched.
 cudaError_t copy_rows(bool to_device, void* dev, const void* host_c, int64_t ts, int64_t hs,
                       int H, int d, int64_t r0, int64_t r1, cudaStream_t s) {
   if (r1 <= r0) return cudaSuccess;
@@ -65,15 +87,14 @@ cudaError_t copy_rows(bool to_device, void* dev, const void* host_c, int64_t ts,
   const size_t drow = static_cast<size_t>(H) * d * 2;  // device token stride (bytes)
   const size_t hpitch = static_cast<size_t>(ts) * 2;
   const size_t rows = static_cast<size_t>(r1 - r0);
+  uint8_t* h = host + static_cast<size_t>(r0) * hpitch;
   if (H == 1 || hs == d) {
-    uint8_t* h = host + static_cast<size_t>(r0) * hpitch;
-    uint8_t* g = devb + static_cast<size_t>(r0) * drow;
-    return to_device ? cudaMemcpy2DAsync(g, drow, h, hpitch, drow, rows, cudaMemcpyHostToDevice, s)
-                     : cudaMemcpy2DAsync(h, hpitch, g, drow, drow, rows, cudaMemcpyDeviceToHost, s);
+    return to_device ? cudaMemcpy2DAsync(devb, drow, h, hpitch, drow, rows, cudaMemcpyHostToDevice, s)
+                     : cudaMemcpy2DAsync(h, hpitch, devb, drow, drow, rows, cudaMemcpyDeviceToHost, s);
   }
-  for (int h = 0; h < H; ++h) {
-    uint8_t* hp = host + static_cast<size_t>(r0) * hpitch + static_cast<size_t>(h) * hs * 2;
-    uint8_t* gp = devb + static_cast<size_t>(r0) * drow + static_cast<size_t>(h) * d * 2;
+  for (int hh = 0; hh < H; ++hh) {
+    uint8_t* hp = h + static_cast<size_t>(hh) * hs * 2;
+    uint8_t* gp = devb + static_cast<size_t>(hh) * d * 2;
     const cudaError_t e =
         to_device
             ? cudaMemcpy2DAsync(gp, drow, hp, hpitch, static_cast<size_t>(d) * 2, rows,
@@ -96,13 +117,13 @@ bool host_strides_ok(int64_t ts, int64_t hs, int H, int d) {
 // The streams and events of one call, released (deferred until the device is
 // done with them) when it goes out of scope.
 struct Resources {
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp[kCompStreams] = {nullptr, nullptr};
   std::vector<cudaEvent_t> events;
   // On an error part-way, the caller's stream still waits for the work the
   // call has enqueued on its own streams, so the caller can free its buffers
   // once it has synchronised that stream.
   void join(cudaStream_t caller) {
-    for (cudaStream_t s : {in, out}) {
+    for (cudaStream_t s : {in, out, comp[0], comp[1]}) {
       cudaEvent_t e;
       if (s && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) {
         if (cudaEventRecord(e, s) == cudaSuccess) cudaStreamWaitEvent(caller, e, 0);
@@ -112,8 +133,8 @@ struct Resources {
   }
   ~Resources() {
     for (cudaEvent_t e : events) cudaEventDestroy(e);
-    if (in) cudaStreamDestroy(in);
-    if (out) cudaStreamDestroy(out);
+    for (cudaStream_t s : {in, out, comp[0], comp[1]})
+      if (s) cudaStreamDestroy(s);
   }
   cudaError_t event(cudaEvent_t* e) {
     const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
@@ -142,13 +163,46 @@ extern "C" int attn_varlen_host_chunks(int B, const int32_t* cu_q, const int32_t
   return n;
 }
 
+namespace {
+Plan plan_of(int B, const int32_t* cu_q, const int32_t* cu_k, int Hq, int Hkv, int d,
+             int chunks) {
+  Plan P;
+  P.cut.assign(static_cast<size_t>(chunks) + 1, 0);
+  P.nc = attn_varlen_host_chunks(B, cu_q, cu_k, chunks, P.cut.data());
+  int Bc = 0;
+  int64_t Tq = 0, Tk = 0;
+  for (int c = 0; c < P.nc; ++c) {
+    const int s = P.cut[c], e = P.cut[c + 1];
+    Bc = e - s > Bc ? e - s : Bc;
+    Tq = cu_q[e] - cu_q[s] > Tq ? cu_q[e] - cu_q[s] : Tq;
+    Tk = cu_k[e] - cu_k[s] > Tk ? cu_k[e] - cu_k[s] : Tk;
+  }
+  const int slots = P.nc < kMaxSlots ? (P.nc > 0 ? P.nc : 1) : kMaxSlots;
+  P.L = layout(B, Hq, Hkv, d, chunks, slots, Bc, Tq, Tk);
+  return P;
+}
+}  // namespace
+
 extern "C" size_t attn_varlen_fvjp_host_buffer_size(int B, int Hq, int Hkv, int head_dim,
                                                      int64_t total_q, int64_t total_k,
                                                      int chunks) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || total_q < 0 || total_k < 0 ||
       chunks < 1)
     return 0;
-  return layout(B, Hq, Hkv, head_dim, total_q, total_k, chunks).total;
+  // any lengths: every slot sized for the whole batch
+  const int slots = chunks < kMaxSlots ? chunks : kMaxSlots;
+  return layout(B, Hq, Hkv, head_dim, chunks, slots, B, total_q, total_k).total;
+}
+
+extern "C" size_t attn_varlen_fvjp_host_buffer_size_for(int B, const int32_t* cu_q,
+                                                         const int32_t* cu_k, int Hq, int Hkv,
+                                                         int head_dim, int chunks) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || chunks < 1 ||
+      (B > 0 && (!cu_q || !cu_k)))
+    return 0;
+  for (int b = 0; b < B; ++b)
+    if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return 0;
+  return plan_of(B, cu_q, cu_k, Hq, Hkv, head_dim, chunks).L.total;
 }
 
 extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
@@ -185,14 +239,13 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
     return ATTN_ERR_INVALID;
   for (int b = 0; b < B; ++b)
     if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return ATTN_ERR_INVALID;
-  const Layout L = layout(B, Hq, Hkv, d, total_q, total_k, chunks);
+  const Plan P = plan_of(B, cu_q, cu_k, Hq, Hkv, d, chunks);
+  const Layout& L = P.L;
   if (!device_buffer || device_buffer_bytes < L.total ||
       (reinterpret_cast<uintptr_t>(device_buffer) & (kAlign - 1)))
     return ATTN_ERR_WORKSPACE;
-
-  // ---- chunks: runs of whole sequences of about equal sum Lq*Lk
-  std::vector<int> cut(static_cast<size_t>(chunks) + 1);
-  const int nc = attn_varlen_host_chunks(B, cu_q, cu_k, chunks, cut.data());
+  const int nc = P.nc;
+  const std::vector<int32_t>& cut = P.cut;
   // rebased cu arrays of every chunk: chunk c's cu_q at [cut[c] + c], its cu_k
   // B + chunks entries later
   std::vector<int32_t> cus(2 * static_cast<size_t>(B + chunks), 0);
@@ -209,7 +262,6 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
   int32_t* status_dev = reinterpret_cast<int32_t*>(base + L.status);
   int32_t* cu_dev = reinterpret_cast<int32_t*>(base + L.cu);
   float* slopes_dev = reinterpret_cast<float*>(base + L.slopes);
-  float* lse_dev = reinterpret_cast<float*>(base + L.lse);
   Resources r;
   cudaEvent_t entry, done;
 #define ATTN_TRY(x)                 \
@@ -221,12 +273,14 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
   } while (0)
   ATTN_TRY(cudaStreamCreateWithFlags(&r.in, cudaStreamNonBlocking));
   ATTN_TRY(cudaStreamCreateWithFlags(&r.out, cudaStreamNonBlocking));
+  for (int i = 0; i < kCompStreams; ++i)
+    ATTN_TRY(cudaStreamCreateWithFlags(&r.comp[i], cudaStreamNonBlocking));
   ATTN_TRY(r.event(&entry));
   ATTN_TRY(r.event(&done));
   // the buffer may still be in use by earlier work on `stream`
   ATTN_TRY(cudaEventRecord(entry, stream));
-  ATTN_TRY(cudaStreamWaitEvent(r.in, entry, 0));
-  ATTN_TRY(cudaStreamWaitEvent(r.out, entry, 0));
+  for (cudaStream_t s : {r.in, r.out, r.comp[0], r.comp[1]})
+    ATTN_TRY(cudaStreamWaitEvent(s, entry, 0));
   ATTN_TRY(cudaMemsetAsync(status_dev, 0, sizeof(int32_t) * chunks, r.in));
   // small host arrays first (cus is pageable: the copy is staged before the
   // call returns)
@@ -237,46 +291,50 @@ extern "C" attn_status attn_varlen_fvjp_fwd_bwd_host(
                                sizeof(float) * (B > 1 ? slopes_batch_stride : Hq),
                                sizeof(float) * Hq, B, cudaMemcpyHostToDevice, r.in));
 
+  // Chunk c uses ring slot c % slots: its inputs go in on `in` once the slot's
+  // previous chunk has come back, it computes on comp[c % 2] (so a chunk's
+  // first kernels overlap the last kernels of the chunk before), and its
+  // results come back on `out`.
   const int64_t qts = static_cast<int64_t>(Hq) * d, kts = static_cast<int64_t>(Hkv) * d;
+  std::vector<cudaEvent_t> out_done(static_cast<size_t>(nc > 0 ? nc : 1));
   for (int c = 0; c < nc; ++c) {
     const int s = cut[c], e = cut[c + 1];
     const int64_t t0 = cu_q[s], t1 = cu_q[e], u0 = cu_k[s], u1 = cu_k[e];
+    uint8_t* slot = base + L.slot0 + static_cast<size_t>(c % L.slots) * L.slot_bytes;
+    cudaStream_t comp = r.comp[c % kCompStreams];
     cudaEvent_t in_done, comp_done;
     ATTN_TRY(r.event(&in_done));
     ATTN_TRY(r.event(&comp_done));
-    // inputs of chunk c
-    ATTN_TRY(copy_rows(true, base + L.q, q, q_ts, q_hs, Hq, d, t0, t1, r.in));
-    ATTN_TRY(copy_rows(true, base + L.dout, dout, do_ts, do_hs, Hq, d, t0, t1, r.in));
-    ATTN_TRY(copy_rows(true, base + L.k, k, k_ts, k_hs, Hkv, d, u0, u1, r.in));
-    ATTN_TRY(copy_rows(true, base + L.v, v, v_ts, v_hs, Hkv, d, u0, u1, r.in));
+    ATTN_TRY(r.event(&out_done[c]));
+    if (c >= L.slots) ATTN_TRY(cudaStreamWaitEvent(r.in, out_done[c - L.slots], 0));
+    ATTN_TRY(copy_rows(true, slot + L.q, q, q_ts, q_hs, Hq, d, t0, t1, r.in));
+    ATTN_TRY(copy_rows(true, slot + L.dout, dout, do_ts, do_hs, Hq, d, t0, t1, r.in));
+    ATTN_TRY(copy_rows(true, slot + L.k, k, k_ts, k_hs, Hkv, d, u0, u1, r.in));
+    ATTN_TRY(copy_rows(true, slot + L.v, v, v_ts, v_hs, Hkv, d, u0, u1, r.in));
     ATTN_TRY(cudaEventRecord(in_done, r.in));
-    // the call on the chunk
-    ATTN_TRY(cudaStreamWaitEvent(stream, in_done, 0));
-    auto at = [&](size_t off, int64_t row, int64_t rowlen) -> uint16_t* {
-      return reinterpret_cast<uint16_t*>(base + off) + row * rowlen;
-    };
+    ATTN_TRY(cudaStreamWaitEvent(comp, in_done, 0));
     const attn_status st = attn_varlen_fvjp_fwd_bwd(
-        dtype, e - s, Hq, Hkv, d, t1 - t0, u1 - u0, at(L.q, t0, qts), qts, d, at(L.k, u0, kts),
-        kts, d, at(L.v, u0, kts), kts, d, at(L.dout, t0, qts), qts, d, cu_dev + s + c,
-        cu_dev + B + chunks + s + c, alibi_slopes ? slopes_dev + static_cast<int64_t>(s) * Hq : nullptr,
-        Hq, causal, window_left, window_right, softcap, scale_multiplier, at(L.out, t0, qts), qts,
-        d, at(L.dq, t0, qts), qts, d, at(L.dk, u0, kts), kts, d, at(L.dv, u0, kts), kts, d,
-        lse_dev + t0 * Hq, base + L.ws, L.ws_bytes, status_dev + c, stream);
+        dtype, e - s, Hq, Hkv, d, t1 - t0, u1 - u0, slot + L.q, qts, d, slot + L.k, kts, d,
+        slot + L.v, kts, d, slot + L.dout, qts, d, cu_dev + s + c, cu_dev + B + chunks + s + c,
+        alibi_slopes ? slopes_dev + static_cast<int64_t>(s) * Hq : nullptr, Hq, causal,
+        window_left, window_right, softcap, scale_multiplier, slot + L.out, qts, d,
+        slot + L.dq, qts, d, slot + L.dk, kts, d, slot + L.dv, kts, d,
+        reinterpret_cast<float*>(slot + L.lse), slot + L.ws, L.ws_bytes, status_dev + c, comp);
     if (st != ATTN_OK) {
       r.join(stream);
       return st;
     }
-    ATTN_TRY(cudaEventRecord(comp_done, stream));
-    // results of chunk c
+    ATTN_TRY(cudaEventRecord(comp_done, comp));
     ATTN_TRY(cudaStreamWaitEvent(r.out, comp_done, 0));
-    ATTN_TRY(copy_rows(false, base + L.out, out, out_ts, out_hs, Hq, d, t0, t1, r.out));
-    ATTN_TRY(copy_rows(false, base + L.dq, dq, dq_ts, dq_hs, Hq, d, t0, t1, r.out));
-    ATTN_TRY(copy_rows(false, base + L.dk, dk, dk_ts, dk_hs, Hkv, d, u0, u1, r.out));
-    ATTN_TRY(copy_rows(false, base + L.dv, dv, dv_ts, dv_hs, Hkv, d, u0, u1, r.out));
+    ATTN_TRY(copy_rows(false, slot + L.out, out, out_ts, out_hs, Hq, d, t0, t1, r.out));
+    ATTN_TRY(copy_rows(false, slot + L.dq, dq, dq_ts, dq_hs, Hq, d, t0, t1, r.out));
+    ATTN_TRY(copy_rows(false, slot + L.dk, dk, dk_ts, dk_hs, Hkv, d, u0, u1, r.out));
+    ATTN_TRY(copy_rows(false, slot + L.dv, dv, dv_ts, dv_hs, Hkv, d, u0, u1, r.out));
     if (t1 > t0)
-      ATTN_TRY(cudaMemcpyAsync(lse + t0 * Hq, lse_dev + t0 * Hq,
+      ATTN_TRY(cudaMemcpyAsync(lse + t0 * Hq, slot + L.lse,
                                sizeof(float) * static_cast<size_t>(t1 - t0) * Hq,
                                cudaMemcpyDeviceToHost, r.out));
+    ATTN_TRY(cudaEventRecord(out_done[c], r.out));
   }
   ATTN_TRY(cudaMemcpyAsync(host_status, status_dev, sizeof(int32_t) * chunks,
                            cudaMemcpyDeviceToHost, r.out));

@@ -166,9 +166,39 @@ def test_host_entry_point_validates_before_touching_the_device(lib):
     bad = np.array([0, 6, 9], dtype=np.int32)
     assert call(cuk=bad.ctypes.data) == -1     # cu_k[B] != total_k
     assert call() == -4                        # no device buffer
-    need = lib.attn_varlen_fvjp_host_buffer_size(2, 16, 1, 160, 9, 12, 2)
+    need = lib.attn_varlen_fvjp_host_buffer_size_for(2, cu_q.ctypes.data, cu_k.ctypes.data, 16,
+                                                     1, 160, 2)
     assert need > lib.attn_varlen_fvjp_workspace_size(2, 16, 9, 12)
+    assert need <= lib.attn_varlen_fvjp_host_buffer_size(2, 16, 1, 160, 9, 12, 2)
     assert call(buf=0x100000, bufb=need - 1) == -4
+    # past every host check the call needs the device: on a machine without
+    # one that is CUDA (-5), and host_status is left as it was (where a GPU
+    # exists the fake pointers would be used, so the check stops here)
+    import torch
+
+    if not torch.cuda.is_available():
+        status[:] = 7
+        assert call(buf=0x100000, bufb=need) == -5
+        assert (status == 7).all()
+
+
+def test_host_buffer_is_slots_of_the_largest_chunk(lib):
+    """The host-buffer call's device buffer holds min(4, chunks) slots sized
+    for the largest chunk: with eight equal sequences in eight chunks it is
+    about half of the whole-batch bound, and it grows with a dominant
+    sequence."""
+    import numpy as np
+
+    def size_for(lengths, chunks):
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        return lib.attn_varlen_fvjp_host_buffer_size_for(len(lengths), cu.ctypes.data,
+                                                         cu.ctypes.data, 16, 1, 128, chunks)
+
+    even = size_for([1000] * 8, 8)
+    bound = lib.attn_varlen_fvjp_host_buffer_size(8, 16, 1, 128, 8000, 8000, 8)
+    assert even < bound / 7          # 4 slots of one sequence vs 4 slots of all eight
+    assert size_for([7000] + [143] * 7, 8) > 4 * even
+    assert size_for([1000] * 8, 1) > 7 * size_for([1000] * 8, 8) / 4
 
 
 def test_host_chunks_cut_whole_sequences_of_balanced_work(lib):
