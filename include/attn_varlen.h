@@ -209,9 +209,11 @@ attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
  * shared by its heads, or NULL).
  *
  * Element (sequence b, query head h, local query i, local key j) is kept when
- * the top 24 bits of splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | j))
- * are at least T = (uint32)(rate * 2^24) (computed in fp32; 2^24, dropping
- * everything, when rate >= 1), and kept weights are scaled by 1 / (1 - rate).
+ * the 16-bit field j mod 4 (bits 16 (j mod 4) and up) of
+ * splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | floor(j / 4))) is at
+ * least T = (uint32)(rate * 2^16) (computed in fp32; 2^16, dropping
+ * everything, when rate >= 1), and kept weights are scaled by 1 / (1 - rate):
+ * one hash per four keys of a row.
  * out = sum_j P_ij keep_ij scale v_j with the undropped softmax P (lse is the
  * undropped one); the backward pass regenerates the same keep bits.  Local
  * positions must stay below 2^24 and head indices below 2^16.  Dropout runs

@@ -38,9 +38,10 @@
  * causes addressed": a counter-based splitmix64 hash of (seed, b, h, row,
  * col), independent of tiling, with one rate or one rate per row):
  *   K_b    = splitmix64(seed ^ b)
- *   x_hij  = splitmix64(K_b ^ (h << 48 | i << 24 | j))  (i, j local positions
- *            below 2^24, h below 2^16: one hash per element)
- *   keep   = (x_ij >> 40) >= T,  T = (uint32)(rate * 2^24) in fp32 (2^24 when
+ *   x_hij  = splitmix64(K_b ^ (h << 48 | i << 24 | floor(j / 4)))  (i, j local
+ *            positions below 2^24, h below 2^16: one hash per four keys)
+ *   u_hij  = the 16-bit field j mod 4 of x_hij, (x_hij >> 16 (j mod 4)) & 0xFFFF
+ *   keep   = u_ij >= T,  T = (uint32)(rate * 2^16) in fp32 (2^16 when
  *            rate >= 1),  scale = 1 / (1 - rate)  (0 when rate >= 1)
  *   with rate = the call's rate, or rates[token] per query token when given.
  *   out_i  = sum_j P_ij keep_ij scale v_j     (lse and P undropped)
@@ -146,10 +147,11 @@ static uint64_t splitmix64(uint64_t x) {
   return z ^ (z >> 31);
 }
 
-/* Threshold and scale of a dropout rate (fp32 rate, as the caller gives it). */
+/* Threshold of a 16-bit draw and scale of a dropout rate (fp32 rate, as the
+ * caller gives it). */
 static void drop_params(float rate, uint32_t *T, double *scale) {
   if (!(rate < 1.0f)) {
-    *T = 1u << 24;
+    *T = 1u << 16;
     *scale = 0.0;
     return;
   }
@@ -158,12 +160,14 @@ static void drop_params(float rate, uint32_t *T, double *scale) {
     *scale = 1.0;
     return;
   }
-  *T = (uint32_t)(rate * 16777216.0f);
+  *T = (uint32_t)(rate * 65536.0f);
   *scale = 1.0 / (1.0 - (double)rate);
 }
 
 /* The dropout factor keep * scale of element (b, h, i, j); 1 without dropout.
- * `token` is the packed query token (for per-token rates). */
+ * `token` is the packed query token (for per-token rates).  One SplitMix64
+ * output serves the four keys 4m .. 4m + 3 of a row: key j takes the 16-bit
+ * field j mod 4 (bits 16 (j mod 4) and up). */
 static double drop_factor(const problem *p, int b, int h, int64_t token, int i, int j) {
   if (!p->dropout) return 1.0;
   const float rate = p->rates ? p->rates[token] : p->rate;
@@ -172,8 +176,9 @@ static double drop_factor(const problem *p, int b, int h, int64_t token, int i, 
   drop_params(rate, &T, &scale);
   const uint64_t kb = splitmix64(p->seed ^ (uint64_t)b);
   const uint64_t x = splitmix64(kb ^ (((uint64_t)h << 48) | ((uint64_t)(uint32_t)i << 24) |
-                                      (uint64_t)(uint32_t)j));
-  return (uint32_t)(x >> 40) >= T ? scale : 0.0;
+                                      (uint64_t)((uint32_t)j >> 2)));
+  const uint32_t u = (uint32_t)(x >> (16 * (j & 3))) & 0xFFFFu;
+  return u >= T ? scale : 0.0;
 }
 
 /* Element idx (in elements, strides already applied) of input array a. */

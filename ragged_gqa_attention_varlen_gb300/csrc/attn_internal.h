@@ -60,9 +60,10 @@ struct Params {
   float* Dbuf;    // [total_q, lse_rs]
   int64_t lse_rs; // row stride of lse and D: every query head of the call
   // counter-based dropout ("ragged flash attention gradient recompute", "Root
-  // causes addressed"): element (b, h, i, j) is kept when the top 24 bits of
-  // splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | j)) reach the
-  // rate's threshold T = rate * 2^24, and then scaled by 1 / (1 - rate)
+  // causes addressed"): element (b, h, i, j) is kept when the 16-bit field
+  // j mod 4 of splitmix64(splitmix64(seed ^ b) ^ (h << 48 | i << 24 | j / 4))
+  // reaches the rate's threshold T = rate * 2^16, and then scaled by
+  // 1 / (1 - rate)
   int dropout;
   uint64_t drop_seed;
   uint32_t drop_T;           // threshold of the call's rate (when drop_tab is null)

@@ -95,7 +95,10 @@ struct Pair {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD, bool DROP>
+// DM: dropout off (0), with the call's one rate (1), or with a rate per query
+// token from the table the schedule kernel builds (2) -- separate instances,
+// so the per-element work of the one-rate case holds no table lookup.
+template <bool BF16, bool MASK, int HD, int DM>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
@@ -104,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tvt, const __grid_constant__ CUtensorMap tqf,
                 const __grid_constant__ CUtensorMap tdof) {
   using namespace kv;
+  constexpr bool DROP = DM != 0;
+  constexpr bool DTAB = DM == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   uint8_t* sK = sm + kOffK;
@@ -563,19 +568,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
         uint64_t kbits = 0;
         if (DROP) {
+          // one hash serves the four keys 4m .. 4m + 3, held by four
+          // neighbouring lanes (key = t.key + r): each lane hashes 16 of the
+          // 64 columns (c = 4k + f, f = its key mod 4) for the group, and
+          // column c's hash is then read from lane f = c mod 4 of the group
           const int dh0 = p.head0 + (st % ngroups) * G;
-#pragma unroll 4
-          for (int c = 0; c < 64; ++c) {
-            const int lc = half * 64 + c;
-            const int it = dtok0 + (lc >> lgG);
-            bool keep = false;
-            if (it < t.Lq) {
-              uint32_t T;
-              float sc;
-              drop_row(p, static_cast<int64_t>(t.q0) + it, T, sc);
-              keep = drop_keep(dkb, drop_hi(dh0 + (lc & (G - 1)), it), t.key + r, T);
+          const int f = lane & 3;
+          const int m = (t.key + r) >> 2;
+          const int src0 = lane & ~3;
+          int t_tok = -1;            // token of the threshold in T (per-token rates)
+          uint32_t T = p.drop_T;
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {  // columns 32 bb .. 32 bb + 31
+            uint32_t hlo[8], hhi[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int lc = half * 64 + 32 * bb + 4 * k + f;
+              const int it = dtok0 + (lc >> lgG);
+              const uint64_t x = drop_hash(dkb, drop_hi(dh0 + (lc & (G - 1)), it), m);
+              hlo[k] = static_cast<uint32_t>(x);
+              hhi[k] = static_cast<uint32_t>(x >> 32);
             }
-            kbits |= static_cast<uint64_t>(keep) << c;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+              const int c = 32 * bb + cc;
+              const uint32_t lo = __shfl_sync(0xffffffffu, hlo[cc >> 2], src0 | (c & 3));
+              const uint32_t hw = __shfl_sync(0xffffffffu, hhi[cc >> 2], src0 | (c & 3));
+              const uint32_t u = ((f < 2 ? lo : hw) >> (16 * (f & 1))) & 0xFFFFu;
+              const int it = dtok0 + ((half * 64 + c) >> lgG);
+              if (DTAB && it != t_tok && it < t.Lq) {  // a new token every G columns
+                T = __ldg(p.drop_tab + t.q0 + it).x;
+                t_tok = it;
+              }
+              kbits |= static_cast<uint64_t>(it < t.Lq && u >= T) << c;
+            }
           }
         }
         // S^T: read it and release SP for dP^T
@@ -615,9 +641,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dropout: P^T for dV is P * keep * scale and dS uses keep * scale * dP
         // (keep bits hashed at the start of the step)
         auto dscale = [&](int c) -> float {  // the scale of column c (its query token)
-          if (!p.drop_tab) return p.drop_scale;
+          if (!DTAB) return p.drop_scale;
+          // per-token rates: loaded where used (a volatile load is not hoisted
+          // ahead of the unrolled element loop, which would hold 64 of them)
           const int it = dtok0 + ((half * 64 + c) >> lgG);
-          return it < t.Lq ? __uint_as_float(__ldg(p.drop_tab + t.q0 + it).y) : 0.f;
+          const volatile uint32_t* e =
+              reinterpret_cast<const volatile uint32_t*>(p.drop_tab + t.q0 + it);
+          return it < t.Lq ? __uint_as_float(e[1]) : 0.f;
         };
         auto pack_p = [&](int c, float a, float bb) -> uint32_t {  // columns c, c + 1
           if (DROP) {
@@ -787,12 +817,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool B, bool M, bool DR>
-auto dkdv_for_d(int d) {
-  if constexpr (DR) {
-    return dkdv_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
+auto dkdv_for_d(int d, bool table) {
+  if constexpr (DR) {  // dropout: head dimension 160 only
+    return table ? dkdv_kernel<B, M, 160, 2> : dkdv_kernel<B, M, 160, 1>;
   } else {
-    return d == 128 ? dkdv_kernel<B, M, 128, false>
-                    : (d == 64 ? dkdv_kernel<B, M, 64, false> : dkdv_kernel<B, M, 160, false>);
+    return d == 128 ? dkdv_kernel<B, M, 128, 0>
+                    : (d == 64 ? dkdv_kernel<B, M, 64, 0> : dkdv_kernel<B, M, 160, 0>);
   }
 }
 
@@ -801,11 +831,12 @@ cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorM
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
                         const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
   const bool m = masked_call(p);
+  const bool tab = p.drop_tab != nullptr;
   auto k = p.dropout
-               ? (p.dtype == 1 ? (m ? dkdv_for_d<true, true, true>(p.d) : dkdv_for_d<true, false, true>(p.d))
-                               : (m ? dkdv_for_d<false, true, true>(p.d) : dkdv_for_d<false, false, true>(p.d)))
-               : (p.dtype == 1 ? (m ? dkdv_for_d<true, true, false>(p.d) : dkdv_for_d<true, false, false>(p.d))
-                               : (m ? dkdv_for_d<false, true, false>(p.d) : dkdv_for_d<false, false, false>(p.d)));
+               ? (p.dtype == 1 ? (m ? dkdv_for_d<true, true, true>(p.d, tab) : dkdv_for_d<true, false, true>(p.d, tab))
+                               : (m ? dkdv_for_d<false, true, true>(p.d, tab) : dkdv_for_d<false, false, true>(p.d, tab)))
+               : (p.dtype == 1 ? (m ? dkdv_for_d<true, true, false>(p.d, tab) : dkdv_for_d<true, false, false>(p.d, tab))
+                               : (m ? dkdv_for_d<false, true, false>(p.d, tab) : dkdv_for_d<false, false, false>(p.d, tab)));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
   k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();

@@ -21,24 +21,34 @@ __host__ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
   return z ^ (z >> 31);
 }
 
-// Threshold and scale of a dropout rate: keep when the hash's top 24 bits
-// are >= T (probability 1 - T / 2^24), and scale kept values by 1/(1 - rate).
+// Threshold and scale of a dropout rate: keep when an element's 16-bit draw
+// is >= T (probability 1 - T / 2^16), and scale kept values by 1/(1 - rate).
 __host__ __device__ __forceinline__ void drop_params(float rate, uint32_t& T, float& scale) {
   if (!(rate < 1.f)) {
-    T = 1u << 24;
+    T = 1u << 16;
     scale = 0.f;
   } else if (!(rate > 0.f)) {
     T = 0u;
     scale = 1.f;
   } else {
-    T = static_cast<uint32_t>(rate * 16777216.0f);
+    T = static_cast<uint32_t>(rate * 65536.0f);
     scale = 1.f / (1.f - rate);
   }
 }
 
-// Dropout of one element: `kb` = splitmix64(seed ^ b), `hi` = h << 48 | i << 24.
-__device__ __forceinline__ bool drop_keep(uint64_t kb, uint64_t hi, int j, uint32_t T) {
-  return static_cast<uint32_t>(splitmix64(kb ^ (hi | static_cast<uint32_t>(j))) >> 40) >= T;
+// The hash of the four keys 4m .. 4m + 3 of one row: `kb` =
+// splitmix64(seed ^ b), `hi` = h << 48 | i << 24, `m` = key / 4.  Key 4m + f
+// draws the 16-bit field f (bits 16 f and up).
+__device__ __forceinline__ uint64_t drop_hash(uint64_t kb, uint64_t hi, int m) {
+  return splitmix64(kb ^ (hi | static_cast<uint32_t>(m)));
+}
+
+// Keep bits of the four keys of one hash (bit f for key 4m + f).
+__device__ __forceinline__ uint32_t drop_keep4(uint64_t x, uint32_t T) {
+  return static_cast<uint32_t>((x & 0xFFFFu) >= T) |
+         (static_cast<uint32_t>(((x >> 16) & 0xFFFFu) >= T) << 1) |
+         (static_cast<uint32_t>(((x >> 32) & 0xFFFFu) >= T) << 2) |
+         (static_cast<uint32_t>((x >> 48) >= T) << 3);
 }
 __device__ __forceinline__ uint64_t drop_hi(int h, int i) {
   return (static_cast<uint64_t>(h) << 48) | (static_cast<uint64_t>(static_cast<uint32_t>(i)) << 24);

@@ -429,9 +429,10 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         // dropout keep bits of this half's 64 keys, hashed while S is computed
         uint64_t kbits = 0;
         if (DROP) {
-#pragma unroll 8
-          for (int c = 0; c < 64; ++c)
-            kbits |= static_cast<uint64_t>(drop_keep(dkb, dhi, key0 + c, dT)) << c;
+#pragma unroll 4
+          for (int c = 0; c < 64; c += 4)  // key0 is a multiple of 64
+            kbits |= static_cast<uint64_t>(drop_keep4(drop_hash(dkb, dhi, (key0 + c) >> 2), dT))
+                     << c;
         }
         auto dropped = [&](float pv, int c) -> float { return ((kbits >> c) & 1) ? pv * dsc : 0.f; };
         if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;

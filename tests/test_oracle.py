@@ -461,7 +461,7 @@ def test_dropout_factors_are_zero_or_the_scale_at_the_rate(oracle_mod):
     scale = 1.0 / (1.0 - float(torch.tensor(rate, dtype=torch.float32)))
     assert torch.all((f == 0) | (f == scale))
     n, kept = f.numel(), int((f > 0).sum())
-    p_keep = 1.0 - int(rate * 2 ** 24) / 2 ** 24
+    p_keep = 1.0 - int(rate * 2 ** 16) / 2 ** 16
     assert abs(kept - n * p_keep) < 5 * math.sqrt(n * p_keep * (1 - p_keep))
     # rate 0 keeps everything at scale 1; rate 1 drops everything
     assert oracle_mod.drop_factor(7, 0.0, 0, 0, 3, 4) == 1.0
@@ -469,6 +469,25 @@ def test_dropout_factors_are_zero_or_the_scale_at_the_rate(oracle_mod):
     # the factor depends on (seed, b, h, i, j) alone
     assert oracle_mod.drop_factor(5, rate, 1, 2, 3, 4) == oracle_mod.drop_factor(5, rate, 1, 2, 3, 4)
     assert len({oracle_mod.drop_factor(s, 0.5, 0, 0, 0, 0) for s in range(64)}) == 2
+
+
+def test_dropout_keys_sharing_a_hash_are_independent_draws(oracle_mod):
+    """The four keys of one hash (j = 4m .. 4m + 3) take separate 16-bit
+    fields: each position keeps at the rate, and two keys of one hash are kept
+    together at the product rate (a field used twice would make them equal)."""
+    rate = 0.5
+    keep = torch.tensor([[oracle_mod.drop_factor(99, rate, 0, h, i, j) > 0 for j in range(64)]
+                         for h in range(4) for i in range(64)], dtype=torch.float64)
+    n = keep.shape[0] * 16
+    for pos in range(4):
+        k = int(keep[:, pos::4].sum())
+        assert abs(k - n * 0.5) < 5 * math.sqrt(n * 0.25), pos
+    for a, b in ((0, 1), (0, 3), (1, 2), (2, 3)):  # inside one hash
+        both = int((keep[:, a::4] * keep[:, b::4]).sum())
+        assert abs(both - n * 0.25) < 5 * math.sqrt(n * 0.25 * 0.75), (a, b)
+    both = int((keep[:, 3::4][:, :-1] * keep[:, 4::4]).sum())  # across two hashes
+    m = keep.shape[0] * 15
+    assert abs(both - m * 0.25) < 5 * math.sqrt(m * 0.25 * 0.75)
 
 
 def test_dropout_rate_zero_is_no_dropout(oracle_mod):
