@@ -625,13 +625,75 @@ def pinned_like(x: torch.Tensor) -> torch.Tensor:
     return base.as_strided(x.shape, x.stride(), x.storage_offset())
 
 
+def gpu_local_cpus(dev):
+    """The host CPUs attached to the GPU's own memory node (from sysfs), or
+    None where that is not published."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        if isinstance(pr.pci_bus_id, str):
+            bus = pr.pci_bus_id.lower()
+        else:  # integer ids: domain:bus:device.function
+            bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        return cpus or None
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+def link_probe(dev, nbytes=1 << 30):
+    """Host-to-device and device-to-host GB/s of one contiguous copy of
+    pinned memory (the link the end-to-end leg runs over)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        best = None
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        out[name] = nbytes / best / 1e9
+    return out
+
+
 def run_e2e(args, p, kw, flops, stream, world):
     """The same call through the host-buffer entry point: inputs in pinned
     host memory, results back in pinned host memory, every step.  The library
     cuts the batch into chunks of whole sequences and overlaps each chunk's
     copies over the host link with the kernels of the others; all of it lies
-    inside the timed region."""
+    inside the timed region.  The process first binds to the host CPUs of
+    the GPU's memory node, so the pinned buffers are allocated next to it."""
     from ragged_gqa_attention_varlen_gb300 import binding
+
+    local = gpu_local_cpus(p.q.device)
+    saved = os.sched_getaffinity(0)
+    if local:
+        try:
+            os.sched_setaffinity(0, local & set(saved) or local)
+        except OSError:
+            local = None
+    try:
+        return _e2e_timed(args, p, kw, flops, stream, world, local)
+    finally:
+        os.sched_setaffinity(0, saved)
+
+
+def _e2e_timed(args, p, kw, flops, stream, world, local):
+    from ragged_gqa_attention_varlen_gb300 import binding
+
+    probe = link_probe(p.q.device)
 
     hq, hk, hv, hdo = (pinned_like(x) for x in (p.q, p.k, p.v, p.dout))
     hcu_q, hcu_k = p.cu_q.cpu(), p.cu_k.cpu()
@@ -687,6 +749,7 @@ def run_e2e(args, p, kw, flops, stream, world):
             "d2h_bytes_per_step": d2h, "chunks": chunks,
             "device_buffer_gb": buf.numel() / 1e9,
             "link_gbs_average": (h2d + d2h) / (ms / 1e3) / 1e9,
+            "link_probe": probe, "cpus_bound_to_gpu_node": bool(local),
             "gpu_launches": binding.launch_count(
                 p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * nc * args.steps}
 

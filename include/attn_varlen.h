@@ -216,8 +216,8 @@ attn_status attn_varlen_fvjp_record_events(void *const *events, int n);
  * one hash per four keys of a row.
  * out = sum_j P_ij keep_ij scale v_j with the undropped softmax P (lse is the
  * undropped one); the backward pass regenerates the same keep bits.  Local
- * positions must stay below 2^24 and head indices below 2^16.  Dropout runs
- * with head_dim 160 only (ATTN_ERR_UNSUPPORTED otherwise); a NaN rate is
+ * positions must stay below 2^24 and head indices below 2^16.  Every head
+ * dimension of the dropout-free calls (160, 128, 64) is accepted; a NaN rate is
  * ATTN_ERR_INVALID.  Results are bitwise repeatable for a fixed seed. */
 attn_status attn_varlen_fvjp_fwd_bwd_dropout(
     attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,

@@ -535,12 +535,8 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
 
 template <bool B, bool M, bool DR>
 auto dq_for_d(int d) {
-  if constexpr (DR) {
-    return dq_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
-  } else {
-    return d == 128 ? dq_kernel<B, M, 128, false>
-                    : (d == 64 ? dq_kernel<B, M, 64, false> : dq_kernel<B, M, 160, false>);
-  }
+  return d == 128 ? dq_kernel<B, M, 128, DR>
+                  : (d == 64 ? dq_kernel<B, M, 64, DR> : dq_kernel<B, M, 160, DR>);
 }
 
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,

@@ -623,12 +623,8 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 
 template <bool B, bool M, bool DR>
 auto fwd_for_d(int d) {
-  if constexpr (DR) {
-    return fwd_kernel<B, M, 160, true>;  // dropout: head dimension 160 only
-  } else {
-    return d == 128 ? fwd_kernel<B, M, 128, false>
-                    : (d == 64 ? fwd_kernel<B, M, 64, false> : fwd_kernel<B, M, 160, false>);
-  }
+  return d == 128 ? fwd_kernel<B, M, 128, DR>
+                  : (d == 64 ? fwd_kernel<B, M, 64, DR> : fwd_kernel<B, M, 160, DR>);
 }
 
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,

@@ -267,7 +267,6 @@ attn_status run_call(
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
   if (head_dim != 160 && head_dim != 128 && head_dim != 64) return ATTN_ERR_UNSUPPORTED;
-  if (drop.on && head_dim != 160) return ATTN_ERR_UNSUPPORTED;
   if (drop.on && !(drop.rate == drop.rate)) return ATTN_ERR_INVALID;
   if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
   if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;

@@ -369,6 +369,10 @@ DROPOUT = [
     dict(lq=[200, 64], lk=[333, 90], Hq=48, dtype=torch.bfloat16, step=2, rate=0.5, causal=True),
     dict(lq=[150, 20], lk=[140, 300], Hq=12, Hkv=4, rate=None),   # per-token rates
     dict(lq=[40, 7], lk=[50, 30], Hq=16, rate=0.0),               # keeps everything
+    dict(lq=[260, 33], lk=[300, 140], Hq=16, d=128, rate=0.3),    # head dimensions 128, 64
+    dict(lq=[190, 70], lk=[150, 270], Hq=8, Hkv=2, d=64, dtype=torch.bfloat16, rate=0.1,
+         causal=True),
+    dict(lq=[120, 9], lk=[200, 45], Hq=16, d=128, rate=None),     # per-token rates, d = 128
 ]
 
 

@@ -41,7 +41,7 @@ def _reduce(parts):
 
 CASES = [
     dict(lq=[600, 40, 90, 30], lk=[700, 50, 60, 20], Hq=16),
-    dict(lq=[500, 40, 90], lk=[300, 50, 600], Hq=16, causal=True, dtype=torch.bfloat16, step=2),
+    dict(lq=[600, 40, 90], lk=[600, 50, 200], Hq=16, causal=True, dtype=torch.bfloat16, step=2),
     dict(lq=[700, 60, 20], lk=[650, 40, 300], Hq=16, Hkv=4, d=128),
 ]
 
