@@ -314,6 +314,9 @@ def run_gpu(args, world, rank, local):
                                 length_scale=args.length_scale, Hkv=args.hkv, d=args.head_dim)
     p.causal, p.window_left, p.window_right = args.causal, args.window_left, args.window_right
     drop = {} if args.dropout is None else dict(dropout_seed=1234, dropout_rate=args.dropout)
+    if drop and not args.dropout_regen:  # keep bits stored by the forward, read by the backward
+        drop["keep_mask"] = torch.empty(binding.dropout_mask_bytes(p.cu_q, p.cu_k, p.Hq, args.hkv),
+                                        dtype=torch.uint8, device=dev)
     flops = counted_flops(p)
     kflops = kernel_flops(p)
     out = torch.empty(p.q.shape, dtype=p.q.dtype, device=dev)
@@ -363,6 +366,8 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError(f"device status {status:#x}")
     value, ms = aggregate(flops, total_s, args.steps, world)
     launches = binding.launch_count(p.B, p.Hq, p.total_q, p.total_k, Hkv=args.hkv) * args.steps
+    if "keep_mask" in drop:  # the mask kernel, once per call
+        launches += args.steps
     pk, kind = peaks()
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     if args.hkv == 1:
@@ -414,7 +419,9 @@ def run_gpu(args, world, rank, local):
                            "" if args.length_scale == 1.0 else f" x{args.length_scale} length") +
                            mask_name(p) + ("" if args.hkv == 1 else f", Hkv={args.hkv}") +
                            ("" if args.head_dim == HEAD_DIM else f", d={args.head_dim}") +
-                           ("" if args.dropout is None else f", dropout {args.dropout}"),
+                           ("" if args.dropout is None else f", dropout {args.dropout}" + (
+                               " (keep bits regenerated)" if args.dropout_regen else
+                               " (keep bits stored)")),
                        "B": p.B, "Hq": p.Hq, "Hkv": args.hkv,
                        "head_dim": args.head_dim, "token_step": 2, "total_q": p.total_q,
                        "total_k": p.total_k, "sum_lq_lk": p.sum_lq_lk(),
@@ -773,7 +780,10 @@ def main():
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="sequence chunks of the end-to-end leg (copies overlap compute)")
     ap.add_argument("--dropout", type=float, default=None,
-                    help="time with counter-based dropout at this rate")
+                    help="time with counter-based dropout at this rate (keep bits stored by "
+                         "the forward, read by the backward)")
+    ap.add_argument("--dropout-regen", action="store_true",
+                    help="with --dropout: the backward regenerates the keep bits instead")
     ap.add_argument("--hkv", type=int, default=1,
                     help="K/V heads (query heads grouped consecutively over them)")
     ap.add_argument("--gated", action="store_true",

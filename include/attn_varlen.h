@@ -95,6 +95,7 @@ typedef enum {
 #define ATTN_DEV_TIMEOUT_DKDV 0x4    /* ... in the dk/dv kernel */
 #define ATTN_DEV_TIMEOUT_DQ 0x8      /* ... in the dq kernel */
 #define ATTN_DEV_SMEM_ALIGN 0x10     /* dynamic shared memory base not 1024-byte aligned */
+#define ATTN_DEV_MASK_SPACE 0x20     /* keep-mask buffer smaller than the lengths need */
 
 /* Largest batch (number of sequences) accepted. */
 #define ATTN_MAX_BATCH 16384
@@ -264,6 +265,83 @@ attn_status attn_varlen_bwd_dropout(
     void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
     void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
     void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* The dropout calls with the keep bits STORED instead of regenerated: the
+ * forward computes each element's keep bit from the hash above once and
+ * writes it to `keep_mask`, and the backward kernels read it there instead of
+ * hashing again.  The bits, and so every result, are bitwise those of the
+ * calls above (the reading of the page is unchanged: a stored copy of the
+ * same counter-based bits).  The pages regenerate the mask in the backward;
+ * this variant trades device memory (one bit per admissible-tile element) for
+ * the backward's hashing.
+ *
+ * Arguments: those of the matching call above plus, after dropout_rates,
+ * `keep_mask` (DEVICE, 256-byte aligned, owned by the caller) and its size
+ * `keep_mask_bytes`, at least attn_varlen_dropout_mask_bytes for the call's
+ * lengths and heads.  attn_varlen_fwd_dropout_mask writes the mask,
+ * attn_varlen_bwd_dropout_mask reads it (it must come from the forward of the
+ * same inputs, seed and rates; the backward then uses the rates only for the
+ * scale), and the fused call does both.  The mask's layout is private to the
+ * library.  A NULL or misaligned keep_mask is ATTN_ERR_INVALID /
+ * ATTN_ERR_ALIGNMENT; a buffer smaller than the lengths need (checked on the
+ * device, where the lengths are) sets ATTN_DEV_MASK_SPACE in the device
+ * status and the kernels then skip their work. */
+attn_status attn_varlen_fvjp_fwd_bwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    void *keep_mask, size_t keep_mask_bytes,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+attn_status attn_varlen_fwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    void *keep_mask, size_t keep_mask_bytes,
+    void *out, int64_t out_tok_stride, int64_t out_head_stride,
+    float *lse, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream);
+
+attn_status attn_varlen_bwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void *q, int64_t q_tok_stride, int64_t q_head_stride,
+    const void *k, int64_t k_tok_stride, int64_t k_head_stride,
+    const void *v, int64_t v_tok_stride, int64_t v_head_stride,
+    const void *dout, int64_t do_tok_stride, int64_t do_head_stride,
+    const int32_t *cu_q, const int32_t *cu_k,
+    const float *alibi_slopes, int64_t slopes_batch_stride,
+    int causal, int window_left, int window_right, float softcap, float scale_multiplier,
+    uint64_t dropout_seed, float dropout_rate, const float *dropout_rates,
+    const void *keep_mask, size_t keep_mask_bytes,
+    const void *out, int64_t out_tok_stride, int64_t out_head_stride, const float *lse,
+    void *dq, int64_t dq_tok_stride, int64_t dq_head_stride,
+    void *dk, int64_t dk_tok_stride, int64_t dk_head_stride,
+    void *dv, int64_t dv_tok_stride, int64_t dv_head_stride,
+    void *workspace, size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* Bytes of keep mask the _mask calls need for these lengths (HOST cu_q,
+ * cu_k of B + 1 entries each): a 256-byte-aligned header of 4 (B + 1) bytes,
+ * then Hkv times 2 KB per (128-row query tile, 128-key tile) pair of every
+ * sequence, that is about Hq * sum_b Lq_b * Lk_b / 8 bytes.  0 for invalid
+ * arguments. */
+size_t attn_varlen_dropout_mask_bytes(int B, const int32_t *cu_q, const int32_t *cu_k, int Hq,
+                                      int Hkv);
 
 /* Forward + full VJP with every input and output in HOST memory, for
  * callers whose data lives on the host (the transfers over the host link are

@@ -19,6 +19,7 @@ _lib = None
 
 ATTN_F16, ATTN_BF16 = 0, 1
 DEV_BAD_CU, DEV_TIMEOUT_FWD, DEV_TIMEOUT_DKDV, DEV_TIMEOUT_DQ = 0x1, 0x2, 0x4, 0x8
+DEV_MASK_SPACE = 0x20
 
 EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_status_string",
            "attn_varlen_fvjp_launch_count", "attn_varlen_fvjp_record_events",
@@ -28,7 +29,9 @@ EXPORTS = ("attn_varlen_fvjp_fwd_bwd", "attn_varlen_fvjp_workspace_size", "attn_
            "attn_varlen_fvjp_fwd_bwd_dropout",
            "attn_varlen_fwd_dropout", "attn_varlen_bwd_dropout", "attn_varlen_host_chunks",
            "attn_varlen_shard_plan", "attn_varlen_sum_partials",
-           "attn_varlen_gated_fvjp_fwd_bwd", "attn_varlen_gated_fwd")
+           "attn_varlen_gated_fvjp_fwd_bwd", "attn_varlen_gated_fwd",
+           "attn_varlen_fvjp_fwd_bwd_dropout_mask", "attn_varlen_fwd_dropout_mask",
+           "attn_varlen_bwd_dropout_mask", "attn_varlen_dropout_mask_bytes")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNELS = ("schedule", "forward", "preprocess", "dkdv", "dq")
 
@@ -96,6 +99,21 @@ def load(path: str = LIB_PATH):
         [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DR +
         [P, L, L, P] + [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
     lib.attn_varlen_bwd_dropout.restype = I
+    DRM = DR + [P, ctypes.c_size_t]  # ... plus the keep mask and its size
+    lib.attn_varlen_fvjp_fwd_bwd_dropout_mask.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DRM +
+        [P, L, L] * 4 + [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fvjp_fwd_bwd_dropout_mask.restype = I
+    lib.attn_varlen_fwd_dropout_mask.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 3 + [P, P, P, L, I, I, I, F, F] + DRM + [P, L, L] +
+        [P, P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_fwd_dropout_mask.restype = I
+    lib.attn_varlen_bwd_dropout_mask.argtypes = (
+        [I, I, I, I, I, L, L] + [P, L, L] * 4 + [P, P, P, L, I, I, I, F, F] + DRM +
+        [P, L, L, P] + [P, L, L] * 3 + [P, ctypes.c_size_t, P, P])
+    lib.attn_varlen_bwd_dropout_mask.restype = I
+    lib.attn_varlen_dropout_mask_bytes.argtypes = [I, P, P, I, I]
+    lib.attn_varlen_dropout_mask_bytes.restype = ctypes.c_size_t
     lib.attn_varlen_gated_fvjp_fwd_bwd.argtypes = (
         [I, I, I, I, I, I, L, L] + [P, L, L] * 6 + [P, P, P, L, I, I, I, F] + [P, L, L] * 6 +
         [P, P, ctypes.c_size_t, P, P])
@@ -180,7 +198,8 @@ def _like(x: torch.Tensor) -> torch.Tensor:
 def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
                           window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
                           out=None, dq=None, dk=None, dv=None, lse=None, workspace=None,
-                          stream=None, dropout_seed=None, dropout_rate=0.0, dropout_rates=None):
+                          stream=None, dropout_seed=None, dropout_rate=0.0, dropout_rates=None,
+                          keep_mask=None):
     """Forward + full VJP in one library call.
 
     q, dout: [T_q, Hq, d]; k, v: [T_k, Hkv, d] CUDA views (fp16 or bf16,
@@ -191,7 +210,10 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
     allocated.  Returns dict(out, dq, dk, dv, lse, workspace).  The call is
     asynchronous on ``stream`` (default: the current stream).  With a
     ``dropout_seed`` the attention weights get counter-based dropout at
-    ``dropout_rate`` (or per query token from ``dropout_rates``)."""
+    ``dropout_rate`` (or per query token from ``dropout_rates``); with a
+    ``keep_mask`` (uint8 CUDA buffer of dropout_mask_bytes) the forward stores
+    the keep bits there and the backward reads them instead of hashing again
+    (bitwise the same results)."""
     lib = load()
     dtype = q.dtype
     if dtype not in (torch.float16, torch.bfloat16):
@@ -230,7 +252,7 @@ def attention_varlen_fvjp(q, k, v, cu_q, cu_k, alibi_slopes, dout, causal=False,
         stream = torch.cuda.current_stream(q.device)
     drop = ([] if dropout_seed is None else
             _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
-    fn = lib.attn_varlen_fvjp_fwd_bwd_dropout if drop else lib.attn_varlen_fvjp_fwd_bwd
+    fn, drop = _drop_fn(lib, "attn_varlen_fvjp_fwd_bwd", drop, keep_mask)
     code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
@@ -286,7 +308,7 @@ def _workspace(workspace, B, Hq, Tq, Tk, device):
 def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window_left=-1,
                          window_right=-1, softcap=3.0, scale_multiplier=0.75, out=None, lse=None,
                          workspace=None, stream=None, dropout_seed=None, dropout_rate=0.0,
-                         dropout_rates=None):
+                         dropout_rates=None, keep_mask=None):
     """Forward only: returns (out, lse).  Same argument rules as
     attention_varlen_fvjp; lse is fp32 [T_q, Hq] (natural log), the value the
     backward call reads back.  Asynchronous on ``stream``."""
@@ -303,7 +325,7 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
         stream = torch.cuda.current_stream(q.device)
     drop = ([] if dropout_seed is None else
             _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
-    fn = lib.attn_varlen_fwd_dropout if drop else lib.attn_varlen_fwd
+    fn, drop = _drop_fn(lib, "attn_varlen_fwd", drop, keep_mask)
     code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
@@ -321,7 +343,8 @@ def attention_varlen_fwd(q, k, v, cu_q, cu_k, alibi_slopes, causal=False, window
 def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, causal=False,
                          window_left=-1, window_right=-1, softcap=3.0, scale_multiplier=0.75,
                          dq=None, dk=None, dv=None, workspace=None, stream=None,
-                         dropout_seed=None, dropout_rate=0.0, dropout_rates=None):
+                         dropout_seed=None, dropout_rate=0.0, dropout_rates=None,
+                         keep_mask=None):
     """Backward only: given the forward's out and lse for the same inputs and
     options, returns (dq, dk, dv).  out and lse are read, not modified.  For
     the same inputs the result is bitwise the one attention_varlen_fvjp gives.
@@ -343,7 +366,7 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
         stream = torch.cuda.current_stream(q.device)
     drop = ([] if dropout_seed is None else
             _dropout_args(dropout_seed, dropout_rate, dropout_rates, Tq))
-    fn = lib.attn_varlen_bwd_dropout if drop else lib.attn_varlen_bwd
+    fn, drop = _drop_fn(lib, "attn_varlen_bwd", drop, keep_mask)
     code = fn(
         ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16, B, Hq, Hkv, q.shape[-1], Tq, Tk,
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), k.stride(0), k.stride(1),
@@ -358,6 +381,36 @@ def attention_varlen_bwd(q, k, v, cu_q, cu_k, alibi_slopes, dout, out, lse, caus
     if code != 0:
         raise AttnError(code, lib.attn_status_string(code).decode())
     return dq, dk, dv
+
+
+def dropout_mask_bytes(cu_q, cu_k, Hq: int, Hkv: int = 1) -> int:
+    """Bytes of keep mask the stored-mask dropout calls need for these lengths
+    (cu_q, cu_k: int32 [B+1], host or device)."""
+    cq = cu_q.detach().to("cpu", torch.int32).contiguous()
+    ck = cu_k.detach().to("cpu", torch.int32).contiguous()
+    n = int(load().attn_varlen_dropout_mask_bytes(cq.numel() - 1, _ptr(cq), _ptr(ck), Hq, Hkv))
+    if n == 0:
+        raise ValueError("invalid lengths or heads for the keep mask")
+    return n
+
+
+def _mask_args(keep_mask):
+    """(pointer, bytes) of a keep-mask buffer: a CUDA uint8 tensor."""
+    if not keep_mask.is_cuda or keep_mask.dtype != torch.uint8 or not keep_mask.is_contiguous():
+        raise ValueError("keep_mask must be a contiguous uint8 CUDA tensor")
+    return [_ptr(keep_mask), keep_mask.numel()]
+
+
+def _drop_fn(lib, name, drop, keep_mask):
+    """The entry point and its dropout arguments: plain, dropout, or dropout
+    with the stored keep mask."""
+    if not drop:
+        if keep_mask is not None:
+            raise ValueError("keep_mask needs a dropout_seed")
+        return getattr(lib, name), []
+    if keep_mask is None:
+        return getattr(lib, name + "_dropout"), drop
+    return getattr(lib, name + "_dropout_mask"), drop + _mask_args(keep_mask)
 
 
 def _check_lse(lse, Tq, Hq):

@@ -71,6 +71,10 @@ struct Params {
   const float* drop_rates;   // per query token [total_q], or null
   uint2* drop_tab;           // per query token (T, scale bits), made by the schedule kernel
   int head0;                 // first query head of this K/V head group (hash input h)
+  // stored keep bits (null: the backward regenerates them from the hash):
+  // written by the forward, read by the backward kernels; layout below
+  uint8_t* drop_mask;
+  uint64_t drop_mask_bytes;
   int32_t* status;
   int32_t* counters;  // [3]: fwd, dkdv, dq tile counters (of this K/V head group)
   int ncounters;      // counters the schedule kernel resets (every group's)
@@ -105,12 +109,27 @@ inline bool masked_call(const Params& p) { return p.causal || p.wl >= 0 || p.wr 
 //   [4B+2, 5B+2)    first such key tile of each order position
 inline int sched_words(int B) { return 5 * B + 2; }
 
+// Keep-mask layout: a header of B + 1 int32 (the prefix over the sequences,
+// in batch order, of their (query tile, key tile) blocks), padded to 256
+// bytes, then K/V head group g's blocks at g * total, and within a group
+// sequence b's block (tb, hg, kt) -- query token block tb, head group hg, key
+// tile kt -- at prefix[b] + (tb * (Hq/G) + hg) * ceil(Lk/128) + kt.  A block
+// is 256 words: word kh * 128 + r holds the keep bits of query row r of the
+// tile (token r / G, head r % G) for keys 64 kh .. 64 kh + 63 of the key tile
+// (bit c for key 64 kh + c), zero for rows past the sequence.
+constexpr int kMaskBlockWords = 2 * kRowsQ;  // 64-bit words per block (2 KB)
+__host__ __device__ constexpr uint64_t drop_mask_header(int B) {
+  return (4ull * (static_cast<uint64_t>(B) + 1) + 255) / 256 * 256;
+}
+
 // Workspace bytes a call uses (host.cu): the status word, tile counters,
 // schedule and D, plus the per-token dropout rate table when `rate_table`.
 // attn_varlen_fvjp_workspace_size reports the size with the table.
 size_t workspace_bytes_needed(int B, int Hq, int64_t total_q, bool rate_table);
 
 cudaError_t launch_sched(const Params& p, cudaStream_t s);
+// The stored keep mask of a dropout call with a mask buffer (every group).
+cudaError_t launch_mask(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
                        const CUtensorMap& tv, int grid, cudaStream_t s);

@@ -562,6 +562,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ktile_decode<MASK>(p, item, t);
       const int nsteps = step_count(t);
       const uint64_t dkb = DROP ? splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b)) : 0;
+      // stored keep mask (written by the mask kernel): step st's block is the
+      // tile's first one plus st blocks of key tiles; the words of a step are
+      // loaded one step ahead
+      const uint64_t* mbase = nullptr;
+      int64_t mstep = 0;
+      const int msh = 32 * (quad & 1);
+      uint32_t mw0 = 0, mw1 = 0;
+      if (DROP && p.drop_mask && nsteps > 0) {
+        mbase = drop_mask_block(p, t.b, t.Lk, t.tb0, 0, t.key / kKeys) + (quad >> 1) * kRowsQ +
+                half * 64 + lane;
+        mstep = static_cast<int64_t>((t.Lk + kKeys - 1) / kKeys) * kMaskBlockWords;
+        mw0 = static_cast<uint32_t>(__ldg(mbase) >> msh);
+        mw1 = static_cast<uint32_t>(__ldg(mbase + 32) >> msh);
+      }
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
         const int b = gg & 1;
@@ -569,7 +583,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this thread's key, hashed while S^T is computed
         const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
         uint64_t kbits = 0;
-        if (DROP) {
+        if (DROP && mbase) {
+          // stored keep mask: the words of this half's 64 columns hold 64
+          // keys each; this warp's 32 keys are one 32-bit half of them, turned
+          // from one column per lane into one key per lane
+          kbits = (static_cast<uint64_t>(bit_transpose32(mw1)) << 32) | bit_transpose32(mw0);
+          if (st + 1 < nsteps) {  // the next step's words, loaded during this one
+            mw0 = static_cast<uint32_t>(__ldg(mbase + (st + 1) * mstep) >> msh);
+            mw1 = static_cast<uint32_t>(__ldg(mbase + (st + 1) * mstep + 32) >> msh);
+          }
+        } else if (DROP) {
           // one hash serves the four keys 4m .. 4m + 3, held by four
           // neighbouring lanes (key = t.key + r): each lane hashes 16 of the
           // 64 columns (c = 4k + f, f = its key mod 4) for the group, and

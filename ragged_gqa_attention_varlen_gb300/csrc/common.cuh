@@ -54,6 +54,22 @@ __device__ __forceinline__ uint64_t drop_hi(int h, int i) {
   return (static_cast<uint64_t>(h) << 48) | (static_cast<uint64_t>(static_cast<uint32_t>(i)) << 24);
 }
 
+// Transpose of a 32 x 32 bit matrix held one row per lane (bit k of lane l's
+// word = element (l, k)): returns lane k's column, bit l = element (l, k).
+// Five exchange rounds swap ever smaller off-diagonal blocks (16 x 16, then
+// 8 x 8, ... 1 x 1): at width j the lanes with bit j set trade their words'
+// low j-bit groups for their partners' high ones.
+__device__ __forceinline__ uint32_t bit_transpose32(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m = 0x0000FFFFu;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1, m ^= m << j) {
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y & m) << j));
+  }
+  return x;
+}
+
 // Threshold and scale of query token `tok` (packed index).
 __device__ __forceinline__ void drop_row(const Params& p, int64_t tok, uint32_t& T, float& scale) {
   if (p.drop_tab) {

@@ -416,10 +416,14 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
       uint64_t dkb = 0, dhi = 0;
       uint32_t dT = 0;
       float dsc = 1.f;
+      // with a stored keep mask: this row's words of the tile's blocks
+      const uint64_t* mrow = nullptr;
       if (DROP) {
         dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b));
         dhi = drop_hi(p.head0 + h, i_loc);
         if (row_valid) drop_row(p, static_cast<int64_t>(t.q0) + i_loc, dT, dsc);
+        if (p.drop_mask)
+          mrow = drop_mask_block(p, t.b, t.Lk, t.tok / (kRowsQ / G), t.hg, 0) + half * kRowsQ + r;
       }
 
       for (int jj = 0, kt = t0; jj < n; ++jj, kt = next_key_tile(t, kt)) {
@@ -429,10 +433,14 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
         // dropout keep bits of this half's 64 keys, hashed while S is computed
         uint64_t kbits = 0;
         if (DROP) {
+          if (mrow) {  // written by the mask kernel
+            kbits = __ldg(mrow + kt * kMaskBlockWords);
+          } else {
 #pragma unroll 4
-          for (int c = 0; c < 64; c += 4)  // key0 is a multiple of 64
-            kbits |= static_cast<uint64_t>(drop_keep4(drop_hash(dkb, dhi, (key0 + c) >> 2), dT))
-                     << c;
+            for (int c = 0; c < 64; c += 4)  // key0 is a multiple of 64
+              kbits |= static_cast<uint64_t>(drop_keep4(drop_hash(dkb, dhi, (key0 + c) >> 2), dT))
+                       << c;
+          }
         }
         auto dropped = [&](float pv, int c) -> float { return ((kbits >> c) & 1) ? pv * dsc : 0.f; };
         if (!(ok = mbar_wait_warp(&bars->s_full[gg & 1], (gg >> 1) & 1, s_abort))) break;

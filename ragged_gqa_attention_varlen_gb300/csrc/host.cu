@@ -247,6 +247,9 @@ struct Dropout {
   uint64_t seed = 0;
   float rate = 0.f;
   const float* rates = nullptr;  // per query token, device
+  void* mask = nullptr;          // stored keep bits (the _mask entry points), device
+  size_t mask_bytes = 0;
+  bool mask_call = false;        // a _mask entry point: the mask must be given
 };
 
 // The three entry points share one body: host-side validation, the tensor
@@ -268,6 +271,10 @@ attn_status run_call(
   if (B < 0 || Hq <= 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID;
   if (head_dim != 160 && head_dim != 128 && head_dim != 64) return ATTN_ERR_UNSUPPORTED;
   if (drop.on && !(drop.rate == drop.rate)) return ATTN_ERR_INVALID;
+  if (drop.mask_call) {
+    if (!drop.mask || drop.mask_bytes < drop_mask_header(B)) return ATTN_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(drop.mask) & 255u) return ATTN_ERR_ALIGNMENT;
+  }
   if (Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
   if (B > ATTN_MAX_BATCH) return ATTN_ERR_UNSUPPORTED;
   if (total_q > INT32_MAX || total_k > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
@@ -369,6 +376,10 @@ attn_status run_call(
     drop_params(drop.rate, p.drop_T, p.drop_scale);
     p.drop_rates = drop.rates;
     p.drop_tab = drop.rates ? reinterpret_cast<uint2*>(wsb + ws.droptab) : nullptr;
+    if (drop.mask_call) {
+      p.drop_mask = static_cast<uint8_t*>(drop.mask);
+      p.drop_mask_bytes = drop.mask_bytes;
+    }
   }
   p.sched = reinterpret_cast<int32_t*>(wsb + ws.sched);
 
@@ -461,6 +472,8 @@ attn_status run_call(
   p0.counters = p.counters;  // the schedule resets every group's counters
   mark(0);
   if (launch_sched(p0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  // the forward of a stored-mask dropout call first writes the keep bits
+  if (fwd && p.drop_mask && launch_mask(p0, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   mark(1);
   Maps m;
   if (fwd) {
@@ -609,6 +622,103 @@ extern "C" attn_status attn_varlen_bwd_dropout(
                   scale_multiplier, const_cast<void*>(out), out_ts, out_hs, dq, dq_ts, dq_hs, dk,
                   dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
                   workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" attn_status attn_varlen_fvjp_fwd_bwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, uint64_t dropout_seed, float dropout_rate,
+    const float* dropout_rates, void* keep_mask, size_t keep_mask_bytes, void* out,
+    int64_t out_ts, int64_t out_hs, void* dq, int64_t dq_ts, int64_t dq_hs, void* dk,
+    int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts, int64_t dv_hs, float* lse,
+    void* workspace, size_t workspace_bytes, int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  dr.mask = keep_mask;
+  dr.mask_bytes = keep_mask_bytes;
+  dr.mask_call = true;
+  return run_call(kModeFwd | kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts,
+                  q_hs, k, k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k,
+                  alibi_slopes, slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, dq, dq_ts, dq_hs, dk, dk_ts, dk_hs, dv,
+                  dv_ts, dv_hs, lse, workspace, workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" attn_status attn_varlen_fwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const int32_t* cu_q, const int32_t* cu_k,
+    const float* alibi_slopes, int64_t slopes_batch_stride, int causal, int window_left,
+    int window_right, float softcap, float scale_multiplier, uint64_t dropout_seed,
+    float dropout_rate, const float* dropout_rates, void* keep_mask, size_t keep_mask_bytes,
+    void* out, int64_t out_ts, int64_t out_hs, float* lse, void* workspace,
+    size_t workspace_bytes, int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  dr.mask = keep_mask;
+  dr.mask_bytes = keep_mask_bytes;
+  dr.mask_call = true;
+  return run_call(kModeFwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, nullptr, 0, 0, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, out, out_ts, out_hs, nullptr, 0, 0, nullptr, 0, 0, nullptr,
+                  0, 0, lse, workspace, workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" attn_status attn_varlen_bwd_dropout_mask(
+    attn_dtype dtype, int B, int Hq, int Hkv, int head_dim, int64_t total_q, int64_t total_k,
+    const void* q, int64_t q_ts, int64_t q_hs, const void* k, int64_t k_ts, int64_t k_hs,
+    const void* v, int64_t v_ts, int64_t v_hs, const void* dout, int64_t do_ts, int64_t do_hs,
+    const int32_t* cu_q, const int32_t* cu_k, const float* alibi_slopes,
+    int64_t slopes_batch_stride, int causal, int window_left, int window_right, float softcap,
+    float scale_multiplier, uint64_t dropout_seed, float dropout_rate,
+    const float* dropout_rates, const void* keep_mask, size_t keep_mask_bytes, const void* out,
+    int64_t out_ts, int64_t out_hs, const float* lse, void* dq, int64_t dq_ts, int64_t dq_hs,
+    void* dk, int64_t dk_ts, int64_t dk_hs, void* dv, int64_t dv_ts, int64_t dv_hs,
+    void* workspace, size_t workspace_bytes, int32_t* device_status, void* stream) {
+  Dropout dr;
+  dr.on = true;
+  dr.seed = dropout_seed;
+  dr.rate = dropout_rate;
+  dr.rates = dropout_rates;
+  // the backward only reads the blocks (the schedule kernel rewrites the
+  // header with the same values)
+  dr.mask = const_cast<void*>(keep_mask);
+  dr.mask_bytes = keep_mask_bytes;
+  dr.mask_call = true;
+  return run_call(kModeBwd, dtype, B, Hq, Hkv, head_dim, total_q, total_k, q, q_ts, q_hs, k,
+                  k_ts, k_hs, v, v_ts, v_hs, dout, do_ts, do_hs, cu_q, cu_k, alibi_slopes,
+                  slopes_batch_stride, causal, window_left, window_right, softcap,
+                  scale_multiplier, const_cast<void*>(out), out_ts, out_hs, dq, dq_ts, dq_hs, dk,
+                  dk_ts, dk_hs, dv, dv_ts, dv_hs, const_cast<float*>(lse), workspace,
+                  workspace_bytes, device_status, stream, dr);
+}
+
+extern "C" size_t attn_varlen_dropout_mask_bytes(int B, const int32_t* cu_q, const int32_t* cu_k,
+                                                 int Hq, int Hkv) {
+  if (B < 0 || B > ATTN_MAX_BATCH || Hq <= 0 || Hkv < 1 || Hq % Hkv ||
+      (B > 0 && (!cu_q || !cu_k)))
+    return 0;
+  const int G = head_group(Hq / Hkv);
+  const int64_t rows_tok = kRowsQ / G, ngroups = Hq / Hkv / G;
+  uint64_t blocks = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t lq = static_cast<int64_t>(cu_q[b + 1]) - cu_q[b];
+    const int64_t lk = static_cast<int64_t>(cu_k[b + 1]) - cu_k[b];
+    if (lq < 0 || lk < 0) return 0;
+    blocks += static_cast<uint64_t>((lq + rows_tok - 1) / rows_tok * ngroups *
+                                    ((lk + kKeys - 1) / kKeys));
+  }
+  return drop_mask_header(B) + blocks * Hkv * 8ull * kMaskBlockWords;
 }
 
 // ------------------------------------------------------------------ gated

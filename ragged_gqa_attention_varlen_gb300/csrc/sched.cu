@@ -102,11 +102,84 @@ __global__ void __launch_bounds__(1024) sched_kernel(Params p) {
     }
     pre_f[B] = acc_f;
     pre_b[B] = acc_b;
+    // stored keep mask: the per-sequence block prefix (its header) and the
+    // check that the caller's buffer holds every K/V head group's blocks
+    if (p.drop_mask) {
+      int32_t* mp = reinterpret_cast<int32_t*>(p.drop_mask);
+      int64_t acc = 0;
+      for (int b = 0; b < B; ++b) {
+        mp[b] = static_cast<int32_t>(acc);
+        const int64_t lq = p.cu_q[b + 1] - p.cu_q[b], lk = p.cu_k[b + 1] - p.cu_k[b];
+        acc += (lq + rows_tok - 1) / rows_tok * ngroups * ((lk + kKeys - 1) / kKeys);
+      }
+      mp[B] = static_cast<int32_t>(acc);
+      const uint64_t need = drop_mask_header(B) + static_cast<uint64_t>(acc) * p.Hkv *
+                                                      (8ull * kMaskBlockWords);
+      if (acc > INT32_MAX || need > p.drop_mask_bytes) *p.status = ATTN_DEV_MASK_SPACE;
+    }
   }
 }
 
 cudaError_t launch_sched(const Params& p, cudaStream_t s) {
   sched_kernel<<<1, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// The stored keep mask of a dropout call: every block of every K/V head
+// group (layout in attn_internal.h), one 2 KB block per CTA at a time; thread
+// w writes word w -- query row r = w % 128 of the tile, keys 64 (w / 128) ..
+// + 63 of the key tile -- from the counter-based hash the forward and
+// backward kernels would otherwise evaluate, zero for rows past the sequence.
+// Launched with group 0's parameters (Hq = heads per K/V head).
+__global__ void __launch_bounds__(256) mask_kernel(Params p) {
+  if (*p.status != 0) return;
+  const int32_t* pre = reinterpret_cast<const int32_t*>(p.drop_mask);
+  const int64_t per_group = pre[p.B];
+  const int64_t total = per_group * p.Hkv;
+  const int G = p.G;
+  const int rows_tok = kRowsQ / G;
+  const int ngroups = p.Hq / G;
+  uint64_t* words = reinterpret_cast<uint64_t*>(p.drop_mask + drop_mask_header(p.B));
+  const int w = threadIdx.x;
+  const int kh = w / kRowsQ, r = w % kRowsQ;
+  for (int64_t n = blockIdx.x; n < total; n += gridDim.x) {
+    const int64_t g = n / per_group;
+    const int local = static_cast<int>(n - g * per_group);
+    int lo = 0, hi = p.B - 1;  // the sequence: largest b with pre[b] <= local
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= local)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int b = lo;
+    const int q0 = p.cu_q[b];
+    const int Lq = p.cu_q[b + 1] - q0;
+    const int Lk = p.cu_k[b + 1] - p.cu_k[b];
+    const int nkt = (Lk + kKeys - 1) / kKeys;
+    const int blk = local - pre[b];
+    const int kt = blk % nkt, rest = blk / nkt;
+    const int hg = rest % ngroups, tb = rest / ngroups;
+    const int i = tb * rows_tok + r / G;
+    uint64_t bits = 0;
+    if (i < Lq) {
+      uint32_t T;
+      float sc;
+      drop_row(p, static_cast<int64_t>(q0) + i, T, sc);
+      const uint64_t dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(b));
+      const uint64_t dhi = drop_hi(static_cast<int>(g) * p.Hq + hg * G + r % G, i);
+      const int key0 = kt * kKeys + kh * 64;
+#pragma unroll 4
+      for (int c = 0; c < 64; c += 4)
+        bits |= static_cast<uint64_t>(drop_keep4(drop_hash(dkb, dhi, (key0 + c) >> 2), T)) << c;
+    }
+    words[n * kMaskBlockWords + w] = bits;
+  }
+}
+
+cudaError_t launch_mask(const Params& p, cudaStream_t s) {
+  mask_kernel<<<152 * 8, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -184,6 +184,19 @@ __device__ __forceinline__ void ktile_decode(const Params& p, int n, KTile& t) {
   }
 }
 
+// Block (tb, hg, kt) of sequence b in this K/V head group's part of the
+// stored keep mask (layout in attn_internal.h).
+__device__ __forceinline__ uint64_t* drop_mask_block(const Params& p, int b, int Lk, int tb,
+                                                     int hg, int kt) {
+  const int32_t* pre = reinterpret_cast<const int32_t*>(p.drop_mask);
+  const int64_t nkt = (Lk + kKeys - 1) / kKeys;
+  const int64_t g = p.head0 / p.Hq;
+  const int64_t blk = g * __ldg(pre + p.B) + __ldg(pre + b) +
+                      (static_cast<int64_t>(tb) * (p.Hq / p.G) + hg) * nkt + kt;
+  return reinterpret_cast<uint64_t*>(p.drop_mask + drop_mask_header(p.B)) +
+         blk * kMaskBlockWords;
+}
+
 // Dynamic tile stream of a persistent CTA.  Warp 0 draws tile numbers from
 // a global counter (so tiles start in the schedule's longest-first order)
 // and publishes them through a four-deep ring in shared memory; every other

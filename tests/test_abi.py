@@ -291,3 +291,50 @@ def test_gated_host_validation_codes(lib):
     assert _gated_call(lib, kgts=2 * 64 + 4) == -3
     assert _gated_call(lib, dkg=None) == -1       # the backward needs both gate gradients
     assert _gated_call(lib, Hkv=3) == -1
+
+
+def test_dropout_mask_bytes_is_the_documented_layout(lib):
+    """attn_varlen_dropout_mask_bytes: a 256-byte-rounded header of B + 1
+    int32, then Hkv groups of 2 KB blocks, one per (query tile, key tile) of
+    every sequence; query tiles are 128/G tokens x G heads with G the largest
+    power of two up to 16 dividing the heads per K/V head."""
+    import numpy as np
+
+    def expect(lq, lk, Hq, Hkv):
+        R = Hq // Hkv
+        G = 16
+        while R % G:
+            G //= 2
+        rows_tok, ngroups = 128 // G, R // G
+        blocks = sum(-(-a // rows_tok) * ngroups * -(-b // 128) for a, b in zip(lq, lk))
+        header = -(-4 * (len(lq) + 1) // 256) * 256
+        return header + Hkv * blocks * 2048
+
+    for lq, lk, Hq, Hkv in (([70, 300, 1], [90, 260, 40], 16, 1), ([0, 5], [7, 0], 12, 4),
+                            ([8000, 129], [128, 12000], 96, 1), ([190, 70], [150, 270], 8, 2),
+                            ([], [], 16, 1)):
+        cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+        cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+        got = lib.attn_varlen_dropout_mask_bytes(len(lq), cu_q.ctypes.data, cu_k.ctypes.data,
+                                                 Hq, Hkv)
+        assert got == expect(lq, lk, Hq, Hkv), (lq, lk, Hq, Hkv)
+    cu = np.array([0, 5], dtype=np.int32)
+    assert lib.attn_varlen_dropout_mask_bytes(1, cu.ctypes.data, cu.ctypes.data, 12, 5) == 0
+    bad = np.array([0, 5, 3], dtype=np.int32)  # decreasing
+    assert lib.attn_varlen_dropout_mask_bytes(2, bad.ctypes.data, bad.ctypes.data, 16, 1) == 0
+
+
+def test_dropout_mask_calls_validate_the_buffer(lib):
+    """The stored-mask calls refuse a missing, short or misaligned keep mask
+    before anything is enqueued."""
+    fake = 0x10000
+    head = [0, 2, 16, 1, 160, 10, 12,
+            fake, 16 * 160, 160, fake, 160, 160, fake, 160, 160, fake, 16 * 160, 160,
+            fake, fake, fake, 16, 0, -1, -1, 3.0, 0.75, 7, 0.1, None]
+    tail = [fake, 16 * 160, 160, fake, 16 * 160, 160, fake, 160, 160, fake, 160, 160,
+            fake, fake, 0, None, None]
+    f = lib.attn_varlen_fvjp_fwd_bwd_dropout_mask
+    assert f(*head, None, 1 << 20, *tail) == -1        # no mask
+    assert f(*head, fake, 16, *tail) == -1             # smaller than the header
+    assert f(*head, fake + 16, 1 << 20, *tail) == -3   # not 256-byte aligned
+    assert f(*head, fake, 1 << 20, *tail) == -4        # valid up to the missing workspace

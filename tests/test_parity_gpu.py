@@ -418,6 +418,37 @@ def test_dropout_parity(oracle_mod, idx):
     for n, x in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
         assert bits_equal(res[n], again[n]), n
         assert bits_equal(res[n], x), n
+    # the keep bits stored by the forward and read by the backward: bitwise
+    # the regenerated ones, fused and split (the mask buffer starts dirty)
+    Hkv = p.k.shape[1]
+    nbytes = BND.dropout_mask_bytes(p.cu_q, p.cu_k, p.Hq, Hkv)
+    km = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    stored = _run_dropout(p, keep_mask=km)
+    km2 = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    out2, lse2 = BND.attention_varlen_fwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, *mask,
+                                          keep_mask=km2, **drop)
+    dq2, dk2, dv2 = BND.attention_varlen_bwd(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes,
+                                             p.dout, out2, lse2, *mask, keep_mask=km2, **drop)
+    torch.cuda.synchronize()
+    for n, x in (("out", out2), ("lse", lse2), ("dq", dq2), ("dk", dk2), ("dv", dv2)):
+        assert bits_equal(res[n], stored[n]), n
+        assert bits_equal(res[n], x), n
+
+
+def test_dropout_mask_too_small_sets_status():
+    """A keep-mask buffer below what the lengths need is caught on the device:
+    the status word carries the mask-space bit and the kernels do nothing."""
+    p = _with_dropout(DROPOUT[0]).to("cuda")
+    nbytes = BND.dropout_mask_bytes(p.cu_q, p.cu_k, p.Hq, p.k.shape[1])
+    km = torch.zeros(nbytes - 2048, dtype=torch.uint8, device="cuda")
+    out = torch.full(p.q.shape, float("nan"), dtype=p.q.dtype, device="cuda")
+    r = BND.attention_varlen_fvjp(p.q, p.k, p.v, p.cu_q, p.cu_k, p.alibi_slopes, p.dout,
+                                  p.causal, p.window_left, p.window_right, p.softcap,
+                                  p.scale_multiplier, dropout_seed=p.dropout_seed,
+                                  dropout_rate=p.dropout_rate, keep_mask=km, out=out)
+    torch.cuda.synchronize()
+    assert BND.device_status(r["workspace"]) & BND.DEV_MASK_SPACE
+    assert bool(torch.isnan(out).all())
 
 
 def test_dropout_seed_changes_the_result():
