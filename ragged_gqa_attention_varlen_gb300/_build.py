@@ -15,7 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libattn_varlen.so")
 OBJDIR = os.path.join(PKG, "_build")
-SOURCES = ["host.cu", "sched.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkdv.cu", "bwd_dkdv_drop.cu", "noalloc.cu",
+SOURCES = ["host.cu", "sched.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkdv.cu", "bwd_dkdv_drop.cu", "bwd_dkdv_dmask.cu",
+           "noalloc.cu",
            "host_pipeline.cu", "shard.cu", "gate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

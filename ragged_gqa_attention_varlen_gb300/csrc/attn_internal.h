@@ -148,6 +148,12 @@ cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUte
                              const CUtensorMap& tv2, const CUtensorMap& tvt,
                              const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
                              cudaStream_t s);
+cudaError_t launch_dkdv_dmask(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
+                              const CUtensorMap& tdo2, const CUtensorMap& tdo,
+                              const CUtensorMap& tk2, const CUtensorMap& tkt,
+                              const CUtensorMap& tv2, const CUtensorMap& tvt,
+                              const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
+                              cudaStream_t s);
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,

@@ -99,7 +99,9 @@ struct Pair {
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
 // DM: dropout off (0), with the call's one rate (1), or with a rate per query
 // token from the table the schedule kernel builds (2) -- separate instances,
-// so the per-element work of the one-rate case holds no table lookup.
+// so the per-element work of the one-rate case holds no table lookup; 3 and 4
+// are 1 and 2 with the keep bits read from the stored mask instead of hashed
+// (separate instances too, so neither path's registers burden the other).
 template <bool BF16, bool MASK, int HD, int DM>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
@@ -110,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tdof) {
   using namespace kv;
   constexpr bool DROP = DM != 0;
-  constexpr bool DTAB = DM == 2;
+  constexpr bool DTAB = DM == 2 || DM == 4;
+  constexpr bool DMASK = DM >= 3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   uint8_t* sK = sm + kOffK;
@@ -561,20 +564,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       KTile t;
       ktile_decode<MASK>(p, item, t);
       const int nsteps = step_count(t);
-      const uint64_t dkb = DROP ? splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b)) : 0;
+      const uint64_t dkb =
+          (DROP && !DMASK) ? splitmix64(p.drop_seed ^ static_cast<uint64_t>(t.b)) : 0;
       // stored keep mask (written by the mask kernel): step st's block is the
-      // tile's first one plus st blocks of key tiles; the words of a step are
-      // loaded one step ahead
-      const uint64_t* mbase = nullptr;
-      int64_t mstep = 0;
-      const int msh = 32 * (quad & 1);
+      // tile's first one plus st rows of key-tile blocks.  Of each 64-bit word
+      // (64 keys of one column) this warp needs the 32-bit half of its 32
+      // keys; the halves of step st + 1 are loaded during step st, once P^T
+      // of step st has gone out (their memory latency then hides behind the
+      // dP^T and dS work)
+      const uint32_t* mbase = nullptr;
+      int mstep = 0;  // 32-bit words from one step's block to the next's
       uint32_t mw0 = 0, mw1 = 0;
-      if (DROP && p.drop_mask && nsteps > 0) {
-        mbase = drop_mask_block(p, t.b, t.Lk, t.tb0, 0, t.key / kKeys) + (quad >> 1) * kRowsQ +
-                half * 64 + lane;
-        mstep = static_cast<int64_t>((t.Lk + kKeys - 1) / kKeys) * kMaskBlockWords;
-        mw0 = static_cast<uint32_t>(__ldg(mbase) >> msh);
-        mw1 = static_cast<uint32_t>(__ldg(mbase + 32) >> msh);
+      if (DMASK && nsteps > 0) {
+        mbase = reinterpret_cast<const uint32_t*>(
+                    drop_mask_block(p, t.b, t.Lk, t.tb0, 0, t.key / kKeys) +
+                    (quad >> 1) * kRowsQ + half * 64 + lane) +
+                (quad & 1);
+        mstep = (t.Lk + kKeys - 1) / kKeys * (2 * kMaskBlockWords);
+        mw0 = __ldg(mbase);
+        mw1 = __ldg(mbase + 64);
       }
       for (int st = 0; st < nsteps; ++st) {
         const uint32_t gg = g + st;
@@ -583,15 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this thread's key, hashed while S^T is computed
         const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
         uint64_t kbits = 0;
-        if (DROP && mbase) {
+        if (DMASK) {
           // stored keep mask: the words of this half's 64 columns hold 64
           // keys each; this warp's 32 keys are one 32-bit half of them, turned
           // from one column per lane into one key per lane
           kbits = (static_cast<uint64_t>(bit_transpose32(mw1)) << 32) | bit_transpose32(mw0);
-          if (st + 1 < nsteps) {  // the next step's words, loaded during this one
-            mw0 = static_cast<uint32_t>(__ldg(mbase + (st + 1) * mstep) >> msh);
-            mw1 = static_cast<uint32_t>(__ldg(mbase + (st + 1) * mstep + 32) >> msh);
-          }
         } else if (DROP) {
           // one hash serves the four keys 4m .. 4m + 3, held by four
           // neighbouring lanes (key = t.key + r): each lane hashes 16 of the
@@ -761,6 +765,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
+        if (DMASK && st + 1 < nsteps) {  // the next step's keep-mask halves
+          const uint32_t* nx = mbase + static_cast<int64_t>(st + 1) * mstep;
+          mw0 = __ldg(nx);
+          mw1 = __ldg(nx + 64);
+        }
         // dP^T: read it and release SP for S^T of the next step (P^T went out
         // first, so dV, and with it the release of the dO slot, starts early)
         if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;

@@ -21,6 +21,8 @@ cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUte
                              const CUtensorMap& tv2, const CUtensorMap& tvt,
                              const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
                              cudaStream_t s) {
+  if (p.drop_mask)  // keep bits read from the stored mask
+    return launch_dkdv_dmask(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid, s);
   const bool m = masked_call(p);
   const bool tab = p.drop_tab != nullptr;
   auto k = p.dtype == 1 ? (m ? dkdv_drop_kernel<true, true>(p.d, tab)
