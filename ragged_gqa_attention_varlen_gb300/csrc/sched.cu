@@ -126,26 +126,35 @@ cudaError_t launch_sched(const Params& p, cudaStream_t s) {
 }
 
 // The stored keep mask of a dropout call: every block of every K/V head
-// group (layout in attn_internal.h), one 2 KB block per CTA at a time; thread
-// w writes word w -- query row r = w % 128 of the tile, keys 64 (w / 128) ..
-// + 63 of the key tile -- from the counter-based hash the forward and
-// backward kernels would otherwise evaluate, zero for rows past the sequence.
+// group (layout in attn_internal.h).  CTA c takes a contiguous run of blocks
+// in layout order, so it decodes (group, sequence, token block, head group,
+// key tile) once and then steps through them; thread w writes word w of each
+// block -- query row r = w % 128 of the tile, keys 64 (w / 128) .. + 63 of
+// the key tile -- from the counter-based hash the forward and backward
+// kernels would otherwise evaluate, zero for rows past the sequence.
 // Launched with group 0's parameters (Hq = heads per K/V head).
 __global__ void __launch_bounds__(256) mask_kernel(Params p) {
   if (*p.status != 0) return;
   const int32_t* pre = reinterpret_cast<const int32_t*>(p.drop_mask);
   const int64_t per_group = pre[p.B];
   const int64_t total = per_group * p.Hkv;
+  const int64_t chunk = (total + gridDim.x - 1) / gridDim.x;
+  int64_t n = static_cast<int64_t>(blockIdx.x) * chunk;
+  const int64_t n_end = min(total, n + chunk);
+  if (n >= n_end) return;
   const int G = p.G;
   const int rows_tok = kRowsQ / G;
   const int ngroups = p.Hq / G;
   uint64_t* words = reinterpret_cast<uint64_t*>(p.drop_mask + drop_mask_header(p.B));
   const int w = threadIdx.x;
   const int kh = w / kRowsQ, r = w % kRowsQ;
-  for (int64_t n = blockIdx.x; n < total; n += gridDim.x) {
-    const int64_t g = n / per_group;
-    const int local = static_cast<int>(n - g * per_group);
-    int lo = 0, hi = p.B - 1;  // the sequence: largest b with pre[b] <= local
+  const int rtok = r / G, rhead = r % G;
+  // decode the run's first block
+  int g = static_cast<int>(n / per_group);
+  const int local = static_cast<int>(n - static_cast<int64_t>(g) * per_group);
+  int b = 0;
+  {
+    int lo = 0, hi = p.B - 1;  // largest b with pre[b] <= local
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (pre[mid] <= local)
@@ -153,28 +162,54 @@ __global__ void __launch_bounds__(256) mask_kernel(Params p) {
       else
         hi = mid - 1;
     }
-    const int b = lo;
-    const int q0 = p.cu_q[b];
-    const int Lq = p.cu_q[b + 1] - q0;
-    const int Lk = p.cu_k[b + 1] - p.cu_k[b];
-    const int nkt = (Lk + kKeys - 1) / kKeys;
-    const int blk = local - pre[b];
-    const int kt = blk % nkt, rest = blk / nkt;
-    const int hg = rest % ngroups, tb = rest / ngroups;
-    const int i = tb * rows_tok + r / G;
+    b = lo;
+  }
+  int q0 = 0, Lq = 0, nkt = 1, ntb = 1;
+  uint64_t dkb = 0;
+  auto enter = [&]() {  // sequence b's lengths and hash key
+    q0 = p.cu_q[b];
+    Lq = p.cu_q[b + 1] - q0;
+    nkt = (p.cu_k[b + 1] - p.cu_k[b] + kKeys - 1) / kKeys;
+    ntb = (Lq + rows_tok - 1) / rows_tok;
+    dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(b));
+  };
+  enter();
+  int blk = local - pre[b];
+  int kt = blk % nkt;
+  blk /= nkt;
+  int hg = blk % ngroups;
+  int tb = blk / ngroups;
+  for (; n < n_end; ++n) {
+    const int i = tb * rows_tok + rtok;
     uint64_t bits = 0;
     if (i < Lq) {
       uint32_t T;
       float sc;
       drop_row(p, static_cast<int64_t>(q0) + i, T, sc);
-      const uint64_t dkb = splitmix64(p.drop_seed ^ static_cast<uint64_t>(b));
-      const uint64_t dhi = drop_hi(static_cast<int>(g) * p.Hq + hg * G + r % G, i);
+      const uint64_t dhi = drop_hi(g * p.Hq + hg * G + rhead, i);
       const int key0 = kt * kKeys + kh * 64;
 #pragma unroll 4
       for (int c = 0; c < 64; c += 4)
         bits |= static_cast<uint64_t>(drop_keep4(drop_hash(dkb, dhi, (key0 + c) >> 2), T)) << c;
     }
     words[n * kMaskBlockWords + w] = bits;
+    // the next block in layout order (sequences without blocks are skipped)
+    if (++kt == nkt) {
+      kt = 0;
+      if (++hg == ngroups) {
+        hg = 0;
+        if (++tb == ntb) {
+          tb = 0;
+          do {
+            if (++b == p.B) {
+              b = 0;
+              ++g;
+            }
+          } while (pre[b + 1] == pre[b] && n + 1 < n_end);
+          enter();
+        }
+      }
+    }
   }
 }
 
