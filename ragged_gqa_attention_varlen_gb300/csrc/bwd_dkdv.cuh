@@ -685,17 +685,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return Pack<BF16>::two(a, bb);
         };
-        auto p_group = [&](int q4, float b0, float b1, float b2, float b3) {
-          const uint64_t z0 = f2_fma(t2[2 * q4], lm.capped ? os2 : is2, f2_make(b0, b1));
-          const uint64_t z1 = f2_fma(t2[2 * q4 + 1], lm.capped ? os2 : is2, f2_make(b2, b3));
+        // columns col .. col + 3, held in pairs 2 s and 2 s + 1 of t2 and pk
+        auto p_group = [&](int s, int col, float b0, float b1, float b2, float b3) {
+          const uint64_t z0 = f2_fma(t2[2 * s], lm.capped ? os2 : is2, f2_make(b0, b1));
+          const uint64_t z1 = f2_fma(t2[2 * s + 1], lm.capped ? os2 : is2, f2_make(b2, b3));
           const uint64_t p0 = f2_make(ex2_approx(f2_lo(z0)), ex2_approx(f2_hi(z0)));
           const uint64_t p1 = f2_make(ex2_approx(f2_lo(z1)), ex2_approx(f2_hi(z1)));
-          pk[2 * q4] = pack_p(4 * q4, f2_lo(p0), f2_hi(p0));
-          pk[2 * q4 + 1] = pack_p(4 * q4 + 2, f2_lo(p1), f2_hi(p1));
+          pk[2 * s] = pack_p(col, f2_lo(p0), f2_hi(p0));
+          pk[2 * s + 1] = pack_p(col + 2, f2_lo(p1), f2_hi(p1));
           // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
-          t2[2 * q4] = lm.capped ? f2_mul(p0, f2_fma(t2[2 * q4], t2[2 * q4], m12)) : f2_mul(p0, m12);
-          t2[2 * q4 + 1] =
-              lm.capped ? f2_mul(p1, f2_fma(t2[2 * q4 + 1], t2[2 * q4 + 1], m12)) : f2_mul(p1, m12);
+          t2[2 * s] = lm.capped ? f2_mul(p0, f2_fma(t2[2 * s], t2[2 * s], m12)) : f2_mul(p0, m12);
+          t2[2 * s + 1] =
+              lm.capped ? f2_mul(p1, f2_fma(t2[2 * s + 1], t2[2 * s + 1], m12)) : f2_mul(p1, m12);
         };
         if ((cols->general[b][0] | cols->general[b][1]) == 0) {
           // one-sided tile: in three passes (all exponents, all exp2, then
@@ -745,11 +746,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bv[v] = adm ? bv[v] : -INFINITY;
               }
             }
-            // the pair arrays are indexed by q4 at run time here: route through
-            // the unrolled form so they stay in registers
+            // The group being processed is always pairs 0 and 1: the pair
+            // arrays turn by one group per iteration (16 turns bring them back
+            // into place), so the loop body indexes them with constants only
+            // and they stay in registers.  This keeps the code of the rare
+            // general steps small: the hot loop's instructions then fit the
+            // instruction caches better.
+            p_group(0, 4 * q4, bv[0], bv[1], bv[2], bv[3]);
+            const uint64_t s0 = t2[0], s1 = t2[1];
+            const uint32_t k0 = pk[0], k1 = pk[1];
 #pragma unroll
-            for (int qq = 0; qq < 16; ++qq)
-              if (qq == q4) p_group(qq, bv[0], bv[1], bv[2], bv[3]);
+            for (int i = 0; i < 30; ++i) {
+              t2[i] = t2[i + 2];
+              pk[i] = pk[i + 2];
+            }
+            t2[30] = s0;
+            t2[31] = s1;
+            pk[30] = k0;
+            pk[31] = k1;
           }
         }
         __syncwarp();

@@ -130,7 +130,9 @@ __device__ __forceinline__ int next_key_tile(const QTile& t, int kt) {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD, bool DROP>
+// FIXED: the call takes the fixed-reference softmax (a softcap of at most
+// kFixedCapMax) -- instances per path, so each holds only its own code.
+template <bool BF16, bool MASK, int HD, bool DROP, bool FIXED>
 __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     fwd_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tk2,
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     // With the softcap every logit of a row lies within 2c of a bound known
     // before any key is seen, so P is taken against that bound: no row max,
     // no exchange between the halves, no rescale of O.
-    const bool fixed = lm.capped && p.softcap <= kFixedCapMax;
+    constexpr bool fixed = FIXED;
     uint32_t g = 0;
     int tcount = 0;
     bool ok = true;
@@ -629,21 +631,26 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool B, bool M, bool DR>
+template <bool B, bool M, bool DR, bool FX>
 auto fwd_for_d(int d) {
-  return d == 128 ? fwd_kernel<B, M, 128, DR>
-                  : (d == 64 ? fwd_kernel<B, M, 64, DR> : fwd_kernel<B, M, 160, DR>);
+  return d == 128 ? fwd_kernel<B, M, 128, DR, FX>
+                  : (d == 64 ? fwd_kernel<B, M, 64, DR, FX> : fwd_kernel<B, M, 160, DR, FX>);
+}
+
+template <bool DR, bool FX>
+auto fwd_pick(const Params& p) {
+  const bool m = masked_call(p);
+  return p.dtype == 1 ? (m ? fwd_for_d<true, true, DR, FX>(p.d) : fwd_for_d<true, false, DR, FX>(p.d))
+                      : (m ? fwd_for_d<false, true, DR, FX>(p.d) : fwd_for_d<false, false, DR, FX>(p.d));
 }
 
 cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                        const CUtensorMap& tk2, const CUtensorMap& tkt, const CUtensorMap& tv2,
                        const CUtensorMap& tv, int grid, cudaStream_t s) {
-  const bool m = masked_call(p);
-  auto k = p.dropout
-               ? (p.dtype == 1 ? (m ? fwd_for_d<true, true, true>(p.d) : fwd_for_d<true, false, true>(p.d))
-                               : (m ? fwd_for_d<false, true, true>(p.d) : fwd_for_d<false, false, true>(p.d)))
-               : (p.dtype == 1 ? (m ? fwd_for_d<true, true, false>(p.d) : fwd_for_d<true, false, false>(p.d))
-                               : (m ? fwd_for_d<false, true, false>(p.d) : fwd_for_d<false, false, false>(p.d)));
+  // the fixed-reference softmax needs a softcap (make_logit_map: capped when > 0)
+  const bool fixed = p.softcap > 0.f && p.softcap <= kFixedCapMax;
+  auto k = p.dropout ? (fixed ? fwd_pick<true, true>(p) : fwd_pick<true, false>(p))
+                     : (fixed ? fwd_pick<false, true>(p) : fwd_pick<false, false>(p));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmem);
   k<<<grid, fwd::kThreadsF, fwd::kSmem, s>>>(p, tq2, tqt, tk2, tkt, tv2, tv);
   return cudaGetLastError();
