@@ -777,7 +777,7 @@ def main():
     ap.add_argument("--window-left", type=int, default=-1)
     ap.add_argument("--window-right", type=int, default=-1)
     ap.add_argument("--head-dim", type=int, default=HEAD_DIM, choices=(64, 128, 160))
-    ap.add_argument("--e2e-chunks", type=int, default=4,
+    ap.add_argument("--e2e-chunks", type=int, default=6,
                     help="sequence chunks of the end-to-end leg (copies overlap compute)")
     ap.add_argument("--dropout", type=float, default=None,
                     help="time with counter-based dropout at this rate (keep bits stored by "

@@ -348,8 +348,10 @@ size_t attn_varlen_dropout_mask_bytes(int B, const int32_t *cu_q, const int32_t 
  * then part of the call).  The pages have no counterpart; it serves the
  * end-to-end path.
  *
- * The batch is cut into `chunks` runs of whole sequences of about equal
- * sum Lq*Lk.  Each chunk goes through one of up to four slots of the device
+ * The batch is cut into `chunks` runs of whole sequences, each of about its
+ * share of the sum of Lq*Lk: equal shares, except that with three chunks or
+ * more the first and the last take a quarter of the others' (their copies in
+ * and out are the ones no computation overlaps).  Each chunk goes through one of up to four slots of the device
  * buffer: its inputs are copied in on one internal stream (once the slot's
  * previous chunk has been copied out), it computes on one of two internal
  * compute streams (chunks alternate between them, so one chunk's first
@@ -397,9 +399,10 @@ attn_status attn_varlen_fvjp_fwd_bwd_host(
 
 /* The chunking attn_varlen_fvjp_fwd_bwd_host uses: writes the sequence
  * boundaries 0 = cuts[0] < cuts[1] < ... < cuts[n] = B of n <= chunks runs of
- * whole sequences (HOST cu arrays; sequence b weighs Lq*Lk + 1, and run c
- * ends at the first sequence where the running weight reaches c/chunks of the
- * total) and returns n (0 for invalid arguments; 1 when B = 0, with
+ * whole sequences (HOST cu arrays; sequence b weighs Lq*Lk + 1, run c has the
+ * share s_c = 1/4 for the first and the last run when chunks >= 3, else 1,
+ * and ends at the first sequence where the running weight reaches
+ * (s_0 + ... + s_c) / (s_0 + ... + s_{chunks-1}) of the total) and returns n (0 for invalid arguments; 1 when B = 0, with
  * cuts = {0, 0}).  `cuts` holds chunks + 1 entries. */
 int attn_varlen_host_chunks(int B, const int32_t *cu_q, const int32_t *cu_k, int chunks,
                             int32_t *cuts);

@@ -152,12 +152,21 @@ extern "C" int attn_varlen_host_chunks(int B, const int32_t* cu_q, const int32_t
   double total = 0;
   for (int b = 0; b < B; ++b)
     total += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
+  // chunk c's share: with three chunks or more the first and the last take a
+  // quarter of the others', so the copies that nothing overlaps (the first
+  // chunk's inputs, the last chunk's results) are short
+  auto share = [&](int c) { return (chunks >= 3 && (c == 0 || c == chunks - 1)) ? 0.25 : 1.0; };
+  double shares = 0;
+  for (int c = 0; c < chunks; ++c) shares += share(c);
   int n = 0;
   cuts[0] = 0;
-  double acc = 0;
+  double acc = 0, bound = total * share(0) / shares;  // where chunk n ends
   for (int b = 0; b < B; ++b) {
     acc += static_cast<double>(cu_q[b + 1] - cu_q[b]) * (cu_k[b + 1] - cu_k[b]) + 1.0;
-    if (n + 1 < chunks && b + 1 < B && acc >= total * (n + 1) / chunks) cuts[++n] = b + 1;
+    if (n + 1 < chunks && b + 1 < B && acc >= bound) {
+      cuts[++n] = b + 1;
+      bound += total * share(n) / shares;
+    }
   }
   cuts[++n] = B;
   return n;

@@ -184,27 +184,37 @@ def test_host_entry_point_validates_before_touching_the_device(lib):
 
 def test_host_buffer_is_slots_of_the_largest_chunk(lib):
     """The host-buffer call's device buffer holds min(4, chunks) slots sized
-    for the largest chunk: with eight equal sequences in eight chunks it is
-    about half of the whole-batch bound, and it grows with a dominant
-    sequence."""
+    for the largest chunk (the chunking's own cuts): within a few per cent
+    of that many buffers of one chunk-sized sequence, far below the
+    whole-batch bound, and never below a dominant sequence's own slot."""
     import numpy as np
+
+    from ragged_gqa_attention_varlen_gb300 import binding
+    import torch
 
     def size_for(lengths, chunks):
         cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
         return lib.attn_varlen_fvjp_host_buffer_size_for(len(lengths), cu.ctypes.data,
                                                          cu.ctypes.data, 16, 1, 128, chunks)
 
-    even = size_for([1000] * 8, 8)
+    lengths = [1000] * 8
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    for chunks in (1, 2, 4, 8):
+        cuts = binding.host_chunks(cu, cu, chunks)
+        n = len(cuts) - 1
+        largest = max(sum(lengths[a:b]) for a, b in zip(cuts, cuts[1:]))
+        model = min(4, n) * size_for([largest], 1)
+        assert abs(size_for(lengths, chunks) - model) <= 0.05 * model, chunks
     bound = lib.attn_varlen_fvjp_host_buffer_size(8, 16, 1, 128, 8000, 8000, 8)
-    assert even < bound / 7          # 4 slots of one sequence vs 4 slots of all eight
-    assert size_for([7000] + [143] * 7, 8) > 4 * even
-    assert size_for([1000] * 8, 1) > 7 * size_for([1000] * 8, 8) / 4
-
+    assert size_for(lengths, 8) < bound / 3
+    assert size_for([7000] + [143] * 7, 8) >= size_for([7000], 1)
 
 def test_host_chunks_cut_whole_sequences_of_balanced_work(lib):
     """The host-buffer entry point's chunking: strictly increasing sequence
     boundaries from 0 to B, at most `chunks` runs, and every run's weight
-    (sum of Lq*Lk + 1) within one sequence's weight of an equal share."""
+    (sum of Lq*Lk + 1) within one sequence's weight of its share: equal
+    shares, except that with three chunks or more the first and the last
+    take a quarter of the others'."""
     import torch
 
     from ragged_gqa_attention_varlen_gb300 import binding
@@ -222,9 +232,11 @@ def test_host_chunks_cut_whole_sequences_of_balanced_work(lib):
         assert 1 <= len(cuts) - 1 <= max(1, min(chunks, B))
         assert all(a < b for a, b in zip(cuts, cuts[1:])) or B == 0
         w = (lq * lk + 1).double()
-        share, wmax = float(w.sum()) / chunks, float(w.max()) if B else 0.0
-        for a, b in zip(cuts, cuts[1:]):
-            assert float(w[a:b].sum()) <= share + wmax + 1e-6
+        shares = [0.25 if chunks >= 3 and c in (0, chunks - 1) else 1.0 for c in range(chunks)]
+        unit, wmax = float(w.sum()) / sum(shares), float(w.max()) if B else 0.0
+        for c, (a, b) in enumerate(zip(cuts, cuts[1:])):
+            if b < B:  # the last run takes whatever is left
+                assert float(w[a:b].sum()) <= shares[c] * unit + wmax + 1e-6
 
 
 def test_python_entry_points_refuse_host_tensors(lib):
