@@ -4,10 +4,17 @@
 
 namespace attn {
 
-template <bool B, bool M>
+template <bool B, bool M, bool C>
 auto dkdv_for_d(int d) {
-  return d == 128 ? dkdv_kernel<B, M, 128, 0>
-                  : (d == 64 ? dkdv_kernel<B, M, 64, 0> : dkdv_kernel<B, M, 160, 0>);
+  return d == 128 ? dkdv_kernel<B, M, 128, 0, C>
+                  : (d == 64 ? dkdv_kernel<B, M, 64, 0, C> : dkdv_kernel<B, M, 160, 0, C>);
+}
+
+template <bool C>
+auto dkdv_pick(const Params& p) {
+  const bool m = masked_call(p);
+  return p.dtype == 1 ? (m ? dkdv_for_d<true, true, C>(p.d) : dkdv_for_d<true, false, C>(p.d))
+                      : (m ? dkdv_for_d<false, true, C>(p.d) : dkdv_for_d<false, false, C>(p.d));
 }
 
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
@@ -16,9 +23,8 @@ cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorM
                         const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
   if (p.dropout)
     return launch_dkdv_drop(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid, s);
-  const bool m = masked_call(p);
-  auto k = p.dtype == 1 ? (m ? dkdv_for_d<true, true>(p.d) : dkdv_for_d<true, false>(p.d))
-                        : (m ? dkdv_for_d<false, true>(p.d) : dkdv_for_d<false, false>(p.d));
+  // instances for capped calls (the logit map's cap test: softcap > 0)
+  auto k = p.softcap > 0.f ? dkdv_pick<true>(p) : dkdv_pick<false>(p);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
   k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();

@@ -102,7 +102,10 @@ struct Pair {
 // so the per-element work of the one-rate case holds no table lookup; 3 and 4
 // are 1 and 2 with the keep bits read from the stored mask instead of hashed
 // (separate instances too, so neither path's registers burden the other).
-template <bool BF16, bool MASK, int HD, int DM>
+// CAP: the call has a softcap (set only on instances launched for capped
+// calls, so their element code holds no uncapped branch); otherwise the cap
+// is read from the parameters at run time.
+template <bool BF16, bool MASK, int HD, int DM, bool CAP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
@@ -551,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float rf = static_cast<float>(r);
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
+    const bool capped = CAP || lm.capped;
     constexpr bool masked = MASK;
     const int wl = p.wl;
     const int wr = right_window(p);
@@ -652,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t is2 = f2_make(lm.in_scale, lm.in_scale);
         const uint64_t os2 = f2_make(lm.out_scale, lm.out_scale);
         const uint64_t m12 = f2_make(-1.f, -1.f);
-        if (lm.capped) {
+        if (capped) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const uint64_t v = f2_mul(t2[i], is2);
@@ -687,16 +691,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // columns col .. col + 3, held in pairs 2 s and 2 s + 1 of t2 and pk
         auto p_group = [&](int s, int col, float b0, float b1, float b2, float b3) {
-          const uint64_t z0 = f2_fma(t2[2 * s], lm.capped ? os2 : is2, f2_make(b0, b1));
-          const uint64_t z1 = f2_fma(t2[2 * s + 1], lm.capped ? os2 : is2, f2_make(b2, b3));
+          const uint64_t z0 = f2_fma(t2[2 * s], capped ? os2 : is2, f2_make(b0, b1));
+          const uint64_t z1 = f2_fma(t2[2 * s + 1], capped ? os2 : is2, f2_make(b2, b3));
           const uint64_t p0 = f2_make(ex2_approx(f2_lo(z0)), ex2_approx(f2_hi(z0)));
           const uint64_t p1 = f2_make(ex2_approx(f2_lo(z1)), ex2_approx(f2_hi(z1)));
           pk[2 * s] = pack_p(col, f2_lo(p0), f2_hi(p0));
           pk[2 * s + 1] = pack_p(col + 2, f2_lo(p1), f2_hi(p1));
           // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
-          t2[2 * s] = lm.capped ? f2_mul(p0, f2_fma(t2[2 * s], t2[2 * s], m12)) : f2_mul(p0, m12);
+          t2[2 * s] = capped ? f2_mul(p0, f2_fma(t2[2 * s], t2[2 * s], m12)) : f2_mul(p0, m12);
           t2[2 * s + 1] =
-              lm.capped ? f2_mul(p1, f2_fma(t2[2 * s + 1], t2[2 * s + 1], m12)) : f2_mul(p1, m12);
+              capped ? f2_mul(p1, f2_fma(t2[2 * s + 1], t2[2 * s + 1], m12)) : f2_mul(p1, m12);
         };
         if ((cols->general[b][0] | cols->general[b][1]) == 0) {
           // one-sided tile: in three passes (all exponents, all exp2, then
@@ -709,8 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 a4 = pa[q4], m4 = pm[q4];
             const uint64_t b0 = f2_fma(f2_make(m4.x, m4.y), r2, f2_make(a4.x, a4.y));
             const uint64_t b1 = f2_fma(f2_make(m4.z, m4.w), r2, f2_make(a4.z, a4.w));
-            z[2 * q4] = f2_fma(t2[2 * q4], lm.capped ? os2 : is2, b0);
-            z[2 * q4 + 1] = f2_fma(t2[2 * q4 + 1], lm.capped ? os2 : is2, b1);
+            z[2 * q4] = f2_fma(t2[2 * q4], capped ? os2 : is2, b0);
+            z[2 * q4 + 1] = f2_fma(t2[2 * q4 + 1], capped ? os2 : is2, b1);
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -719,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             pk[i] = pack_p(2 * i, f2_lo(z[i]), f2_hi(z[i]));
             // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
-            t2[i] = lm.capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
+            t2[i] = capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
           }
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:

@@ -87,7 +87,9 @@ __device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity) {
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
-template <bool BF16, bool MASK, int HD, bool DROP>
+// CAP: the call has a softcap (instances for capped calls hold no uncapped
+// branch in their element code); otherwise read at run time.
+template <bool BF16, bool MASK, int HD, bool DROP, bool CAP = false>
 __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     dq_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tq2,
               const __grid_constant__ CUtensorMap tqt, const __grid_constant__ CUtensorMap tdo2,
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
+    const bool capped = CAP || lm.capped;
     constexpr bool masked = MASK;
     const int lgG = __ffs(G) - 1;  // G is a power of two
     // This lane's Q row of a tile into TMEM: features 80*half..80*half+79 as
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
         for (int b = 0; b < 2; ++b) {
           float* xb = x + b * 32;
           float th[32];
-          if (lm.capped) {
+          if (capped) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
           }
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           for (int c = 0; c < 32; ++c) {
             const float bias =
                 fmaf(-slope2, fabsf(pos0 - static_cast<float>(b * 32 + c)), -lse2);
-            xb[c] = lm.capped ? fmaf(th[c], lm.out_scale, bias) : fmaf(xb[c], lm.in_scale, bias);
+            xb[c] = capped ? fmaf(th[c], lm.out_scale, bias) : fmaf(xb[c], lm.in_scale, bias);
           }
           if (edge) {
 #pragma unroll
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
           }
 #pragma unroll
           for (int c = 0; c < 32; ++c) xb[c] = ex2_approx(xb[c]);  // P
-          if (lm.capped) {
+          if (capped) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) xb[c] *= fmaf(-th[c], th[c], 1.f);  // P (1 - tanh^2)
           }
@@ -541,22 +544,28 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool B, bool M, bool DR>
+template <bool B, bool M, bool DR, bool C>
 auto dq_for_d(int d) {
-  return d == 128 ? dq_kernel<B, M, 128, DR>
-                  : (d == 64 ? dq_kernel<B, M, 64, DR> : dq_kernel<B, M, 160, DR>);
+  return d == 128 ? dq_kernel<B, M, 128, DR, C>
+                  : (d == 64 ? dq_kernel<B, M, 64, DR, C> : dq_kernel<B, M, 160, DR, C>);
+}
+
+template <bool DR, bool C>
+auto dq_pick(const Params& p) {
+  const bool m = masked_call(p);
+  return p.dtype == 1 ? (m ? dq_for_d<true, true, DR, C>(p.d) : dq_for_d<true, false, DR, C>(p.d))
+                      : (m ? dq_for_d<false, true, DR, C>(p.d) : dq_for_d<false, false, DR, C>(p.d));
 }
 
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s) {
-  const bool m = masked_call(p);
-  auto k = p.dropout
-               ? (p.dtype == 1 ? (m ? dq_for_d<true, true, true>(p.d) : dq_for_d<true, false, true>(p.d))
-                               : (m ? dq_for_d<false, true, true>(p.d) : dq_for_d<false, false, true>(p.d)))
-               : (p.dtype == 1 ? (m ? dq_for_d<true, true, false>(p.d) : dq_for_d<true, false, false>(p.d))
-                               : (m ? dq_for_d<false, true, false>(p.d) : dq_for_d<false, false, false>(p.d)));
+  // capped calls without dropout take the instances with a known cap (the
+  // logit map's cap test: softcap > 0)
+  const bool cap = p.softcap > 0.f;
+  auto k = p.dropout ? dq_pick<true, false>(p)
+                     : (cap ? dq_pick<false, true>(p) : dq_pick<false, false>(p));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
   // With `overlap` the launch is a programmatic dependent of the kernel before
   // it (dk/dv, which signals at its start): dq reads nothing dk/dv writes, so

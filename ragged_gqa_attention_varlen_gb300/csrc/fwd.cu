@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const LogitMap lm = make_logit_map(p);
+    const bool capped = FIXED || lm.capped;  // the fixed reference needs a cap
     constexpr bool masked = MASK;
     // With the softcap every logit of a row lies within 2c of a bound known
     // before any key is seen, so P is taken against that bound: no row max,
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(fwd::kThreadsF, 1)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           float* xb = x + b * 32;
-          if (lm.capped) {
+          if (capped) {
             float th[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) th[c] = tanh_approx(xb[c] * lm.in_scale);
