@@ -4,15 +4,18 @@
 
 namespace attn {
 
-template <bool B, bool M, int DM>
+template <bool B, bool M, int DM, bool C>
 auto dkdv_drop_for_d(int d) {
-  return d == 128 ? dkdv_kernel<B, M, 128, DM>
-                  : (d == 64 ? dkdv_kernel<B, M, 64, DM> : dkdv_kernel<B, M, 160, DM>);
+  return d == 128 ? dkdv_kernel<B, M, 128, DM, C>
+                  : (d == 64 ? dkdv_kernel<B, M, 64, DM, C> : dkdv_kernel<B, M, 160, DM, C>);
 }
 
+// the call's one rate takes instances with a known cap when the call is
+// capped (softcap > 0); per-token rates read the cap at run time
 template <bool B, bool M>
-auto dkdv_drop_kernel(int d, bool table) {
-  return table ? dkdv_drop_for_d<B, M, 2>(d) : dkdv_drop_for_d<B, M, 1>(d);
+auto dkdv_drop_kernel(int d, bool table, bool cap) {
+  return table ? dkdv_drop_for_d<B, M, 2, false>(d)
+               : (cap ? dkdv_drop_for_d<B, M, 1, true>(d) : dkdv_drop_for_d<B, M, 1, false>(d));
 }
 
 cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
@@ -25,10 +28,11 @@ cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUte
     return launch_dkdv_dmask(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid, s);
   const bool m = masked_call(p);
   const bool tab = p.drop_tab != nullptr;
-  auto k = p.dtype == 1 ? (m ? dkdv_drop_kernel<true, true>(p.d, tab)
-                             : dkdv_drop_kernel<true, false>(p.d, tab))
-                        : (m ? dkdv_drop_kernel<false, true>(p.d, tab)
-                             : dkdv_drop_kernel<false, false>(p.d, tab));
+  const bool cap = p.softcap > 0.f;
+  auto k = p.dtype == 1 ? (m ? dkdv_drop_kernel<true, true>(p.d, tab, cap)
+                             : dkdv_drop_kernel<true, false>(p.d, tab, cap))
+                        : (m ? dkdv_drop_kernel<false, true>(p.d, tab, cap)
+                             : dkdv_drop_kernel<false, false>(p.d, tab, cap));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
   k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
   return cudaGetLastError();

@@ -561,10 +561,10 @@ cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,
                       int grid, bool overlap, cudaStream_t s) {
-  // capped calls without dropout take the instances with a known cap (the
-  // logit map's cap test: softcap > 0)
+  // capped calls take the instances with a known cap (the logit map's cap
+  // test: softcap > 0)
   const bool cap = p.softcap > 0.f;
-  auto k = p.dropout ? dq_pick<true, false>(p)
+  auto k = p.dropout ? (cap ? dq_pick<true, true>(p) : dq_pick<true, false>(p))
                      : (cap ? dq_pick<false, true>(p) : dq_pick<false, false>(p));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::kSmem);
   // With `overlap` the launch is a programmatic dependent of the kernel before
