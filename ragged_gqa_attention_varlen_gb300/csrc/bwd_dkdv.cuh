@@ -35,6 +35,7 @@
 // operands (of dK and dV) and use three 128-byte-swizzled 64-feature chunks
 // (48 KB); Q has two slots, dO one.
 #pragma once
+#include <type_traits>
 #include "../../include/attn_varlen.h"
 #include "common.cuh"
 #include "sched.cuh"
@@ -94,6 +95,43 @@ struct Pair {
     return v;
   }
 };
+
+// The order in which a key tile walks its query steps.  Step st is token
+// block tb(st / ngroups), head group st % ngroups.  The steps whose columns'
+// aligned keys may lie inside the tile (the "band" of token blocks [tbA, tbB),
+// whose bias need not be one line per column over the tile's keys) go last.
+// Without a mask the step loop then runs in two parts: the other steps with
+// the one-sided element code only, then the band.  With a mask every step may
+// be cut, so one loop checks each step; the order is the same, so a window
+// wider than every sequence gives bitwise the unmasked results.
+struct StepMap {
+  int tb0, nA, nC, tbA, tbB;
+  // token block of the j-th block in the walk: [tb0, tbA), [tbB, ..), [tbA, tbB)
+  __device__ __forceinline__ int tb(int j) const {
+    return j < nA ? tb0 + j : (j < nA + nC ? tbB + (j - nA) : tbA + (j - nA - nC));
+  }
+};
+
+__device__ __forceinline__ StepMap step_map(const KTile& t, int step_tok) {
+  StepMap m;
+  m.tb0 = t.tb0;
+  m.nA = t.ntb;
+  m.nC = 0;
+  m.tbA = m.tbB = t.tb0 + t.ntb;
+  // tokens i with 0 < i + Lk - Lq - key < 127 (and i < Lq) straddle the tile
+  const int off = t.Lk - t.Lq;
+  const int lo = max(0, t.key - off + 1), hi = min(t.Lq - 1, t.key - off + kKeys - 2);
+  if (lo > hi) return m;
+  m.tbA = max(t.tb0, lo / step_tok);
+  m.tbB = min(t.tb0 + t.ntb, hi / step_tok + 1);
+  if (m.tbA >= m.tbB) {
+    m.tbA = m.tbB = t.tb0 + t.ntb;
+    return m;
+  }
+  m.nA = m.tbA - t.tb0;
+  m.nC = t.tb0 + t.ntb - m.tbB;
+  return m;
+}
 
 // HD: the head dimension (160, 128 or 64) -- the MMA shapes and the stores
 // follow it; the shared-memory and TMEM layouts are those of 160 features.
@@ -237,9 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 1) tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, key);
       if (lane == 2) tma_load_3d(sV, &tv2, &bars->kv_full, 0, key, 0);
       if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
+      const StepMap sm = step_map(t, step_tok);
       if (lane >= 4 && lane < 6) {
         for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
-          const int ptok = t.q0 + (t.tb0 + sp / ngroups) * step_tok;
+          const int ptok = t.q0 + sm.tb(sp / ngroups) * step_tok;
           const int ph0 = (sp % ngroups) * G;
           if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
           if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
@@ -250,21 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tiles of step st + kPrefetch are requested into L2 while step st is
       // loaded, so the loads that the ring can afford to wait for hit L2.
       constexpr int kPrefetch = 4;
-      // step st = (token block stb, head group shg); (ptb, phg) is step
-      // st + kPrefetch; both advance without a division per step
-      auto advance = [&](int& tb, int& hg) {
-        if (++hg == ngroups) {
-          hg = 0;
-          ++tb;
-        }
-      };
-      int stb = t.tb0, shg = 0, ptb = t.tb0 + kPrefetch / ngroups, phg = kPrefetch % ngroups;
-      for (int st = 0; st < nsteps; ++st, ++ndo, advance(stb, shg), advance(ptb, phg)) {
-        const int tok = t.q0 + stb * step_tok;
-        const int h0 = shg * G;
+      for (int st = 0; st < nsteps; ++st, ++ndo) {
+        const int tok = t.q0 + sm.tb(st / ngroups) * step_tok;
+        const int h0 = (st % ngroups) * G;
         if (lane >= 4 && lane < 6 && st + kPrefetch < nsteps) {
-          const int ptok = t.q0 + ptb * step_tok;
-          const int ph0 = phg * G;
+          const int ptok = t.q0 + sm.tb((st + kPrefetch) / ngroups) * step_tok;
+          const int ph0 = ((st + kPrefetch) % ngroups) * G;
           if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
           if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
         }
@@ -430,9 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u = lane;
     constexpr bool masked = MASK;
     const int lgGs = __ffs(G) - 1;  // G is a power of two
-    struct Pos {  // a (key tile, query step) of this CTA; st = tb * ngroups + hg
+    struct Pos {  // a (key tile, query step) of this CTA: step st is (tb, hg)
       int item, st, tb, hg, nsteps;
       KTile t;
+      StepMap sm;
     };
     struct Vals {
       float lse[4], sl2[4], D[4];
@@ -450,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (q.item < ntiles) {
         ktile_decode<MASK>(p, q.item, q.t);
         q.nsteps = step_count(q.t);
-        q.tb = q.t.tb0;
+        q.sm = step_map(q.t, step_tok);
+        q.tb = q.sm.tb(0);
         if (q.nsteps > 0) return;
         q.item = take();
       }
@@ -459,10 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       Pos n = q;
       if (q.item >= ntiles) return n;
       if (++n.st < n.nsteps) {
-        if (++n.hg == ngroups) {
-          n.hg = 0;
-          ++n.tb;
-        }
+        n.hg = n.st % ngroups;
+        n.tb = n.sm.tb(n.st / ngroups);
         return n;
       }
       n.item = take();
@@ -576,24 +606,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // keys; the halves of step st + 1 are loaded during step st, once P^T
       // of step st has gone out (their memory latency then hides behind the
       // dP^T and dS work)
+      const StepMap sm = step_map(t, step_tok);
       const uint32_t* mbase = nullptr;
-      int mstep = 0;  // 32-bit words from one step's block to the next's
+      int mstep = 0;  // 32-bit words from one block (token block, head group) to the next
       uint32_t mw0 = 0, mw1 = 0;
+      // the mask words of step st: its block relative to the tile's first
+      auto mwords = [&](int s_) {
+        return mbase + static_cast<int64_t>((sm.tb(s_ / ngroups) - t.tb0) * ngroups +
+                                            s_ % ngroups) * mstep;
+      };
       if (DMASK && nsteps > 0) {
         mbase = reinterpret_cast<const uint32_t*>(
                     drop_mask_block(p, t.b, t.Lk, t.tb0, 0, t.key / kKeys) +
                     (quad >> 1) * kRowsQ + half * 64 + lane) +
                 (quad & 1);
         mstep = (t.Lk + kKeys - 1) / kKeys * (2 * kMaskBlockWords);
-        mw0 = __ldg(mbase);
-        mw1 = __ldg(mbase + 64);
+        mw0 = __ldg(mwords(0));
+        mw1 = __ldg(mwords(0) + 64);
       }
-      for (int st = 0; st < nsteps; ++st) {
+      // one step of the walk; K = 0: a step outside the band (one-sided element
+      // code only), 1: a band step (general code only), 2: with a mask, either,
+      // by the staging warp's flag
+      auto step = [&](int st, auto kind) -> bool {
+        constexpr int K = decltype(kind)::value;
         const uint32_t gg = g + st;
         const int b = gg & 1;
+        const int tb = sm.tb(st / ngroups);
         // dropout keep bits of this step's 64 columns (query token, head) for
         // this thread's key, hashed while S^T is computed
-        const int dtok0 = DROP ? (t.tb0 + st / ngroups) * step_tok : 0;
+        const int dtok0 = DROP ? tb * step_tok : 0;
         uint64_t kbits = 0;
         if (DMASK) {
           // stored keep mask: the words of this half's 64 columns hold 64
@@ -638,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // S^T: read it and release SP for dP^T
-        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) break;
+        if (!(ok = mbar_wait_warp(&bars->s_full, gg & 1, s_abort))) return false;
         tc_fence_after();
         const uint32_t spbuf = tmem + kColSP + half * 64 + lane_addr;
         uint64_t t2[32];  // column pairs: S, then tanh, then -P (1 - tanh^2)
@@ -667,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the base-2 bias -slope2 * |i + Lk - Lq - j| - lse2 formed from the
         // staged column scalars (a + m * j when the tile lies on one side of
         // every column's aligned key)
-        if (!(ok = mbar_wait_warp(&bars->am_full[b], (gg >> 1) & 1, s_abort))) break;
+        if (!(ok = mbar_wait_warp(&bars->am_full[b], (gg >> 1) & 1, s_abort))) return false;
         const float4* pa = reinterpret_cast<const float4*>(cols->a[b] + half * 64);
         const float4* pm = reinterpret_cast<const float4*>(cols->m[b] + half * 64);
         uint32_t pk[32];
@@ -702,7 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           t2[2 * s + 1] =
               capped ? f2_mul(p1, f2_fma(t2[2 * s + 1], t2[2 * s + 1], m12)) : f2_mul(p1, m12);
         };
-        if ((cols->general[b][0] | cols->general[b][1]) == 0) {
+        // K = 0 steps are one-sided by the walk's order; in the band (and
+        // with a mask) the staging warp's flag tells
+        const bool gen = K != 0 && (cols->general[b][0] | cols->general[b][1]) != 0;
+        if (!gen) {
           // one-sided tile: in three passes (all exponents, all exp2, then
           // the packing and chain factors), so the 64 MUFU operations issue
           // back to back
@@ -725,12 +769,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             // -P (1 - tanh^2) = P (tanh^2 - 1); dS = this * (D - dP)
             t2[i] = capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
           }
+        } else if (K == 1) {
+          // a general band step (no mask): the general bias per element, then
+          // the same exp2 and packing passes as a one-sided step
+          const int tok0 = tb * step_tok;
+          const int off = t.Lk - t.Lq - t.key;
+          uint64_t z[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 a4 = pa[q4], m4 = pm[q4];
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+            float bv[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int c = half * 64 + q4 * 4 + v;
+              const float prel = static_cast<float>(tok0 + (c >> lgG) + off);
+              const float sl = prel <= 0.f ? -mv[v] : mv[v];
+              bv[v] = fmaf(-sl, fabsf(prel - rf), fmaf(mv[v], prel, av[v]));
+            }
+            z[2 * q4] = f2_fma(t2[2 * q4], capped ? os2 : is2, f2_make(bv[0], bv[1]));
+            z[2 * q4 + 1] = f2_fma(t2[2 * q4 + 1], capped ? os2 : is2, f2_make(bv[2], bv[3]));
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            z[i] = f2_make(ex2_approx(f2_lo(z[i])), ex2_approx(f2_hi(z[i])));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            pk[i] = pack_p(2 * i, f2_lo(z[i]), f2_hi(z[i]));
+            t2[i] = capped ? f2_mul(z[i], f2_fma(t2[i], t2[i], m12)) : f2_mul(z[i], m12);
+          }
         } else {
           // some column's aligned key lies inside the tile, or a mask applies:
           // prel = i + Lk - Lq - key0 of column c is tok0 + c / G + off,
           // a + m * prel = -lse2, and the column's slope2 is m where its
           // scalars were staged for keys left of prel (prel > 0), else -m
-          const int tok0 = (t.tb0 + st / ngroups) * step_tok;
+          const int tok0 = tb * step_tok;
           const int off = t.Lk - t.Lq - t.key;
 #pragma unroll 1
           for (int q4 = 0; q4 < 16; ++q4) {
@@ -774,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->am_empty[b]);
         // P^T pairs: this half's 64 columns -> 32 pair columns at 448 + 32*half,
         // once dK of the previous step has read X
-        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->dk_done, (gg - 1) & 1, s_abort))) break;
+        if (gg >= 1 && !(ok = mbar_wait_warp(&bars->dk_done, (gg - 1) & 1, s_abort))) return false;
         tc_fence_after();
         const uint32_t xbuf = tmem + kColX + half * 32 + lane_addr;
         tmem_st16(xbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
@@ -784,13 +858,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
         if (DMASK && st + 1 < nsteps) {  // the next step's keep-mask halves
-          const uint32_t* nx = mbase + static_cast<int64_t>(st + 1) * mstep;
+          const uint32_t* nx = mwords(st + 1);
           mw0 = __ldg(nx);
           mw1 = __ldg(nx + 64);
         }
         // dP^T: read it and release SP for S^T of the next step (P^T went out
         // first, so dV, and with it the release of the dO slot, starts early)
-        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) break;
+        if (!(ok = mbar_wait_warp(&bars->dp_full, gg & 1, s_abort))) return false;
         tc_fence_after();
         float d[64];
         tmem_ld32(spbuf, *reinterpret_cast<float(*)[32]>(d));
@@ -804,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 64; ++c) d[c] = ((kbits >> c) & 1) ? d[c] * dscale(c) : 0.f;
         }
         // dS^T = P (1 - tanh^2) (dP - D) = t2 (D - dP), D per group of 4 columns
-        if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) break;
+        if (!(ok = mbar_wait_warp(&bars->d_full, gg & 1, s_abort))) return false;
         {
           const float4* pd = reinterpret_cast<const float4*>(cols->D + half * 64);
 #pragma unroll
@@ -821,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->d_empty);
         // dS^T pairs over P^T once dV has read it
-        if (!(ok = mbar_wait_warp(&bars->dv_done, gg & 1, s_abort))) break;
+        if (!(ok = mbar_wait_warp(&bars->dv_done, gg & 1, s_abort))) return false;
         tc_fence_after();
         tmem_st16(xbuf, *reinterpret_cast<uint32_t(*)[16]>(pk));
         tmem_st16(xbuf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
@@ -829,6 +903,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->ds_full);
+        return true;
+      };
+      if (!MASK) {
+        const int n_one = (sm.nA + sm.nC) * ngroups;
+        int st = 0;
+        for (; st < n_one && ok; ++st) ok = step(st, std::integral_constant<int, 0>{});
+        for (; st < nsteps && ok; ++st) ok = step(st, std::integral_constant<int, 1>{});
+      } else {
+        for (int st = 0; st < nsteps && ok; ++st) ok = step(st, std::integral_constant<int, 2>{});
       }
       if (!ok) break;
       g += nsteps;
