@@ -112,12 +112,15 @@ struct StepMap {
   }
 };
 
-__device__ __forceinline__ StepMap step_map(const KTile& t, int step_tok) {
+// band_last false: the natural order (the dropout instances walk it: their
+// keep-mask reads and hashing keep the tiles of a sequence closer together so)
+__device__ __forceinline__ StepMap step_map(const KTile& t, int step_tok, bool band_last) {
   StepMap m;
   m.tb0 = t.tb0;
   m.nA = t.ntb;
   m.nC = 0;
   m.tbA = m.tbB = t.tb0 + t.ntb;
+  if (!band_last) return m;
   // tokens i with 0 < i + Lk - Lq - key < 127 (and i < Lq) straddle the tile
   const int off = t.Lk - t.Lq;
   const int lo = max(0, t.key - off + 1), hi = min(t.Lq - 1, t.key - off + kKeys - 2);
@@ -155,6 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool DROP = DM != 0;
   constexpr bool DTAB = DM == 2 || DM == 4;
   constexpr bool DMASK = DM >= 3;
+  // without dropout the walk puts the band last (masked or not, so that a
+  // window wider than every sequence stays bitwise the unmasked call), and
+  // without a mask the step loop splits there
+  constexpr bool kBandLast = !DROP;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   uint8_t* sK = sm + kOffK;
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 1) tma_load_2d(sK + 2 * kTile, &tkt, &bars->kv_full, 2 * kChunk, key);
       if (lane == 2) tma_load_3d(sV, &tv2, &bars->kv_full, 0, key, 0);
       if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
-      const StepMap sm = step_map(t, step_tok);
+      const StepMap sm = step_map(t, step_tok, kBandLast);
       if (lane >= 4 && lane < 6) {
         for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
           const int ptok = t.q0 + sm.tb(sp / ngroups) * step_tok;
@@ -481,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (q.item < ntiles) {
         ktile_decode<MASK>(p, q.item, q.t);
         q.nsteps = step_count(q.t);
-        q.sm = step_map(q.t, step_tok);
+        q.sm = step_map(q.t, step_tok, kBandLast);
         q.tb = q.sm.tb(0);
         if (q.nsteps > 0) return;
         q.item = take();
@@ -606,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // keys; the halves of step st + 1 are loaded during step st, once P^T
       // of step st has gone out (their memory latency then hides behind the
       // dP^T and dS work)
-      const StepMap sm = step_map(t, step_tok);
+      const StepMap sm = step_map(t, step_tok, kBandLast);
       const uint32_t* mbase = nullptr;
       int mstep = 0;  // 32-bit words from one block (token block, head group) to the next
       uint32_t mw0 = 0, mw1 = 0;
@@ -905,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->ds_full);
         return true;
       };
-      if (!MASK) {
+      if (kBandLast && !MASK) {
         const int n_one = (sm.nA + sm.nC) * ngroups;
         int st = 0;
         for (; st < n_one && ok; ++st) ok = step(st, std::integral_constant<int, 0>{});
