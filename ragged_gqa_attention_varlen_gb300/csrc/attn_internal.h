@@ -136,24 +136,21 @@ cudaError_t launch_fwd(const Params& p, const CUtensorMap& tq2, const CUtensorMa
 cudaError_t launch_preprocess(const Params& p, cudaStream_t s);
 // Tensor maps: *2 load feature chunks 0-1 of a tile in one box; tq/tdo load
 // chunk 2 (features 128..191, the part past 159 filled with zeros); tkt/tvt
-// load features 128..159 with the 64-byte swizzle; tqf/tdof cover a whole
-// query tile unswizzled (L2 prefetches).
+// load features 128..159 with the 64-byte swizzle.
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                         const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
-                        const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s);
+                        int grid, cudaStream_t s);
 cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                              const CUtensorMap& tdo2, const CUtensorMap& tdo,
                              const CUtensorMap& tk2, const CUtensorMap& tkt,
                              const CUtensorMap& tv2, const CUtensorMap& tvt,
-                             const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
-                             cudaStream_t s);
+                             int grid, cudaStream_t s);
 cudaError_t launch_dkdv_dmask(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                               const CUtensorMap& tdo2, const CUtensorMap& tdo,
                               const CUtensorMap& tk2, const CUtensorMap& tkt,
                               const CUtensorMap& tv2, const CUtensorMap& tvt,
-                              const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
-                              cudaStream_t s);
+                              int grid, cudaStream_t s);
 cudaError_t launch_dq(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tqt,
                       const CUtensorMap& tdo2, const CUtensorMap& tdot, const CUtensorMap& tk2,
                       const CUtensorMap& tk, const CUtensorMap& tv2, const CUtensorMap& tvt,

@@ -20,13 +20,13 @@ auto dkdv_pick(const Params& p) {
 cudaError_t launch_dkdv(const Params& p, const CUtensorMap& tq2, const CUtensorMap& tq,
                         const CUtensorMap& tdo2, const CUtensorMap& tdo, const CUtensorMap& tk2,
                         const CUtensorMap& tkt, const CUtensorMap& tv2, const CUtensorMap& tvt,
-                        const CUtensorMap& tqf, const CUtensorMap& tdof, int grid, cudaStream_t s) {
+                        int grid, cudaStream_t s) {
   if (p.dropout)
-    return launch_dkdv_drop(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid, s);
+    return launch_dkdv_drop(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, grid, s);
   // instances for capped calls (the logit map's cap test: softcap > 0)
   auto k = p.softcap > 0.f ? dkdv_pick<true>(p) : dkdv_pick<false>(p);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-  k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
+  k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
   return cudaGetLastError();
 }
 

@@ -152,8 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo2,
                 const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk2,
                 const __grid_constant__ CUtensorMap tkt, const __grid_constant__ CUtensorMap tv2,
-                const __grid_constant__ CUtensorMap tvt, const __grid_constant__ CUtensorMap tqf,
-                const __grid_constant__ CUtensorMap tdof) {
+                const __grid_constant__ CUtensorMap tvt) {
   using namespace kv;
   constexpr bool DROP = DM != 0;
   constexpr bool DTAB = DM == 2 || DM == 4;
@@ -252,15 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tq);
       prefetch_tensormap(&tdo2);
       prefetch_tensormap(&tdo);
-    } else if (lane < 6) {
-      prefetch_tensormap(lane == 4 ? &tqf : &tdof);
     } else if (lane < 8) {
       prefetch_tensormap(&tk2);
       prefetch_tensormap(&tkt);
       prefetch_tensormap(&tv2);
       prefetch_tensormap(&tvt);
     }
-    constexpr int kPrefetchHead = 4;  // the first steps of a key tile, prefetched with K/V
     uint32_t nkv = 0, ndo = 0;
     Pair nq;
     bool ok = true;
@@ -283,28 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 2) tma_load_3d(sV, &tv2, &bars->kv_full, 0, key, 0);
       if (lane == 3) tma_load_2d(sV + 2 * kTile, &tvt, &bars->kv_full, 2 * kChunk, key);
       const StepMap sm = step_map(t, step_tok, kBandLast);
-      if (lane >= 4 && lane < 6) {
-        for (int sp = 0; sp < kPrefetchHead && sp < nsteps; ++sp) {
-          const int ptok = t.q0 + sm.tb(sp / ngroups) * step_tok;
-          const int ph0 = (sp % ngroups) * G;
-          if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
-          if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
-        }
-      }
       ++nkv;
-      // Q and dO stream from memory (a sequence's Q alone can exceed L2): the
-      // tiles of step st + kPrefetch are requested into L2 while step st is
-      // loaded, so the loads that the ring can afford to wait for hit L2.
-      constexpr int kPrefetch = 4;
+      // Q and dO stream from memory (a sequence's Q alone can exceed L2).
+      // No L2 prefetch ahead of the loads: with every SM prefetching a few
+      // steps ahead the prefetches crowded the memory system and made the
+      // kernel about 5 % slower (and the SMs' step rates 15 % apart).
       for (int st = 0; st < nsteps; ++st, ++ndo) {
         const int tok = t.q0 + sm.tb(st / ngroups) * step_tok;
         const int h0 = (st % ngroups) * G;
-        if (lane >= 4 && lane < 6 && st + kPrefetch < nsteps) {
-          const int ptok = t.q0 + sm.tb((st + kPrefetch) / ngroups) * step_tok;
-          const int ph0 = ((st + kPrefetch) % ngroups) * G;
-          if (lane == 4) tma_prefetch_3d(&tqf, 0, ph0, ptok);
-          if (lane == 5) tma_prefetch_3d(&tdof, 0, ph0, ptok);
-        }
         // Q of the step into slot g & 1
         const int s = (nq.c0 + nq.c1) & 1;
         const uint32_t n = nq.bump(s);

@@ -22,10 +22,9 @@ cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUte
                              const CUtensorMap& tdo2, const CUtensorMap& tdo,
                              const CUtensorMap& tk2, const CUtensorMap& tkt,
                              const CUtensorMap& tv2, const CUtensorMap& tvt,
-                             const CUtensorMap& tqf, const CUtensorMap& tdof, int grid,
-                             cudaStream_t s) {
+                             int grid, cudaStream_t s) {
   if (p.drop_mask)  // keep bits read from the stored mask
-    return launch_dkdv_dmask(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof, grid, s);
+    return launch_dkdv_dmask(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, grid, s);
   const bool m = masked_call(p);
   const bool tab = p.drop_tab != nullptr;
   const bool cap = p.softcap > 0.f;
@@ -34,7 +33,7 @@ cudaError_t launch_dkdv_drop(const Params& p, const CUtensorMap& tq2, const CUte
                         : (m ? dkdv_drop_kernel<false, true>(p.d, tab, cap)
                              : dkdv_drop_kernel<false, false>(p.d, tab, cap));
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::kSmem);
-  k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt, tqf, tdof);
+  k<<<grid, kThreads, kv::kSmem, s>>>(p, tq2, tq, tdo2, tdo, tk2, tkt, tv2, tvt);
   return cudaGetLastError();
 }
 

@@ -147,23 +147,6 @@ bool encode_kv_pair(CUtensorMap* m, int dtype, int d, const void* base, int64_t 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A whole query tile (d features x G heads x rows/G tokens) as one
-// unswizzled box, for L2 prefetches only.
-bool encode_q_full(CUtensorMap* m, int dtype, int d, const void* base, int64_t T, int H,
-                   int64_t ts, int64_t hs, int G, int rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(T)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs) * 2, static_cast<cuuint64_t>(ts) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(G),
-                       static_cast<cuuint32_t>(rows / G)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return encode_fn()(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -407,7 +390,7 @@ attn_status run_call(
   // ---- TMA tensor maps of one K/V head group (all of them when Hkv = 1)
   if (!encode_fn()) return ATTN_ERR_CUDA;
   struct Maps {
-    CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2, tqf, tdof;
+    CUtensorMap tq, tdo, tqt, tdot, tk, tv, tkt, tvt, tq2, tdo2, tk2, tv2;
   };
   const int R = Hq / Hkv;  // query heads per K/V head
   auto group_params = [&](int g) {
@@ -434,8 +417,7 @@ attn_status run_call(
   auto encode_group = [&](const Params& pg, int g, Maps& m) -> bool {
     const void* kg = static_cast<const uint16_t*>(k) + static_cast<int64_t>(g) * k_hs;
     const void* vg = static_cast<const uint16_t*>(v) + static_cast<int64_t>(g) * v_hs;
-    if (!encode_q_full(&m.tqf, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
-        !encode_q_pair(&m.tq2, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
+    if (!encode_q_pair(&m.tq2, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
         !encode_kv_pair(&m.tk2, dtype, head_dim, kg, total_k, k_ts) ||
         !encode_kv_pair(&m.tv2, dtype, head_dim, vg, total_k, v_ts) ||
         !encode_q(&m.tq, dtype, head_dim, pg.q, total_q, R, q_ts, q_hs, p.G, kRowsQ) ||
@@ -444,8 +426,7 @@ attn_status run_call(
         !encode_kv(&m.tkt, dtype, head_dim, kg, total_k, k_ts, true) ||
         !encode_kv(&m.tvt, dtype, head_dim, vg, total_k, v_ts, true))
       return false;
-    if (bwd && (!encode_q_full(&m.tdof, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
-                !encode_q_pair(&m.tdo2, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
+    if (bwd && (!encode_q_pair(&m.tdo2, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
                 !encode_q(&m.tdo, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ) ||
                 !encode_q(&m.tdot, dtype, head_dim, pg.dout, total_q, R, do_ts, do_hs, p.G, kRowsQ, true)))
       return false;
@@ -491,8 +472,8 @@ attn_status run_call(
   for (int g = 0; g < Hkv; ++g) {
     const Params pg = group_params(g);
     if (!encode_group(pg, g, m)) return ATTN_ERR_ALIGNMENT;
-    if (launch_dkdv(pg, m.tq2, m.tq, m.tdo2, m.tdo, m.tk2, m.tkt, m.tv2, m.tvt, m.tqf, m.tdof,
-                    grid_k, stream) != cudaSuccess)
+    if (launch_dkdv(pg, m.tq2, m.tq, m.tdo2, m.tdo, m.tk2, m.tkt, m.tv2, m.tvt, grid_k,
+                    stream) != cudaSuccess)
       return ATTN_ERR_CUDA;
     mark(4);
     // dq may overlap the tail of dk/dv (no per-kernel events in between)
