@@ -217,6 +217,31 @@ def test_negative_slope_parity(oracle_mod, case):
     parity(p, oracle_mod)
 
 
+# ------------------------------------------------ dk/dv's diagonal band
+# A dk/dv key tile walks the query steps whose columns' aligned keys fall
+# inside the tile (the band) after all others, and without a mask the steps
+# outside the band take the one-sided bias form only.  Steep slopes make a
+# wrong bias form visible; the lengths put the band at the tile's start, end
+# and middle, with Lq != Lk (the aligned key shifted) and token blocks of 8,
+# 16, 32, 64 and 128 tokens (query heads per K/V head 16, 8, 4, 2 and 3).
+
+BAND = [
+    dict(lq=[300, 129, 40], lk=[300, 129, 40], Hq=16),
+    dict(lq=[250, 70], lk=[400, 64], Hq=8, dtype=torch.bfloat16),
+    dict(lq=[500, 33], lk=[260, 300], Hq=8, Hkv=2),
+    dict(lq=[190, 257], lk=[450, 127], Hq=4, Hkv=2, d=128),
+    dict(lq=[333, 128], lk=[333, 200], Hq=6, Hkv=2, dtype=torch.bfloat16, d=64),
+]
+
+
+@pytest.mark.parametrize("case", BAND, ids=[f"band{i}" for i in range(len(BAND))])
+def test_dkdv_band_parity(oracle_mod, case):
+    case = dict(case)
+    lq, lk, Hq = case.pop("lq"), case.pop("lk"), case.pop("Hq")
+    p = W.custom(lq, lk, Hq, slope_max=0.8, **case)
+    parity(p, oracle_mod)
+
+
 def test_window_wider_than_every_sequence_is_bitwise_unmasked():
     """A two-sided window that admits every pair takes the unmasked code path
     on every tile, so the result is bitwise the unmasked call's."""
