@@ -119,7 +119,18 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
     }
   }
   __syncthreads();
-  if (*s_status != 0 || static_cast<int>(blockIdx.x) >= ntiles) return;
+  // Launched as a programmatic dependent of dk/dv, this grid may start before
+  // dk/dv ends; every CTA waits for dk/dv to complete before exiting, so the
+  // work after dq in the stream (the next K/V head group, or the next call,
+  // whose schedule kernel resets the tile counters dk/dv draws from) never
+  // overlaps dk/dv.  Without a prerequisite grid the wait returns at once.
+  auto wait_prerequisite = [&]() {
+    if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  };
+  if (*s_status != 0 || static_cast<int>(blockIdx.x) >= ntiles) {
+    wait_prerequisite();
+    return;
+  }
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
@@ -542,6 +553,7 @@ __global__ void __launch_bounds__(dqk::kThreadsDQ, 1)
   if (tid == 0 && *s_abort) atomicOr(p.status, ATTN_DEV_TIMEOUT_DQ);
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  wait_prerequisite();
 }
 
 template <bool B, bool M, bool DR, bool C>
